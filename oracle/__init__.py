@@ -1,0 +1,269 @@
+"""fp64 CPU oracle for the mHC residual-stream ops (test infrastructure).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline leg are the only code that may import this package.  The CUDA
+library never calls it, and the two share no code; only the seeded input
+generators in ``mhc_inputs`` feed both.
+
+The arithmetic lives in ``mhc_oracle.c`` (plain C, double accumulators,
+ascending loops, OpenMP over independent tokens).  This module compiles it
+with gcc (``build()``) and wraps each entry point with numpy arrays.  The
+layer composition (forward: proj_rms_compute_h, h_aggregate, h_post_bda;
+backward: the three op backwards plus the three-way gradient sum) is written
+out here from those functions.
+
+Sources are the three web pages the C file names: the rwkv-ops mhu_ffi.cu
+FFI handlers, the Megatron-Core ``core.fusions.fused_mhc_kernels`` API page,
+and RL-Kernel PR #383 (P1 start kit for mHC + RMSNorm).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mhc_oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle_mhc.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no -ffast-math, no FMA contraction)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
+           "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        P = ctypes.c_void_p
+        sig = {
+            "orc_sinkhorn_fwd": [P, P, i64, i32, i32, f64],
+            "orc_sinkhorn_bwd": [P, P, P, i64, i32, i32, f64],
+            "orc_proj_rms_compute_h_fwd": [P, P, P, P, i64, i32, i64, i32, f64, f64,
+                                           P, P, P, P, P],
+            "orc_proj_rms_compute_h_bwd": [P, P, P, P, P, P, P, i64, i32, i64, i32, f64,
+                                           f64, P, P, P, P],
+            "orc_h_aggregate_fwd": [P, P, i64, i32, i64, P],
+            "orc_h_aggregate_bwd": [P, P, P, i64, i32, i64, P, P],
+            "orc_h_post_bda_fwd": [P, P, P, P, P, i64, i32, i64, P],
+            "orc_h_post_bda_bwd": [P, P, P, P, P, P, i64, i32, i64, P, P, P, P, P],
+            "orc_rmsnorm_fwd": [P, i64, i64, f64, P, P],
+            "orc_rmsnorm_bwd": [P, P, i64, i64, f64, P],
+            "orc_num_threads": [],
+        }
+        for name, args in sig.items():
+            fn = getattr(_lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+    return _lib
+
+
+def num_threads() -> int:
+    """Threads the oracle's OpenMP regions use."""
+    return int(_L().orc_num_threads())
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _f64(a):
+    """Any input as a contiguous float64 array.
+
+    uint16 arrays are bf16 bit patterns and are widened exactly; float32 and
+    float64 arrays are converted (exactly) as they are.
+    """
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+
+
+def _check(rc, name):
+    if rc != 0:
+        raise RuntimeError(f"oracle {name} failed with code {rc}")
+
+
+def controller_width(n):
+    return n * n + 2 * n
+
+
+# --------------------------------------------------------------------------
+# Sinkhorn (rwkv-ops SinkhornFwdHost/BwdHost; Megatron fused_sinkhorn)
+# --------------------------------------------------------------------------
+
+def sinkhorn_fwd(logits, iters, eps):
+    """P = Sinkhorn(exp(logits)) for logits [..., n, n]; returns fp64."""
+    lg = _f64(logits)
+    n = lg.shape[-1]
+    M = lg.size // (n * n)
+    P = np.empty(lg.shape, dtype=np.float64)
+    _check(_L().orc_sinkhorn_fwd(_p(lg), _p(P), M, n, iters, float(eps)), "sinkhorn_fwd")
+    return P
+
+
+def sinkhorn_bwd(dP, logits, iters, eps):
+    """Gradient of the unrolled Sinkhorn map with respect to the logits."""
+    lg, g = _f64(logits), _f64(dP)
+    n = lg.shape[-1]
+    M = lg.size // (n * n)
+    d = np.empty(lg.shape, dtype=np.float64)
+    _check(_L().orc_sinkhorn_bwd(_p(g), _p(lg), _p(d), M, n, iters, float(eps)), "sinkhorn_bwd")
+    return d
+
+
+# --------------------------------------------------------------------------
+# proj_rms_compute_h (Megatron fused_proj_rms_compute_h; RL-Kernel fp32_gemm_rms)
+# --------------------------------------------------------------------------
+
+def proj_rms_compute_h_fwd(x, W, alpha, b, n, iters, eps_sk, eps_rms):
+    """x [T, n, C] (bf16 bits or float) -> dict(H_pre, H_post, H_res, u, r) in fp64."""
+    x = _f64(x)
+    T, C = x.shape[0], x.shape[-1]
+    O = controller_width(n)
+    H_pre = np.empty((T, n)); H_post = np.empty((T, n)); H_res = np.empty((T, n, n))
+    u = np.empty((T, O)); r = np.empty(T)
+    _check(_L().orc_proj_rms_compute_h_fwd(
+        _p(x), _p(_f64(W)), _p(_f64(alpha)), _p(_f64(b)), T, n, C, iters, float(eps_sk),
+        float(eps_rms), _p(H_pre), _p(H_post), _p(H_res), _p(u), _p(r)), "proj_fwd")
+    return {"H_pre": H_pre, "H_post": H_post, "H_res": H_res, "u": u, "r": r}
+
+
+def proj_rms_compute_h_bwd(dH_pre, dH_post, dH_res, x, W, alpha, b, n, iters, eps_sk,
+                           eps_rms, *, want_dx=True, want_dW=True):
+    """Returns dict(dx [T,n,C] or None, dW [K,O] or None, dalpha [3], db [O])."""
+    x = _f64(x)
+    T, C = x.shape[0], x.shape[-1]
+    O = controller_width(n)
+    dx = np.empty((T, n, C)) if want_dx else None
+    dW = np.empty((n * C, O)) if want_dW else None
+    dalpha = np.empty(3); db = np.empty(O)
+    _check(_L().orc_proj_rms_compute_h_bwd(
+        _p(_f64(dH_pre)), _p(_f64(dH_post)), _p(_f64(dH_res)), _p(x), _p(_f64(W)),
+        _p(_f64(alpha)), _p(_f64(b)), T, n, C, iters, float(eps_sk), float(eps_rms),
+        _p(dx), _p(dW), _p(dalpha), _p(db)), "proj_bwd")
+    return {"dx": dx, "dW": dW, "dalpha": dalpha, "db": db}
+
+
+# --------------------------------------------------------------------------
+# h_aggregate (Megatron fused_h_aggregate / FusedHAggregate; rwkv StreamAggregate)
+# --------------------------------------------------------------------------
+
+def h_aggregate_fwd(x, H_pre):
+    x = _f64(x)
+    T, n, C = x.shape
+    y = np.empty((T, C))
+    _check(_L().orc_h_aggregate_fwd(_p(x), _p(_f64(H_pre)), T, n, C, _p(y)), "agg_fwd")
+    return y
+
+
+def h_aggregate_bwd(dy, x, H_pre, *, want_dx=True):
+    x = _f64(x)
+    T, n, C = x.shape
+    dx = np.empty((T, n, C)) if want_dx else None
+    dH = np.empty((T, n))
+    _check(_L().orc_h_aggregate_bwd(_p(_f64(dy)), _p(x), _p(_f64(H_pre)), T, n, C, _p(dx),
+                                    _p(dH)), "agg_bwd")
+    return {"dx": dx, "dH_pre": dH}
+
+
+# --------------------------------------------------------------------------
+# h_post_bda (Megatron fused_h_post_bda / _torch_h_post_bda_bwd; rwkv MhcPostOp)
+# --------------------------------------------------------------------------
+
+def h_post_bda_fwd(res, f, bias, H_res, H_post):
+    res = _f64(res)
+    T, n, C = res.shape
+    out = np.empty((T, n, C))
+    _check(_L().orc_h_post_bda_fwd(_p(res), _p(_f64(f)), _p(None if bias is None else _f64(bias)),
+                                   _p(_f64(H_res)), _p(_f64(H_post)), T, n, C, _p(out)),
+           "post_fwd")
+    return out
+
+
+def h_post_bda_bwd(dout, res, f, bias, H_res, H_post, *, want_dres=True, want_df=True,
+                   want_dbias=True):
+    res = _f64(res)
+    T, n, C = res.shape
+    dres = np.empty((T, n, C)) if want_dres else None
+    df = np.empty((T, C)) if want_df else None
+    dbias = np.empty(C) if want_dbias else None
+    dHres = np.empty((T, n, n)); dHpost = np.empty((T, n))
+    _check(_L().orc_h_post_bda_bwd(
+        _p(_f64(dout)), _p(res), _p(_f64(f)), _p(None if bias is None else _f64(bias)),
+        _p(_f64(H_res)), _p(_f64(H_post)), T, n, C, _p(dres), _p(df), _p(dbias), _p(dHres),
+        _p(dHpost)), "post_bwd")
+    return {"dres": dres, "df": df, "dbias": dbias, "dH_res": dHres, "dH_post": dHpost}
+
+
+# --------------------------------------------------------------------------
+# Standalone RMSNorm (rwkv RMSNormFwdHost / RMSNormBwdHost)
+# --------------------------------------------------------------------------
+
+def rmsnorm_fwd(x, eps):
+    x = _f64(x)
+    rows, cols = x.shape
+    y = np.empty((rows, cols)); rstd = np.empty(rows)
+    _check(_L().orc_rmsnorm_fwd(_p(x), rows, cols, float(eps), _p(y), _p(rstd)), "rms_fwd")
+    return y, rstd
+
+
+def rmsnorm_bwd(dy, x, eps):
+    x = _f64(x)
+    rows, cols = x.shape
+    dx = np.empty((rows, cols))
+    _check(_L().orc_rmsnorm_bwd(_p(_f64(dy)), _p(x), rows, cols, float(eps), _p(dx)), "rms_bwd")
+    return dx
+
+
+# --------------------------------------------------------------------------
+# One mHC layer: forward = proj_rms_compute_h -> h_aggregate -> h_post_bda
+# (Megatron fused_mhc_kernels: the four fused ops); backward = the three op
+# backwards and the three-way sum of the residual gradient (fused_add_3).
+# f (the sub-layer output) and the upstream grads dout, dy are inputs.
+# --------------------------------------------------------------------------
+
+def layer_fwd(inp, n, iters, eps_sk, eps_rms):
+    h = proj_rms_compute_h_fwd(inp["x"], inp["W"], inp["alpha"], inp["b"], n, iters, eps_sk,
+                               eps_rms)
+    y = h_aggregate_fwd(inp["x"], h["H_pre"])
+    out = h_post_bda_fwd(inp["x"], inp["f"], inp["bias"], h["H_res"], h["H_post"])
+    return dict(h, y=y, out=out)
+
+
+def layer_bwd(inp, fwd, n, iters, eps_sk, eps_rms, *, want_dx=True):
+    """Gradients of L = <dout, out> + <dy, y> for one layer.
+
+    With want_dx=False only the per-token reductions and the parameter grads
+    are formed (dW, dalpha, db, dbias); the [T, n, C] and [T, C] tensors are
+    skipped, which lets full-size runs stay within host memory.
+    """
+    pb = h_post_bda_bwd(inp["dout"], inp["x"], inp["f"], inp["bias"], fwd["H_res"],
+                        fwd["H_post"], want_dres=want_dx, want_df=want_dx)
+    ab = h_aggregate_bwd(inp["dy"], inp["x"], fwd["H_pre"], want_dx=want_dx)
+    prb = proj_rms_compute_h_bwd(ab["dH_pre"], pb["dH_post"], pb["dH_res"], inp["x"], inp["W"],
+                                 inp["alpha"], inp["b"], n, iters, eps_sk, eps_rms,
+                                 want_dx=want_dx)
+    res = {"dW": prb["dW"], "dalpha": prb["dalpha"], "db": prb["db"], "dbias": pb["dbias"],
+           "dH_pre": ab["dH_pre"], "dH_post": pb["dH_post"], "dH_res": pb["dH_res"]}
+    if want_dx:
+        res["dx"] = pb["dres"] + ab["dx"] + prb["dx"]
+        res["df"] = pb["df"]
+    return res
