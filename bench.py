@@ -1,0 +1,453 @@
+"""Benchmark: mHC layer forward + backward on GB300, tokens/s and HBM roofline.
+
+One step = one pass of the whole hot path over one seeded synthetic batch:
+  mhc_layer_fwd (proj_rms_compute_h -> h_aggregate -> h_post_bda)
+  mhc_layer_bwd (post_bda, aggregate/compute_h and residual-gradient passes)
+  rmsnorm_fwd + rmsnorm_bwd on a standalone [T, C] bf16 tensor
+Default workload: T=16384 tokens, n=4 streams, C=4096 (7B-scale), seed 3.
+
+`python bench.py [--gpus N --steps K --warmup W]` prints one JSON line.
+Under torchrun each rank runs its own batch (weak scaling; the layer needs
+no exchange between ranks).  `--impl reference` times the fp64 CPU oracle on
+a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mhc_inputs as mi  # noqa: E402
+
+ITERS, EPS_SK, EPS_RMS, EPS_NORM = 20, 1e-6, 1e-6, 1e-6
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "mHC layer fwd+bwd tokens/sec on 1 GB300; achieved HBM GB/s vs ~8 TB/s peak"
+
+
+# ---------------------------------------------------------------------------
+# byte model
+# ---------------------------------------------------------------------------
+
+def model_bytes(T, n, C):
+    """Bytes one step must move through HBM (U = one bf16 [T, C] tensor).
+
+    layer fwd (4n+2)U: projection reads x (nU); aggregate reads x, writes y
+    ((n+1)U); post_bda reads x and f, writes out ((2n+1)U).
+    layer bwd (6n+4)U: post_bda pass reads dout, x, f, writes df ((2n+2)U);
+    aggregate/compute_h pass reads x, dy ((n+1)U); residual-gradient pass
+    reads x, dy, dout, writes dx ((3n+1)U).
+    RMSNorm: fwd 2U, bwd 3U.  Small terms (W, H, u, r, dW) are left out.
+    """
+    U = T * C * 2
+    return {"layer_fwd": (4 * n + 2) * U, "layer_bwd": (6 * n + 4) * U, "rmsnorm": 5 * U}
+
+
+def kernel_bytes(name, T, n, C):
+    """Algorithmic bytes of one launch of a library kernel in the layer step."""
+    U = T * C * 2
+    O = n * n + 2 * n
+    K = n * C
+    small = T * O * 4
+    table = {
+        "k_proj_gemm": n * U + K * O * 4,
+        "k_proj_tc": n * U + K * O * 4,
+        "k_compute_h_fwd": small,
+        "k_agg_fwd": (n + 1) * U,
+        "k_post_fwd": (2 * n + 1) * U,
+        "k_post_bwd_tok": (2 * n + 2) * U,
+        "k_agg_bwd": (n + 1) * U,
+        "k_compute_h_bwd": 3 * small,
+        "k_dx": (3 * n + 1) * U,
+        "k_dW_partial": n * U,
+        "k_dbias_partial": n * U,
+        "k_rms_fwd": 2 * U,
+        "k_rms_bwd": 3 * U,
+    }
+    return table.get(name)
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def csrc_hash():
+    d = os.path.join(ROOT, "layers_proj_rms_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+    except Exception:
+        return None
+    if d.get("csrc_hash") != csrc_hash():
+        return None
+    e = d.get("kernels", {}).get(workload, {}).get(kernel)
+    return None if e is None else float(e)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class Clocks:
+    Q = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.proc = None
+        self.out = None
+        try:
+            self.out = open(os.path.join("/tmp", f"mhc_clocks_{os.getpid()}.csv"), "w")
+            self.path = self.out.name
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    sm.append(float(f[0]))
+                    mx.append(float(f[1]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world):
+    import torch
+
+    import layers_proj_rms_gb300 as M
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    T, n, C, w_std, seed = mi.LAYER_WORKLOADS[args.workload]
+    O = n * n + 2 * n
+    inp = mi.layer_inputs(T, n, C, seed + 1000 * rank, w_std=w_std, rmsnorm=True)
+
+    def h2d_src(a):
+        t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
+        return t.pin_memory()
+
+    host_in = {k: h2d_src(v) for k, v in inp.items()}
+    bf = torch.bfloat16
+
+    def dev_of(k):
+        h = host_in[k]
+        t = h.to(dev)
+        return t.view(bf) if h.dtype == torch.int16 else t
+
+    d = {k: dev_of(k) for k in host_in}
+    e = lambda *s, dt=torch.float32: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+    o = {"H_pre": e(T, n), "H_post": e(T, n), "H_res": e(T, n, n), "u": e(T, O), "r": e(T),
+         "y": e(T, C, dt=bf), "out": e(T, n, C, dt=bf), "dx": e(T, n, C, dt=bf),
+         "df": e(T, C, dt=bf), "dW": e(n * C, O), "dalpha": e(3), "db": e(O), "dbias": e(C),
+         "yn": e(T, C, dt=bf), "rstd": e(T), "dxn": e(T, C, dt=bf)}
+    wsf = M.workspace(M.OP_LAYER_FWD, T, n, C, dev)
+    wsb = M.workspace(M.OP_LAYER_BWD, T, n, C, dev)
+
+    def step():
+        M.mhc_layer_fwd(d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"], ITERS, EPS_SK,
+                        EPS_RMS, o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"],
+                        o["out"], wsf)
+        M.mhc_layer_bwd(d["dout"], d["dy"], d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"],
+                        o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], ITERS, EPS_SK,
+                        EPS_RMS, o["dx"], o["df"], o["dW"], o["dalpha"], o["db"], o["dbias"], wsb)
+        M.rmsnorm_fwd(d["x_norm"], o["yn"], o["rstd"], EPS_NORM)
+        M.rmsnorm_bwd(d["dy_norm"], d["x_norm"], o["rstd"], o["dxn"], EPS_NORM)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    clocks = Clocks(dev.index if dev.index is not None else 0)
+    # keep the GPU busy ~1 s before the timed region so the clock samples
+    # taken around it are under load
+    t_end = time.time() + 1.0
+    while time.time() < t_end:
+        step()
+        torch.cuda.synchronize()
+    barrier()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    import ctypes
+
+    M.lib.mhc_profiler_enable(1)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    M.lib.mhc_profiler_enable(0)
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    assert M.mhc_device_error() == 0, "a kernel reported a device fault"
+
+    class KT(ctypes.Structure):
+        _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
+                    ("total_ms", ctypes.c_double)]
+
+    buf = (KT * 64)()
+    M.lib.mhc_profiler_collect.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    nk = M.lib.mhc_profiler_collect(ctypes.cast(buf, ctypes.c_void_p), 64)
+    kernels = {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(nk)}
+    launches = int(sum(v[0] for v in kernels.values()))
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: pinned host inputs -> device -> step -> host grads ----
+    e2e = None
+    if not args.no_e2e:
+        out_host = {k: torch.empty(o[k].shape, dtype=o[k].dtype, pin_memory=True)
+                    for k in ("dW", "dalpha", "db", "dbias")}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(v.numel() * v.element_size() for v in out_host.values())
+
+        def e2e_step():
+            for k, h in host_in.items():
+                dst = d[k].view(torch.int16) if d[k].dtype == bf else d[k]
+                dst.copy_(h, non_blocking=True)
+            step()
+            for k, h in out_host.items():
+                h.copy_(o[k], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ev1.record(stream)
+        barrier()
+        ems = ev0.elapsed_time(ev1) / args.steps
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": T * world / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "api": "pinned host -> cudaMemcpyAsync -> mhc_layer_fwd/bwd + rmsnorm_fwd/bwd -> "
+                      "host dW, dalpha, db, dbias"}
+
+    if rank != 0:
+        return None
+    mb = model_bytes(T, n, C)
+    total_b = sum(mb.values())
+    peak, peak_kind = measured_hbm_peak()
+    # dominant kernel
+    top = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else None
+    roof = None
+    if top:
+        name, (nl, tot) = top
+        avg_ms = tot / nl
+        kb = kernel_bytes(name, T, n, C)
+        if kb is not None:
+            ach = kb / (avg_ms / 1e3) / 1e9
+            roof = {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+                    "unit": "GB/s", "frac": round(ach / peak, 4),
+                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
+                    "traffic": ncu_traffic(name, args.workload),
+                    "algorithmic_bytes_per_launch": int(kb), "avg_launch_ms": round(avg_ms, 4),
+                    "share_of_step": round(tot / (ms * args.steps), 4)}
+    res = {
+        "metric": METRIC,
+        "value": T * world / (ms / 1e3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 residual/grad tensors, random-init W)",
+        "config": {"workload": args.workload, "T": T, "n": n, "C": C, "w_std": w_std,
+                   "seed": seed, "iters": ITERS, "global_batch_tokens": T * world,
+                   "step": "mhc_layer_fwd + mhc_layer_bwd + rmsnorm_fwd + rmsnorm_bwd",
+                   "l2": "inputs larger than L2 (x alone is %d MB per step)" % (T * n * C * 2 >> 20),
+                   "parallelism": f"replicas x{world} (tokens sharded, no collective)"},
+        "hbm": {"model_bytes_per_step": int(total_b),
+                "achieved_gbs": round(total_b / (ms / 1e3) / 1e9, 1),
+                "frac_of_nominal_8tbs": round(total_b / (ms / 1e3) / 1e9 / NOMINAL_HBM_GBS, 4),
+                "frac_of_measured": round(total_b / (ms / 1e3) / 1e9 / peak, 4)},
+        "roofline": roof,
+        "kernels": {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
+                        "share": round(v[1] / (ms * args.steps), 4)} for k, v in
+                    sorted(kernels.items(), key=lambda kv: -kv[1][1])},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return res
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_step(orc, sub, n):
+    f = orc.layer_fwd(sub, n, ITERS, EPS_SK, EPS_RMS)
+    orc.layer_bwd(sub, f, n, ITERS, EPS_SK, EPS_RMS)
+    _, rstd = orc.rmsnorm_fwd(sub["x_norm"], EPS_NORM)
+    orc.rmsnorm_bwd(sub["dy_norm"], sub["x_norm"], EPS_NORM)
+
+
+def sample_of(inp, tokens):
+    sub = dict(inp)
+    for k in ("x", "f", "dout", "dy", "x_norm", "dy_norm"):
+        sub[k] = inp[k][:tokens]
+    return sub
+
+
+def cpu_baseline(args, tokens):
+    import oracle as orc
+    orc.build()
+    T, n, C, w_std, seed = mi.LAYER_WORKLOADS[args.workload]
+    inp = mi.layer_inputs(T, n, C, seed, w_std=w_std, rmsnorm=True)
+    sub = sample_of(inp, tokens)
+    t0 = time.time()
+    oracle_step(orc, sub, n)
+    dt = time.time() - t0
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": orc.num_threads(), "kind": "oracle",
+            "seconds": round(dt, 2),
+            "sample": f"first {tokens} of the {T} tokens of the seeded batch: full layer fwd+bwd "
+                      f"(all outputs) and RMSNorm fwd+bwd on those rows, fp64 C oracle"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step one bounded sample."""
+    import oracle as orc
+    orc.build()
+    T, n, C, w_std, seed = mi.LAYER_WORKLOADS[args.workload]
+    tokens = args.ref_tokens
+    inp = mi.layer_inputs(T, n, C, seed, w_std=w_std, rmsnorm=True)
+    sub = sample_of(inp, tokens)
+    for _ in range(args.warmup):
+        oracle_step(orc, sub, n)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle_step(orc, sub, n)
+    dt = (time.time() - t0) / args.steps
+    v = tokens / dt
+    sample = (f"first {tokens} of the {T} tokens of the seeded batch per step: full layer "
+              f"fwd+bwd and RMSNorm fwd+bwd, fp64 C oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "T": T, "n": n, "C": C,
+                                        "sample_tokens": tokens},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="7b_fwdbwd_T16384_n4_C4096",
+                    choices=[k for k in mi.LAYER_WORKLOADS if "fwd_" not in k])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=4096)
+    ap.add_argument("--ref-tokens", type=int, default=1024)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args, args.cpu_tokens)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,445 @@
+// The C ABI of libmhc (declared in include/mhc.h): host-side validation,
+// status codes, workspace sizing and dispatch to the kernel launchers.
+// Nothing here allocates device memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "../../include/mhc.h"
+#include "launch.h"
+
+using mhc::bf16;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+mhc_status fail(mhc_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+// The device-side fault word (see mhc_device_error).
+__device__ int g_fault_word;
+
+int *fault_ptr()
+{
+    static int *ptrs[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int *>(p);
+    }
+    return ptrs[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Check {
+    mhc_status st = MHC_OK;
+    const char *fn;
+    explicit Check(const char *f) : fn(f) { g_msg[0] = '\0'; }
+
+    Check &ptr(const void *p, const char *name)
+    {
+        if (st == MHC_OK && !p) st = fail(MHC_ERR_NULL_PTR, "%s: %s is NULL", fn, name);
+        if (st == MHC_OK && p && !aligned16(p))
+            st = fail(MHC_ERR_MISALIGNED, "%s: %s is not 16-byte aligned", fn, name);
+        return *this;
+    }
+    Check &opt(const void *p, const char *name)  // may be NULL
+    {
+        if (st == MHC_OK && p && !aligned16(p))
+            st = fail(MHC_ERR_MISALIGNED, "%s: %s is not 16-byte aligned", fn, name);
+        return *this;
+    }
+    Check &count(int64_t v, const char *name)
+    {
+        if (st == MHC_OK && v < 0) st = fail(MHC_ERR_BAD_SHAPE, "%s: %s = %lld < 0", fn, name, (long long)v);
+        return *this;
+    }
+    Check &nstreams(int n)
+    {
+        if (st == MHC_OK && n != 4 && n != 8)
+            st = fail(MHC_ERR_UNSUPPORTED_N, "%s: n = %d (supported: 4, 8)", fn, n);
+        return *this;
+    }
+    Check &channels(int64_t C, const char *name = "C")
+    {
+        if (st == MHC_OK && (C < 8 || C % 8 != 0))
+            st = fail(MHC_ERR_BAD_SHAPE, "%s: %s = %lld must be a positive multiple of 8", fn, name,
+                      (long long)C);
+        if (st == MHC_OK && C > (int64_t(1) << 30))
+            st = fail(MHC_ERR_BAD_SHAPE, "%s: %s = %lld too large", fn, name, (long long)C);
+        return *this;
+    }
+    Check &fits(int64_t a, int64_t b, const char *what)  // a*b elements must fit in int64 / 2^62
+    {
+        if (st == MHC_OK && a > 0 && b > 0 && a > (int64_t(1) << 62) / b)
+            st = fail(MHC_ERR_BAD_SHAPE, "%s: %s overflows", fn, what);
+        return *this;
+    }
+    Check &iters(int it)
+    {
+        if (st == MHC_OK && (it < 0 || it > MHC_MAX_ITERS))
+            st = fail(MHC_ERR_BAD_ARG, "%s: iters = %d outside [0, %d]", fn, it, MHC_MAX_ITERS);
+        return *this;
+    }
+    Check &eps(float e, const char *name)
+    {
+        if (st == MHC_OK && !(e >= 0.f && isfinite(e)))
+            st = fail(MHC_ERR_BAD_ARG, "%s: %s = %g must be finite and >= 0", fn, name, double(e));
+        return *this;
+    }
+    Check &ws(const void *p, size_t have, size_t need)
+    {
+        if (st == MHC_OK && have < need)
+            st = fail(MHC_ERR_WORKSPACE_TOO_SMALL, "%s: workspace %zu bytes < %zu needed", fn, have,
+                      need);
+        if (st == MHC_OK && need > 0 && !p)
+            st = fail(MHC_ERR_NULL_PTR, "%s: workspace is NULL", fn);
+        if (st == MHC_OK && p && (reinterpret_cast<uintptr_t>(p) & 255u))
+            st = fail(MHC_ERR_MISALIGNED, "%s: workspace is not 256-byte aligned", fn);
+        return *this;
+    }
+    Check &device()
+    {
+        if (st != MHC_OK) return *this;
+        int dev = -1;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            st = fail(MHC_ERR_NO_DEVICE, "%s: no CUDA device (%s)", fn, cudaGetErrorString(e));
+        }
+        return *this;
+    }
+};
+
+mhc_status launched(const char *fn, cudaError_t e)
+{
+    if (e != cudaSuccess)
+        return fail(MHC_ERR_CUDA, "%s: CUDA error %s (%s)", fn, cudaGetErrorName(e),
+                    cudaGetErrorString(e));
+    return MHC_OK;
+}
+
+size_t layer_fwd_ws(int64_t T, int n, int64_t C) { return mhc::proj_fwd_ws_bytes(T, n, C); }
+
+// With no tokens every sum over tokens is zero.
+mhc_status zero_param_grads(Check &ck, float *dW, int64_t nW, float *dalpha, float *db,
+                            int64_t nb, float *dbias, int64_t nbias, cudaStream_t s)
+{
+    if (ck.device().st) return ck.st;
+    cudaError_t e = cudaMemsetAsync(dW, 0, size_t(nW) * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dalpha, 0, 3 * sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(db, 0, size_t(nb) * sizeof(float), s);
+    if (e == cudaSuccess && dbias) e = cudaMemsetAsync(dbias, 0, size_t(nbias) * sizeof(float), s);
+    return launched(ck.fn, e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mhc_status_string(mhc_status s)
+{
+    switch (s) {
+    case MHC_OK: return "ok";
+    case MHC_ERR_NULL_PTR: return "null pointer";
+    case MHC_ERR_BAD_SHAPE: return "bad shape";
+    case MHC_ERR_MISALIGNED: return "misaligned pointer";
+    case MHC_ERR_UNSUPPORTED_N: return "unsupported number of streams";
+    case MHC_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MHC_ERR_BAD_ARG: return "bad argument";
+    case MHC_ERR_CUDA: return "CUDA error";
+    case MHC_ERR_NO_DEVICE: return "no CUDA device";
+    case MHC_ERR_DEVICE_FAULT: return "device-side fault reported";
+    }
+    return "unknown status";
+}
+
+const char *mhc_last_error(void) { return g_msg; }
+
+int mhc_version(void) { return 100; }
+
+mhc_status mhc_device_error(int *code, mhc_stream_t stream)
+{
+    Check ck("mhc_device_error");
+    if (ck.device().st) return ck.st;
+    int *p = fault_ptr();
+    if (!p) return fail(MHC_ERR_CUDA, "mhc_device_error: fault word unavailable");
+    int v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, p, sizeof v, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess && v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyAsync(p, &zero, sizeof zero, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    if (e != cudaSuccess) return launched("mhc_device_error", e);
+    if (code) *code = v;
+    if (v != 0) return fail(MHC_ERR_DEVICE_FAULT, "a kernel reported fault code %d", v);
+    return MHC_OK;
+}
+
+size_t mhc_workspace_bytes(mhc_op op, int64_t T, int n, int64_t C)
+{
+    if (T < 0 || (n != 4 && n != 8) || C < 8 || C % 8 != 0) return 0;
+    switch (op) {
+    case MHC_OP_PROJ_RMS_COMPUTE_H_FWD: return mhc::proj_fwd_ws_bytes(T, n, C);
+    case MHC_OP_PROJ_RMS_COMPUTE_H_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
+    case MHC_OP_H_POST_BDA_BWD: return mhc::dbias_ws_bytes(T, C);
+    case MHC_OP_LAYER_FWD: return layer_fwd_ws(T, n, C);
+    case MHC_OP_LAYER_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
+    }
+    return 0;
+}
+
+mhc_status mhc_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int iters,
+                            float eps, mhc_stream_t stream)
+{
+    Check ck("mhc_sinkhorn_fwd");
+    ck.count(M, "M").nstreams(n).fits(M, n * n, "M*n*n").iters(iters).eps(eps, "eps");
+    if (ck.st || M == 0) return ck.st;
+    ck.ptr(logits, "logits").ptr(P, "P");
+    if (ck.st) return ck.st;
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_sinkhorn_fwd(logits, P, M, n, iters, eps, stream));
+}
+
+mhc_status mhc_sinkhorn_bwd(const float *dP, const float *logits, float *dlogits, int64_t M,
+                            int n, int iters, float eps, mhc_stream_t stream)
+{
+    Check ck("mhc_sinkhorn_bwd");
+    ck.count(M, "M").nstreams(n).fits(M, n * n, "M*n*n").iters(iters).eps(eps, "eps");
+    if (ck.st || M == 0) return ck.st;
+    ck.ptr(dP, "dP").ptr(logits, "logits").ptr(dlogits, "dlogits");
+    if (ck.st) return ck.st;
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_sinkhorn_bwd(dP, logits, dlogits, M, n, iters, eps, stream));
+}
+
+mhc_status mhc_proj_rms_compute_h_fwd(const mhc_bf16 *x, const float *W, const float *alpha3,
+                                      const float *b, int64_t T, int n, int64_t C, int iters,
+                                      float eps_sk, float eps_rms, float *H_pre, float *H_post,
+                                      float *H_res, float *u_save, float *r_save, void *ws,
+                                      size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_proj_rms_compute_h_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x, "x").ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(H_pre, "H_pre");
+    ck.ptr(H_post, "H_post").ptr(H_res, "H_res").opt(u_save, "u_save").opt(r_save, "r_save");
+    ck.ws(ws, ws_bytes, mhc::proj_fwd_ws_bytes(T, n, C)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_proj_fwd(reinterpret_cast<const bf16 *>(x), W, alpha3, b,
+                                                T, n, C, iters, eps_sk, eps_rms, H_pre, H_post,
+                                                H_res, u_save, r_save, ws, fault_ptr(), stream));
+}
+
+mhc_status mhc_proj_rms_compute_h_bwd(const float *dH_pre, const float *dH_post,
+                                      const float *dH_res, const mhc_bf16 *x, const float *W,
+                                      const float *alpha3, const float *b, const float *u_save,
+                                      const float *r_save, int64_t T, int n, int64_t C,
+                                      int iters, float eps_sk, float eps_rms, mhc_bf16 *dx,
+                                      float *dW, float *dalpha3, float *db, void *ws,
+                                      size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_proj_rms_compute_h_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    ck.ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(dW, "dW").ptr(dalpha3, "dalpha3");
+    ck.ptr(db, "db");
+    if (ck.st) return ck.st;
+    if (T == 0) return zero_param_grads(ck, dW, int64_t(n) * C * (n * n + 2 * n), dalpha3, db,
+                                        n * n + 2 * n, nullptr, 0, stream);
+    ck.ptr(dH_pre, "dH_pre").ptr(dH_post, "dH_post").ptr(dH_res, "dH_res").ptr(x, "x");
+    ck.ptr(u_save, "u_save").ptr(r_save, "r_save").ptr(dx, "dx");
+    ck.ws(ws, ws_bytes, mhc::proj_bwd_ws_bytes(T, n, C)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_proj_bwd(dH_pre, dH_post, dH_res,
+                                                reinterpret_cast<const bf16 *>(x), W, alpha3, b,
+                                                u_save, r_save, T, n, C, iters, eps_sk, eps_rms,
+                                                reinterpret_cast<bf16 *>(dx), dW, dalpha3, db, ws,
+                                                fault_ptr(), stream));
+}
+
+mhc_status mhc_h_aggregate_fwd(const mhc_bf16 *x, const float *H_pre, mhc_bf16 *y, int64_t T,
+                               int n, int64_t C, mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x, "x").ptr(H_pre, "H_pre").ptr(y, "y");
+    if (ck.st) return ck.st;
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggregate_fwd(reinterpret_cast<const bf16 *>(x), H_pre,
+                                                     reinterpret_cast<bf16 *>(y), T, n, C, stream));
+}
+
+mhc_status mhc_h_aggregate_bwd(const mhc_bf16 *dy, const mhc_bf16 *x, const float *H_pre,
+                               mhc_bf16 *dx, float *dH_pre, int64_t T, int n, int64_t C,
+                               mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(dy, "dy").ptr(x, "x").ptr(H_pre, "H_pre").ptr(dx, "dx").ptr(dH_pre, "dH_pre");
+    if (ck.st) return ck.st;
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggregate_bwd(
+                               reinterpret_cast<const bf16 *>(dy), reinterpret_cast<const bf16 *>(x),
+                               H_pre, reinterpret_cast<bf16 *>(dx), dH_pre, T, n, C, stream));
+}
+
+mhc_status mhc_h_post_bda_fwd(const mhc_bf16 *residual, const mhc_bf16 *f, const mhc_bf16 *bias,
+                              const float *H_res, const float *H_post, mhc_bf16 *out, int64_t T,
+                              int n, int64_t C, mhc_stream_t stream)
+{
+    Check ck("mhc_h_post_bda_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(residual, "residual").ptr(f, "f").opt(bias, "bias").ptr(H_res, "H_res");
+    ck.ptr(H_post, "H_post").ptr(out, "out");
+    if (ck.st) return ck.st;
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_post_fwd(reinterpret_cast<const bf16 *>(residual),
+                                                reinterpret_cast<const bf16 *>(f),
+                                                reinterpret_cast<const bf16 *>(bias), H_res, H_post,
+                                                reinterpret_cast<bf16 *>(out), T, n, C, stream));
+}
+
+mhc_status mhc_h_post_bda_bwd(const mhc_bf16 *dout, const mhc_bf16 *residual, const mhc_bf16 *f,
+                              const mhc_bf16 *bias, const float *H_res, const float *H_post,
+                              mhc_bf16 *dresidual, mhc_bf16 *df, float *dbias, float *dH_res,
+                              float *dH_post, int64_t T, int n, int64_t C, void *ws,
+                              size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_h_post_bda_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").opt(dbias, "dbias");
+    if (ck.st) return ck.st;
+    if (T == 0) {
+        if (dbias) {  // an empty sum is zero
+            if (ck.device().st) return ck.st;
+            return launched(ck.fn, cudaMemsetAsync(dbias, 0, size_t(C) * sizeof(float), stream));
+        }
+        return MHC_OK;
+    }
+    ck.ptr(dout, "dout").ptr(residual, "residual").ptr(f, "f").opt(bias, "bias");
+    ck.ptr(H_res, "H_res").ptr(H_post, "H_post").ptr(dresidual, "dresidual").ptr(df, "df");
+    ck.ptr(dH_res, "dH_res").ptr(dH_post, "dH_post");
+    ck.ws(ws, ws_bytes, dbias ? mhc::dbias_ws_bytes(T, C) : 0).device();
+    if (ck.st) return ck.st;
+    const bf16 *g = reinterpret_cast<const bf16 *>(dout);
+    cudaError_t e = mhc::launch_post_bwd_tok(
+        g, reinterpret_cast<const bf16 *>(residual), reinterpret_cast<const bf16 *>(f),
+        reinterpret_cast<const bf16 *>(bias), H_res, H_post, reinterpret_cast<bf16 *>(dresidual),
+        reinterpret_cast<bf16 *>(df), dH_res, dH_post, T, n, C, stream);
+    if (e == cudaSuccess && dbias) e = mhc::launch_dbias(g, H_post, dbias, T, n, C, ws, stream);
+    return launched(ck.fn, e);
+}
+
+static int64_t kMaxRmsCols = 32768;
+
+mhc_status rmsnorm_fwd(const mhc_bf16 *x, mhc_bf16 *y, float *rstd, int64_t rows, int64_t cols,
+                       float eps, mhc_stream_t stream)
+{
+    Check ck("rmsnorm_fwd");
+    ck.count(rows, "rows").channels(cols, "cols").fits(rows, cols, "rows*cols").eps(eps, "eps");
+    if (ck.st == MHC_OK && cols > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "rmsnorm_fwd: cols = %lld > %lld", (long long)cols,
+                     (long long)kMaxRmsCols);
+    if (ck.st || rows == 0) return ck.st;
+    ck.ptr(x, "x").ptr(y, "y").opt(rstd, "rstd").device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_rms_fwd(reinterpret_cast<const bf16 *>(x),
+                                               reinterpret_cast<bf16 *>(y), rstd, rows, cols, eps,
+                                               stream));
+}
+
+mhc_status rmsnorm_bwd(const mhc_bf16 *dy, const mhc_bf16 *x, const float *rstd, mhc_bf16 *dx,
+                       int64_t rows, int64_t cols, float eps, mhc_stream_t stream)
+{
+    Check ck("rmsnorm_bwd");
+    ck.count(rows, "rows").channels(cols, "cols").fits(rows, cols, "rows*cols").eps(eps, "eps");
+    if (ck.st == MHC_OK && cols > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "rmsnorm_bwd: cols = %lld > %lld", (long long)cols,
+                     (long long)kMaxRmsCols);
+    if (ck.st || rows == 0) return ck.st;
+    ck.ptr(dy, "dy").ptr(x, "x").opt(rstd, "rstd").ptr(dx, "dx").device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_rms_bwd(reinterpret_cast<const bf16 *>(dy),
+                                               reinterpret_cast<const bf16 *>(x), rstd,
+                                               reinterpret_cast<bf16 *>(dx), rows, cols, eps,
+                                               stream));
+}
+
+mhc_status mhc_layer_fwd(const mhc_bf16 *x, const float *W, const float *alpha3, const float *b,
+                         const mhc_bf16 *f, const mhc_bf16 *bias, int64_t T, int n, int64_t C,
+                         int iters, float eps_sk, float eps_rms, float *H_pre, float *H_post,
+                         float *H_res, float *u_save, float *r_save, mhc_bf16 *y,
+                         mhc_bf16 *out, void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_layer_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x, "x").ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(f, "f").opt(bias, "bias");
+    ck.ptr(H_pre, "H_pre").ptr(H_post, "H_post").ptr(H_res, "H_res").ptr(u_save, "u_save");
+    ck.ptr(r_save, "r_save").ptr(y, "y").ptr(out, "out");
+    ck.ws(ws, ws_bytes, layer_fwd_ws(T, n, C)).device();
+    if (ck.st) return ck.st;
+    const bf16 *xb = reinterpret_cast<const bf16 *>(x);
+    cudaError_t e = mhc::launch_proj_fwd(xb, W, alpha3, b, T, n, C, iters, eps_sk, eps_rms, H_pre,
+                                         H_post, H_res, u_save, r_save, ws, fault_ptr(), stream);
+    if (e == cudaSuccess)
+        e = mhc::launch_aggregate_fwd(xb, H_pre, reinterpret_cast<bf16 *>(y), T, n, C, stream);
+    if (e == cudaSuccess)
+        e = mhc::launch_post_fwd(xb, reinterpret_cast<const bf16 *>(f),
+                                 reinterpret_cast<const bf16 *>(bias), H_res, H_post,
+                                 reinterpret_cast<bf16 *>(out), T, n, C, stream);
+    return launched(ck.fn, e);
+}
+
+mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const mhc_bf16 *x,
+                         const float *W, const float *alpha3, const float *b, const mhc_bf16 *f,
+                         const mhc_bf16 *bias, const float *H_pre, const float *H_post,
+                         const float *H_res, const float *u_save, const float *r_save,
+                         int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms,
+                         mhc_bf16 *dx, mhc_bf16 *df, float *dW, float *dalpha3, float *db,
+                         float *dbias, void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_layer_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    ck.ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").opt(bias, "bias").ptr(dW, "dW");
+    ck.ptr(dalpha3, "dalpha3").ptr(db, "db").opt(dbias, "dbias");
+    if (ck.st == MHC_OK && bias && !dbias)
+        ck.st = fail(MHC_ERR_NULL_PTR, "mhc_layer_bwd: dbias is NULL but bias is given");
+    if (ck.st) return ck.st;
+    if (T == 0) return zero_param_grads(ck, dW, int64_t(n) * C * (n * n + 2 * n), dalpha3, db,
+                                        n * n + 2 * n, dbias, C, stream);
+    ck.ptr(dout, "dout").ptr(dy, "dy").ptr(x, "x").ptr(f, "f").ptr(H_pre, "H_pre");
+    ck.ptr(H_post, "H_post").ptr(H_res, "H_res").ptr(u_save, "u_save").ptr(r_save, "r_save");
+    ck.ptr(dx, "dx").ptr(df, "df");
+    ck.ws(ws, ws_bytes, mhc::proj_bwd_ws_bytes(T, n, C)).device();
+    if (ck.st) return ck.st;
+    return launched(
+        ck.fn, mhc::launch_layer_bwd(reinterpret_cast<const bf16 *>(dout),
+                                     reinterpret_cast<const bf16 *>(dy),
+                                     reinterpret_cast<const bf16 *>(x), W, alpha3, b,
+                                     reinterpret_cast<const bf16 *>(f),
+                                     reinterpret_cast<const bf16 *>(bias), H_pre, H_post, H_res,
+                                     u_save, r_save, T, n, C, iters, eps_sk, eps_rms,
+                                     reinterpret_cast<bf16 *>(dx), reinterpret_cast<bf16 *>(df),
+                                     dW, dalpha3, db, dbias, ws, fault_ptr(), stream));
+}
+
+}  // extern "C"

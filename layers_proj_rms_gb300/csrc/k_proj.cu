@@ -1,0 +1,579 @@
+// proj_rms_compute_h forward and backward, and the layer backward's
+// residual-gradient pass.
+//
+// Definitions: Megatron-Core fused_mhc_kernels (fused_proj_rms_compute_h,
+// _torch_proj_rms_compute_h(x, weight, alpha_pre, alpha_post, alpha_res,
+// bias, n, eps, compute_h_eps)), RL-Kernel PR #383 (fp32_gemm_rms: r =
+// 1/(q + eps), q = sqrt(s/K), backward term -r^2 x/(K q) guarded at an
+// all-zero row; three alpha scalars over PRE/POST/COMB), rwkv-ops mhu_ffi.cu
+// (MhcPreOpFwdHost: H_pre after sigmoid, H_post after 2*sigmoid, H_res after
+// Sinkhorn; MhcPreOpBwdHost: gradient back to the raw logits).
+//
+// Forward:  k_proj_gemm (split-K partial u = x W and s = sum x^2, fp32)
+//           k_compute_h_fwd (sum of partials, r, z, gates, Sinkhorn)
+// Backward: k_compute_h_bwd (per-token du, dz, dalpha terms, RMS coefficient)
+//           k_dx (du W^T + coef x [+ H_res dout + H_pre dy]), k_dW_partial,
+//           fixed-order reductions for dW, dalpha, db.
+#include "launch.h"
+#include "sinkhorn.cuh"
+
+namespace mhc {
+
+template <int N>
+struct Dims {
+    static constexpr int O = N * N + 2 * N;
+    static constexpr int OP = (O + 7) / 8;  // logits per thread in the GEMM (o = og + 8p)
+};
+
+// ---------------------------------------------------------------------------
+// Forward GEMM: partial u[s][t][o] = sum_{k in split s} x[t][k] W[k][o],
+// partial ss[s][t] = sum_{k in split s} x[t][k]^2.
+// CTA: 64 tokens x one K split, 128 threads; thread (mg, og) owns tokens
+// 4*mg..4*mg+3 and logits og, og+8, ...
+// ---------------------------------------------------------------------------
+constexpr int kGM = 64, kGK = 64, kGThreads = 128, kXPad = 2;
+
+template <int N>
+__global__ void __launch_bounds__(kGThreads)
+    k_proj_gemm(const bf16 *__restrict__ x, const float *__restrict__ W, float *__restrict__ upart,
+                float *__restrict__ spart, int64_t T, int64_t K, int64_t kchunk)
+{
+    constexpr int O = Dims<N>::O, OP = Dims<N>::OP;
+    __shared__ __align__(16) uint16_t xs[kGM][kGK + kXPad];
+    __shared__ __align__(16) float wsm[kGK * O];
+    const int tid = threadIdx.x, mg = tid >> 3, og = tid & 7;
+    const int64_t t0 = int64_t(blockIdx.x) * kGM;
+    const int64_t split = blockIdx.y;
+    const int64_t kb = split * kchunk, ke = min(K, kb + kchunk);
+    float acc[4][OP];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int p = 0; p < OP; ++p) acc[q][p] = 0.f;
+    float ssq = 0.f;  // threads < 64: sum of squares of row tid
+    for (int64_t k0 = kb; k0 < ke; k0 += kGK) {
+        __syncthreads();
+        // x tile: 64 rows x 64 k = 512 chunks of 8
+        for (int ch = tid; ch < kGM * (kGK / 8); ch += kGThreads) {
+            const int row = ch >> 3, cc = ch & 7;
+            const int64_t t = t0 + row, k = k0 + cc * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (t < T && k < ke) v = __ldg(reinterpret_cast<const uint4 *>(x + t * K + k));
+            uint32_t *d = reinterpret_cast<uint32_t *>(&xs[row][cc * 8]);
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        }
+        // W tile: rows k0..k0+63, O floats each
+        for (int e = tid; e < kGK * O; e += kGThreads) {
+            const int64_t k = k0 + e / O;
+            wsm[e] = (k < ke) ? __ldg(W + k0 * O + e) : 0.f;
+        }
+        __syncthreads();
+        if (tid < kGM) {
+#pragma unroll 8
+            for (int kk = 0; kk < kGK; ++kk) {
+                const float v = __uint_as_float(uint32_t(xs[tid][kk]) << 16);
+                ssq = fmaf(v, v, ssq);
+            }
+        }
+#pragma unroll 4
+        for (int kk = 0; kk < kGK; ++kk) {
+            float xv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) xv[q] = __uint_as_float(uint32_t(xs[mg * 4 + q][kk]) << 16);
+#pragma unroll
+            for (int p = 0; p < OP; ++p) {
+                const int o = og + 8 * p;
+                const float w = (o < O) ? wsm[kk * O + o] : 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[q][p] = fmaf(xv[q], w, acc[q][p]);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int64_t t = t0 + mg * 4 + q;
+        if (t < T)
+#pragma unroll
+            for (int p = 0; p < OP; ++p) {
+                const int o = og + 8 * p;
+                if (o < O) upart[(split * T + t) * O + o] = acc[q][p];
+            }
+    }
+    if (tid < kGM && t0 + tid < T) spart[split * T + t0 + tid] = ssq;
+}
+
+// ---------------------------------------------------------------------------
+// compute_h forward.  A group of N lanes per token, lane i owns row i of the
+// n x n block and logits pre[i], post[i], res[i][0..N).
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(128)
+    k_compute_h_fwd(const float *__restrict__ upart, const float *__restrict__ spart, int splits,
+                    const float *__restrict__ alpha, const float *__restrict__ b, int64_t T,
+                    int64_t K, int iters, float eps_sk, float eps_rms, float *__restrict__ Hpre,
+                    float *__restrict__ Hpost, float *__restrict__ Hres,
+                    float *__restrict__ u_save, float *__restrict__ r_save)
+{
+    constexpr int O = Dims<N>::O;
+    const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t t = gt / N;
+    const int i = int(gt % N);
+    const bool live = t < T;
+    const int64_t tt = live ? t : 0;
+    float s = 0.f, upre = 0.f, upost = 0.f, ures[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) ures[j] = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+        const float *u = upart + (int64_t(sp) * T + tt) * O;
+        s += __ldg(spart + int64_t(sp) * T + tt);
+        upre += __ldg(u + i);
+        upost += __ldg(u + N + i);
+#pragma unroll
+        for (int j = 0; j < N; ++j) ures[j] += __ldg(u + 2 * N + i * N + j);
+    }
+    const float q = sqrtf(s / float(K));
+    const float r = 1.0f / (q + eps_rms);
+    const float a0 = __ldg(alpha), a1 = __ldg(alpha + 1), a2 = __ldg(alpha + 2);
+    const float zpre = a0 * r * upre + __ldg(b + i);
+    const float zpost = a1 * r * upost + __ldg(b + N + i);
+    float a[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) a[j] = expf(a2 * r * ures[j] + __ldg(b + 2 * N + i * N + j));
+    sk_forward<N>(a, iters, eps_sk, nullptr, 0);
+    if (live) {
+        Hpre[t * N + i] = sigmoidf_(zpre);
+        Hpost[t * N + i] = 2.0f * sigmoidf_(zpost);
+#pragma unroll
+        for (int j = 0; j < N; ++j) Hres[(t * N + i) * N + j] = a[j];
+        if (u_save) {
+            u_save[t * O + i] = upre;
+            u_save[t * O + N + i] = upost;
+#pragma unroll
+            for (int j = 0; j < N; ++j) u_save[t * O + 2 * N + i * N + j] = ures[j];
+        }
+        if (r_save && i == 0) r_save[t] = r;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// compute_h backward.  Same lane layout.  Per token writes
+//   du[t][o] = alpha_seg r dz[o],  dz[t][o],  ga[t][seg] = sum_{o in seg} dz r u,
+//   coef[t] = -dr r^2 / (K q) with dr = sum_o dz alpha_seg u and q = 1/r - eps_rms
+//   (coef = 0 when q <= 0: an all-zero row has zero RMS gradient).
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(128)
+    k_compute_h_bwd(const float *__restrict__ dHpre, const float *__restrict__ dHpost,
+                    const float *__restrict__ dHres, const float *__restrict__ u_save,
+                    const float *__restrict__ r_save, const float *__restrict__ alpha,
+                    const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
+                    float eps_rms, float *__restrict__ du, float *__restrict__ dz,
+                    float *__restrict__ ga, float *__restrict__ coef)
+{
+    constexpr int O = Dims<N>::O;
+    extern __shared__ float sk_store[];  // [2*iters][blockDim.x]
+    const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t t = gt / N;
+    const int i = int(gt % N);
+    const bool live = t < T;
+    const int64_t tt = live ? t : 0;
+    const float *u = u_save + tt * O;
+    const float r = __ldg(r_save + tt);
+    const float a0 = __ldg(alpha), a1 = __ldg(alpha + 1), a2 = __ldg(alpha + 2);
+    const float upre = __ldg(u + i), upost = __ldg(u + N + i);
+    const float zpre = a0 * r * upre + __ldg(b + i);
+    const float zpost = a1 * r * upost + __ldg(b + N + i);
+    float ures[N], e[N], a[N], g[N];
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        ures[j] = __ldg(u + 2 * N + i * N + j);
+        e[j] = expf(a2 * r * ures[j] + __ldg(b + 2 * N + i * N + j));
+        a[j] = e[j];
+        g[j] = live ? __ldg(dHres + (tt * N + i) * N + j) : 0.f;
+    }
+    float *store = sk_store + threadIdx.x;
+    sk_forward<N>(a, iters, eps_sk, store, blockDim.x);
+    sk_backward<N>(g, a, e, iters, store, blockDim.x);  // g = dz_res row i
+    const float sp = sigmoidf_(zpre), so = sigmoidf_(zpost);
+    const float dzpre = (live ? __ldg(dHpre + tt * N + i) : 0.f) * sp * (1.f - sp);
+    const float dzpost = (live ? __ldg(dHpost + tt * N + i) : 0.f) * 2.f * so * (1.f - so);
+    float gres = 0.f, dres_dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        gres = fmaf(g[j], ures[j], gres);
+    }
+    float gpre = dzpre * upre, gpost = dzpost * upost;
+    dres_dot = gres;
+    // sums over the N lanes of the group
+#pragma unroll
+    for (int m = 1; m < N; m <<= 1) {
+        gpre += __shfl_xor_sync(kFull, gpre, m);
+        gpost += __shfl_xor_sync(kFull, gpost, m);
+        dres_dot += __shfl_xor_sync(kFull, dres_dot, m);
+    }
+    if (live) {
+        float *dut = du + t * O, *dzt = dz + t * O;
+        dut[i] = a0 * r * dzpre;
+        dut[N + i] = a1 * r * dzpost;
+        dzt[i] = dzpre;
+        dzt[N + i] = dzpost;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            dut[2 * N + i * N + j] = a2 * r * g[j];
+            dzt[2 * N + i * N + j] = g[j];
+        }
+        if (i == 0) {
+            ga[t * 4 + 0] = gpre * r;
+            ga[t * 4 + 1] = gpost * r;
+            ga[t * 4 + 2] = dres_dot * r;
+            ga[t * 4 + 3] = 0.f;
+            const float dr = a0 * gpre + a1 * gpost + a2 * dres_dot;
+            const float q = 1.0f / r - eps_rms;
+            coef[t] = (q > 0.f) ? -dr * r * r / (float(K) * q) : 0.f;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Residual-gradient pass.  CTA: 32 tokens x (N streams x CW channels), one
+// thread per (stream j, channel c), W row k = j*C + c kept in registers.
+//   dx[t][j][c] = sum_o du[t][o] W[k][o] + coef[t] x[t][j][c]
+//               [+ H_pre[t][j] dy[t][c] + sum_i H_res[t][j][i] dout[t][i][c]]
+// ---------------------------------------------------------------------------
+constexpr int kDxTT = 32, kDxThreads = 256;
+
+template <int N, bool LAYER>
+__global__ void __launch_bounds__(kDxThreads)
+    k_dx(const float *__restrict__ du, const float *__restrict__ coef, const float *__restrict__ W,
+         const bf16 *__restrict__ x, const bf16 *__restrict__ dy, const bf16 *__restrict__ dout,
+         const float *__restrict__ Hpre, const float *__restrict__ Hres, bf16 *__restrict__ dx,
+         int64_t T, int64_t C)
+{
+    constexpr int O = Dims<N>::O, CW = kDxThreads / N;
+    __shared__ float du_s[kDxTT * O];
+    __shared__ float coef_s[kDxTT];
+    __shared__ float hp_s[LAYER ? kDxTT * N : 1];
+    __shared__ float hr_s[LAYER ? kDxTT * N * N : 1];
+    const int tid = threadIdx.x;
+    const int j = tid / CW;
+    const int64_t c = int64_t(blockIdx.x) * CW + tid % CW;
+    const int64_t t0 = int64_t(blockIdx.y) * kDxTT;
+    const bool cv = c < C;
+    const int64_t K = N * C;
+    const int64_t k = j * C + c;
+    float wr[O];
+#pragma unroll
+    for (int o = 0; o < O; ++o) wr[o] = cv ? __ldg(W + k * O + o) : 0.f;
+    const int nt = int(min(int64_t(kDxTT), T - t0));
+    for (int e = tid; e < nt * O; e += kDxThreads) du_s[e] = __ldg(du + t0 * O + e);
+    for (int e = tid; e < nt; e += kDxThreads) coef_s[e] = __ldg(coef + t0 + e);
+    if (LAYER) {
+        for (int e = tid; e < nt * N; e += kDxThreads) hp_s[e] = __ldg(Hpre + t0 * N + e);
+        for (int e = tid; e < nt * N * N; e += kDxThreads) hr_s[e] = __ldg(Hres + t0 * N * N + e);
+    }
+    __syncthreads();
+    if (!cv) return;
+    const uint16_t *xu = reinterpret_cast<const uint16_t *>(x);
+    const uint16_t *dyu = reinterpret_cast<const uint16_t *>(dy);
+    const uint16_t *du16 = reinterpret_cast<const uint16_t *>(dout);
+    for (int tl = 0; tl < nt; ++tl) {
+        const int64_t t = t0 + tl;
+        float acc = 0.f;
+#pragma unroll
+        for (int o = 0; o < O; ++o) acc = fmaf(du_s[tl * O + o], wr[o], acc);
+        acc = fmaf(coef_s[tl], __uint_as_float(uint32_t(xu[t * K + k]) << 16), acc);
+        if (LAYER) {
+            acc = fmaf(hp_s[tl * N + j], __uint_as_float(uint32_t(dyu[t * C + c]) << 16), acc);
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                acc = fmaf(hr_s[(tl * N + j) * N + i],
+                           __uint_as_float(uint32_t(du16[(t * N + i) * C + c]) << 16), acc);
+        }
+        dx[t * K + k] = __float2bfloat16_rn(acc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dW partials: part[s][k][o] = sum_{t in split s} x[t][k] du[t][o]
+// ---------------------------------------------------------------------------
+constexpr int kWThreads = 256, kWTT = 32;
+
+template <int N>
+__global__ void __launch_bounds__(kWThreads)
+    k_dW_partial(const bf16 *__restrict__ x, const float *__restrict__ du, float *__restrict__ part,
+                 int64_t T, int64_t K, int64_t splits)
+{
+    constexpr int O = Dims<N>::O;
+    __shared__ float du_s[kWTT * O];
+    const int64_t k = int64_t(blockIdx.x) * kWThreads + threadIdx.x;
+    const int64_t s = blockIdx.y;
+    const int64_t tb = T * s / splits, te = T * (s + 1) / splits;
+    const uint16_t *xu = reinterpret_cast<const uint16_t *>(x);
+    float acc[O];
+#pragma unroll
+    for (int o = 0; o < O; ++o) acc[o] = 0.f;
+    for (int64_t t0 = tb; t0 < te; t0 += kWTT) {
+        const int nt = int(min(int64_t(kWTT), te - t0));
+        __syncthreads();
+        for (int e = threadIdx.x; e < nt * O; e += kWThreads) du_s[e] = __ldg(du + t0 * O + e);
+        __syncthreads();
+        if (k < K)
+            for (int tl = 0; tl < nt; ++tl) {
+                const float xv = __uint_as_float(uint32_t(xu[(t0 + tl) * K + k]) << 16);
+#pragma unroll
+                for (int o = 0; o < O; ++o) acc[o] = fmaf(xv, du_s[tl * O + o], acc[o]);
+            }
+    }
+    if (k < K)
+#pragma unroll
+        for (int o = 0; o < O; ++o) part[(s * K + k) * O + o] = acc[o];
+}
+
+// out[j] = sum_r part[r][j], r ascending
+__global__ void k_sum_rows_p(const float *__restrict__ part, float *__restrict__ out,
+                             int64_t rows, int64_t cols)
+{
+    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.f;
+    for (int64_t r = 0; r < rows; ++r) acc += part[r * cols + c];
+    out[c] = acc;
+}
+
+// out[j] = sum_t a[t][j] (stride lda), one block per column, fixed tree.
+__global__ void __launch_bounds__(256)
+    k_sum_cols(const float *__restrict__ a, int64_t lda, int64_t rows, float *__restrict__ out)
+{
+    __shared__ float red[256];
+    const int j = blockIdx.x;
+    float acc = 0.f;
+    for (int64_t r = threadIdx.x; r < rows; r += 256) acc += a[r * lda + j];
+    red[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) out[j] = red[0];
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static int64_t gemm_splits(int64_t T, int64_t K)
+{
+    const int64_t mt = (T + kGM - 1) / kGM;
+    const int64_t kblocks = (K + kGK - 1) / kGK;
+    int64_t s = (int64_t(kSplitSms) * 6 + mt - 1) / mt;
+    if (s > kblocks) s = kblocks;
+    if (s > 16) s = 16;
+    return s < 1 ? 1 : s;
+}
+
+size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C)
+{
+    const int64_t O = int64_t(n) * n + 2 * n;
+    const int64_t S = gemm_splits(T, int64_t(n) * C);
+    return ws_align(size_t(S * T * O) * 4) + ws_align(size_t(S * T) * 4);
+}
+
+template <int N>
+static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alpha,
+                                 const float *b, int64_t T, int64_t C, int iters, float eps_sk,
+                                 float eps_rms, float *Hpre, float *Hpost, float *Hres,
+                                 float *u_save, float *r_save, void *ws, cudaStream_t s)
+{
+    constexpr int O = Dims<N>::O;
+    const int64_t K = int64_t(N) * C;
+    const int64_t S = gemm_splits(T, K);
+    int64_t kchunk = (K + S - 1) / S;
+    kchunk = (kchunk + kGK - 1) / kGK * kGK;
+    const int64_t S_used = (K + kchunk - 1) / kchunk;
+    char *p = static_cast<char *>(ws);
+    float *upart = reinterpret_cast<float *>(p);
+    float *spart = reinterpret_cast<float *>(p + ws_align(size_t(S * T * O) * 4));
+    dim3 g(unsigned((T + kGM - 1) / kGM), unsigned(S_used));
+    {
+        MHC_PROF("k_proj_gemm", s);
+        k_proj_gemm<N><<<g, kGThreads, 0, s>>>(x, W, upart, spart, T, K, kchunk);
+    }
+    const int64_t threads = T * N;
+    {
+        MHC_PROF("k_compute_h_fwd", s);
+        k_compute_h_fwd<N><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+            upart, spart, int(S_used), alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+            u_save, r_save);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,
+                            int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms,
+                            float *Hpre, float *Hpost, float *Hres, float *u_save, float *r_save,
+                            void *ws, int *fault, cudaStream_t s)
+{
+    (void)fault;
+    if (n == 4)
+        return proj_fwd_impl<4>(x, W, alpha, b, T, C, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                                u_save, r_save, ws, s);
+    return proj_fwd_impl<8>(x, W, alpha, b, T, C, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                            u_save, r_save, ws, s);
+}
+
+static int64_t dW_splits(int64_t T, int64_t K)
+{
+    const int64_t kb = (K + kWThreads - 1) / kWThreads;
+    int64_t s = (int64_t(kSplitSms) * 4 + kb - 1) / kb;
+    if (s > (T + kWTT - 1) / kWTT) s = (T + kWTT - 1) / kWTT;
+    if (s > 32) s = 32;
+    return s < 1 ? 1 : s;
+}
+
+// workspace layout of the backward (each piece 256-byte aligned):
+//   du [T][O], dz [T][O], ga [T][4], coef [T], dHpre/dHpost [T][N], dHres [T][N][N],
+//   dW partials [S][K][O], dbias partials
+struct BwdWs {
+    float *du, *dz, *ga, *coef, *dHpre, *dHpost, *dHres, *dWpart;
+    void *dbias_ws;
+    size_t bytes;
+};
+
+static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
+{
+    const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * C;
+    BwdWs w;
+    char *p = static_cast<char *>(base);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        char *q = p ? p + off : nullptr;
+        off += ws_align(bytes);
+        return q;
+    };
+    w.du = reinterpret_cast<float *>(take(size_t(T * O) * 4));
+    w.dz = reinterpret_cast<float *>(take(size_t(T * O) * 4));
+    w.ga = reinterpret_cast<float *>(take(size_t(T * 4) * 4));
+    w.coef = reinterpret_cast<float *>(take(size_t(T) * 4));
+    w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
+    w.dHpost = reinterpret_cast<float *>(take(size_t(T * n) * 4));
+    w.dHres = reinterpret_cast<float *>(take(size_t(T * n * n) * 4));
+    w.dWpart = reinterpret_cast<float *>(take(size_t(dW_splits(T, K)) * size_t(K * O) * 4));
+    w.dbias_ws = take(dbias_ws_bytes(T, C));
+    w.bytes = off;
+    return w;
+}
+
+size_t proj_bwd_ws_bytes(int64_t T, int n, int64_t C) { return carve_bwd(nullptr, T, n, C).bytes; }
+
+struct LayerBwd {
+    const bf16 *dout, *dy, *f, *bias;
+    const float *Hpre, *Hpost, *Hres;
+    bf16 *df;
+    float *dbias;
+};
+
+template <int N>
+static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float *dHres,
+                            const bf16 *x, const float *W, const float *alpha, const float *b,
+                            const float *u_save, const float *r_save, int64_t T, int64_t C,
+                            int iters, float eps_sk, float eps_rms, const LayerBwd *L, bf16 *dx,
+                            float *dW, float *dalpha, float *db, void *ws, cudaStream_t s)
+{
+    constexpr int O = Dims<N>::O;
+    const int64_t K = int64_t(N) * C;
+    BwdWs w = carve_bwd(ws, T, N, C);
+    cudaError_t e;
+    if (L) {
+        // pass 1: dH_res, dH_post and df from dout
+        e = launch_post_bwd_tok(L->dout, x, L->f, L->bias, L->Hres, L->Hpost, nullptr, L->df,
+                                w.dHres, w.dHpost, T, N, C, s);
+        if (e != cudaSuccess) return e;
+        // pass 2: dH_pre = sum_c dy x
+        e = launch_aggregate_bwd(L->dy, x, L->Hpre, nullptr, w.dHpre, T, N, C, s);
+        if (e != cudaSuccess) return e;
+        dHpre = w.dHpre;
+        dHpost = w.dHpost;
+        dHres = w.dHres;
+    }
+    const size_t smem = size_t(2) * iters * 128 * sizeof(float);
+    e = cudaFuncSetAttribute(k_compute_h_bwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    {
+        MHC_PROF("k_compute_h_bwd", s);
+        k_compute_h_bwd<N><<<unsigned((T * N + 127) / 128), 128, smem, s>>>(
+            dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du, w.dz,
+            w.ga, w.coef);
+    }
+    // pass 3: residual gradient, dW, dbias
+    constexpr int CW = kDxThreads / N;
+    dim3 gdx(unsigned((C + CW - 1) / CW), unsigned((T + kDxTT - 1) / kDxTT));
+    if (L) {
+        MHC_PROF("k_dx", s);
+        k_dx<N, true><<<gdx, kDxThreads, 0, s>>>(w.du, w.coef, W, x, L->dy, L->dout, L->Hpre,
+                                                 L->Hres, dx, T, C);
+    } else {
+            MHC_PROF("k_dx", s);
+            k_dx<N, false><<<gdx, kDxThreads, 0, s>>>(w.du, w.coef, W, x, nullptr, nullptr, nullptr,
+                                                      nullptr, dx, T, C);
+        }
+    const int64_t S = dW_splits(T, K);
+    dim3 gw(unsigned((K + kWThreads - 1) / kWThreads), unsigned(S));
+    {
+        MHC_PROF("k_dW_partial", s);
+        k_dW_partial<N><<<gw, kWThreads, 0, s>>>(x, w.du, w.dWpart, T, K, S);
+    }
+    {
+        MHC_PROF("k_sum_rows_p", s);
+        k_sum_rows_p<<<unsigned((K * O + 255) / 256), 256, 0, s>>>(w.dWpart, dW, S, K * O);
+    }
+    {
+        MHC_PROF("k_sum_cols", s);
+        k_sum_cols<<<3, 256, 0, s>>>(w.ga, 4, T, dalpha);
+    }
+    {
+        MHC_PROF("k_sum_cols", s);
+        k_sum_cols<<<O, 256, 0, s>>>(w.dz, O, T, db);
+    }
+    if (L && L->dbias) {
+        e = launch_dbias(L->dout, L->Hpost, L->dbias, T, N, C, w.dbias_ws, s);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                            const bf16 *x, const float *W, const float *alpha, const float *b,
+                            const float *u_save, const float *r_save, int64_t T, int n,
+                            int64_t C, int iters, float eps_sk, float eps_rms, bf16 *dx,
+                            float *dW, float *dalpha, float *db, void *ws, int *fault,
+                            cudaStream_t s)
+{
+    (void)fault;
+    if (n == 4)
+        return bwd_impl<4>(dHpre, dHpost, dHres, x, W, alpha, b, u_save, r_save, T, C, iters,
+                           eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, s);
+    return bwd_impl<8>(dHpre, dHpost, dHres, x, W, alpha, b, u_save, r_save, T, C, iters,
+                       eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, s);
+}
+
+cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
+                             const float *alpha, const float *b, const bf16 *f,
+                             const bf16 *bias, const float *Hpre, const float *Hpost,
+                             const float *Hres, const float *u_save, const float *r_save,
+                             int64_t T, int n, int64_t C, int iters, float eps_sk,
+                             float eps_rms, bf16 *dx, bf16 *df, float *dW, float *dalpha,
+                             float *db, float *dbias, void *ws, int *fault, cudaStream_t s)
+{
+    (void)fault;
+    const LayerBwd L{dout, dy, f, bias, Hpre, Hpost, Hres, df, dbias};
+    if (n == 4)
+        return bwd_impl<4>(nullptr, nullptr, nullptr, x, W, alpha, b, u_save, r_save, T, C,
+                           iters, eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, s);
+    return bwd_impl<8>(nullptr, nullptr, nullptr, x, W, alpha, b, u_save, r_save, T, C, iters,
+                       eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, s);
+}
+
+}  // namespace mhc

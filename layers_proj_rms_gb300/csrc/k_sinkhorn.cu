@@ -1,0 +1,128 @@
+// Batched Sinkhorn-Knopp forward and backward: one launch for all M
+// matrices (rwkv-ops mhu_ffi.cu SinkhornFwdHost/SinkhornBwdHost run one
+// launch per matrix from a host loop; here each lane owns one row and a
+// group of n lanes owns one matrix).
+#include "launch.h"
+#include "sinkhorn.cuh"
+
+namespace mhc {
+
+constexpr int kSkThreads = 128;
+
+template <int N>
+__device__ __forceinline__ void load_row(const float *p, float (&v)[N])
+{
+    const float4 *q = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+    for (int h = 0; h < N / 4; ++h) {
+        const float4 w = __ldg(q + h);
+        v[4 * h] = w.x;
+        v[4 * h + 1] = w.y;
+        v[4 * h + 2] = w.z;
+        v[4 * h + 3] = w.w;
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void store_row(float *p, const float (&v)[N])
+{
+    float4 *q = reinterpret_cast<float4 *>(p);
+#pragma unroll
+    for (int h = 0; h < N / 4; ++h)
+        q[h] = make_float4(v[4 * h], v[4 * h + 1], v[4 * h + 2], v[4 * h + 3]);
+}
+
+template <int N>
+__global__ void __launch_bounds__(kSkThreads)
+    k_sinkhorn_fwd(const float *__restrict__ logits, float *__restrict__ P, int64_t rows,
+                   int iters, float eps)
+{
+    const int64_t row = int64_t(blockIdx.x) * kSkThreads + threadIdx.x;  // = m*N + i
+    const bool live = row < rows;
+    float a[N];
+    if (live) {
+        load_row<N>(logits + row * N, a);
+#pragma unroll
+        for (int j = 0; j < N; ++j) a[j] = expf(a[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) a[j] = 1.f;
+    }
+    sk_forward<N>(a, iters, eps, nullptr, 0);
+    if (live) store_row<N>(P + row * N, a);
+}
+
+template <int N>
+__global__ void __launch_bounds__(kSkThreads)
+    k_sinkhorn_bwd(const float *__restrict__ dP, const float *__restrict__ logits,
+                   float *__restrict__ dlogits, int64_t rows, int iters, float eps)
+{
+    extern __shared__ float sk_store[];  // [2*iters][kSkThreads]
+    const int64_t row = int64_t(blockIdx.x) * kSkThreads + threadIdx.x;
+    const bool live = row < rows;
+    float a[N], e[N], g[N];
+    if (live) {
+        load_row<N>(logits + row * N, e);
+        load_row<N>(dP + row * N, g);
+#pragma unroll
+        for (int j = 0; j < N; ++j) e[j] = expf(e[j]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            e[j] = 1.f;
+            g[j] = 0.f;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) a[j] = e[j];
+    float *store = sk_store + threadIdx.x;
+    sk_forward<N>(a, iters, eps, store, kSkThreads);
+    sk_backward<N>(g, a, e, iters, store, kSkThreads);
+    if (live) store_row<N>(dlogits + row * N, g);
+}
+
+static size_t sk_smem(int iters) { return size_t(2) * iters * kSkThreads * sizeof(float); }
+
+cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int iters,
+                                float eps, cudaStream_t s)
+{
+    const int64_t rows = M * n;
+    const unsigned grid = unsigned((rows + kSkThreads - 1) / kSkThreads);
+    if (n == 4) {
+        MHC_PROF("k_sinkhorn_fwd", s);
+        k_sinkhorn_fwd<4><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
+    } else {
+            MHC_PROF("k_sinkhorn_fwd", s);
+            k_sinkhorn_fwd<8><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
+        }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_sinkhorn_bwd(const float *dP, const float *logits, float *dlogits, int64_t M,
+                                int n, int iters, float eps, cudaStream_t s)
+{
+    const int64_t rows = M * n;
+    const unsigned grid = unsigned((rows + kSkThreads - 1) / kSkThreads);
+    const size_t smem = sk_smem(iters);
+    cudaError_t e;
+    if (n == 4) {
+        e = cudaFuncSetAttribute(k_sinkhorn_bwd<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sk_smem(64)));
+        if (e != cudaSuccess) return e;
+        {
+            MHC_PROF("k_sinkhorn_bwd", s);
+            k_sinkhorn_bwd<4><<<grid, kSkThreads, smem, s>>>(dP, logits, dlogits, rows, iters, eps);
+        }
+    } else {
+        e = cudaFuncSetAttribute(k_sinkhorn_bwd<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(sk_smem(64)));
+        if (e != cudaSuccess) return e;
+        {
+            MHC_PROF("k_sinkhorn_bwd", s);
+            k_sinkhorn_bwd<8><<<grid, kSkThreads, smem, s>>>(dP, logits, dlogits, rows, iters, eps);
+        }
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -1,0 +1,555 @@
+// HBM-streaming kernels of the mHC layer: h_aggregate fwd/bwd, h_post_bda
+// fwd/bwd (per-token part and the dbias column sum) and the standalone
+// RMSNorm fwd/bwd.  Every global access is a 16-byte vector of 8 bf16
+// values; all sums are fp32 in a fixed order (no atomics).
+//
+// Definitions: Megatron-Core fused_mhc_kernels (fused_h_aggregate,
+// _torch_h_aggregate_bwd, fused_h_post_bda "H_res.T @ residual + H_post *
+// (x + bias)", _torch_h_post_bda_bwd) and rwkv-ops mhu_ffi.cu
+// (StreamAggregateFwd/Bwd, MhcPostOpFwdHost/BwdHost, RMSNormFwdHost/BwdHost).
+#include "launch.h"
+
+namespace mhc {
+
+static int g_num_sms[64];
+
+int num_sms()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (g_num_sms[dev] == 0) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        g_num_sms[dev] = v > 0 ? v : 1;
+    }
+    return g_num_sms[dev];
+}
+
+static unsigned grid_for(int64_t work, int per_sm)
+{
+    const int64_t cap = int64_t(num_sms()) * per_sm;
+    return unsigned(work < cap ? (work > 0 ? work : 1) : cap);
+}
+
+static int threads_for(int64_t C8)
+{
+    int t = int((C8 + 31) / 32) * 32;
+    return t < 256 ? t : 256;
+}
+
+// ---------------------------------------------------------------------------
+// h_aggregate forward: y[t][c] = sum_i H_pre[t][i] x[t][i][c]
+// One block walks tokens; each thread one 8-wide chunk of c at a time.
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_agg_fwd(const bf16 *__restrict__ x, const float *__restrict__ Hpre, bf16 *__restrict__ y,
+              int64_t T, int64_t C8)
+{
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        float h[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) h[i] = __ldg(Hpre + t * N + i);
+        for (int64_t c8 = threadIdx.x; c8 < C8; c8 += blockDim.x) {
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                float v[8];
+                unpack8(ld_stream(x + ((t * N + i) * C8 + c8) * 8), v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(h[i], v[e], acc[e]);
+            }
+            st_stream(y + (t * C8 + c8) * 8, pack8(acc));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// h_aggregate backward: dx[t][i][c] = H_pre[t][i] dy[t][c] (if dx != null),
+// dH_pre[t][i] = sum_c dy[t][c] x[t][i][c].  One warp per token.
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_agg_bwd(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
+              const float *__restrict__ Hpre, bf16 *__restrict__ dx, float *__restrict__ dHpre,
+              int64_t T, int64_t C8)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        float h[N], part[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            h[i] = __ldg(Hpre + t * N + i);
+            part[i] = 0.f;
+        }
+        for (int64_t c8 = lane; c8 < C8; c8 += 32) {
+            float g[8];
+            unpack8(ld_stream(dy + (t * C8 + c8) * 8), g);
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                float v[8];
+                const int64_t off = ((t * N + i) * C8 + c8) * 8;
+                unpack8(ld_stream(x + off), v);
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(g[e], v[e], acc);
+                part[i] += acc;
+                if (dx) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = h[i] * g[e];
+                    st_stream(dx + off, pack8(o));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) part[i] = warp_sum(part[i]);
+        if (lane == 0)
+#pragma unroll
+            for (int i = 0; i < N; ++i) dHpre[t * N + i] = part[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// h_post_bda forward:
+//   out[t][i][c] = sum_j H_res[t][j][i] res[t][j][c] + H_post[t][i] (f[t][c] + bias[c])
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_post_fwd(const bf16 *__restrict__ res, const bf16 *__restrict__ f,
+               const bf16 *__restrict__ bias, const float *__restrict__ Hres,
+               const float *__restrict__ Hpost, bf16 *__restrict__ out, int64_t T, int64_t C8)
+{
+    __shared__ float hs[N * N + N];
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        __syncthreads();
+        for (int e = threadIdx.x; e < N * N + N; e += blockDim.x)
+            hs[e] = e < N * N ? __ldg(Hres + t * N * N + e) : __ldg(Hpost + t * N + e - N * N);
+        __syncthreads();
+        for (int64_t c8 = threadIdx.x; c8 < C8; c8 += blockDim.x) {
+            float fb[8];
+            unpack8(ld_stream(f + (t * C8 + c8) * 8), fb);
+            if (bias) {
+                float bv[8];
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8)), bv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) fb[e] += bv[e];
+            }
+            uint4 xr[N];
+#pragma unroll
+            for (int j = 0; j < N; ++j) xr[j] = ld_stream(res + ((t * N + j) * C8 + c8) * 8);
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                float acc[8];
+                const float hp = hs[N * N + i];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = hp * fb[e];
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float v[8];
+                    unpack8(xr[j], v);
+                    const float w = hs[j * N + i];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+                }
+                st_stream(out + ((t * N + i) * C8 + c8) * 8, pack8(acc));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// h_post_bda backward, per-token part.  One warp per token:
+//   dres[t][j][c]  = sum_i H_res[t][j][i] dout[t][i][c]     (if dres != null)
+//   df[t][c]       = sum_i H_post[t][i] dout[t][i][c]        (if df != null)
+//   dH_res[t][j][i] = sum_c res[t][j][c] dout[t][i][c]
+//   dH_post[t][i]  = sum_c dout[t][i][c] (f[t][c] + bias[c])
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_post_bwd_tok(const bf16 *__restrict__ dout, const bf16 *__restrict__ res,
+                   const bf16 *__restrict__ f, const bf16 *__restrict__ bias,
+                   const float *__restrict__ Hres, const float *__restrict__ Hpost,
+                   bf16 *__restrict__ dres, bf16 *__restrict__ df, float *__restrict__ dHres,
+                   float *__restrict__ dHpost, int64_t T, int64_t C8)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        const float *hr = Hres + t * N * N;  // read through L1 where used
+        float hp[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) hp[i] = __ldg(Hpost + t * N + i);
+        float aR[N * N], aP[N];
+#pragma unroll
+        for (int e = 0; e < N * N; ++e) aR[e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < N; ++i) aP[i] = 0.f;
+        for (int64_t c8 = lane; c8 < C8; c8 += 32) {
+            uint4 dr[N], xr[N];
+#pragma unroll
+            for (int i = 0; i < N; ++i) dr[i] = ld_stream(dout + ((t * N + i) * C8 + c8) * 8);
+#pragma unroll
+            for (int j = 0; j < N; ++j) xr[j] = ld_stream(res + ((t * N + j) * C8 + c8) * 8);
+            float fb[8];
+            unpack8(ld_stream(f + (t * C8 + c8) * 8), fb);
+            if (bias) {
+                float bv[8];
+                unpack8(__ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8)), bv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) fb[e] += bv[e];
+            }
+            float dfv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                float d[8];
+                unpack8(dr[i], d);
+                float sp = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    sp = fmaf(d[e], fb[e], sp);
+                    dfv[e] = fmaf(hp[i], d[e], dfv[e]);
+                }
+                aP[i] += sp;
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float v[8];
+                    unpack8(xr[j], v);
+                    float s = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) s = fmaf(v[e], d[e], s);
+                    aR[j * N + i] += s;
+                }
+            }
+            if (df) st_stream(df + (t * C8 + c8) * 8, pack8(dfv));
+            if (dres) {
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int i = 0; i < N; ++i) {
+                        float d[8];
+                        unpack8(dr[i], d);
+#pragma unroll
+                        const float w = __ldg(hr + j * N + i);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = fmaf(w, d[e], o[e]);
+                    }
+                    st_stream(dres + ((t * N + j) * C8 + c8) * 8, pack8(o));
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < N * N; ++e) aR[e] = warp_sum(aR[e]);
+#pragma unroll
+        for (int i = 0; i < N; ++i) aP[i] = warp_sum(aP[i]);
+        if (lane == 0) {
+#pragma unroll
+            for (int e = 0; e < N * N; ++e) dHres[t * N * N + e] = aR[e];
+#pragma unroll
+            for (int i = 0; i < N; ++i) dHpost[t * N + i] = aP[i];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// dbias[c] = sum_t sum_i H_post[t][i] dout[t][i][c]: every thread owns one
+// 8-wide chunk of c and a contiguous token range; partials per range are
+// then summed in ascending range order.
+// ---------------------------------------------------------------------------
+static int64_t dbias_splits(int64_t T, int64_t C8)
+{
+    const int64_t cblocks = (C8 + 255) / 256;
+    int64_t s = (int64_t(kSplitSms) * 4 + cblocks - 1) / cblocks;
+    if (s > T) s = T;
+    if (s > 256) s = 256;
+    return s < 1 ? 1 : s;
+}
+
+size_t dbias_ws_bytes(int64_t T, int64_t C)
+{
+    return ws_align(size_t(dbias_splits(T, C / 8)) * size_t(C) * sizeof(float));
+}
+
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_dbias_partial(const bf16 *__restrict__ dout, const float *__restrict__ Hpost,
+                    float *__restrict__ part, int64_t T, int64_t C8, int64_t splits)
+{
+    const int64_t c8 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t s = blockIdx.y;
+    const int64_t t0 = T * s / splits, t1 = T * (s + 1) / splits;
+    if (c8 >= C8) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t t = t0; t < t1; ++t) {
+        float dfv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float h = __ldg(Hpost + t * N + i);
+            float d[8];
+            unpack8(ld_stream(dout + ((t * N + i) * C8 + c8) * 8), d);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dfv[e] = fmaf(h, d[e], dfv[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] += dfv[e];
+    }
+    float4 *p = reinterpret_cast<float4 *>(part + (s * C8 + c8) * 8);
+    p[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    p[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+}
+
+__global__ void k_sum_rows(const float *__restrict__ part, float *__restrict__ out, int64_t rows,
+                           int64_t cols)
+{
+    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= cols) return;
+    float acc = 0.f;
+    for (int64_t r = 0; r < rows; ++r) acc += part[r * cols + c];
+    out[c] = acc;
+}
+
+cudaError_t launch_dbias(const bf16 *dout, const float *Hpost, float *dbias, int64_t T, int n,
+                         int64_t C, void *ws, cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const int64_t splits = dbias_splits(T, C8);
+    float *part = static_cast<float *>(ws);
+    dim3 grid(unsigned((C8 + 255) / 256), unsigned(splits));
+    if (n == 4) {
+        MHC_PROF("k_dbias_partial", s);
+        k_dbias_partial<4><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
+    } else {
+            MHC_PROF("k_dbias_partial", s);
+            k_dbias_partial<8><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
+        }
+    {
+        MHC_PROF("k_sum_rows", s);
+        k_sum_rows<<<unsigned((C + 255) / 256), 256, 0, s>>>(part, dbias, splits, C);
+    }
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Standalone RMSNorm, one block per row, the row held in registers
+// (R chunks of 8 values per thread).
+//   fwd: rho = 1/sqrt(sum x^2 / cols + eps), y = x rho
+//   bwd: dx = rho dy - rho^3 x (sum dy x) / cols
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float block_sum(float v, float *red)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = 0.f;
+    const int nw = blockDim.x >> 5;
+    for (int i = 0; i < nw; ++i) r += red[i];
+    return r;
+}
+
+template <int R>
+__global__ void __launch_bounds__(256)
+    k_rms_fwd(const bf16 *__restrict__ x, bf16 *__restrict__ y, float *__restrict__ rstd,
+              int64_t rows, int64_t C8, float inv_cols, float eps)
+{
+    __shared__ float red[8];
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        uint4 v[R];
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = threadIdx.x + int64_t(q) * blockDim.x;
+            if (c8 < C8) {
+                v[q] = ld_stream(x + (r * C8 + c8) * 8);
+                float f[8];
+                unpack8(v[q], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+            }
+        }
+        s = block_sum(s, red);
+        const float rho = rsqrtf(s * inv_cols + eps);
+        if (rstd && threadIdx.x == 0) rstd[r] = rho;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = threadIdx.x + int64_t(q) * blockDim.x;
+            if (c8 < C8) {
+                float f[8];
+                unpack8(v[q], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] *= rho;
+                st_stream(y + (r * C8 + c8) * 8, pack8(f));
+            }
+        }
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(256)
+    k_rms_bwd(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
+              const float *__restrict__ rstd, bf16 *__restrict__ dx, int64_t rows, int64_t C8,
+              float inv_cols, float eps)
+{
+    __shared__ float red[8];
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        uint4 vx[R], vg[R];
+        float d = 0.f, s = 0.f;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = threadIdx.x + int64_t(q) * blockDim.x;
+            if (c8 < C8) {
+                vx[q] = ld_stream(x + (r * C8 + c8) * 8);
+                vg[q] = ld_stream(dy + (r * C8 + c8) * 8);
+                float a[8], g[8];
+                unpack8(vx[q], a);
+                unpack8(vg[q], g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    d = fmaf(g[e], a[e], d);
+                    s = fmaf(a[e], a[e], s);
+                }
+            }
+        }
+        d = block_sum(d, red);
+        float rho;
+        if (rstd) {
+            rho = __ldg(rstd + r);
+        } else {
+            s = block_sum(s, red);
+            rho = rsqrtf(s * inv_cols + eps);
+        }
+        const float k2 = rho * rho * rho * d * inv_cols;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = threadIdx.x + int64_t(q) * blockDim.x;
+            if (c8 < C8) {
+                float a[8], g[8], o[8];
+                unpack8(vx[q], a);
+                unpack8(vg[q], g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = rho * g[e] - k2 * a[e];
+                st_stream(dx + (r * C8 + c8) * 8, pack8(o));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int64_t T, int n,
+                                 int64_t C, cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const unsigned g = grid_for(T, 8);
+    const int th = threads_for(C8);
+    if (n == 4) {
+        MHC_PROF("k_agg_fwd", s);
+        k_agg_fwd<4><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+    } else {
+            MHC_PROF("k_agg_fwd", s);
+            k_agg_fwd<8><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+        }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_aggregate_bwd(const bf16 *dy, const bf16 *x, const float *Hpre, bf16 *dx,
+                                 float *dHpre, int64_t T, int n, int64_t C, cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const unsigned g = grid_for((T + 7) / 8, 8);
+    if (n == 4) {
+        MHC_PROF("k_agg_bwd", s);
+        k_agg_bwd<4><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
+    } else {
+            MHC_PROF("k_agg_bwd", s);
+            k_agg_bwd<8><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
+        }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, const float *Hres,
+                            const float *Hpost, bf16 *out, int64_t T, int n, int64_t C,
+                            cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const unsigned g = grid_for(T, 8);
+    const int th = threads_for(C8);
+    if (n == 4) {
+        MHC_PROF("k_post_fwd", s);
+        k_post_fwd<4><<<g, th, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+    } else {
+            MHC_PROF("k_post_fwd", s);
+            k_post_fwd<8><<<g, th, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+        }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_post_bwd_tok(const bf16 *dout, const bf16 *res, const bf16 *f,
+                                const bf16 *bias, const float *Hres, const float *Hpost,
+                                bf16 *dres, bf16 *df, float *dHres, float *dHpost, int64_t T,
+                                int n, int64_t C, cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const unsigned g = grid_for((T + 7) / 8, 8);
+    if (n == 4) {
+        MHC_PROF("k_post_bwd_tok", s);
+        k_post_bwd_tok<4><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
+                                            dHpost, T, C8);
+    } else {
+            MHC_PROF("k_post_bwd_tok", s);
+            k_post_bwd_tok<8><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
+                                                dHpost, T, C8);
+        }
+    return cudaGetLastError();
+}
+
+// rows of up to 256 threads x R chunks x 8 values
+static int rms_R(int64_t C8)
+{
+    if (C8 <= 256 * 4) return 4;
+    if (C8 <= 256 * 16) return 16;
+    return 0;
+}
+
+cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, int64_t cols,
+                           float eps, cudaStream_t s)
+{
+    const int64_t C8 = cols / 8;
+    const unsigned g = grid_for(rows, 8);
+    const int th = threads_for((C8 + 3) / 4);
+    const float ic = 1.0f / float(cols);
+    if (rms_R(C8) == 4) {
+        MHC_PROF("k_rms_fwd", s);
+        k_rms_fwd<4><<<g, th, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+    } else {
+            MHC_PROF("k_rms_fwd", s);
+            k_rms_fwd<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf16 *dx,
+                           int64_t rows, int64_t cols, float eps, cudaStream_t s)
+{
+    const int64_t C8 = cols / 8;
+    const unsigned g = grid_for(rows, 8);
+    const int th = threads_for((C8 + 3) / 4);
+    const float ic = 1.0f / float(cols);
+    if (rms_R(C8) == 4) {
+        MHC_PROF("k_rms_bwd", s);
+        k_rms_bwd<4><<<g, th, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+    } else {
+            MHC_PROF("k_rms_bwd", s);
+            k_rms_bwd<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        }
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -1,0 +1,92 @@
+// Host-side launchers of the mHC kernels (C++ linkage, internal to libmhc).
+// Arguments are already validated by the C-ABI layer in abi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace mhc {
+
+typedef __nv_bfloat16 bf16;
+
+// Workspace carving: every sub-buffer starts on a 256-byte boundary.
+inline size_t ws_align(size_t b) { return (b + 255) & ~size_t(255); }
+
+constexpr int kMaxIters = 64;
+// Split counts of the split reductions are chosen for this many SMs on every
+// device, so that results do not depend on the device's SM count.
+constexpr int kSplitSms = 152;
+
+int num_sms();
+
+// Per-kernel event timing (prof.cu); a no-op unless mhc_profiler_enable(1).
+void prof_begin(const char *name, cudaStream_t s);
+void prof_end(cudaStream_t s);
+struct ProfScope {
+    cudaStream_t s_;
+    ProfScope(const char *name, cudaStream_t s) : s_(s) { prof_begin(name, s); }
+    ~ProfScope() { prof_end(s_); }
+};
+#define MHC_PROF_CAT2(a, b) a##b
+#define MHC_PROF_CAT(a, b) MHC_PROF_CAT2(a, b)
+// Time the launch(es) in the rest of the enclosing scope under `name`.
+#define MHC_PROF(name, s) ::mhc::ProfScope MHC_PROF_CAT(prof_scope_, __LINE__)(name, s)
+
+// k_sinkhorn.cu
+cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int iters,
+                                float eps, cudaStream_t s);
+cudaError_t launch_sinkhorn_bwd(const float *dP, const float *logits, float *dlogits, int64_t M,
+                                int n, int iters, float eps, cudaStream_t s);
+
+// k_stream.cu
+cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int64_t T, int n,
+                                 int64_t C, cudaStream_t s);
+cudaError_t launch_aggregate_bwd(const bf16 *dy, const bf16 *x, const float *Hpre, bf16 *dx,
+                                 float *dHpre, int64_t T, int n, int64_t C, cudaStream_t s);
+cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, const float *Hres,
+                            const float *Hpost, bf16 *out, int64_t T, int n, int64_t C,
+                            cudaStream_t s);
+// Per-token part of the post_bda backward: dres (nullable), df (nullable),
+// dH_res, dH_post.
+cudaError_t launch_post_bwd_tok(const bf16 *dout, const bf16 *res, const bf16 *f,
+                                const bf16 *bias, const float *Hres, const float *Hpost,
+                                bf16 *dres, bf16 *df, float *dHres, float *dHpost, int64_t T,
+                                int n, int64_t C, cudaStream_t s);
+// dbias[c] = sum_t sum_i H_post[t][i] dout[t][i][c]; scratch: dbias_ws_bytes.
+size_t dbias_ws_bytes(int64_t T, int64_t C);
+cudaError_t launch_dbias(const bf16 *dout, const float *Hpost, float *dbias, int64_t T, int n,
+                         int64_t C, void *ws, cudaStream_t s);
+cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, int64_t cols,
+                           float eps, cudaStream_t s);
+cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf16 *dx,
+                           int64_t rows, int64_t cols, float eps, cudaStream_t s);
+
+// k_proj.cu
+size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C);
+cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,
+                            int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms,
+                            float *Hpre, float *Hpost, float *Hres, float *u_save, float *r_save,
+                            void *ws, int *fault, cudaStream_t s);
+// Backward of proj_rms_compute_h (standalone op); workspace proj_bwd_ws_bytes.
+size_t proj_bwd_ws_bytes(int64_t T, int n, int64_t C);
+cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                            const bf16 *x, const float *W, const float *alpha, const float *b,
+                            const float *u_save, const float *r_save, int64_t T, int n,
+                            int64_t C, int iters, float eps_sk, float eps_rms, bf16 *dx,
+                            float *dW, float *dalpha, float *db, void *ws, int *fault,
+                            cudaStream_t s);
+// Layer backward (three passes over HBM): post_bda per-token reductions and
+// df; aggregate reduction for dH_pre with the compute_h backward; the
+// residual-gradient pass dx = H_res dout + H_pre dy + du W^T + coef x, with
+// dW and dbias.  Workspace proj_bwd_ws_bytes.
+cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
+                             const float *alpha, const float *b, const bf16 *f,
+                             const bf16 *bias, const float *Hpre, const float *Hpost,
+                             const float *Hres, const float *u_save, const float *r_save,
+                             int64_t T, int n, int64_t C, int iters, float eps_sk,
+                             float eps_rms, bf16 *dx, bf16 *df, float *dW, float *dalpha,
+                             float *db, float *dbias, void *ws, int *fault, cudaStream_t s);
+
+}  // namespace mhc

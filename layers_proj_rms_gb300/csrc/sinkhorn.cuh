@@ -1,0 +1,102 @@
+// Sinkhorn-Knopp on n x n matrices held by groups of n lanes.
+//
+// Definition (rwkv-ops mhu_ffi.cu SinkhornFwdHost/SinkhornBwdHost; Megatron-Core
+// fused_mhc_kernels fused_sinkhorn): A = exp(z); then `iters` times divide
+// every row by (row sum + eps), then every column by (column sum + eps).  The
+// backward is the exact gradient of that unrolled map.
+//
+// Layout in registers: a group of N consecutive lanes (N in {4, 8}, aligned
+// to N) holds one matrix; lane i of the group holds row i as N floats.  Row
+// sums are local; column sums are a butterfly over the group's lanes.  All
+// 32 lanes of the warp must call these functions together (the shuffles use
+// the full mask); a group without work runs on dummy data.
+#pragma once
+
+#include "common.cuh"
+
+namespace mhc {
+
+template <int N>
+__device__ __forceinline__ void sk_colsum(const float (&v)[N], float (&cs)[N])
+{
+#pragma unroll
+    for (int j = 0; j < N; ++j) cs[j] = v[j];
+#pragma unroll
+    for (int m = 1; m < N; m <<= 1)
+#pragma unroll
+        for (int j = 0; j < N; ++j) cs[j] += __shfl_xor_sync(kFull, cs[j], m);
+}
+
+// Forward.  a: in exp(z) row, out the row of P.  If `store` is not null the
+// denominators of every step are kept for the backward: store[(2k)*stride]
+// is (this lane's row sum + eps) at the row step of iteration k, and
+// store[(2k+1)*stride] is (column (lane % N)'s sum + eps) at its column step.
+template <int N>
+__device__ __forceinline__ void sk_forward(float (&a)[N], int iters, float eps, float *store,
+                                           int stride)
+{
+    const int i = threadIdx.x & (N - 1);
+    for (int k = 0; k < iters; ++k) {
+        float rs = 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) rs += a[j];
+        const float rd = rs + eps;
+#pragma unroll
+        for (int j = 0; j < N; ++j) a[j] = a[j] / rd;
+        float cs[N];
+        sk_colsum<N>(a, cs);
+        float cd_mine = 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            const float cd = cs[j] + eps;
+            a[j] = a[j] / cd;
+            if (j == i) cd_mine = cd;
+        }
+        if (store) {
+            store[(2 * k) * stride] = rd;
+            store[(2 * k + 1) * stride] = cd_mine;
+        }
+    }
+}
+
+// Backward.  On entry g holds this lane's row of dL/dP, a the row of P (the
+// forward output) and e the row of exp(z); `store` the denominators written
+// by sk_forward.  On exit g holds the row of dL/dz.  a is consumed: walking
+// the steps in reverse, each intermediate matrix is rebuilt by multiplying
+// back the stored denominator.
+//   column step Y = X / cd_j:  dX[i][j] = (dY[i][j] - sum_i' dY[i'][j] Y[i'][j]) / cd_j
+//   row step    Y = X / rd_i:  dX[i][j] = (dY[i][j] - sum_j' dY[i][j'] Y[i][j']) / rd_i
+template <int N>
+__device__ __forceinline__ void sk_backward(float (&g)[N], float (&a)[N], const float (&e)[N],
+                                            int iters, const float *store, int stride)
+{
+    const int lane = threadIdx.x & (kWarp - 1);
+    const int base = lane & ~(N - 1);
+    for (int k = iters - 1; k >= 0; --k) {
+        const float rd = store[(2 * k) * stride];
+        const float cd_mine = store[(2 * k + 1) * stride];
+        float ga[N], dot[N], cd[N];
+#pragma unroll
+        for (int j = 0; j < N; ++j) ga[j] = g[j] * a[j];
+        sk_colsum<N>(ga, dot);
+#pragma unroll
+        for (int j = 0; j < N; ++j) cd[j] = __shfl_sync(kFull, cd_mine, base + j);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            g[j] = (g[j] - dot[j]) / cd[j];
+            a[j] = a[j] * cd[j];
+        }
+        float rdot = 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) rdot += g[j] * a[j];
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            g[j] = (g[j] - rdot) / rd;
+            a[j] = a[j] * rd;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < N; ++j) g[j] = g[j] * e[j];
+}
+
+}  // namespace mhc

@@ -116,6 +116,7 @@ def rmsnorm_inputs(rows: int, cols: int, seed: int) -> dict:
 # The workloads, by what they are.  Each entry: (T, n, C, w_std, seed).
 LAYER_WORKLOADS = {
     "tiny_T256_n4_C256": (256, 4, 256, 0.02, 0),
+    "mid_T4096_n4_C4096": (4096, 4, 4096, 0.02, 5),
     "7b_fwd_T16384_n4_C4096": (16384, 4, 4096, 0.02, 2),
     "7b_fwdbwd_T16384_n4_C4096": (16384, 4, 4096, 0.02, 3),
     "wide_T8192_n8_C7168": (8192, 8, 7168, 0.01, 4),

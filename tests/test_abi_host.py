@@ -1,0 +1,123 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports
+every symbol include/mhc.h declares, and rejects bad arguments on the host
+before touching a device (no kernel is launched by these tests)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhc.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from layers_proj_rms_gb300 import build as B
+    B.build()
+    import layers_proj_rms_gb300 as m
+    return m.lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^MHC_API\s+[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_op_set():
+    names = set(declared_functions())
+    for op in ["mhc_sinkhorn_fwd", "mhc_sinkhorn_bwd", "mhc_proj_rms_compute_h_fwd",
+               "mhc_proj_rms_compute_h_bwd", "mhc_h_aggregate_fwd", "mhc_h_aggregate_bwd",
+               "mhc_h_post_bda_fwd", "mhc_h_post_bda_bwd", "rmsnorm_fwd", "rmsnorm_bwd",
+               "mhc_layer_fwd", "mhc_layer_bwd"]:
+        assert op in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(L):
+    for s in range(10):
+        assert L.mhc_status_string(s)
+    assert L.mhc_version() >= 100
+
+
+A = 0x10000  # a 16-byte-aligned fake device address; never dereferenced
+
+
+def test_validation_errors_without_gpu(L):
+    f = L.mhc_h_aggregate_fwd
+    # unsupported n
+    assert f(A, A, A, 16, 5, 64, None) == 4
+    assert b"n = 5" in L.mhc_last_error()
+    # C not a multiple of 8
+    assert f(A, A, A, 16, 4, 60, None) == 2
+    # null pointer
+    assert f(None, A, A, 16, 4, 64, None) == 1
+    # misaligned pointer
+    assert f(A + 2, A, A, 16, 4, 64, None) == 3
+    # negative T
+    assert f(A, A, A, -1, 4, 64, None) == 2
+    # T = 0 is a no-op and needs no pointers
+    assert f(None, None, None, 0, 4, 64, None) == 0
+    # all valid: reaches the device check, which fails here (no GPU)
+    rc = f(A, A, A, 16, 4, 64, None)
+    assert rc in (0, 8, 7)
+    if rc:
+        assert L.mhc_last_error()
+
+
+def test_sinkhorn_iters_and_eps_checks(L):
+    f = L.mhc_sinkhorn_fwd
+    assert f(A, A, 10, 4, 65, ctypes.c_float(1e-6), None) == 6
+    assert f(A, A, 10, 4, -1, ctypes.c_float(1e-6), None) == 6
+    assert f(A, A, 10, 4, 20, ctypes.c_float(float("nan")), None) == 6
+    assert f(A, A, 10, 4, 20, ctypes.c_float(-1.0), None) == 6
+    assert f(A, A, 10, 6, 20, ctypes.c_float(1e-6), None) == 4
+
+
+def test_workspace_sizes(L):
+    ws = L.mhc_workspace_bytes
+    for op in (1, 2, 3, 4, 5):
+        a = ws(op, 256, 4, 256)
+        b = ws(op, 16384, 4, 4096)
+        assert a > 0 and b >= a and a % 256 == 0
+    assert ws(1, 256, 5, 256) == 0
+    assert ws(9, 256, 4, 256) == 0
+
+
+def test_workspace_checks(L):
+    f = L.mhc_proj_rms_compute_h_fwd
+    need = L.mhc_workspace_bytes(1, 256, 4, 256)
+    args = [A, A, A, A, 256, 4, 256, 20, ctypes.c_float(1e-6), ctypes.c_float(1e-6), A, A, A,
+            None, None]
+    assert f(*args, A, ctypes.c_size_t(need - 1), None) == 5
+    assert f(*args, None, ctypes.c_size_t(need), None) == 1
+    assert f(*args, A + 16, ctypes.c_size_t(need), None) == 3
+
+
+def test_layer_bwd_requires_dbias_with_bias(L):
+    from layers_proj_rms_gb300 import _lib  # noqa: F401  (argtypes)
+    f = L.mhc_layer_bwd
+    rc = f(A, A, A, A, A, A, A, A, A, A, A, A, A, 64, 4, 64, 20, 1e-6, 1e-6, A, A, A, A, A, None,
+           A, 1 << 30, None)
+    assert rc == 1 and b"dbias" in L.mhc_last_error()
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    """The binding never falls back: a missing libmhc.so is an ImportError."""
+    import subprocess
+    import sys
+    code = ("import sys, os; sys.path.insert(0, %r);"
+            "import layers_proj_rms_gb300._lib as L" % ROOT)
+    env = dict(os.environ)
+    lib = os.path.join(ROOT, "layers_proj_rms_gb300", "_build", "libmhc.so")
+    hidden = lib + ".hidden_for_test"
+    os.rename(lib, hidden)
+    try:
+        r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    finally:
+        os.rename(hidden, lib)
+    assert r.returncode != 0 and "libmhc.so is missing" in r.stderr

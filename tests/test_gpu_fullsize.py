@@ -1,0 +1,88 @@
+"""GPU parity at the benchmark's full sizes, through the same entry points and
+workspace sizes that bench.py times:
+
+  * 7B-scale layer fwd+bwd: T=16384, n=4, C=4096, W ~ N(0, 0.02), seed 3,
+    plus the standalone RMSNorm fwd+bwd on [16384, 4096];
+  * wide-stream layer fwd+bwd: T=8192, n=8, C=7168, W ~ N(0, 0.01), seed 4.
+
+Per-token outputs (H_*, y, out, dx, df) are compared on a sample of tokens
+(the oracle recomputes exactly those rows); the sums over all tokens (dW,
+dalpha, db, dbias) are compared in full."""
+import numpy as np
+import pytest
+import torch
+
+import mhc_inputs as mi
+from tests._util import err_bf16, err_grad, err_h
+from tests.test_gpu_ops import ITERS, EPS_SK, EPS_RMS, run_layer
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    import layers_proj_rms_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return m
+
+
+def _sample(T, seed, k=48):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    idx = np.unique(np.concatenate([[0, T - 1], rng.choice(T, size=k, replace=False)]))
+    return idx
+
+
+def _full_layer_check(M, orc, T, n, C, w_std, seed):
+    inp = mi.layer_inputs(T, n, C, seed, w_std=w_std)
+    o = run_layer(M, inp, T, n, C)
+    # sums over all tokens
+    f64 = {k: orc._f64(v) for k, v in inp.items()}
+    ref_f = orc.proj_rms_compute_h_fwd(f64["x"], inp["W"], inp["alpha"], inp["b"], n, ITERS,
+                                       EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(f64, ref_f, n, ITERS, EPS_SK, EPS_RMS, want_dx=False)
+    err_h(o["H_pre"], ref_f["H_pre"])
+    err_h(o["H_post"], ref_f["H_post"])
+    err_h(o["H_res"], ref_f["H_res"])
+    err_grad(o["dW"], ref_b["dW"])
+    err_grad(o["dalpha"], ref_b["dalpha"])
+    err_grad(o["db"], ref_b["db"])
+    err_grad(o["dbias"], ref_b["dbias"])
+    # per-token tensors on sampled tokens
+    idx = _sample(T, seed)
+    sub = dict(inp)
+    for k in ("x", "f", "dout", "dy"):
+        sub[k] = inp[k][idx]
+    sf = orc.layer_fwd(sub, n, ITERS, EPS_SK, EPS_RMS)
+    sb = orc.layer_bwd(sub, sf, n, ITERS, EPS_SK, EPS_RMS)
+    ti = torch.from_numpy(idx).cuda()
+    err_bf16(o["y"][ti], sf["y"])
+    err_bf16(o["out"][ti], sf["out"])
+    err_bf16(o["dx"][ti], sb["dx"])
+    err_bf16(o["df"][ti], sb["df"])
+    err_grad(o["u"][ti], sf["u"], rel=1e-5)
+
+
+def test_layer_7b_T16384_n4_C4096(M, orc):
+    _full_layer_check(M, orc, 16384, 4, 4096, 0.02, 3)
+
+
+def test_layer_wide_T8192_n8_C7168(M, orc):
+    _full_layer_check(M, orc, 8192, 8, 7168, 0.01, 4)
+
+
+def test_rmsnorm_16384x4096(M, orc):
+    inp = mi.layer_inputs(16384, 4, 4096, 3, grads=False, rmsnorm=True)
+    x = torch.from_numpy(inp["x_norm"].view(np.int16)).view(torch.bfloat16).cuda()
+    dy = torch.from_numpy(inp["dy_norm"].view(np.int16)).view(torch.bfloat16).cuda()
+    y, dx = torch.empty_like(x), torch.empty_like(x)
+    rstd = torch.empty(16384, device="cuda")
+    M.rmsnorm_fwd(x, y, rstd, 1e-6)
+    M.rmsnorm_bwd(dy, x, rstd, dx, 1e-6)
+    torch.cuda.synchronize()
+    idx = _sample(16384, 33, k=256)
+    ry, rr = orc.rmsnorm_fwd(inp["x_norm"][idx], 1e-6)
+    ti = torch.from_numpy(idx).cuda()
+    err_bf16(y[ti], ry)
+    err_grad(rstd[ti], rr, rel=1e-6)
+    err_bf16(dx[ti], orc.rmsnorm_bwd(inp["dy_norm"][idx], inp["x_norm"][idx], 1e-6))

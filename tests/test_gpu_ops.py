@@ -1,0 +1,358 @@
+"""GPU parity: every libmhc op against the fp64 oracle on the same seeded
+inputs, element by element, at sizes that span several tiles and a ragged
+tail, plus the degenerate cases (one token, an all-zero token, T = 0,
+zero iterations) and out-of-bounds canaries around every output."""
+import numpy as np
+import pytest
+import torch
+
+import mhc_inputs as mi
+from tests._util import dev_bf16, dev_f32, err_bf16, err_grad, err_h, host
+
+pytestmark = pytest.mark.gpu
+
+ITERS, EPS_SK, EPS_RMS = 20, 1e-6, 1e-6
+SENTINEL = 7680.0  # exact in bf16 and fp32
+
+
+@pytest.fixture(scope="module")
+def M():
+    import layers_proj_rms_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return m
+
+
+def canary(shape, dtype, pad=64):
+    """A tensor view with `pad` sentinel elements on both sides."""
+    n = int(np.prod(shape))
+    buf = torch.full((n + 2 * pad,), SENTINEL, dtype=dtype, device="cuda")
+    return buf, buf[pad:pad + n].view(shape)
+
+
+def check_canary(buf, pad=64):
+    h = buf.float().cpu().numpy()
+    assert np.all(h[:pad] == SENTINEL) and np.all(h[-pad:] == SENTINEL), "write out of bounds"
+
+
+# ---------------------------------------------------------------------------
+# Sinkhorn
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [4, 8])
+@pytest.mark.parametrize("Mb,iters", [(1, 20), (7, 20), (129, 20), (33, 0), (40, 1), (64, 64)])
+def test_sinkhorn(M, orc, n, Mb, iters):
+    inp = mi.sinkhorn_inputs(Mb, n, seed=100 + Mb)
+    lg, dP = dev_f32(inp["logits"]), dev_f32(inp["dP"])
+    bufP, P = canary((Mb, n, n), torch.float32)
+    bufD, dl = canary((Mb, n, n), torch.float32)
+    M.mhc_sinkhorn_fwd(lg, P, iters, EPS_SK)
+    M.mhc_sinkhorn_bwd(dP, lg, dl, iters, EPS_SK)
+    torch.cuda.synchronize()
+    check_canary(bufP)
+    check_canary(bufD)
+    if iters == 0:
+        err_grad(P, orc.sinkhorn_fwd(inp["logits"], iters, EPS_SK), rel=1e-6)
+    else:
+        err_h(P, orc.sinkhorn_fwd(inp["logits"], iters, EPS_SK))
+    err_grad(dl, orc.sinkhorn_bwd(inp["dP"], inp["logits"], iters, EPS_SK))
+
+
+def test_sinkhorn_batched_8x4096(M, orc):
+    """Batched fwd+bwd on [8, 4096, 4, 4] N(0,1) logits, seed 1."""
+    inp = mi.sinkhorn_inputs(8 * 4096, 4, seed=1)
+    lg = dev_f32(inp["logits"]).view(8, 4096, 4, 4)
+    dP = dev_f32(inp["dP"]).view(8, 4096, 4, 4)
+    P = torch.empty_like(lg)
+    dl = torch.empty_like(lg)
+    M.mhc_sinkhorn_fwd(lg, P, ITERS, EPS_SK)
+    M.mhc_sinkhorn_bwd(dP, lg, dl, ITERS, EPS_SK)
+    torch.cuda.synchronize()
+    refP = orc.sinkhorn_fwd(inp["logits"], ITERS, EPS_SK)
+    err_h(P.view(-1, 4, 4), refP)
+    err_grad(dl.view(-1, 4, 4), orc.sinkhorn_bwd(inp["dP"], inp["logits"], ITERS, EPS_SK))
+
+
+# ---------------------------------------------------------------------------
+# proj_rms_compute_h
+# ---------------------------------------------------------------------------
+
+SHAPES = [(256, 4, 256, 0), (1, 4, 8, 1), (3, 8, 8, 2), (129, 4, 264, 3), (67, 8, 64, 4),
+          (200, 8, 136, 5)]
+
+
+def _proj_inputs(T, n, C, seed, stress):
+    if stress:  # gates and Sinkhorn far from the near-uniform regime
+        return mi.layer_inputs(T, n, C, seed, w_std=0.05, alpha=1.0, b_std=1.0)
+    return mi.layer_inputs(T, n, C, seed)
+
+
+@pytest.mark.parametrize("T,n,C,seed", SHAPES)
+@pytest.mark.parametrize("stress", [False, True])
+def test_proj_rms_compute_h(M, orc, T, n, C, seed, stress):
+    inp = _proj_inputs(T, n, C, seed, stress)
+    O = n * n + 2 * n
+    x, W = dev_bf16(inp["x"]), dev_f32(inp["W"])
+    a, b = dev_f32(inp["alpha"]), dev_f32(inp["b"])
+    Hp, Hq, Hr = (torch.empty(T, n, device="cuda"), torch.empty(T, n, device="cuda"),
+                  torch.empty(T, n, n, device="cuda"))
+    bu, u = canary((T, O), torch.float32)
+    r = torch.empty(T, device="cuda")
+    ws = M.workspace(M.OP_PROJ_RMS_COMPUTE_H_FWD, T, n, C)
+    M.mhc_proj_rms_compute_h_fwd(x, W, a, b, ITERS, EPS_SK, EPS_RMS, Hp, Hq, Hr, u, r, ws)
+    torch.cuda.synchronize()
+    check_canary(bu)
+    ref = orc.proj_rms_compute_h_fwd(inp["x"], inp["W"], inp["alpha"], inp["b"], n, ITERS,
+                                     EPS_SK, EPS_RMS)
+    err_h(Hp, ref["H_pre"])
+    err_h(Hq, ref["H_post"])
+    err_h(Hr, ref["H_res"])
+    err_grad(u, ref["u"], rel=1e-5)
+    err_grad(r, ref["r"], rel=1e-6)
+    # backward from seeded upstream grads
+    rng = np.random.Generator(np.random.PCG64(seed + 1000))
+    dHp = rng.standard_normal((T, n), dtype=np.float32)
+    dHq = rng.standard_normal((T, n), dtype=np.float32)
+    dHr = rng.standard_normal((T, n, n), dtype=np.float32)
+    bdx, dx = canary((T, n, C), torch.bfloat16)
+    dW = torch.empty(n * C, O, device="cuda")
+    da, db = torch.empty(3, device="cuda"), torch.empty(O, device="cuda")
+    wsb = M.workspace(M.OP_PROJ_RMS_COMPUTE_H_BWD, T, n, C)
+    M.mhc_proj_rms_compute_h_bwd(dev_f32(dHp), dev_f32(dHq), dev_f32(dHr), x, W, a, b, u, r,
+                                 ITERS, EPS_SK, EPS_RMS, dx, dW, da, db, wsb)
+    torch.cuda.synchronize()
+    check_canary(bdx)
+    g = orc.proj_rms_compute_h_bwd(dHp, dHq, dHr, inp["x"], inp["W"], inp["alpha"], inp["b"], n,
+                                   ITERS, EPS_SK, EPS_RMS)
+    err_bf16(dx, g["dx"])
+    err_grad(dW, g["dW"])
+    err_grad(da, g["dalpha"])
+    err_grad(db, g["db"])
+
+
+def test_proj_zero_token(M, orc):
+    """An all-zero token: r = 1/eps, z = b, finite gradients."""
+    T, n, C = 40, 4, 64
+    inp = mi.layer_inputs(T, n, C, 7, alpha=1.0, b_std=0.5)
+    inp["x"][5] = 0
+    O = n * n + 2 * n
+    x, W = dev_bf16(inp["x"]), dev_f32(inp["W"])
+    a, b = dev_f32(inp["alpha"]), dev_f32(inp["b"])
+    Hp, Hq, Hr = (torch.empty(T, n, device="cuda"), torch.empty(T, n, device="cuda"),
+                  torch.empty(T, n, n, device="cuda"))
+    u, r = torch.empty(T, O, device="cuda"), torch.empty(T, device="cuda")
+    M.mhc_proj_rms_compute_h_fwd(x, W, a, b, ITERS, EPS_SK, EPS_RMS, Hp, Hq, Hr, u, r,
+                                 M.workspace(M.OP_PROJ_RMS_COMPUTE_H_FWD, T, n, C))
+    ref = orc.proj_rms_compute_h_fwd(inp["x"], inp["W"], inp["alpha"], inp["b"], n, ITERS,
+                                     EPS_SK, EPS_RMS)
+    err_h(Hp, ref["H_pre"])
+    err_h(Hr, ref["H_res"])
+    dH = [np.ones((T, n), np.float32), np.ones((T, n), np.float32), np.ones((T, n, n), np.float32)]
+    dx = torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(n * C, O, device="cuda")
+    da, db = torch.empty(3, device="cuda"), torch.empty(O, device="cuda")
+    M.mhc_proj_rms_compute_h_bwd(*[dev_f32(d) for d in dH], x, W, a, b, u, r, ITERS, EPS_SK,
+                                 EPS_RMS, dx, dW, da, db,
+                                 M.workspace(M.OP_PROJ_RMS_COMPUTE_H_BWD, T, n, C))
+    torch.cuda.synchronize()
+    g = orc.proj_rms_compute_h_bwd(*dH, inp["x"], inp["W"], inp["alpha"], inp["b"], n, ITERS,
+                                   EPS_SK, EPS_RMS)
+    err_bf16(dx, g["dx"])
+    err_grad(dW, g["dW"])
+
+
+# ---------------------------------------------------------------------------
+# h_aggregate, h_post_bda
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,n,C,seed", SHAPES)
+def test_aggregate(M, orc, T, n, C, seed):
+    inp = mi.layer_inputs(T, n, C, seed)
+    rng = np.random.Generator(np.random.PCG64(seed + 2000))
+    Hpre = rng.uniform(0, 1, size=(T, n)).astype(np.float32)
+    x = dev_bf16(inp["x"])
+    by, y = canary((T, C), torch.bfloat16)
+    M.mhc_h_aggregate_fwd(x, dev_f32(Hpre), y)
+    bdx, dx = canary((T, n, C), torch.bfloat16)
+    dH = torch.empty(T, n, device="cuda")
+    M.mhc_h_aggregate_bwd(dev_bf16(inp["dy"]), x, dev_f32(Hpre), dx, dH)
+    torch.cuda.synchronize()
+    check_canary(by)
+    check_canary(bdx)
+    err_bf16(y, orc.h_aggregate_fwd(inp["x"], Hpre))
+    g = orc.h_aggregate_bwd(inp["dy"], inp["x"], Hpre)
+    err_bf16(dx, g["dx"])
+    err_grad(dH, g["dH_pre"])
+
+
+@pytest.mark.parametrize("T,n,C,seed", SHAPES)
+@pytest.mark.parametrize("with_bias", [True, False])
+def test_post_bda(M, orc, T, n, C, seed, with_bias):
+    inp = mi.layer_inputs(T, n, C, seed)
+    rng = np.random.Generator(np.random.PCG64(seed + 3000))
+    Hres = rng.uniform(0, 0.5, size=(T, n, n)).astype(np.float32)
+    Hpost = rng.uniform(0, 2, size=(T, n)).astype(np.float32)
+    bias_bits = inp["bias"] if with_bias else None
+    x, f = dev_bf16(inp["x"]), dev_bf16(inp["f"])
+    bias = dev_bf16(bias_bits) if with_bias else None
+    bo, out = canary((T, n, C), torch.bfloat16)
+    M.mhc_h_post_bda_fwd(x, f, bias, dev_f32(Hres), dev_f32(Hpost), out)
+    bdr, dres = canary((T, n, C), torch.bfloat16)
+    bdf, df = canary((T, C), torch.bfloat16)
+    dbias = torch.empty(C, device="cuda")
+    dHr, dHp = torch.empty(T, n, n, device="cuda"), torch.empty(T, n, device="cuda")
+    M.mhc_h_post_bda_bwd(dev_bf16(inp["dout"]), x, f, bias, dev_f32(Hres), dev_f32(Hpost), dres,
+                         df, dbias, dHr, dHp, M.workspace(M.OP_H_POST_BDA_BWD, T, n, C))
+    torch.cuda.synchronize()
+    for bfr in (bo, bdr, bdf):
+        check_canary(bfr)
+    err_bf16(out, orc.h_post_bda_fwd(inp["x"], inp["f"], bias_bits, Hres, Hpost))
+    g = orc.h_post_bda_bwd(inp["dout"], inp["x"], inp["f"], bias_bits, Hres, Hpost)
+    err_bf16(dres, g["dres"])
+    err_bf16(df, g["df"])
+    err_grad(dbias, g["dbias"])
+    err_grad(dHr, g["dH_res"])
+    err_grad(dHp, g["dH_post"])
+
+
+def test_post_bda_identity_is_exact_copy(M):
+    """H_res = I, H_post = 0: the output is the residual, bit for bit."""
+    T, n, C = 33, 4, 72
+    inp = mi.layer_inputs(T, n, C, 9)
+    x = dev_bf16(inp["x"])
+    out = torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda")
+    Hres = torch.eye(n, device="cuda").expand(T, n, n).contiguous()
+    M.mhc_h_post_bda_fwd(x, dev_bf16(inp["f"]), dev_bf16(inp["bias"]), Hres,
+                         torch.zeros(T, n, device="cuda"), out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), x.view(torch.int16))
+
+
+def test_aggregate_one_hot_is_exact_select(M):
+    T, n, C = 31, 8, 40
+    inp = mi.layer_inputs(T, n, C, 10)
+    sel = np.arange(T) % n
+    H = np.zeros((T, n), np.float32)
+    H[np.arange(T), sel] = 1.0
+    x = dev_bf16(inp["x"])
+    y = torch.empty(T, C, dtype=torch.bfloat16, device="cuda")
+    M.mhc_h_aggregate_fwd(x, dev_f32(H), y)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), x[torch.arange(T), torch.from_numpy(sel)].view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("rows,cols", [(1, 8), (37, 264), (256, 4096), (5, 8200), (3, 32768)])
+def test_rmsnorm(M, orc, rows, cols):
+    inp = mi.rmsnorm_inputs(rows, cols, seed=rows + cols)
+    x, dy = dev_bf16(inp["x"]), dev_bf16(inp["dy"])
+    by, y = canary((rows, cols), torch.bfloat16)
+    rstd = torch.empty(rows, device="cuda")
+    M.rmsnorm_fwd(x, y, rstd, 1e-6)
+    bdx, dx = canary((rows, cols), torch.bfloat16)
+    M.rmsnorm_bwd(dy, x, rstd, dx, 1e-6)
+    dx2 = torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")
+    M.rmsnorm_bwd(dy, x, None, dx2, 1e-6)
+    torch.cuda.synchronize()
+    check_canary(by)
+    check_canary(bdx)
+    ry, rr = orc.rmsnorm_fwd(inp["x"], 1e-6)
+    err_bf16(y, ry)
+    err_grad(rstd, rr, rel=1e-6)
+    rdx = orc.rmsnorm_bwd(inp["dy"], inp["x"], 1e-6)
+    err_bf16(dx, rdx)
+    err_bf16(dx2, rdx)
+
+
+# ---------------------------------------------------------------------------
+# The layer
+# ---------------------------------------------------------------------------
+
+def run_layer(M, inp, T, n, C):
+    O = n * n + 2 * n
+    t = {k: (dev_bf16(v) if v.dtype == np.uint16 else dev_f32(v)) for k, v in inp.items()}
+    o = {
+        "H_pre": torch.empty(T, n, device="cuda"), "H_post": torch.empty(T, n, device="cuda"),
+        "H_res": torch.empty(T, n, n, device="cuda"), "u": torch.empty(T, O, device="cuda"),
+        "r": torch.empty(T, device="cuda"),
+        "y": torch.empty(T, C, dtype=torch.bfloat16, device="cuda"),
+        "out": torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda"),
+        "dx": torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda"),
+        "df": torch.empty(T, C, dtype=torch.bfloat16, device="cuda"),
+        "dW": torch.empty(n * C, O, device="cuda"), "dalpha": torch.empty(3, device="cuda"),
+        "db": torch.empty(O, device="cuda"), "dbias": torch.empty(C, device="cuda"),
+    }
+    wsf = M.workspace(M.OP_LAYER_FWD, T, n, C)
+    wsb = M.workspace(M.OP_LAYER_BWD, T, n, C)
+    M.mhc_layer_fwd(t["x"], t["W"], t["alpha"], t["b"], t["f"], t["bias"], ITERS, EPS_SK, EPS_RMS,
+                    o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"], o["out"], wsf)
+    M.mhc_layer_bwd(t["dout"], t["dy"], t["x"], t["W"], t["alpha"], t["b"], t["f"], t["bias"],
+                    o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], ITERS, EPS_SK, EPS_RMS,
+                    o["dx"], o["df"], o["dW"], o["dalpha"], o["db"], o["dbias"], wsb)
+    torch.cuda.synchronize()
+    return o
+
+
+def check_layer(o, ref_f, ref_b):
+    err_h(o["H_pre"], ref_f["H_pre"])
+    err_h(o["H_post"], ref_f["H_post"])
+    err_h(o["H_res"], ref_f["H_res"])
+    err_bf16(o["y"], ref_f["y"])
+    err_bf16(o["out"], ref_f["out"])
+    err_bf16(o["dx"], ref_b["dx"])
+    err_bf16(o["df"], ref_b["df"])
+    err_grad(o["dW"], ref_b["dW"])
+    err_grad(o["dalpha"], ref_b["dalpha"])
+    err_grad(o["db"], ref_b["db"])
+    err_grad(o["dbias"], ref_b["dbias"])
+
+
+@pytest.mark.parametrize("T,n,C,seed", SHAPES)
+@pytest.mark.parametrize("stress", [False, True])
+def test_layer(M, orc, T, n, C, seed, stress):
+    inp = _proj_inputs(T, n, C, seed, stress)
+    o = run_layer(M, inp, T, n, C)
+    ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
+    check_layer(o, ref_f, ref_b)
+
+
+def test_layer_is_deterministic(M):
+    T, n, C = 300, 4, 512
+    inp = mi.layer_inputs(T, n, C, 11)
+    a = run_layer(M, inp, T, n, C)
+    b = run_layer(M, inp, T, n, C)
+    for k in a:
+        assert torch.equal(a[k].view(torch.uint8) if a[k].dtype != torch.bfloat16 else
+                           a[k].view(torch.int16),
+                           b[k].view(torch.uint8) if b[k].dtype != torch.bfloat16 else
+                           b[k].view(torch.int16)), k
+
+
+def test_empty_token_count(M):
+    """T = 0: forward calls do nothing, parameter grads come back zero."""
+    n, C = 4, 64
+    O = n * n + 2 * n
+    e = lambda *s: torch.empty(*s, device="cuda")  # noqa: E731
+    dW = torch.full((n * C, O), 5.0, device="cuda")
+    da, db, dbias = torch.full((3,), 5.0, device="cuda"), e(O).fill_(5), e(C).fill_(5)
+    x = torch.empty(0, n, C, dtype=torch.bfloat16, device="cuda")
+    z = lambda *s: torch.empty(*s, device="cuda")  # noqa: E731
+    M.mhc_layer_bwd(torch.empty(0, n, C, dtype=torch.bfloat16, device="cuda"),
+                    torch.empty(0, C, dtype=torch.bfloat16, device="cuda"), x,
+                    z(n * C, O), z(3), z(O), torch.empty(0, C, dtype=torch.bfloat16, device="cuda"),
+                    torch.zeros(C, dtype=torch.bfloat16, device="cuda"), z(0, n), z(0, n),
+                    z(0, n, n), z(0, O), z(0), ITERS, EPS_SK, EPS_RMS,
+                    torch.empty(0, n, C, dtype=torch.bfloat16, device="cuda"),
+                    torch.empty(0, C, dtype=torch.bfloat16, device="cuda"), dW, da, db, dbias,
+                    None)
+    torch.cuda.synchronize()
+    assert float(dW.abs().sum()) == 0 and float(da.abs().sum()) == 0
+    assert float(db.abs().sum()) == 0 and float(dbias.abs().sum()) == 0
+
+
+def test_no_device_fault_reported(M):
+    assert M.mhc_device_error() == 0
