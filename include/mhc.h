@@ -258,6 +258,36 @@ MHC_API mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const
                          mhc_bf16 *dx, mhc_bf16 *df, float *dW, float *dalpha3, float *db,
                          float *dbias, void *ws, size_t ws_bytes, mhc_stream_t stream);
 
+/* ------------------------------------------------------------------ */
+/* Allocation-free variant.  The web pages have no counterpart of this  */
+/* entry point; it exists for callers that cannot allocate device       */
+/* memory for a workspace: allocator-free runtimes, plugins that may    */
+/* not own device memory, paths that must not call cudaMalloc/cudaFree  */
+/* (they can synchronise the device).                                   */
+/* ------------------------------------------------------------------ */
+
+/* Size of the fixed scratch array the variant below uses (8 MiB).  It is
+ * device global memory inside the library image, held on every GPU that
+ * loads the library until the process exits. */
+#define MHC_NOALLOC_SCRATCH_BYTES (((size_t)8) << 20)
+
+/* mhc_proj_rms_compute_h_fwd without a workspace argument: the same
+ * computation and outputs, with the scratch taken from the library's fixed
+ * array.  Calls that would need more scratch than MHC_NOALLOC_SCRATCH_BYTES
+ * (mhc_workspace_bytes(MHC_OP_PROJ_RMS_COMPUTE_H_FWD, T, n, C)) return
+ * MHC_ERR_WORKSPACE_TOO_SMALL without launching anything.  Allocates no
+ * memory.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device; make it before any stream
+ * capture.  All calls share the one array: calls that overlap on the GPU
+ * race on it and must be ordered by the caller (same stream, or events). */
+MHC_API mhc_status mhc_proj_rms_compute_h_fwd_noalloc(const mhc_bf16 *x, const float *W,
+                                                      const float *alpha3, const float *b,
+                                                      int64_t T, int n, int64_t C, int iters,
+                                                      float eps_sk, float eps_rms,
+                                                      float *H_pre, float *H_post,
+                                                      float *H_res, float *u_save,
+                                                      float *r_save, mhc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,7 @@ __all__ = [
     "mhc_proj_rms_compute_h_bwd", "mhc_h_aggregate_fwd", "mhc_h_aggregate_bwd",
     "mhc_h_post_bda_fwd", "mhc_h_post_bda_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "mhc_layer_fwd",
     "mhc_layer_bwd", "OP_PROJ_RMS_COMPUTE_H_FWD", "OP_PROJ_RMS_COMPUTE_H_BWD",
-    "OP_H_POST_BDA_BWD", "OP_LAYER_FWD", "OP_LAYER_BWD",
+    "OP_H_POST_BDA_BWD", "OP_LAYER_FWD", "OP_LAYER_BWD", "mhc_proj_rms_compute_h_fwd_noalloc",
 ]
 
 

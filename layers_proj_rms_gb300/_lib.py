@@ -48,6 +48,8 @@ _SIGS = {
     "mhc_layer_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                       _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "mhc_device_error": [ctypes.POINTER(ctypes.c_int), _P],
+    "mhc_proj_rms_compute_h_fwd_noalloc": [_P, _P, _P, _P, _I64, _I, _I64, _I, _F, _F, _P, _P,
+                                           _P, _P, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -256,3 +258,17 @@ def mhc_layer_bwd(dout, dy, x, W, alpha3, b, f, bias, H_pre, H_post, H_res, u_sa
         _ptr(dx, _BF, (T, n, C), "dx"), _ptr(df, _BF, (T, C), "df"),
         _ptr(dW, _F32, (n * C, O), "dW"), _ptr(dalpha3, _F32, (3,), "dalpha3"),
         _ptr(db, _F32, (O,), "db"), _ptr(dbias, _F32, (C,), "dbias"), wp, wb, _stream(stream)))
+
+
+def mhc_proj_rms_compute_h_fwd_noalloc(x, W, alpha3, b, iters, eps_sk, eps_rms, H_pre, H_post,
+                                       H_res, u_save=None, r_save=None, stream=None):
+    """mhc_proj_rms_compute_h_fwd with the library's fixed scratch array
+    instead of a caller workspace (for callers that cannot allocate)."""
+    T, n, C = x.shape
+    O = _O(n)
+    _ok(lib.mhc_proj_rms_compute_h_fwd_noalloc(
+        _ptr(x, _BF, name="x"), _ptr(W, _F32, (n * C, O), "W"), _ptr(alpha3, _F32, (3,), "alpha3"),
+        _ptr(b, _F32, (O,), "b"), T, n, C, iters, eps_sk, eps_rms,
+        _ptr(H_pre, _F32, (T, n), "H_pre"), _ptr(H_post, _F32, (T, n), "H_post"),
+        _ptr(H_res, _F32, (T, n, n), "H_res"), _ptr(u_save, _F32, (T, O), "u_save"),
+        _ptr(r_save, _F32, (T,), "r_save"), _stream(stream)))

@@ -145,6 +145,8 @@ mhc_status zero_param_grads(Check &ck, float *dW, int64_t nW, float *dalpha, flo
 
 }  // namespace
 
+void mhc::set_error_message(const char *msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 extern "C" {
 
 const char *mhc_status_string(mhc_status s)

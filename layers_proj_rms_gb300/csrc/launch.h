@@ -21,6 +21,9 @@ constexpr int kSplitSms = 152;
 
 int num_sms();
 
+// Sets the thread-local text that mhc_last_error() returns (abi.cu).
+void set_error_message(const char *msg);
+
 // Per-kernel event timing (prof.cu); a no-op unless mhc_profiler_enable(1).
 void prof_begin(const char *name, cudaStream_t s);
 void prof_end(cudaStream_t s);
