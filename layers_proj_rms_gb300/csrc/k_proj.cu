@@ -9,8 +9,9 @@
 // (MhcPreOpFwdHost: H_pre after sigmoid, H_post after 2*sigmoid, H_res after
 // Sinkhorn; MhcPreOpBwdHost: gradient back to the raw logits).
 //
-// Forward:  k_proj_gemm (split-K partial u = x W and s = sum x^2, fp32)
-//           k_compute_h_fwd (sum of partials, r, z, gates, Sinkhorn)
+// Forward:  k_proj_tc (k_proj_tc.cu: split-K partial u = x W and s = sum x^2
+//           on the tensor cores), k_compute_h_fwd (sum of partials, r, z,
+//           gates, Sinkhorn)
 // Backward: k_compute_h_bwd (per-token du, dz, dalpha terms, RMS coefficient)
 //           k_dx (du W^T + coef x [+ H_res dout + H_pre dy]), k_dW_partial,
 //           fixed-order reductions for dW, dalpha, db.
@@ -24,86 +25,6 @@ struct Dims {
     static constexpr int O = N * N + 2 * N;
     static constexpr int OP = (O + 7) / 8;  // logits per thread in the GEMM (o = og + 8p)
 };
-
-// ---------------------------------------------------------------------------
-// Forward GEMM: partial u[s][t][o] = sum_{k in split s} x[t][k] W[k][o],
-// partial ss[s][t] = sum_{k in split s} x[t][k]^2.
-// CTA: 64 tokens x one K split, 128 threads; thread (mg, og) owns tokens
-// 4*mg..4*mg+3 and logits og, og+8, ...
-// ---------------------------------------------------------------------------
-constexpr int kGM = 64, kGK = 64, kGThreads = 128, kXPad = 2;
-
-template <int N>
-__global__ void __launch_bounds__(kGThreads)
-    k_proj_gemm(const bf16 *__restrict__ x, const float *__restrict__ W, float *__restrict__ upart,
-                float *__restrict__ spart, int64_t T, int64_t K, int64_t kchunk)
-{
-    constexpr int O = Dims<N>::O, OP = Dims<N>::OP;
-    __shared__ __align__(16) uint16_t xs[kGM][kGK + kXPad];
-    __shared__ __align__(16) float wsm[kGK * O];
-    const int tid = threadIdx.x, mg = tid >> 3, og = tid & 7;
-    const int64_t t0 = int64_t(blockIdx.x) * kGM;
-    const int64_t split = blockIdx.y;
-    const int64_t kb = split * kchunk, ke = min(K, kb + kchunk);
-    float acc[4][OP];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int p = 0; p < OP; ++p) acc[q][p] = 0.f;
-    float ssq = 0.f;  // threads < 64: sum of squares of row tid
-    for (int64_t k0 = kb; k0 < ke; k0 += kGK) {
-        __syncthreads();
-        // x tile: 64 rows x 64 k = 512 chunks of 8
-        for (int ch = tid; ch < kGM * (kGK / 8); ch += kGThreads) {
-            const int row = ch >> 3, cc = ch & 7;
-            const int64_t t = t0 + row, k = k0 + cc * 8;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (t < T && k < ke) v = __ldg(reinterpret_cast<const uint4 *>(x + t * K + k));
-            uint32_t *d = reinterpret_cast<uint32_t *>(&xs[row][cc * 8]);
-            d[0] = v.x;
-            d[1] = v.y;
-            d[2] = v.z;
-            d[3] = v.w;
-        }
-        // W tile: rows k0..k0+63, O floats each
-        for (int e = tid; e < kGK * O; e += kGThreads) {
-            const int64_t k = k0 + e / O;
-            wsm[e] = (k < ke) ? __ldg(W + k0 * O + e) : 0.f;
-        }
-        __syncthreads();
-        if (tid < kGM) {
-#pragma unroll 8
-            for (int kk = 0; kk < kGK; ++kk) {
-                const float v = __uint_as_float(uint32_t(xs[tid][kk]) << 16);
-                ssq = fmaf(v, v, ssq);
-            }
-        }
-#pragma unroll 4
-        for (int kk = 0; kk < kGK; ++kk) {
-            float xv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) xv[q] = __uint_as_float(uint32_t(xs[mg * 4 + q][kk]) << 16);
-#pragma unroll
-            for (int p = 0; p < OP; ++p) {
-                const int o = og + 8 * p;
-                const float w = (o < O) ? wsm[kk * O + o] : 0.f;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) acc[q][p] = fmaf(xv[q], w, acc[q][p]);
-            }
-        }
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int64_t t = t0 + mg * 4 + q;
-        if (t < T)
-#pragma unroll
-            for (int p = 0; p < OP; ++p) {
-                const int o = og + 8 * p;
-                if (o < O) upart[(split * T + t) * O + o] = acc[q][p];
-            }
-    }
-    if (tid < kGM && t0 + tid < T) spart[split * T + t0 + tid] = ssq;
-}
 
 // ---------------------------------------------------------------------------
 // compute_h forward.  A group of N lanes per token, lane i owns row i of the
@@ -363,48 +284,39 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static int64_t gemm_splits(int64_t T, int64_t K)
-{
-    const int64_t mt = (T + kGM - 1) / kGM;
-    const int64_t kblocks = (K + kGK - 1) / kGK;
-    int64_t s = (int64_t(kSplitSms) * 6 + mt - 1) / mt;
-    if (s > kblocks) s = kblocks;
-    if (s > 16) s = 16;
-    return s < 1 ? 1 : s;
-}
-
+// forward workspace: W_hl [2O][K] bf16, partials upart [S][T][O], spart [S][T]
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C)
 {
-    const int64_t O = int64_t(n) * n + 2 * n;
-    const int64_t S = gemm_splits(T, int64_t(n) * C);
-    return ws_align(size_t(S * T * O) * 4) + ws_align(size_t(S * T) * 4);
+    const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * C;
+    const int64_t S = proj_tc_splits(T, K);
+    return ws_align(size_t(2 * O * K) * 2) + ws_align(size_t(S * T * O) * 4) +
+           ws_align(size_t(S * T) * 4);
 }
 
 template <int N>
 static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alpha,
                                  const float *b, int64_t T, int64_t C, int iters, float eps_sk,
                                  float eps_rms, float *Hpre, float *Hpost, float *Hres,
-                                 float *u_save, float *r_save, void *ws, cudaStream_t s)
+                                 float *u_save, float *r_save, void *ws, int *fault,
+                                 cudaStream_t s)
 {
     constexpr int O = Dims<N>::O;
     const int64_t K = int64_t(N) * C;
-    const int64_t S = gemm_splits(T, K);
-    int64_t kchunk = (K + S - 1) / S;
-    kchunk = (kchunk + kGK - 1) / kGK * kGK;
-    const int64_t S_used = (K + kchunk - 1) / kchunk;
+    const int64_t S = proj_tc_splits(T, K);
     char *p = static_cast<char *>(ws);
+    bf16 *Whl = reinterpret_cast<bf16 *>(p);
+    p += ws_align(size_t(2 * O * K) * 2);
     float *upart = reinterpret_cast<float *>(p);
-    float *spart = reinterpret_cast<float *>(p + ws_align(size_t(S * T * O) * 4));
-    dim3 g(unsigned((T + kGM - 1) / kGM), unsigned(S_used));
-    {
-        MHC_PROF("k_proj_gemm", s);
-        k_proj_gemm<N><<<g, kGThreads, 0, s>>>(x, W, upart, spart, T, K, kchunk);
-    }
+    p += ws_align(size_t(S * T * O) * 4);
+    float *spart = reinterpret_cast<float *>(p);
+    int S_used = 1;
+    cudaError_t e = launch_proj_partials(x, W, T, N, C, Whl, upart, spart, &S_used, fault, s);
+    if (e != cudaSuccess) return e;
     const int64_t threads = T * N;
     {
         MHC_PROF("k_compute_h_fwd", s);
         k_compute_h_fwd<N><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
-            upart, spart, int(S_used), alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+            upart, spart, S_used, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
             u_save, r_save);
     }
     return cudaGetLastError();
@@ -415,12 +327,11 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
                             float *Hpre, float *Hpost, float *Hres, float *u_save, float *r_save,
                             void *ws, int *fault, cudaStream_t s)
 {
-    (void)fault;
     if (n == 4)
         return proj_fwd_impl<4>(x, W, alpha, b, T, C, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
-                                u_save, r_save, ws, s);
+                                u_save, r_save, ws, fault, s);
     return proj_fwd_impl<8>(x, W, alpha, b, T, C, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
-                            u_save, r_save, ws, s);
+                            u_save, r_save, ws, fault, s);
 }
 
 static int64_t dW_splits(int64_t T, int64_t K)

@@ -1,0 +1,304 @@
+// Forward projection of proj_rms_compute_h on the 5th-generation tensor
+// cores (tcgen05): per token t and K split s,
+//   upart[s][t][o] = sum_{k in s} x[t][k] W[k][o],   spart[s][t] = sum_{k in s} x[t][k]^2.
+//
+// Megatron's fused projection runs this on TF32 MMA with split-K (RL-Kernel
+// PR #383, follow-up commit on the Megatron mHC source).  Here the operands
+// are bf16: x is already bf16, and W (fp32) is split into W_hi = bf16(W) and
+// W_lo = bf16(W - W_hi), stacked as 2*O rows of one B operand, so one MMA of
+// N = 2*O gives x.W_hi and x.W_lo and their fp32 sum carries W to ~2^-17
+// relative error (x.W in fp32 semantics, well inside the 1e-5 bound on H).
+//
+// CTA: 128 tokens x one K split; 6 warps:
+//   warp 0      TMA producer: x tile [128 x 64] and W_hl tile [2O x 64] per
+//               stage, both in the 128-byte swizzle layout
+//   warp 1      TMEM allocation, MMA issue (one thread), commits
+//   warps 2..5  sum of squares of their token rows from the same smem tiles
+//               while the MMAs run; then the epilogue (TMEM -> partials)
+// Every wait is bounded; a timeout reports a fault code and the CTA unwinds.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace mhc {
+
+template <int N>
+struct ProjTc {
+    static constexpr int O = N * N + 2 * N;
+    static constexpr int NB = 2 * O;  // MMA N: hi rows then lo rows (48 or 160)
+    static constexpr int BM = 128, BK = 64;
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = NB * BK * 2;
+    static constexpr int STAGE = A_BYTES + B_BYTES;  // multiple of 1024
+    static constexpr int STAGES = (N == 4) ? 6 : 5;
+    static constexpr int TMEM_COLS = NB <= 64 ? 64 : 256;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+};
+
+// W [K][O] fp32 -> W_hl [2O][K] bf16 (rows o: bf16(W[:,o]); rows O+o: the remainder)
+template <int N>
+__global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, int64_t K)
+{
+    constexpr int O = N * N + 2 * N;
+    const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+#pragma unroll 4
+    for (int o = 0; o < O; ++o) {
+        const float w = __ldg(W + k * O + o);
+        const bf16 hi = __float2bfloat16_rn(w);
+        const bf16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
+        Whl[int64_t(o) * K + k] = hi;
+        Whl[int64_t(O + o) * K + k] = lo;
+    }
+}
+
+template <int N>
+__global__ void __launch_bounds__(192, 1)
+    k_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
+              float *__restrict__ upart, float *__restrict__ spart, int64_t T, int kb_per_split,
+              int kb_total, int *fault)
+{
+    using P = ProjTc<N>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P::STAGES * P::STAGE);
+    uint64_t *empty = full + P::STAGES;
+    uint64_t *acc_bar = empty + P::STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t m0 = int64_t(blockIdx.x) * P::BM;
+    const int split = blockIdx.y;
+    const int kb0 = split * kb_per_split;
+    const int kb1 = min(kb_total, kb0 + kb_per_split);
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1 + 4);
+        }
+        tc::mbar_init(acc_bar, 1);
+        *abort_flag = 0;
+        tc::fence_barrier_init();
+        tc::tma_prefetch_desc(&tmx);
+        tc::tma_prefetch_desc(&tmw);
+    }
+    if (warp == 1) tc::tmem_alloc(tmem_slot, P::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nkb && !*abort_flag; ++i) {
+                const int s = i % P::STAGES;
+                if (i >= P::STAGES &&
+                    !tc::mbar_wait(&empty[s], ((i / P::STAGES) & 1) ^ 1, fault,
+                                   tc::kFaultTimeoutEmpty)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                uint8_t *st = smem + s * P::STAGE;
+                tc::mbar_arrive_expect_tx(&full[s], P::STAGE);
+                tc::tma_load_2d(st, &tmx, (kb0 + i) * P::BK, int(m0), &full[s]);
+                tc::tma_load_2d(st + P::A_BYTES, &tmw, (kb0 + i) * P::BK, 0, &full[s]);
+                issued = i + 1;
+            }
+            // do not leave while copies into this CTA's shared memory are in flight
+            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
+                tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, fault,
+                              tc::kFaultTimeoutMisc);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(P::BM, P::NB);
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % P::STAGES;
+                if (*abort_flag ||
+                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t a = tc::smem_u32(smem + s * P::STAGE);
+                const uint32_t b = a + P::A_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < P::BK / 16; ++kk)
+                    tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
+                                 tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                                 (i > 0 || kk > 0) ? 1u : 0u);
+                tc::mma_commit(&empty[s]);
+            }
+            tc::mma_commit(acc_bar);
+            tc::mbar_wait(acc_bar, 0, fault, tc::kFaultTimeoutAcc);
+        }
+        __syncwarp();
+    } else {
+        // warps 2..5: token row r of the tile = TMEM lane r
+        const int q = warp & 3;
+        const int r = q * 32 + lane;
+        float ssq = 0.f;
+        bool ok = true;
+        for (int i = 0; i < nkb; ++i) {
+            const int s = i % P::STAGES;
+            if (*abort_flag ||
+                !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            const uint4 *row = reinterpret_cast<const uint4 *>(smem + s * P::STAGE + r * 128);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float f[8];
+                unpack8(row[c], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);
+        }
+        if (ok && !tc::mbar_wait(acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
+        tc::tc_fence_after();
+        const int64_t t = m0 + r;
+        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+        constexpr int O = P::O;
+        if (N == 4) {
+            float v[48];
+#pragma unroll
+            for (int c = 0; c < 3; ++c) {
+                float w[16];
+                tc::tmem_ld16(trow + c * 16, w);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
+            }
+            if (ok && t < T) {
+                float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
+#pragma unroll
+                for (int o4 = 0; o4 < O / 4; ++o4)
+                    dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
+                                          v[4 * o4 + 2] + v[O + 4 * o4 + 2],
+                                          v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
+                spart[int64_t(split) * T + t] = ssq;
+            }
+        } else {
+#pragma unroll 1
+            for (int c = 0; c < O / 16; ++c) {
+                float hi[16], lo[16];
+                tc::tmem_ld16(trow + c * 16, hi);
+                tc::tmem_ld16(trow + O + c * 16, lo);
+                tc::tmem_ld_wait();
+                if (ok && t < T) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        upart + (int64_t(split) * T + t) * O + c * 16);
+#pragma unroll
+                    for (int o4 = 0; o4 < 4; ++o4)
+                        dst[o4] = make_float4(hi[4 * o4] + lo[4 * o4], hi[4 * o4 + 1] + lo[4 * o4 + 1],
+                                              hi[4 * o4 + 2] + lo[4 * o4 + 2],
+                                              hi[4 * o4 + 3] + lo[4 * o4 + 3]);
+                }
+            }
+            if (ok && t < T) spart[int64_t(split) * T + t] = ssq;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tmem, P::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box [box_rows][box_cols].
+static bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                          uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int proj_tc_splits(int64_t T, int64_t K)
+{
+    const int64_t mt = (T + 127) / 128;
+    const int64_t kb = (K + 63) / 64;
+    int64_t s = kSplitSms / mt;
+    if (s < 1) s = 1;
+    if (s > kb) s = kb;
+    if (s > 32) s = 32;
+    return int(s);
+}
+
+template <int N>
+static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_t C, bf16 *Whl,
+                                float *upart, float *spart, int S, int *fault, cudaStream_t s)
+{
+    using P = ProjTc<N>;
+    const int64_t K = int64_t(N) * C;
+    {
+        MHC_PROF("k_w_split", s);
+        k_w_split<N><<<unsigned((K + 255) / 256), 256, 0, s>>>(W, Whl, K);
+    }
+    CUtensorMap tmx, tmw;
+    if (!make_map_bf16(&tmx, x, uint64_t(T), uint64_t(K), P::BM, P::BK,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bf16(&tmw, Whl, uint64_t(P::NB), uint64_t(K), P::NB, P::BK,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_proj_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         P::SMEM);
+    if (e != cudaSuccess) return e;
+    const int kb_total = int((K + P::BK - 1) / P::BK);
+    const int kps = (kb_total + S - 1) / S;
+    const int S_used = (kb_total + kps - 1) / kps;
+    dim3 grid(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used));
+    {
+        MHC_PROF("k_proj_tc", s);
+        k_proj_tc<N><<<grid, 192, P::SMEM, s>>>(tmx, tmw, upart, spart, T, kps, kb_total, fault);
+    }
+    return cudaGetLastError();
+}
+
+// Returns the number of K splits actually used (partials upart[0..S_used)).
+cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n, int64_t C,
+                                 bf16 *Whl, float *upart, float *spart, int *splits_used,
+                                 int *fault, cudaStream_t s)
+{
+    const int64_t K = int64_t(n) * C;
+    const int S = proj_tc_splits(T, K);
+    const int kb_total = int((K + 63) / 64);
+    const int kps = (kb_total + S - 1) / S;
+    *splits_used = (kb_total + kps - 1) / kps;
+    if (n == 4) return proj_tc_impl<4>(x, W, T, C, Whl, upart, spart, S, fault, s);
+    return proj_tc_impl<8>(x, W, T, C, Whl, upart, spart, S, fault, s);
+}
+
+}  // namespace mhc

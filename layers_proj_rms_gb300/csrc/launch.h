@@ -66,6 +66,12 @@ cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, in
 cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf16 *dx,
                            int64_t rows, int64_t cols, float eps, cudaStream_t s);
 
+// k_proj_tc.cu: tensor-core projection partials of the forward
+int proj_tc_splits(int64_t T, int64_t K);
+cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n, int64_t C,
+                                 bf16 *Whl, float *upart, float *spart, int *splits_used,
+                                 int *fault, cudaStream_t s);
+
 // k_proj.cu
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C);
 cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,

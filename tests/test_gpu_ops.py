@@ -107,7 +107,7 @@ def test_proj_rms_compute_h(M, orc, T, n, C, seed, stress):
     err_h(Hp, ref["H_pre"])
     err_h(Hq, ref["H_post"])
     err_h(Hr, ref["H_res"])
-    err_grad(u, ref["u"], rel=1e-5)
+    err_grad(u, ref["u"])
     err_grad(r, ref["r"], rel=1e-6)
     # backward from seeded upstream grads
     rng = np.random.Generator(np.random.PCG64(seed + 1000))
