@@ -1,0 +1,579 @@
+// Residual-gradient pass of the mHC layer backward on tcgen05 tensor cores.
+//
+// For a slice of CW channels across all n streams (a set of 128 flattened
+// residual indices k = j*C + c) and a contiguous range of tokens, one CTA
+// computes
+//   dx[t][j][c] = sum_o du[t][o] W[k][o] + coef[t] x[t][j][c]
+//               [+ H_pre[t][j] dy[t][c] + sum_i H_res[t][j][i] dout[t][i][c]]   (layer)
+//   dW[k][o]   += sum_t x[t][k] du[t][o]
+//   dbias[c]   += sum_t sum_i H_post[t][i] dout[t][i][c]                        (layer)
+// i.e. the projection backward of RL-Kernel PR #383 (fp32_gemm_rms: dx_gemm
+// + dx_rms, dW) fused with the aggregate and post-mix residual gradients and
+// the three-way sum (Megatron-Core fused_mhc_kernels fused_add_3).
+//
+// du (fp32) arrives as bf16 hi | lo halves (du_hl[t][0..O) = bf16(du),
+// du_hl[t][O..2O) = bf16(du - hi)), which together carry du to ~2^-17; W is
+// split the same way into W_hi and W_lo.
+// Per tile of 128 tokens:
+//   MMA 1 (dx_gemm): D2[t][k] = du_hi.W_hi + du_lo.W_hi + du_hi.W_lo (the
+//          dropped du_lo.W_lo is ~2^-18 relative): M = 128 tokens, N = 128 k,
+//          K = 2*O against Wd = [W_hi | W_hi], then K = O against W_lo
+//   MMA 2 (dW):      D1[k][o'] += sum_t x[t][k] du_hl[t][o'], M = 128 k,
+//          N = 2*O, K = tokens; hi and lo columns of D1 are summed at the end.
+//          Both operands are read MN-major straight from the TMA tiles.
+//   epilogue: D2 + the elementwise terms -> dx (bf16); dbias column sums.
+// D2 is double-buffered in TMEM so the next tile's MMAs overlap the
+// epilogue; D1 accumulates over the whole token range and is written as this
+// split's dW partial.  For n = 4 the producer also stages dout and dy through
+// shared memory (every DRAM access a whole 64-byte row); for n = 8 (16-channel
+// slices) the epilogue reads them from global memory.
+// Warps: 0 TMA producer, 1 TMEM + MMA issue, 2..9 epilogue (two warps per
+// TMEM lane quadrant, each half of the slice's channels).
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace mhc {
+
+template <int N>
+struct BwdTc {
+    static constexpr int O = N * N + 2 * N;     // 24 / 80
+    static constexpr int CW = 128 / N;          // channels per stream: 32 / 16
+    static constexpr int HC = CW / 2;           // channels per epilogue thread: 16 / 8
+    static constexpr int TT = 128;              // tokens per tile
+    static constexpr int XROW = CW * 2;         // bytes of one token row of a stream box
+    static constexpr uint32_t XSWZ = N == 4 ? tc::kSwz64 : tc::kSwz32;
+    static constexpr int XBOX = TT * XROW;      // bytes of one stream box
+    static constexpr int X_BYTES = N * XBOX;    // 32 KB
+    static constexpr bool STAGE_G = N == 4;     // dout and dy through shared memory
+    static constexpr int G_BYTES = STAGE_G ? N * XBOX : 0;
+    static constexpr int Y_BYTES = STAGE_G ? XBOX : 0;
+    static constexpr int DU_ATOMS = N == 4 ? 1 : 3;
+    static constexpr int DU_COLS = 64 * DU_ATOMS;       // hi [0,O) | lo [O,2O) | zeros
+    static constexpr int DU_ATOM_BYTES = TT * 128;
+    static constexpr int DU_BYTES = DU_ATOMS * DU_ATOM_BYTES;
+    static constexpr int G_OFF = X_BYTES, Y_OFF = G_OFF + G_BYTES, DU_OFF = Y_OFF + Y_BYTES;
+    static constexpr int STAGE = DU_OFF + DU_BYTES;     // 88 KB / 80 KB
+    static constexpr int STAGES = 2;
+    // Wd = [W_hi | W_hi | W_lo | 0] in bf16, planes of 64 columns (128-byte
+    // rows, 128-byte swizzle); the W_lo block is padded to whole K steps.
+    static constexpr int NW = 2 * O;                    // 48 / 160
+    static constexpr int KSTEP_A = NW / 16;             // du_hl . [W_hi | W_hi]: 3 / 10
+    static constexpr int KSTEP_B = (O + 15) / 16;       // du_hi . W_lo: 2 / 5
+    static constexpr int W_COLS = NW + 16 * KSTEP_B;    // 80 / 240
+    static constexpr int W_PLANES = (W_COLS + 63) / 64; // 2 / 4
+    static constexpr int W_PLANE_BYTES = 128 * 128;
+    static constexpr int W_BYTES = W_PLANES * W_PLANE_BYTES;
+    static constexpr int D2_COL = 0, D1_COL = 256;      // D2 buffers at 0 and 128
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int SMEM = STAGES * STAGE + W_BYTES + 1024;
+    static constexpr int THREADS = 320;
+    static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0, "alignment");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+// W [K][O] fp32 -> Wd [planes][K][64] bf16 with row k = [W_hi | W_hi | W_lo | 0],
+// W_hi = bf16(W), W_lo = bf16(W - W_hi).
+template <int N>
+__global__ void k_w_planes(const float *__restrict__ W, bf16 *__restrict__ Wd, int64_t K)
+{
+    using P = BwdTc<N>;
+    constexpr int O = P::O;
+    const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (k >= K) return;
+    for (int p = 0; p < P::W_PLANES; ++p)
+        for (int pc = 0; pc < 64; pc += 8) {
+            uint16_t hbits[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int c = p * 64 + pc + e;
+                bf16 v = __float2bfloat16_rn(0.f);
+                if (c < 3 * O) {
+                    const float w = __ldg(W + k * O + (c % O));
+                    const bf16 hi = __float2bfloat16_rn(w);
+                    v = c < 2 * O ? hi : __float2bfloat16_rn(w - __bfloat162float(hi));
+                }
+                hbits[e] = *reinterpret_cast<uint16_t *>(&v);
+            }
+            uint4 q;
+            q.x = hbits[0] | (uint32_t(hbits[1]) << 16);
+            q.y = hbits[2] | (uint32_t(hbits[3]) << 16);
+            q.z = hbits[4] | (uint32_t(hbits[5]) << 16);
+            q.w = hbits[6] | (uint32_t(hbits[7]) << 16);
+            *reinterpret_cast<uint4 *>(Wd + (int64_t(p) * K + k) * 64 + pc) = q;
+        }
+}
+
+// Column sums over the 32 lanes of a warp: on entry every lane holds COLS
+// values, on exit lane l holds the warp total of column (l % COLS).
+template <int COLS>
+__device__ __forceinline__ float warp_column_sum(float (&v)[COLS])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = COLS / 2; w >= 1; w >>= 1) {
+        const bool upper = (lane & w) != 0;
+#pragma unroll
+        for (int k = 0; k < w; ++k) {
+            const float send = upper ? v[k] : v[k + w];
+            const float keep = upper ? v[k + w] : v[k];
+            v[k] = keep + __shfl_xor_sync(kFull, send, w);
+        }
+    }
+    float r = v[0];
+#pragma unroll
+    for (int m = COLS; m < 32; m <<= 1) r += __shfl_xor_sync(kFull, r, m);
+    return r;
+}
+
+struct BwdTcArgs {
+    const bf16 *dout, *dy;
+    const float *coef, *Hpre, *Hres, *Hpost;
+    bf16 *dx;
+    float *dWpart;     // [splits][K][O]
+    float *dbiaspart;  // [splits][C] (layer only)
+    int64_t T, C;
+    int tiles_per_split, tiles_total;
+    int *fault;
+};
+
+// 16-byte chunk `chunk` of token row r of a stream box in the 64-byte (n=4)
+// or 32-byte (n=8) swizzle layout that TMA writes.
+template <int N>
+__device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
+{
+    constexpr int XROW = BwdTc<N>::XROW;
+    const int phys = N == 4 ? (chunk ^ ((r >> 1) & 3)) : (chunk ^ ((r >> 2) & 1));
+    return *reinterpret_cast<const uint4 *>(box + r * XROW + phys * 16);
+}
+
+template <int N, bool LAYER>
+__global__ void __launch_bounds__(320, 1)
+    k_bwd_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmdu,
+             const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmg,
+             const __grid_constant__ CUtensorMap tmy, const BwdTcArgs a)
+{
+    using P = BwdTc<N>;
+    constexpr int O = P::O, CW = P::CW, HC = P::HC;
+    constexpr bool SG = LAYER && P::STAGE_G;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full[P::STAGES], empty[P::STAGES];
+    __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    __shared__ float bias_red[4][CW];
+
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *wtile = smem + P::STAGES * P::STAGE;
+    volatile int *abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t C = a.C, K = int64_t(N) * C;
+    const int64_t c0 = int64_t(blockIdx.x) * CW;
+    const int split = blockIdx.y;
+    const int tile0 = split * a.tiles_per_split;
+    const int ntiles = min(a.tiles_total, tile0 + a.tiles_per_split) - tile0;
+    constexpr uint32_t stage_tx = SG ? P::STAGE : P::X_BYTES + P::DU_BYTES;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&empty[s], 1 + 8);
+        }
+        tc::mbar_init(&wfull, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(&d2full[b], 1);
+            tc::mbar_init(&d2empty[b], 8);
+        }
+        tc::mbar_init(&d1full, 1);
+        abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&tmem_slot, P::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmx);
+            tc::tma_prefetch_desc(&tmdu);
+            tc::tma_prefetch_desc(&tmw);
+            if (SG) {
+                tc::tma_prefetch_desc(&tmg);
+                tc::tma_prefetch_desc(&tmy);
+            }
+            tc::mbar_arrive_expect_tx(&wfull, P::W_BYTES);
+            for (int p = 0; p < P::W_PLANES; ++p)
+                for (int j = 0; j < N; ++j)
+                    tc::tma_load_2d(wtile + p * P::W_PLANE_BYTES + j * CW * 128, &tmw, 0,
+                                    int(int64_t(p) * K + int64_t(j) * C + c0), &wfull);
+            int issued = 0;
+            for (int i = 0; i < ntiles && !*abort_v; ++i) {
+                const int s = i % P::STAGES;
+                if (i >= P::STAGES &&
+                    !tc::mbar_wait(&empty[s], ((i / P::STAGES) & 1) ^ 1, a.fault,
+                                   tc::kFaultTimeoutEmpty)) {
+                    *abort_v = 1;
+                    break;
+                }
+                uint8_t *st = smem + s * P::STAGE;
+                const int t0 = (tile0 + i) * P::TT;
+                tc::mbar_arrive_expect_tx(&full[s], stage_tx);
+                for (int j = 0; j < N; ++j)
+                    tc::tma_load_2d(st + j * P::XBOX, &tmx, int(int64_t(j) * C + c0), t0, &full[s]);
+                for (int u = 0; u < P::DU_ATOMS; ++u)
+                    tc::tma_load_2d(st + P::DU_OFF + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0,
+                                    &full[s]);
+                if (SG) {
+                    for (int j = 0; j < N; ++j)
+                        tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
+                                        int(int64_t(j) * C + c0), t0, &full[s]);
+                    tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &full[s]);
+                }
+                issued = i + 1;
+            }
+            tc::mbar_wait(&wfull, 0, a.fault, tc::kFaultTimeoutMisc);
+            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
+                tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
+                              tc::kFaultTimeoutMisc);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_dx = tc::idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t idesc_dw = tc::idesc_bf16_f32(128, P::NW, 1, 1);
+            bool ok = tc::mbar_wait(&wfull, 0, a.fault, tc::kFaultTimeoutFull);
+            const uint32_t wb = tc::smem_u32(wtile);
+            for (int i = 0; ok && i < ntiles; ++i) {
+                const int s = i % P::STAGES, b = i & 1;
+                if (*abort_v ||
+                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                const uint32_t xs = tc::smem_u32(smem + s * P::STAGE);
+                const uint32_t dus = xs + P::DU_OFF;
+                // dW += x^T du_hl over the tile's 128 tokens, 16 per step
+#pragma unroll
+                for (int ks = 0; ks < P::TT / 16; ++ks) {
+                    const uint64_t ad =
+                        tc::make_desc(xs + ks * 16 * P::XROW, P::XBOX, 8 * P::XROW, P::XSWZ);
+                    const uint64_t bd =
+                        tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES, 1024, tc::kSwz128);
+                    tc::mma_bf16(tmem + P::D1_COL, ad, bd, idesc_dw, (i > 0 || ks > 0) ? 1u : 0u);
+                }
+                // dx accumulator b must have been drained by the epilogue (tile i-2)
+                if (i >= 2 &&
+                    !tc::mbar_wait(&d2empty[b], ((i >> 1) - 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                // K steps: du_hl[0,2O) against [W_hi | W_hi], then du_hi against W_lo
+#pragma unroll
+                for (int kk = 0; kk < P::KSTEP_A + P::KSTEP_B; ++kk) {
+                    const int acol = kk < P::KSTEP_A ? 16 * kk : 16 * (kk - P::KSTEP_A);
+                    const int bcol = 16 * kk;
+                    const uint64_t ad =
+                        tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES + (acol % 64) * 2, 16,
+                                      1024, tc::kSwz128);
+                    const uint64_t bd =
+                        tc::make_desc(wb + (bcol / 64) * P::W_PLANE_BYTES + (bcol % 64) * 2, 16,
+                                      1024, tc::kSwz128);
+                    tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&d2full[b]);
+                tc::mma_commit(&empty[s]);
+            }
+            if (!ok) *abort_v = 1;
+            tc::mma_commit(&d1full);
+            tc::mbar_wait(&d1full, 0, a.fault, tc::kFaultTimeoutAcc);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;              // TMEM lane quadrant
+        const int h = (warp - 2) >> 2;       // which half of the channels
+        const int r = q * 32 + lane;         // token row in the tile / k row of dW
+        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+        float bias_acc[HC / 8];  // lane l: running total of channel chunk*8 + (l % 8)
+#pragma unroll
+        for (int u = 0; u < HC / 8; ++u) bias_acc[u] = 0.f;
+        bool ok = true;
+        for (int i = 0; i < ntiles; ++i) {
+            const int s = i % P::STAGES, b = i & 1;
+            const int64_t t = int64_t(tile0 + i) * P::TT + r;
+            const bool valid = t < a.T;
+            float coef = 0.f, hpre[N], hpost[N];
+#pragma unroll
+            for (int j = 0; j < N; ++j) hpre[j] = hpost[j] = 0.f;
+            uint4 g[N], gy;
+            // dout / dy chunk u of this thread's channels: from the staged
+            // tiles (n = 4) or from global memory (n = 8)
+            auto fetch = [&](int u, const uint8_t *st) {
+                const int chunk = h * (HC / 8) + u;
+                const int64_t cc = c0 + chunk * 8;
+                if (SG) {
+#pragma unroll
+                    for (int ii = 0; ii < N; ++ii)
+                        g[ii] = box_chunk<N>(st + P::G_OFF + ii * P::XBOX, r, chunk);
+                    gy = box_chunk<N>(st + P::Y_OFF, r, chunk);
+                } else if (LAYER && valid && cc < C) {
+#pragma unroll
+                    for (int ii = 0; ii < N; ++ii) g[ii] = ld_stream(a.dout + ((t * N + ii) * C + cc));
+                    gy = ld_stream(a.dy + (t * C + cc));
+                } else {
+#pragma unroll
+                    for (int ii = 0; ii < N; ++ii) g[ii] = make_uint4(0, 0, 0, 0);
+                    gy = make_uint4(0, 0, 0, 0);
+                }
+            };
+            if (!SG) fetch(0, nullptr);  // global loads in flight while waiting
+            if (valid) {
+                coef = __ldg(a.coef + t);
+                if (LAYER) {
+#pragma unroll
+                    for (int j = 0; j < N; ++j) {
+                        hpre[j] = __ldg(a.Hpre + t * N + j);
+                        hpost[j] = __ldg(a.Hpost + t * N + j);
+                    }
+                }
+            }
+            if (*abort_v ||
+                !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
+                !tc::mbar_wait(&d2full[b], (i >> 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+            const uint8_t *st = smem + s * P::STAGE;
+#pragma unroll
+            for (int u = 0; u < HC / 8; ++u) {
+                if (SG || u > 0) fetch(u, st);
+                const int chunk = h * (HC / 8) + u;
+                const bool cvalid = c0 + chunk * 8 < C;  // the last slice may pass C
+                float gyv[8];
+                unpack8(gy, gyv);
+                if (LAYER) {
+                    // dbias: column sums over the tile of df = sum_i H_post[i] dout_i
+                    float df[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) df[e] = 0.f;
+#pragma unroll
+                    for (int ii = 0; ii < N; ++ii) {
+                        float dv[8];
+                        unpack8(g[ii], dv);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) df[e] = fmaf(hpost[ii], dv[e], df[e]);
+                    }
+                    bias_acc[u] += warp_column_sum<8>(df);
+                }
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float acc[8];
+                    tc::tmem_ld8(trow + P::D2_COL + b * 128 + j * CW + chunk * 8, acc);
+                    float xv[8];
+                    unpack8(box_chunk<N>(st + j * P::XBOX, r, chunk), xv);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(coef, xv[e], acc[e]);
+                    if (LAYER) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(hpre[j], gyv[e], acc[e]);
+#pragma unroll
+                        for (int ii = 0; ii < N; ++ii) {
+                            const float w = valid ? __ldg(a.Hres + (t * N + j) * N + ii) : 0.f;
+                            float dv[8];
+                            unpack8(g[ii], dv);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, dv[e], acc[e]);
+                        }
+                    }
+                    if (valid && cvalid)
+                        st_stream(a.dx + ((t * N + j) * C + c0 + chunk * 8), pack8(acc));
+                }
+            }
+            // D2 buffer b and the stage have been read: release them
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&d2empty[b]);
+                tc::mbar_arrive(&empty[s]);
+            }
+        }
+        if (!ok) *abort_v = 1;
+        // dW partial of this split: D1 rows are the 128 k of the slice
+        const bool krow = c0 + (r % CW) < C;  // dW row exists
+        if (ok && h == 0 && tc::mbar_wait(&d1full, 0, a.fault, tc::kFaultTimeoutAcc)) {
+            tc::tc_fence_after();
+            const int j = r / CW, c = r % CW;
+            float *dst = a.dWpart + (int64_t(split) * K + int64_t(j) * C + c0 + c) * O;
+            if (O == 24) {
+                float v[48];
+#pragma unroll
+                for (int m = 0; m < 3; ++m) {
+                    float w16[16];
+                    tc::tmem_ld16(trow + P::D1_COL + m * 16, w16);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[m * 16 + e] = w16[e];
+                }
+#pragma unroll
+                for (int o4 = 0; o4 < O / 4; ++o4)
+                    if (krow)
+                        reinterpret_cast<float4 *>(dst)[o4] = make_float4(
+                            v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
+                            v[4 * o4 + 2] + v[O + 4 * o4 + 2], v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
+            } else {
+#pragma unroll 1
+                for (int m = 0; m < O / 16; ++m) {
+                    float hi[16], lo[16];
+                    tc::tmem_ld16(trow + P::D1_COL + m * 16, hi);
+                    tc::tmem_ld16(trow + P::D1_COL + O + m * 16, lo);
+                    tc::tmem_ld_wait();
+#pragma unroll
+                    for (int o4 = 0; o4 < 4; ++o4)
+                        if (krow)
+                            reinterpret_cast<float4 *>(dst + m * 16)[o4] = make_float4(
+                                hi[4 * o4] + lo[4 * o4], hi[4 * o4 + 1] + lo[4 * o4 + 1],
+                                hi[4 * o4 + 2] + lo[4 * o4 + 2], hi[4 * o4 + 3] + lo[4 * o4 + 3]);
+                }
+            }
+        }
+        if (LAYER && lane < 8) {
+#pragma unroll
+            for (int u = 0; u < HC / 8; ++u) bias_red[q][h * HC + u * 8 + lane] = bias_acc[u];
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (LAYER && threadIdx.x < CW && c0 + threadIdx.x < C && !abort_flag) {
+        const float v = bias_red[0][threadIdx.x] + bias_red[1][threadIdx.x] +
+                        bias_red[2][threadIdx.x] + bias_red[3][threadIdx.x];
+        a.dbiaspart[int64_t(split) * C + c0 + threadIdx.x] = v;
+    }
+    if (warp == 1) tc::tmem_dealloc(tmem, P::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_bwd()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+static bool map2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
+                  uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle sw)
+{
+    auto fn = encode_fn_bwd();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int bwd_tc_du_cols(int n) { return n == 4 ? BwdTc<4>::DU_COLS : BwdTc<8>::DU_COLS; }
+
+size_t bwd_tc_wb_bytes(int n, int64_t C)
+{
+    const int64_t K = int64_t(n) * C;
+    const int planes = n == 4 ? BwdTc<4>::W_PLANES : BwdTc<8>::W_PLANES;
+    return size_t(K) * planes * 64 * 2;
+}
+
+int bwd_tc_splits(int64_t T, int n, int64_t C)
+{
+    const int64_t slices = (C + 128 / n - 1) / (128 / n);
+    const int64_t tiles = (T + 127) / 128;
+    int64_t s = int64_t(kSplitSms) / (slices > 0 ? slices : 1);
+    if (s < 1) s = 1;
+    if (s > tiles) s = tiles;
+    if (s > 8) s = 8;
+    return int(s);
+}
+
+template <int N, bool LAYER>
+static cudaError_t bwd_tc_impl(const bf16 *x, const float *W, const bf16 *du_hl, bf16 *Wd,
+                               const BwdTcArgs &args, int splits, cudaStream_t s)
+{
+    using P = BwdTc<N>;
+    const int64_t T = args.T, C = args.C, K = int64_t(N) * C;
+    {
+        MHC_PROF("k_w_planes", s);
+        k_w_planes<N><<<unsigned((K + 255) / 256), 256, 0, s>>>(W, Wd, K);
+    }
+    CUtensorMap tmx, tmdu, tmw, tmg, tmy;
+    const CUtensorMapSwizzle xsw = N == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!map2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
+        !map2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
+               CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !map2d(&tmw, Wd, uint64_t(P::W_PLANES * K), 64, P::CW, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    tmg = tmx;
+    tmy = tmx;
+    if (LAYER && P::STAGE_G) {
+        if (!map2d(&tmg, args.dout, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
+            !map2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
+            return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_tc<N, LAYER>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(unsigned((C + P::CW - 1) / P::CW), unsigned(splits));
+    {
+        MHC_PROF("k_bwd_tc", s);
+        k_bwd_tc<N, LAYER><<<grid, P::THREADS, P::SMEM, s>>>(tmx, tmdu, tmw, tmg, tmy, args);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
+                          bf16 *Wd, int64_t T, int n, int64_t C, const bf16 *dout,
+                          const bf16 *dy, const float *Hpre, const float *Hres,
+                          const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
+                          int splits, int *fault, cudaStream_t s)
+{
+    BwdTcArgs a;
+    a.dout = dout;
+    a.dy = dy;
+    a.coef = coef;
+    a.Hpre = Hpre;
+    a.Hres = Hres;
+    a.Hpost = Hpost;
+    a.dx = dx;
+    a.dWpart = dWpart;
+    a.dbiaspart = dbiaspart;
+    a.T = T;
+    a.C = C;
+    a.tiles_total = int((T + 127) / 128);
+    a.tiles_per_split = (a.tiles_total + splits - 1) / splits;
+    a.fault = fault;
+    const bool layer = dout != nullptr;
+    if (n == 4)
+        return layer ? bwd_tc_impl<4, true>(x, W, du_hl, Wd, a, splits, s)
+                     : bwd_tc_impl<4, false>(x, W, du_hl, Wd, a, splits, s);
+    return layer ? bwd_tc_impl<8, true>(x, W, du_hl, Wd, a, splits, s)
+                 : bwd_tc_impl<8, false>(x, W, du_hl, Wd, a, splits, s);
+}
+
+}  // namespace mhc

@@ -12,9 +12,10 @@
 // Forward:  k_proj_tc (k_proj_tc.cu: split-K partial u = x W and s = sum x^2
 //           on the tensor cores), k_compute_h_fwd (sum of partials, r, z,
 //           gates, Sinkhorn)
-// Backward: k_compute_h_bwd (per-token du, dz, dalpha terms, RMS coefficient)
-//           k_dx (du W^T + coef x [+ H_res dout + H_pre dy]), k_dW_partial,
-//           fixed-order reductions for dW, dalpha, db.
+// Backward: k_compute_h_bwd (per-token du as bf16 hi|lo, dz, dalpha terms,
+//           RMS coefficient), k_bwd_tc (k_bwd_tc.cu: du W^T + coef x [+ H_res
+//           dout + H_pre dy], dW and dbias partials on the tensor cores),
+//           fixed-order reductions for dW, dbias, dalpha, db.
 #include "launch.h"
 #include "sinkhorn.cuh"
 
@@ -91,7 +92,7 @@ __global__ void __launch_bounds__(128)
                     const float *__restrict__ dHres, const float *__restrict__ u_save,
                     const float *__restrict__ r_save, const float *__restrict__ alpha,
                     const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
-                    float eps_rms, float *__restrict__ du, float *__restrict__ dz,
+                    float eps_rms, bf16 *__restrict__ du_hl, int du_cols, float *__restrict__ dz,
                     float *__restrict__ ga, float *__restrict__ coef)
 {
     constexpr int O = Dims<N>::O;
@@ -136,16 +137,26 @@ __global__ void __launch_bounds__(128)
         dres_dot += __shfl_xor_sync(kFull, dres_dot, m);
     }
     if (live) {
-        float *dut = du + t * O, *dzt = dz + t * O;
-        dut[i] = a0 * r * dzpre;
-        dut[N + i] = a1 * r * dzpost;
+        // du = alpha_seg r dz, stored as bf16 hi (columns [0,O)) and the bf16
+        // remainder (columns [O,2O)); zero columns pad the row to du_cols.
+        bf16 *dut = du_hl + t * du_cols;
+        float *dzt = dz + t * O;
+        auto put = [&](int o, float v) {
+            const bf16 hi = __float2bfloat16_rn(v);
+            dut[o] = hi;
+            dut[O + o] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        };
+        put(i, a0 * r * dzpre);
+        put(N + i, a1 * r * dzpost);
         dzt[i] = dzpre;
         dzt[N + i] = dzpost;
 #pragma unroll
         for (int j = 0; j < N; ++j) {
-            dut[2 * N + i * N + j] = a2 * r * g[j];
+            put(2 * N + i * N + j, a2 * r * g[j]);
             dzt[2 * N + i * N + j] = g[j];
         }
+        if (i == 0)
+            for (int o = 2 * O; o < du_cols; ++o) dut[o] = __float2bfloat16_rn(0.f);
         if (i == 0) {
             ga[t * 4 + 0] = gpre * r;
             ga[t * 4 + 1] = gpost * r;
@@ -156,101 +167,6 @@ __global__ void __launch_bounds__(128)
             coef[t] = (q > 0.f) ? -dr * r * r / (float(K) * q) : 0.f;
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// Residual-gradient pass.  CTA: 32 tokens x (N streams x CW channels), one
-// thread per (stream j, channel c), W row k = j*C + c kept in registers.
-//   dx[t][j][c] = sum_o du[t][o] W[k][o] + coef[t] x[t][j][c]
-//               [+ H_pre[t][j] dy[t][c] + sum_i H_res[t][j][i] dout[t][i][c]]
-// ---------------------------------------------------------------------------
-constexpr int kDxTT = 32, kDxThreads = 256;
-
-template <int N, bool LAYER>
-__global__ void __launch_bounds__(kDxThreads)
-    k_dx(const float *__restrict__ du, const float *__restrict__ coef, const float *__restrict__ W,
-         const bf16 *__restrict__ x, const bf16 *__restrict__ dy, const bf16 *__restrict__ dout,
-         const float *__restrict__ Hpre, const float *__restrict__ Hres, bf16 *__restrict__ dx,
-         int64_t T, int64_t C)
-{
-    constexpr int O = Dims<N>::O, CW = kDxThreads / N;
-    __shared__ float du_s[kDxTT * O];
-    __shared__ float coef_s[kDxTT];
-    __shared__ float hp_s[LAYER ? kDxTT * N : 1];
-    __shared__ float hr_s[LAYER ? kDxTT * N * N : 1];
-    const int tid = threadIdx.x;
-    const int j = tid / CW;
-    const int64_t c = int64_t(blockIdx.x) * CW + tid % CW;
-    const int64_t t0 = int64_t(blockIdx.y) * kDxTT;
-    const bool cv = c < C;
-    const int64_t K = N * C;
-    const int64_t k = j * C + c;
-    float wr[O];
-#pragma unroll
-    for (int o = 0; o < O; ++o) wr[o] = cv ? __ldg(W + k * O + o) : 0.f;
-    const int nt = int(min(int64_t(kDxTT), T - t0));
-    for (int e = tid; e < nt * O; e += kDxThreads) du_s[e] = __ldg(du + t0 * O + e);
-    for (int e = tid; e < nt; e += kDxThreads) coef_s[e] = __ldg(coef + t0 + e);
-    if (LAYER) {
-        for (int e = tid; e < nt * N; e += kDxThreads) hp_s[e] = __ldg(Hpre + t0 * N + e);
-        for (int e = tid; e < nt * N * N; e += kDxThreads) hr_s[e] = __ldg(Hres + t0 * N * N + e);
-    }
-    __syncthreads();
-    if (!cv) return;
-    const uint16_t *xu = reinterpret_cast<const uint16_t *>(x);
-    const uint16_t *dyu = reinterpret_cast<const uint16_t *>(dy);
-    const uint16_t *du16 = reinterpret_cast<const uint16_t *>(dout);
-    for (int tl = 0; tl < nt; ++tl) {
-        const int64_t t = t0 + tl;
-        float acc = 0.f;
-#pragma unroll
-        for (int o = 0; o < O; ++o) acc = fmaf(du_s[tl * O + o], wr[o], acc);
-        acc = fmaf(coef_s[tl], __uint_as_float(uint32_t(xu[t * K + k]) << 16), acc);
-        if (LAYER) {
-            acc = fmaf(hp_s[tl * N + j], __uint_as_float(uint32_t(dyu[t * C + c]) << 16), acc);
-#pragma unroll
-            for (int i = 0; i < N; ++i)
-                acc = fmaf(hr_s[(tl * N + j) * N + i],
-                           __uint_as_float(uint32_t(du16[(t * N + i) * C + c]) << 16), acc);
-        }
-        dx[t * K + k] = __float2bfloat16_rn(acc);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// dW partials: part[s][k][o] = sum_{t in split s} x[t][k] du[t][o]
-// ---------------------------------------------------------------------------
-constexpr int kWThreads = 256, kWTT = 32;
-
-template <int N>
-__global__ void __launch_bounds__(kWThreads)
-    k_dW_partial(const bf16 *__restrict__ x, const float *__restrict__ du, float *__restrict__ part,
-                 int64_t T, int64_t K, int64_t splits)
-{
-    constexpr int O = Dims<N>::O;
-    __shared__ float du_s[kWTT * O];
-    const int64_t k = int64_t(blockIdx.x) * kWThreads + threadIdx.x;
-    const int64_t s = blockIdx.y;
-    const int64_t tb = T * s / splits, te = T * (s + 1) / splits;
-    const uint16_t *xu = reinterpret_cast<const uint16_t *>(x);
-    float acc[O];
-#pragma unroll
-    for (int o = 0; o < O; ++o) acc[o] = 0.f;
-    for (int64_t t0 = tb; t0 < te; t0 += kWTT) {
-        const int nt = int(min(int64_t(kWTT), te - t0));
-        __syncthreads();
-        for (int e = threadIdx.x; e < nt * O; e += kWThreads) du_s[e] = __ldg(du + t0 * O + e);
-        __syncthreads();
-        if (k < K)
-            for (int tl = 0; tl < nt; ++tl) {
-                const float xv = __uint_as_float(uint32_t(xu[(t0 + tl) * K + k]) << 16);
-#pragma unroll
-                for (int o = 0; o < O; ++o) acc[o] = fmaf(xv, du_s[tl * O + o], acc[o]);
-            }
-    }
-    if (k < K)
-#pragma unroll
-        for (int o = 0; o < O; ++o) part[(s * K + k) * O + o] = acc[o];
 }
 
 // out[j] = sum_r part[r][j], r ascending
@@ -334,21 +250,14 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
                             u_save, r_save, ws, fault, s);
 }
 
-static int64_t dW_splits(int64_t T, int64_t K)
-{
-    const int64_t kb = (K + kWThreads - 1) / kWThreads;
-    int64_t s = (int64_t(kSplitSms) * 4 + kb - 1) / kb;
-    if (s > (T + kWTT - 1) / kWTT) s = (T + kWTT - 1) / kWTT;
-    if (s > 32) s = 32;
-    return s < 1 ? 1 : s;
-}
-
 // workspace layout of the backward (each piece 256-byte aligned):
-//   du [T][O], dz [T][O], ga [T][4], coef [T], dHpre/dHpost [T][N], dHres [T][N][N],
-//   dW partials [S][K][O], dbias partials
+//   du_hl [T][du_cols] bf16, dz [T][O], ga [T][4], coef [T], dHpre/dHpost [T][N],
+//   dHres [T][N][N], Wb (bf16 W for the tensor cores), dW partials [S][K][O],
+//   dbias partials [S][C]
 struct BwdWs {
-    float *du, *dz, *ga, *coef, *dHpre, *dHpost, *dHres, *dWpart;
-    void *dbias_ws;
+    bf16 *du_hl, *Wb;
+    float *dz, *ga, *coef, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
+    int splits;
     size_t bytes;
 };
 
@@ -363,15 +272,17 @@ static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
         off += ws_align(bytes);
         return q;
     };
-    w.du = reinterpret_cast<float *>(take(size_t(T * O) * 4));
+    w.splits = bwd_tc_splits(T, n, C);
+    w.du_hl = reinterpret_cast<bf16 *>(take(size_t(T) * bwd_tc_du_cols(n) * 2));
     w.dz = reinterpret_cast<float *>(take(size_t(T * O) * 4));
     w.ga = reinterpret_cast<float *>(take(size_t(T * 4) * 4));
     w.coef = reinterpret_cast<float *>(take(size_t(T) * 4));
     w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
     w.dHpost = reinterpret_cast<float *>(take(size_t(T * n) * 4));
     w.dHres = reinterpret_cast<float *>(take(size_t(T * n * n) * 4));
-    w.dWpart = reinterpret_cast<float *>(take(size_t(dW_splits(T, K)) * size_t(K * O) * 4));
-    w.dbias_ws = take(dbias_ws_bytes(T, C));
+    w.Wb = reinterpret_cast<bf16 *>(take(bwd_tc_wb_bytes(n, C)));
+    w.dWpart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(K * O) * 4));
+    w.dbiaspart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(C) * 4));
     w.bytes = off;
     return w;
 }
@@ -390,7 +301,8 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
                             const bf16 *x, const float *W, const float *alpha, const float *b,
                             const float *u_save, const float *r_save, int64_t T, int64_t C,
                             int iters, float eps_sk, float eps_rms, const LayerBwd *L, bf16 *dx,
-                            float *dW, float *dalpha, float *db, void *ws, cudaStream_t s)
+                            float *dW, float *dalpha, float *db, void *ws, int *fault,
+                            cudaStream_t s)
 {
     constexpr int O = Dims<N>::O;
     const int64_t K = int64_t(N) * C;
@@ -415,30 +327,26 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     {
         MHC_PROF("k_compute_h_bwd", s);
         k_compute_h_bwd<N><<<unsigned((T * N + 127) / 128), 128, smem, s>>>(
-            dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du, w.dz,
-            w.ga, w.coef);
+            dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
+            bwd_tc_du_cols(N), w.dz, w.ga, w.coef);
     }
-    // pass 3: residual gradient, dW, dbias
-    constexpr int CW = kDxThreads / N;
-    dim3 gdx(unsigned((C + CW - 1) / CW), unsigned((T + kDxTT - 1) / kDxTT));
-    if (L) {
-        MHC_PROF("k_dx", s);
-        k_dx<N, true><<<gdx, kDxThreads, 0, s>>>(w.du, w.coef, W, x, L->dy, L->dout, L->Hpre,
-                                                 L->Hres, dx, T, C);
-    } else {
-            MHC_PROF("k_dx", s);
-            k_dx<N, false><<<gdx, kDxThreads, 0, s>>>(w.du, w.coef, W, x, nullptr, nullptr, nullptr,
-                                                      nullptr, dx, T, C);
-        }
-    const int64_t S = dW_splits(T, K);
-    dim3 gw(unsigned((K + kWThreads - 1) / kWThreads), unsigned(S));
-    {
-        MHC_PROF("k_dW_partial", s);
-        k_dW_partial<N><<<gw, kWThreads, 0, s>>>(x, w.du, w.dWpart, T, K, S);
-    }
+    // pass 3: residual gradient, dW and dbias on the tensor cores
+    const int tiles = int((T + 127) / 128);
+    const int tps = (tiles + w.splits - 1) / w.splits;
+    const int splits_used = (tiles + tps - 1) / tps;
+    e = launch_bwd_tc(x, W, w.du_hl, w.coef, w.Wb, T, N, C, L ? L->dout : nullptr,
+                      L ? L->dy : nullptr, L ? L->Hpre : nullptr, L ? L->Hres : nullptr,
+                      L ? L->Hpost : nullptr, dx, w.dWpart, w.dbiaspart, splits_used, fault, s);
+    if (e != cudaSuccess) return e;
     {
         MHC_PROF("k_sum_rows_p", s);
-        k_sum_rows_p<<<unsigned((K * O + 255) / 256), 256, 0, s>>>(w.dWpart, dW, S, K * O);
+        k_sum_rows_p<<<unsigned((K * O + 255) / 256), 256, 0, s>>>(w.dWpart, dW, splits_used,
+                                                                   K * O);
+    }
+    if (L && L->dbias) {
+        MHC_PROF("k_sum_rows_p", s);
+        k_sum_rows_p<<<unsigned((C + 255) / 256), 256, 0, s>>>(w.dbiaspart, L->dbias,
+                                                               splits_used, C);
     }
     {
         MHC_PROF("k_sum_cols", s);
@@ -447,10 +355,6 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     {
         MHC_PROF("k_sum_cols", s);
         k_sum_cols<<<O, 256, 0, s>>>(w.dz, O, T, db);
-    }
-    if (L && L->dbias) {
-        e = launch_dbias(L->dout, L->Hpost, L->dbias, T, N, C, w.dbias_ws, s);
-        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -462,12 +366,11 @@ cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float
                             float *dW, float *dalpha, float *db, void *ws, int *fault,
                             cudaStream_t s)
 {
-    (void)fault;
     if (n == 4)
         return bwd_impl<4>(dHpre, dHpost, dHres, x, W, alpha, b, u_save, r_save, T, C, iters,
-                           eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, s);
+                           eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, fault, s);
     return bwd_impl<8>(dHpre, dHpost, dHres, x, W, alpha, b, u_save, r_save, T, C, iters,
-                       eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, s);
+                       eps_sk, eps_rms, nullptr, dx, dW, dalpha, db, ws, fault, s);
 }
 
 cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
@@ -478,13 +381,12 @@ cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, co
                              float eps_rms, bf16 *dx, bf16 *df, float *dW, float *dalpha,
                              float *db, float *dbias, void *ws, int *fault, cudaStream_t s)
 {
-    (void)fault;
     const LayerBwd L{dout, dy, f, bias, Hpre, Hpost, Hres, df, dbias};
     if (n == 4)
         return bwd_impl<4>(nullptr, nullptr, nullptr, x, W, alpha, b, u_save, r_save, T, C,
-                           iters, eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, s);
+                           iters, eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, fault, s);
     return bwd_impl<8>(nullptr, nullptr, nullptr, x, W, alpha, b, u_save, r_save, T, C, iters,
-                       eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, s);
+                       eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, fault, s);
 }
 
 }  // namespace mhc

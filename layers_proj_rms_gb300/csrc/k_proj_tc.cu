@@ -154,11 +154,15 @@ __global__ void __launch_bounds__(192, 1)
                 ok = false;
                 break;
             }
+            // The row's eight 16-byte chunks, in an order that differs per
+            // lane: rows that share banks (r and r+8, r+16, ...) then read
+            // different chunks, so a warp's loads are free of bank conflicts.
+            // The sum of squares does not depend on the order.
             const uint4 *row = reinterpret_cast<const uint4 *>(smem + s * P::STAGE + r * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float f[8];
-                unpack8(row[c], f);
+                unpack8(row[c ^ (lane & 7)], f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
             }

@@ -72,6 +72,16 @@ cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n
                                  bf16 *Whl, float *upart, float *spart, int *splits_used,
                                  int *fault, cudaStream_t s);
 
+// k_bwd_tc.cu: residual-gradient pass of the backward on the tensor cores
+int bwd_tc_du_cols(int n);
+size_t bwd_tc_wb_bytes(int n, int64_t C);
+int bwd_tc_splits(int64_t T, int n, int64_t C);
+cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
+                          bf16 *Wb, int64_t T, int n, int64_t C, const bf16 *dout,
+                          const bf16 *dy, const float *Hpre, const float *Hres,
+                          const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
+                          int splits, int *fault, cudaStream_t s);
+
 // k_proj.cu
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C);
 cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,

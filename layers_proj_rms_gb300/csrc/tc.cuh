@@ -163,6 +163,37 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 32 lanes x 32 bits, 8 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
+{
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // ---- descriptors -----------------------------------------------------------
@@ -184,15 +215,37 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr)
     return d;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
+// Swizzle modes of the descriptor (bits 61-63) and the matching TMA modes.
+enum : uint32_t { kSwz128 = 2, kSwz64 = 4, kSwz32 = 6 };
+
+// General descriptor: start address, leading and stride byte offsets, swizzle.
+// K-major swizzled operands use only the stride byte offset (distance between
+// 8-row groups).  MN-major swizzled operands: the leading byte offset is the
+// distance between swizzle atoms along M (or N), the stride byte offset the
+// distance between 8-row groups along K.
+__device__ __forceinline__ uint64_t make_desc(uint32_t smem_addr, uint32_t lbo_bytes,
+                                              uint32_t sbo_bytes, uint32_t swizzle)
 {
-    return (1u << 4)                  // D format f32
-           | (1u << 7)                // A format bf16
-           | (1u << 10)               // B format bf16
-           | (uint32_t(N >> 3) << 17) // N / 8
-           | (uint32_t(M >> 4) << 24);// M / 16
+    uint64_t d = 0;
+    d |= uint64_t((smem_addr & 0x3FFFF) >> 4);
+    d |= uint64_t((lbo_bytes >> 4) & 0x3FFF) << 16;
+    d |= uint64_t((sbo_bytes >> 4) & 0x3FFF) << 32;
+    d |= uint64_t(1) << 46;
+    d |= uint64_t(swizzle) << 61;
+    return d;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 accumulator,
+// shape M x N; a_mn / b_mn select MN-major (transposed) operands.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn = 0, int b_mn = 0)
+{
+    return (1u << 4)                   // D format f32
+           | (1u << 7)                 // A format bf16
+           | (1u << 10)                // B format bf16
+           | (uint32_t(a_mn) << 15)    // A major-ness: 0 K-major, 1 MN-major
+           | (uint32_t(b_mn) << 16)    // B major-ness
+           | (uint32_t(N >> 3) << 17)  // N / 8
+           | (uint32_t(M >> 4) << 24); // M / 16
 }
 
 }  // namespace tc
