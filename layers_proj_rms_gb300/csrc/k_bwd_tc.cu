@@ -27,8 +27,9 @@
 // split's dW partial.  For n = 4 the producer also stages dout and dy through
 // shared memory (every DRAM access a whole 64-byte row); for n = 8 (16-channel
 // slices) the epilogue reads them from global memory.
-// Warps: 0 TMA producer, 1 TMEM + MMA issue, 2..9 epilogue (two warps per
-// TMEM lane quadrant, each half of the slice's channels).
+// Warps: 0 TMA producer, 1 TMEM + MMA issue, 2.. epilogue: CW/8 warps per
+// TMEM lane quadrant, each thread one token row x one 8-channel chunk of
+// every stream (16 epilogue warps for n = 4, 8 for n = 8).
 #include <cudaTypedefs.h>
 
 #include "launch.h"
@@ -40,7 +41,8 @@ template <int N>
 struct BwdTc {
     static constexpr int O = N * N + 2 * N;     // 24 / 80
     static constexpr int CW = 128 / N;          // channels per stream: 32 / 16
-    static constexpr int HC = CW / 2;           // channels per epilogue thread: 16 / 8
+    static constexpr int CHUNKS = CW / 8;       // 8-channel chunks per stream slice: 4 / 2
+    static constexpr int EPI_WARPS = 4 * CHUNKS;        // 16 / 8
     static constexpr int TT = 128;              // tokens per tile
     static constexpr int XROW = CW * 2;         // bytes of one token row of a stream box
     static constexpr uint32_t XSWZ = N == 4 ? tc::kSwz64 : tc::kSwz32;
@@ -68,7 +70,7 @@ struct BwdTc {
     static constexpr int D2_COL = 0, D1_COL = 256;      // D2 buffers at 0 and 128
     static constexpr int TMEM_COLS = 512;
     static constexpr int SMEM = STAGES * STAGE + W_BYTES + 1024;
-    static constexpr int THREADS = 320;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
     static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory");
 };
@@ -149,13 +151,13 @@ __device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
 }
 
 template <int N, bool LAYER>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmdu,
              const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmg,
              const __grid_constant__ CUtensorMap tmy, const BwdTcArgs a)
 {
     using P = BwdTc<N>;
-    constexpr int O = P::O, CW = P::CW, HC = P::HC;
+    constexpr int O = P::O, CW = P::CW;
     constexpr bool SG = LAYER && P::STAGE_G;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[P::STAGES], empty[P::STAGES];
@@ -180,12 +182,12 @@ __global__ void __launch_bounds__(320, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1 + 8);
+            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
         }
         tc::mbar_init(&wfull, 1);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&d2full[b], 1);
-            tc::mbar_init(&d2empty[b], 8);
+            tc::mbar_init(&d2empty[b], P::EPI_WARPS);
         }
         tc::mbar_init(&d1full, 1);
         abort_flag = 0;
@@ -299,42 +301,26 @@ __global__ void __launch_bounds__(320, 1)
     } else {
         // ------------------------------------------------------------ epilogue
         const int q = warp & 3;              // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;       // which half of the channels
+        const int h = (warp - 2) >> 2;       // this thread's 8-channel chunk of every stream
         const int r = q * 32 + lane;         // token row in the tile / k row of dW
         const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-        float bias_acc[HC / 8];  // lane l: running total of channel chunk*8 + (l % 8)
-#pragma unroll
-        for (int u = 0; u < HC / 8; ++u) bias_acc[u] = 0.f;
+        const int64_t cc = c0 + h * 8;       // first channel of the chunk
+        const bool cvalid = cc < C;          // the last slice may pass C
+        float bias_acc = 0.f;                // lane l: running total of channel cc + (l % 8)
         bool ok = true;
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % P::STAGES, b = i & 1;
             const int64_t t = int64_t(tile0 + i) * P::TT + r;
             const bool valid = t < a.T;
-            float coef = 0.f, hpre[N], hpost[N];
+            // per-token inputs, fetched before waiting on the tensor cores
+            float coef = 0.f, hpre[N], hpost[N], hres[LAYER ? N * N : 1];
 #pragma unroll
             for (int j = 0; j < N; ++j) hpre[j] = hpost[j] = 0.f;
-            uint4 g[N], gy;
-            // dout / dy chunk u of this thread's channels: from the staged
-            // tiles (n = 4) or from global memory (n = 8)
-            auto fetch = [&](int u, const uint8_t *st) {
-                const int chunk = h * (HC / 8) + u;
-                const int64_t cc = c0 + chunk * 8;
-                if (SG) {
 #pragma unroll
-                    for (int ii = 0; ii < N; ++ii)
-                        g[ii] = box_chunk<N>(st + P::G_OFF + ii * P::XBOX, r, chunk);
-                    gy = box_chunk<N>(st + P::Y_OFF, r, chunk);
-                } else if (LAYER && valid && cc < C) {
+            for (int e = 0; e < (LAYER ? N * N : 1); ++e) hres[e] = 0.f;
+            uint4 g[N], gy = make_uint4(0, 0, 0, 0);
 #pragma unroll
-                    for (int ii = 0; ii < N; ++ii) g[ii] = ld_stream(a.dout + ((t * N + ii) * C + cc));
-                    gy = ld_stream(a.dy + (t * C + cc));
-                } else {
-#pragma unroll
-                    for (int ii = 0; ii < N; ++ii) g[ii] = make_uint4(0, 0, 0, 0);
-                    gy = make_uint4(0, 0, 0, 0);
-                }
-            };
-            if (!SG) fetch(0, nullptr);  // global loads in flight while waiting
+            for (int ii = 0; ii < N; ++ii) g[ii] = make_uint4(0, 0, 0, 0);
             if (valid) {
                 coef = __ldg(a.coef + t);
                 if (LAYER) {
@@ -342,6 +328,19 @@ __global__ void __launch_bounds__(320, 1)
                     for (int j = 0; j < N; ++j) {
                         hpre[j] = __ldg(a.Hpre + t * N + j);
                         hpost[j] = __ldg(a.Hpost + t * N + j);
+                    }
+#pragma unroll
+                    for (int e = 0; e < N * N; e += 4) {
+                        const float4 v = __ldg(reinterpret_cast<const float4 *>(a.Hres + t * N * N + e));
+                        hres[e] = v.x;
+                        hres[e + 1] = v.y;
+                        hres[e + 2] = v.z;
+                        hres[e + 3] = v.w;
+                    }
+                    if (!SG && cvalid) {
+#pragma unroll
+                        for (int ii = 0; ii < N; ++ii) g[ii] = ld_stream(a.dout + ((t * N + ii) * C + cc));
+                        gy = ld_stream(a.dy + (t * C + cc));
                     }
                 }
             }
@@ -353,51 +352,48 @@ __global__ void __launch_bounds__(320, 1)
             }
             tc::tc_fence_after();
             const uint8_t *st = smem + s * P::STAGE;
+            if (SG) {
 #pragma unroll
-            for (int u = 0; u < HC / 8; ++u) {
-                if (SG || u > 0) fetch(u, st);
-                const int chunk = h * (HC / 8) + u;
-                const bool cvalid = c0 + chunk * 8 < C;  // the last slice may pass C
-                float gyv[8];
+                for (int ii = 0; ii < N; ++ii) g[ii] = box_chunk<N>(st + P::G_OFF + ii * P::XBOX, r, h);
+                gy = box_chunk<N>(st + P::Y_OFF, r, h);
+            }
+            // mix[j][e] = H_pre[j] dy[e] + sum_i H_res[j][i] dout_i[e];  df = sum_i H_post[i] dout_i
+            float mix[LAYER ? N : 1][8];
+            if (LAYER) {
+                float gyv[8], df[8];
                 unpack8(gy, gyv);
-                if (LAYER) {
-                    // dbias: column sums over the tile of df = sum_i H_post[i] dout_i
-                    float df[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) df[e] = 0.f;
+                for (int j = 0; j < N; ++j)
 #pragma unroll
-                    for (int ii = 0; ii < N; ++ii) {
-                        float dv[8];
-                        unpack8(g[ii], dv);
+                    for (int e = 0; e < 8; ++e) mix[j][e] = hpre[j] * gyv[e];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) df[e] = fmaf(hpost[ii], dv[e], df[e]);
-                    }
-                    bias_acc[u] += warp_column_sum<8>(df);
+                for (int e = 0; e < 8; ++e) df[e] = 0.f;
+#pragma unroll
+                for (int ii = 0; ii < N; ++ii) {
+                    float dv[8];
+                    unpack8(g[ii], dv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) df[e] = fmaf(hpost[ii], dv[e], df[e]);
+#pragma unroll
+                    for (int j = 0; j < N; ++j)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) mix[j][e] = fmaf(hres[j * N + ii], dv[e], mix[j][e]);
                 }
+                bias_acc += warp_column_sum<8>(df);
+            }
 #pragma unroll
-                for (int j = 0; j < N; ++j) {
-                    float acc[8];
-                    tc::tmem_ld8(trow + P::D2_COL + b * 128 + j * CW + chunk * 8, acc);
-                    float xv[8];
-                    unpack8(box_chunk<N>(st + j * P::XBOX, r, chunk), xv);
-                    tc::tmem_ld_wait();
+            for (int j = 0; j < N; ++j) {
+                float acc[8];
+                tc::tmem_ld8(trow + P::D2_COL + b * 128 + j * CW + h * 8, acc);
+                float xv[8];
+                unpack8(box_chunk<N>(st + j * P::XBOX, r, h), xv);
+                tc::tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(coef, xv[e], acc[e]);
-                    if (LAYER) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = fmaf(hpre[j], gyv[e], acc[e]);
-#pragma unroll
-                        for (int ii = 0; ii < N; ++ii) {
-                            const float w = valid ? __ldg(a.Hres + (t * N + j) * N + ii) : 0.f;
-                            float dv[8];
-                            unpack8(g[ii], dv);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, dv[e], acc[e]);
-                        }
-                    }
-                    if (valid && cvalid)
-                        st_stream(a.dx + ((t * N + j) * C + c0 + chunk * 8), pack8(acc));
+                for (int e = 0; e < 8; ++e) {
+                    acc[e] = fmaf(coef, xv[e], acc[e]);
+                    if (LAYER) acc[e] += mix[j][e];
                 }
+                if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8(acc));
             }
             // D2 buffer b and the stage have been read: release them
             tc::tc_fence_before();
@@ -408,7 +404,8 @@ __global__ void __launch_bounds__(320, 1)
             }
         }
         if (!ok) *abort_v = 1;
-        // dW partial of this split: D1 rows are the 128 k of the slice
+        // dW partial of this split: D1 rows are the 128 k of the slice; the
+        // chunk-0 warps write it
         const bool krow = c0 + (r % CW) < C;  // dW row exists
         if (ok && h == 0 && tc::mbar_wait(&d1full, 0, a.fault, tc::kFaultTimeoutAcc)) {
             tc::tc_fence_after();
@@ -446,10 +443,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
             }
         }
-        if (LAYER && lane < 8) {
-#pragma unroll
-            for (int u = 0; u < HC / 8; ++u) bias_red[q][h * HC + u * 8 + lane] = bias_acc[u];
-        }
+        if (LAYER && lane < 8) bias_red[q][h * 8 + lane] = bias_acc;
     }
     tc::tc_fence_before();
     __syncthreads();
