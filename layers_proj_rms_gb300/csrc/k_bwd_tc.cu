@@ -21,7 +21,9 @@
 //   MMA 2 (dW):      D1[k][o'] += sum_t x[t][k] du_hl[t][o'], M = 128 k,
 //          N = 2*O, K = tokens; hi and lo columns of D1 are summed at the end.
 //          Both operands are read MN-major straight from the TMA tiles.
-//   epilogue: D2 + the elementwise terms -> dx (bf16); dbias column sums.
+//   MMA 3 (n = 4, dbias): D3[k][o'] += sum_t dout[t][k] du_hl[t][o'] with
+//          H_post hi | lo stored in du_hl columns [2O, 2O+2n)
+//   epilogue: D2 + the elementwise terms -> dx (bf16).
 // D2 is double-buffered in TMEM so the next tile's MMAs overlap the
 // epilogue; D1 accumulates over the whole token range and is written as this
 // split's dW partial.  For n = 4 the producer also stages dout and dy through
@@ -68,6 +70,9 @@ struct BwdTc {
     static constexpr int W_PLANE_BYTES = 128 * 128;
     static constexpr int W_BYTES = W_PLANES * W_PLANE_BYTES;
     static constexpr int D2_COL = 0, D1_COL = 256;      // D2 buffers at 0 and 128
+    // n = 4: dbias on the tensor cores, D3[k][o'] += sum_t dout[t][k] du_hl[t][o'];
+    // columns 2O+i (hi) and 2O+N+i (lo) of du_hl hold H_post[t][i]
+    static constexpr int D3_COL = 320, D3_N = 64;
     static constexpr int TMEM_COLS = 512;
     static constexpr int SMEM = STAGES * STAGE + W_BYTES + 1024;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
@@ -270,6 +275,19 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES, 1024, tc::kSwz128);
                     tc::mma_bf16(tmem + P::D1_COL, ad, bd, idesc_dw, (i > 0 || ks > 0) ? 1u : 0u);
                 }
+                if (SG) {
+                    // dbias: dout^T [du_hl | H_post hi | H_post lo] over the tile
+                    constexpr uint32_t idesc_db = tc::idesc_bf16_f32(128, P::D3_N, 1, 1);
+#pragma unroll
+                    for (int ks = 0; ks < P::TT / 16; ++ks) {
+                        const uint64_t ad = tc::make_desc(xs + P::G_OFF + ks * 16 * P::XROW,
+                                                          P::XBOX, 8 * P::XROW, P::XSWZ);
+                        const uint64_t bd = tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES,
+                                                          1024, tc::kSwz128);
+                        tc::mma_bf16(tmem + P::D3_COL, ad, bd, idesc_db,
+                                     (i > 0 || ks > 0) ? 1u : 0u);
+                    }
+                }
                 // dx accumulator b must have been drained by the epilogue (tile i-2)
                 if (i >= 2 &&
                     !tc::mbar_wait(&d2empty[b], ((i >> 1) - 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
@@ -379,21 +397,32 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) mix[j][e] = fmaf(hres[j * N + ii], dv[e], mix[j][e]);
                 }
-                bias_acc += warp_column_sum<8>(df);
+                if (!SG) bias_acc += warp_column_sum<8>(df);
             }
+            // dx_gemm of this chunk for every stream: all TMEM loads, one wait
+            constexpr int JB = N == 4 ? 4 : 2;  // streams per batch of TMEM loads
 #pragma unroll
-            for (int j = 0; j < N; ++j) {
-                float acc[8];
-                tc::tmem_ld8(trow + P::D2_COL + b * 128 + j * CW + h * 8, acc);
-                float xv[8];
-                unpack8(box_chunk<N>(st + j * P::XBOX, r, h), xv);
+            for (int j0 = 0; j0 < N; j0 += JB) {
+                float acc[JB][8];
+#pragma unroll
+                for (int jj = 0; jj < JB; ++jj)
+                    tc::tmem_ld8(trow + P::D2_COL + b * 128 + (j0 + jj) * CW + h * 8, acc[jj]);
+                uint4 xr[JB];
+#pragma unroll
+                for (int jj = 0; jj < JB; ++jj) xr[jj] = box_chunk<N>(st + (j0 + jj) * P::XBOX, r, h);
                 tc::tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    acc[e] = fmaf(coef, xv[e], acc[e]);
-                    if (LAYER) acc[e] += mix[j][e];
+                for (int jj = 0; jj < JB; ++jj) {
+                    const int j = j0 + jj;
+                    float xv[8];
+                    unpack8(xr[jj], xv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        acc[jj][e] = fmaf(coef, xv[e], acc[jj][e]);
+                        if (LAYER) acc[jj][e] += mix[j][e];
+                    }
+                    if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8(acc[jj]));
                 }
-                if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8(acc));
             }
             // D2 buffer b and the stage have been read: release them
             tc::tc_fence_before();
@@ -443,7 +472,21 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 }
             }
         }
-        if (LAYER && lane < 8) bias_red[q][h * 8 + lane] = bias_acc;
+        if (LAYER && !SG && lane < 8) bias_red[q][h * 8 + lane] = bias_acc;
+        if (SG && h == 0) {
+            // D3 row r is k = stream q, channel lane: its dbias term is the
+            // stream's H_post column pair
+            float v = 0.f;
+            if (ok) {
+                float d3[16];
+                tc::tmem_ld16(trow + P::D3_COL + 2 * O, d3);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < N; ++e)
+                    if (e == q) v = d3[e] + d3[N + e];
+            }
+            bias_red[q][lane] = v;
+        }
     }
     tc::tc_fence_before();
     __syncthreads();

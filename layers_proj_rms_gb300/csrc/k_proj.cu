@@ -155,8 +155,14 @@ __global__ void __launch_bounds__(128)
             put(2 * N + i * N + j, a2 * r * g[j]);
             dzt[2 * N + i * N + j] = g[j];
         }
+        // columns [2O, 2O+2N): H_post[i] as bf16 hi | lo (the dbias MMA of the
+        // residual-gradient pass reads them), then zeros
+        const float hp = 2.0f * so;
+        const bf16 hph = __float2bfloat16_rn(hp);
+        dut[2 * O + i] = hph;
+        dut[2 * O + N + i] = __float2bfloat16_rn(hp - __bfloat162float(hph));
         if (i == 0)
-            for (int o = 2 * O; o < du_cols; ++o) dut[o] = __float2bfloat16_rn(0.f);
+            for (int o = 2 * O + 2 * N; o < du_cols; ++o) dut[o] = __float2bfloat16_rn(0.f);
         if (i == 0) {
             ga[t * 4 + 0] = gpre * r;
             ga[t * 4 + 1] = gpost * r;
