@@ -9,7 +9,7 @@
 // N = 2*O gives x.W_hi and x.W_lo and their fp32 sum carries W to ~2^-17
 // relative error (x.W in fp32 semantics, well inside the 1e-5 bound on H).
 //
-// CTA: 128 tokens x one K split; 6 warps:
+// CTA: 128 tokens x one K split (K splits chosen for about two CTAs per SM); 6 warps:
 //   warp 0      TMA producer: x tile [128 x 64] and W_hl tile [2O x 64] per
 //               stage, both in the 128-byte swizzle layout
 //   warp 1      TMEM allocation, MMA issue (one thread), commits
@@ -31,7 +31,7 @@ struct ProjTc {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = NB * BK * 2;
     static constexpr int STAGE = A_BYTES + B_BYTES;  // multiple of 1024
-    static constexpr int STAGES = (N == 4) ? 6 : 5;
+    static constexpr int STAGES = (N == 4) ? 4 : 3;  // two CTAs per SM
     static constexpr int TMEM_COLS = NB <= 64 ? 64 : 256;
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
@@ -55,7 +55,7 @@ __global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, i
 }
 
 template <int N>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, 2)
     k_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
               float *__restrict__ upart, float *__restrict__ spart, int64_t T, int kb_per_split,
               int kb_total, int *fault)
@@ -254,7 +254,7 @@ int proj_tc_splits(int64_t T, int64_t K)
 {
     const int64_t mt = (T + 127) / 128;
     const int64_t kb = (K + 63) / 64;
-    int64_t s = kSplitSms / mt;
+    int64_t s = (2 * int64_t(kSplitSms)) / mt;  // about two CTAs per SM
     if (s < 1) s = 1;
     if (s > kb) s = kb;
     if (s > 32) s = 32;

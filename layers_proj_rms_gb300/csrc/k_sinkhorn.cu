@@ -92,9 +92,9 @@ cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n,
         MHC_PROF("k_sinkhorn_fwd", s);
         k_sinkhorn_fwd<4><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
     } else {
-            MHC_PROF("k_sinkhorn_fwd", s);
-            k_sinkhorn_fwd<8><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
-        }
+        MHC_PROF("k_sinkhorn_fwd", s);
+        k_sinkhorn_fwd<8><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
+    }
     return cudaGetLastError();
 }
 

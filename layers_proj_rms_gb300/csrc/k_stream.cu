@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------------------
 // h_aggregate backward: dx[t][i][c] = H_pre[t][i] dy[t][c] (if dx != null),
-// dH_pre[t][i] = sum_c dy[t][c] x[t][i][c].  One warp per token.
+// dH_pre[t][i] = sum_c dy[t][c] x[t][i][c].  One warp per token; each lane
+// keeps U chunks of 8 channels (with all n streams) in flight.
 // ---------------------------------------------------------------------------
 template <int N>
 __global__ void __launch_bounds__(256)
@@ -75,6 +76,7 @@ __global__ void __launch_bounds__(256)
               const float *__restrict__ Hpre, bf16 *__restrict__ dx, float *__restrict__ dHpre,
               int64_t T, int64_t C8)
 {
+    constexpr int U = N == 4 ? 4 : 2;
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
     for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
@@ -85,23 +87,37 @@ __global__ void __launch_bounds__(256)
             h[i] = __ldg(Hpre + t * N + i);
             part[i] = 0.f;
         }
-        for (int64_t c8 = lane; c8 < C8; c8 += 32) {
-            float g[8];
-            unpack8(ld_stream(dy + (t * C8 + c8) * 8), g);
+        for (int64_t base = lane; base < C8; base += 32 * U) {
+            uint4 gv[U], xv[U][N];
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-                float v[8];
-                const int64_t off = ((t * N + i) * C8 + c8) * 8;
-                unpack8(ld_stream(x + off), v);
-                float acc = 0.f;
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 < C8) {
+                    gv[u] = ld_stream(dy + (t * C8 + c8) * 8);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc = fmaf(g[e], v[e], acc);
-                part[i] += acc;
-                if (dx) {
-                    float o[8];
+                    for (int i = 0; i < N; ++i) xv[u][i] = ld_stream(x + ((t * N + i) * C8 + c8) * 8);
+                }
+            }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = h[i] * g[e];
-                    st_stream(dx + off, pack8(o));
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 >= C8) continue;
+                float g[8];
+                unpack8(gv[u], g);
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    float v[8];
+                    unpack8(xv[u][i], v);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(g[e], v[e], acc);
+                    part[i] += acc;
+                    if (dx) {
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) o[e] = h[i] * g[e];
+                        st_stream(dx + ((t * N + i) * C8 + c8) * 8, pack8(o));
+                    }
                 }
             }
         }
@@ -116,6 +132,7 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // h_post_bda forward:
 //   out[t][i][c] = sum_j H_res[t][j][i] res[t][j][c] + H_post[t][i] (f[t][c] + bias[c])
+// One warp per token; each lane keeps U chunks of 8 channels in flight.
 // ---------------------------------------------------------------------------
 template <int N>
 __global__ void __launch_bounds__(256)
@@ -123,39 +140,60 @@ __global__ void __launch_bounds__(256)
                const bf16 *__restrict__ bias, const float *__restrict__ Hres,
                const float *__restrict__ Hpost, bf16 *__restrict__ out, int64_t T, int64_t C8)
 {
-    __shared__ float hs[N * N + N];
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        __syncthreads();
-        for (int e = threadIdx.x; e < N * N + N; e += blockDim.x)
-            hs[e] = e < N * N ? __ldg(Hres + t * N * N + e) : __ldg(Hpost + t * N + e - N * N);
-        __syncthreads();
-        for (int64_t c8 = threadIdx.x; c8 < C8; c8 += blockDim.x) {
-            float fb[8];
-            unpack8(ld_stream(f + (t * C8 + c8) * 8), fb);
-            if (bias) {
-                float bv[8];
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8)), bv);
+    constexpr int U = N == 4 ? 2 : 1;
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        float hr[N * N], hp[N];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) fb[e] += bv[e];
+        for (int e = 0; e < N * N; e += 4) {
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(Hres + t * N * N + e));
+            hr[e] = v.x;
+            hr[e + 1] = v.y;
+            hr[e + 2] = v.z;
+            hr[e + 3] = v.w;
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) hp[i] = __ldg(Hpost + t * N + i);
+        for (int64_t base = lane; base < C8; base += 32 * U) {
+            uint4 fv[U], bv[U], xr[U][N];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 < C8) {
+                    fv[u] = ld_stream(f + (t * C8 + c8) * 8);
+                    bv[u] = bias ? __ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8))
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < N; ++j) xr[u][j] = ld_stream(res + ((t * N + j) * C8 + c8) * 8);
+                }
             }
-            uint4 xr[N];
 #pragma unroll
-            for (int j = 0; j < N; ++j) xr[j] = ld_stream(res + ((t * N + j) * C8 + c8) * 8);
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 >= C8) continue;
+                float fb[8], bb[8];
+                unpack8(fv[u], fb);
+                unpack8(bv[u], bb);
 #pragma unroll
-            for (int i = 0; i < N; ++i) {
-                float acc[8];
-                const float hp = hs[N * N + i];
+                for (int e = 0; e < 8; ++e) fb[e] += bb[e];
+                float acc[N][8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = hp * fb[e];
+                for (int i = 0; i < N; ++i)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[i][e] = hp[i] * fb[e];
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
                     float v[8];
-                    unpack8(xr[j], v);
-                    const float w = hs[j * N + i];
+                    unpack8(xr[u][j], v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+                    for (int i = 0; i < N; ++i)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(hr[j * N + i], v[e], acc[i][e]);
                 }
-                st_stream(out + ((t * N + i) * C8 + c8) * 8, pack8(acc));
+#pragma unroll
+                for (int i = 0; i < N; ++i) st_stream(out + ((t * N + i) * C8 + c8) * 8, pack8(acc[i]));
             }
         }
     }
@@ -324,9 +362,9 @@ cudaError_t launch_dbias(const bf16 *dout, const float *Hpost, float *dbias, int
         MHC_PROF("k_dbias_partial", s);
         k_dbias_partial<4><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
     } else {
-            MHC_PROF("k_dbias_partial", s);
-            k_dbias_partial<8><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
-        }
+        MHC_PROF("k_dbias_partial", s);
+        k_dbias_partial<8><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
+    }
     {
         MHC_PROF("k_sum_rows", s);
         k_sum_rows<<<unsigned((C + 255) / 256), 256, 0, s>>>(part, dbias, splits, C);
@@ -351,6 +389,108 @@ __device__ __forceinline__ float block_sum(float v, float *red)
     const int nw = blockDim.x >> 5;
     for (int i = 0; i < nw; ++i) r += red[i];
     return r;
+}
+
+// Rows of at most 32*R chunks: one warp per row, the row in registers.
+template <int R>
+__global__ void __launch_bounds__(256)
+    k_rms_fwd_w(const bf16 *__restrict__ x, bf16 *__restrict__ y, float *__restrict__ rstd,
+                int64_t rows, int64_t C8, float inv_cols, float eps)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        uint4 v[R];
+        float s = 0.f;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) v[q] = ld_stream(x + (r * C8 + c8) * 8);
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) {
+                float f[8];
+                unpack8(v[q], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+            }
+        }
+        s = warp_sum(s);
+        const float rho = rsqrtf(s * inv_cols + eps);
+        if (rstd && lane == 0) rstd[r] = rho;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) {
+                float f[8];
+                unpack8(v[q], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] *= rho;
+                st_stream(y + (r * C8 + c8) * 8, pack8(f));
+            }
+        }
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(256)
+    k_rms_bwd_w(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
+                const float *__restrict__ rstd, bf16 *__restrict__ dx, int64_t rows, int64_t C8,
+                float inv_cols, float eps)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+         r += warps) {
+        uint4 vx[R], vg[R];
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) {
+                vx[q] = ld_stream(x + (r * C8 + c8) * 8);
+                vg[q] = ld_stream(dy + (r * C8 + c8) * 8);
+            }
+        }
+        float d = 0.f, s = 0.f;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) {
+                float a[8], g[8];
+                unpack8(vx[q], a);
+                unpack8(vg[q], g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    d = fmaf(g[e], a[e], d);
+                    s = fmaf(a[e], a[e], s);
+                }
+            }
+        }
+        d = warp_sum(d);
+        float rho;
+        if (rstd) {
+            rho = __ldg(rstd + r);
+        } else {
+            s = warp_sum(s);
+            rho = rsqrtf(s * inv_cols + eps);
+        }
+        const float k2 = rho * rho * rho * d * inv_cols;
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+            const int64_t c8 = lane + 32 * q;
+            if (c8 < C8) {
+                float a[8], g[8], o[8];
+                unpack8(vx[q], a);
+                unpack8(vg[q], g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = rho * g[e] - k2 * a[e];
+                st_stream(dx + (r * C8 + c8) * 8, pack8(o));
+            }
+        }
+    }
 }
 
 template <int R>
@@ -453,9 +593,9 @@ cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int6
         MHC_PROF("k_agg_fwd", s);
         k_agg_fwd<4><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
     } else {
-            MHC_PROF("k_agg_fwd", s);
-            k_agg_fwd<8><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
-        }
+        MHC_PROF("k_agg_fwd", s);
+        k_agg_fwd<8><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+    }
     return cudaGetLastError();
 }
 
@@ -468,9 +608,9 @@ cudaError_t launch_aggregate_bwd(const bf16 *dy, const bf16 *x, const float *Hpr
         MHC_PROF("k_agg_bwd", s);
         k_agg_bwd<4><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
     } else {
-            MHC_PROF("k_agg_bwd", s);
-            k_agg_bwd<8><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
-        }
+        MHC_PROF("k_agg_bwd", s);
+        k_agg_bwd<8><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
+    }
     return cudaGetLastError();
 }
 
@@ -479,15 +619,14 @@ cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, co
                             cudaStream_t s)
 {
     const int64_t C8 = C / 8;
-    const unsigned g = grid_for(T, 8);
-    const int th = threads_for(C8);
+    const unsigned g = grid_for((T + 7) / 8, 8);
     if (n == 4) {
         MHC_PROF("k_post_fwd", s);
-        k_post_fwd<4><<<g, th, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+        k_post_fwd<4><<<g, 256, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
     } else {
-            MHC_PROF("k_post_fwd", s);
-            k_post_fwd<8><<<g, th, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
-        }
+        MHC_PROF("k_post_fwd", s);
+        k_post_fwd<8><<<g, 256, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+    }
     return cudaGetLastError();
 }
 
@@ -503,10 +642,10 @@ cudaError_t launch_post_bwd_tok(const bf16 *dout, const bf16 *res, const bf16 *f
         k_post_bwd_tok<4><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
                                             dHpost, T, C8);
     } else {
-            MHC_PROF("k_post_bwd_tok", s);
-            k_post_bwd_tok<8><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
-                                                dHpost, T, C8);
-        }
+        MHC_PROF("k_post_bwd_tok", s);
+        k_post_bwd_tok<8><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
+                                            dHpost, T, C8);
+    }
     return cudaGetLastError();
 }
 
@@ -522,16 +661,29 @@ cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, in
                            float eps, cudaStream_t s)
 {
     const int64_t C8 = cols / 8;
-    const unsigned g = grid_for(rows, 8);
-    const int th = threads_for((C8 + 3) / 4);
     const float ic = 1.0f / float(cols);
+    if (C8 <= 32 * 16) {
+        const unsigned g = grid_for((rows + 7) / 8, 8);
+        if (C8 <= 32 * 4) {
+            MHC_PROF("k_rms_fwd", s);
+            k_rms_fwd_w<4><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        } else if (C8 <= 32 * 8) {
+            MHC_PROF("k_rms_fwd", s);
+            k_rms_fwd_w<8><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        } else {
+            MHC_PROF("k_rms_fwd", s);
+            k_rms_fwd_w<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        }
+        return cudaGetLastError();
+    }
+    const unsigned g = grid_for(rows, 8);
     if (rms_R(C8) == 4) {
         MHC_PROF("k_rms_fwd", s);
-        k_rms_fwd<4><<<g, th, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        k_rms_fwd<4><<<g, threads_for((C8 + 3) / 4), 0, s>>>(x, y, rstd, rows, C8, ic, eps);
     } else {
-            MHC_PROF("k_rms_fwd", s);
-            k_rms_fwd<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
-        }
+        MHC_PROF("k_rms_fwd", s);
+        k_rms_fwd<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+    }
     return cudaGetLastError();
 }
 
@@ -539,16 +691,29 @@ cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf1
                            int64_t rows, int64_t cols, float eps, cudaStream_t s)
 {
     const int64_t C8 = cols / 8;
-    const unsigned g = grid_for(rows, 8);
-    const int th = threads_for((C8 + 3) / 4);
     const float ic = 1.0f / float(cols);
+    if (C8 <= 32 * 16) {
+        const unsigned g = grid_for((rows + 7) / 8, 8);
+        if (C8 <= 32 * 4) {
+            MHC_PROF("k_rms_bwd", s);
+            k_rms_bwd_w<4><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        } else if (C8 <= 32 * 8) {
+            MHC_PROF("k_rms_bwd", s);
+            k_rms_bwd_w<8><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        } else {
+            MHC_PROF("k_rms_bwd", s);
+            k_rms_bwd_w<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        }
+        return cudaGetLastError();
+    }
+    const unsigned g = grid_for(rows, 8);
     if (rms_R(C8) == 4) {
         MHC_PROF("k_rms_bwd", s);
-        k_rms_bwd<4><<<g, th, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        k_rms_bwd<4><<<g, threads_for((C8 + 3) / 4), 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
     } else {
-            MHC_PROF("k_rms_bwd", s);
-            k_rms_bwd<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
-        }
+        MHC_PROF("k_rms_bwd", s);
+        k_rms_bwd<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+    }
     return cudaGetLastError();
 }
 
