@@ -64,6 +64,18 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v)
                  : "memory");
 }
 
+// 16-byte load from shared memory by 32-bit shared address (an explicit
+// ld.shared; a generic pointer derived by integer arithmetic would go
+// through the generic path).
+__device__ __forceinline__ uint4 lds128(uint32_t saddr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(saddr));
+    return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

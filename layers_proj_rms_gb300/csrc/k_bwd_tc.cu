@@ -152,7 +152,7 @@ __device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
 {
     constexpr int XROW = BwdTc<N>::XROW;
     const int phys = N == 4 ? (chunk ^ ((r >> 1) & 3)) : (chunk ^ ((r >> 2) & 1));
-    return *reinterpret_cast<const uint4 *>(box + r * XROW + phys * 16);
+    return lds128(tc::smem_u32(box) + r * XROW + phys * 16);
 }
 
 template <int N, bool LAYER>

@@ -158,11 +158,11 @@ __global__ void __launch_bounds__(192, 2)
             // lane: rows that share banks (r and r+8, r+16, ...) then read
             // different chunks, so a warp's loads are free of bank conflicts.
             // The sum of squares does not depend on the order.
-            const uint4 *row = reinterpret_cast<const uint4 *>(smem + s * P::STAGE + r * 128);
+            const uint32_t row = tc::smem_u32(smem + s * P::STAGE + r * 128);
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 float f[8];
-                unpack8(row[c ^ (lane & 7)], f);
+                unpack8(lds128(row + (c ^ (lane & 7)) * 16), f);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
             }
