@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256)
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C)
 {
     const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * C;
-    const int64_t S = proj_tc_splits(T, K);
+    const int64_t S = proj_tc_splits(T, n, K);
     return ws_align(size_t(2 * O * K) * 2) + ws_align(size_t(S * T * O) * 4) +
            ws_align(size_t(S * T) * 4);
 }
@@ -224,7 +224,7 @@ static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alp
 {
     constexpr int O = Dims<N>::O;
     const int64_t K = int64_t(N) * C;
-    const int64_t S = proj_tc_splits(T, K);
+    const int64_t S = proj_tc_splits(T, N, K);
     char *p = static_cast<char *>(ws);
     bf16 *Whl = reinterpret_cast<bf16 *>(p);
     p += ws_align(size_t(2 * O * K) * 2);

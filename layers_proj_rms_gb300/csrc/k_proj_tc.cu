@@ -23,19 +23,28 @@
 
 namespace mhc {
 
-template <int N>
-struct ProjTc {
+// A stage holds KBS consecutive 64-wide k-blocks (KBS boxes issued back to
+// back, so each token row is read in KBS*128 contiguous bytes); STG stages;
+// MINB CTAs per SM.
+template <int N, int KBS_, int STG_, int MINB_>
+struct ProjTcCfg {
     static constexpr int O = N * N + 2 * N;
     static constexpr int NB = 2 * O;  // MMA N: hi rows then lo rows (48 or 160)
-    static constexpr int BM = 128, BK = 64;
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = NB * BK * 2;
-    static constexpr int STAGE = A_BYTES + B_BYTES;  // multiple of 1024
-    static constexpr int STAGES = (N == 4) ? 4 : 3;  // two CTAs per SM
+    static constexpr int BM = 128, BK = 64, KBS = KBS_, STAGES = STG_, MINB = MINB_;
+    static constexpr int A_SUB = BM * BK * 2;
+    static constexpr int B_SUB = NB * BK * 2;
+    static constexpr int A_BYTES = KBS * A_SUB;
+    static constexpr int STAGE = KBS * (A_SUB + B_SUB);  // multiple of 1024
     static constexpr int TMEM_COLS = NB <= 64 ? 64 : 256;
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
-    static_assert(STAGE % 1024 == 0, "stage must keep 1024-byte alignment");
+    static_assert(A_SUB % 1024 == 0 && B_SUB % 1024 == 0, "sub-tiles keep 1024-byte alignment");
+    static_assert(SMEM * MINB <= 232448, "shared memory");
 };
+template <int N> struct ProjTcSel;
+template <> struct ProjTcSel<4> { using type = ProjTcCfg<4, 1, 4, 2>; };
+template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 2, 2, 1>; };
+template <int N>
+using ProjTc = typename ProjTcSel<N>::type;
 
 // W [K][O] fp32 -> W_hl [2O][K] bf16 (rows o: bf16(W[:,o]); rows O+o: the remainder)
 template <int N>
@@ -54,13 +63,12 @@ __global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, i
     }
 }
 
-template <int N>
-__global__ void __launch_bounds__(192, 2)
+template <int N, class P>
+__global__ void __launch_bounds__(192, P::MINB)
     k_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
               float *__restrict__ upart, float *__restrict__ spart, int64_t T, int kb_per_split,
               int kb_total, int *fault)
 {
-    using P = ProjTc<N>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -73,9 +81,9 @@ __global__ void __launch_bounds__(192, 2)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t m0 = int64_t(blockIdx.x) * P::BM;
     const int split = blockIdx.y;
-    const int kb0 = split * kb_per_split;
+    const int kb0 = split * kb_per_split;  // kb_per_split is a multiple of KBS
     const int kb1 = min(kb_total, kb0 + kb_per_split);
-    const int nkb = kb1 - kb0;
+    const int nkb = (kb1 - kb0 + P::KBS - 1) / P::KBS;  // stages; a partial last one reads zeros
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
@@ -107,8 +115,12 @@ __global__ void __launch_bounds__(192, 2)
                 }
                 uint8_t *st = smem + s * P::STAGE;
                 tc::mbar_arrive_expect_tx(&full[s], P::STAGE);
-                tc::tma_load_2d(st, &tmx, (kb0 + i) * P::BK, int(m0), &full[s]);
-                tc::tma_load_2d(st + P::A_BYTES, &tmw, (kb0 + i) * P::BK, 0, &full[s]);
+                for (int j = 0; j < P::KBS; ++j)
+                    tc::tma_load_2d(st + j * P::A_SUB, &tmx, (kb0 + i * P::KBS + j) * P::BK,
+                                    int(m0), &full[s]);
+                for (int j = 0; j < P::KBS; ++j)
+                    tc::tma_load_2d(st + P::A_BYTES + j * P::B_SUB, &tmw,
+                                    (kb0 + i * P::KBS + j) * P::BK, 0, &full[s]);
                 issued = i + 1;
             }
             // do not leave while copies into this CTA's shared memory are in flight
@@ -127,13 +139,16 @@ __global__ void __launch_bounds__(192, 2)
                     break;
                 }
                 tc::tc_fence_after();
-                const uint32_t a = tc::smem_u32(smem + s * P::STAGE);
-                const uint32_t b = a + P::A_BYTES;
+                const uint32_t a0 = tc::smem_u32(smem + s * P::STAGE);
 #pragma unroll
-                for (int kk = 0; kk < P::BK / 16; ++kk)
-                    tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
-                                 tc::desc_kmajor_sw128(b + kk * 32), idesc,
-                                 (i > 0 || kk > 0) ? 1u : 0u);
+                for (int j = 0; j < P::KBS; ++j) {
+                    const uint32_t a = a0 + j * P::A_SUB, b = a0 + P::A_BYTES + j * P::B_SUB;
+#pragma unroll
+                    for (int kk = 0; kk < P::BK / 16; ++kk)
+                        tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
+                                     tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                                     (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc::mma_commit(&empty[s]);
             }
             tc::mma_commit(acc_bar);
@@ -158,13 +173,16 @@ __global__ void __launch_bounds__(192, 2)
             // lane: rows that share banks (r and r+8, r+16, ...) then read
             // different chunks, so a warp's loads are free of bank conflicts.
             // The sum of squares does not depend on the order.
-            const uint32_t row = tc::smem_u32(smem + s * P::STAGE + r * 128);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float f[8];
-                unpack8(lds128(row + (c ^ (lane & 7)) * 16), f);
+            for (int j = 0; j < P::KBS; ++j) {
+                const uint32_t row = tc::smem_u32(smem + s * P::STAGE + j * P::A_SUB + r * 128);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
+                for (int c = 0; c < 8; ++c) {
+                    float f[8];
+                    unpack8(lds128(row + (c ^ (lane & 7)) * 16), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
+                }
             }
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&empty[s]);
@@ -250,22 +268,30 @@ static bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int proj_tc_splits(int64_t T, int64_t K)
+int proj_tc_splits(int64_t T, int n, int64_t K)
 {
     const int64_t mt = (T + 127) / 128;
     const int64_t kb = (K + 63) / 64;
-    int64_t s = (2 * int64_t(kSplitSms)) / mt;  // about two CTAs per SM
+    const int minb = n == 4 ? ProjTc<4>::MINB : ProjTc<8>::MINB;
+    int64_t s = (int64_t(kSplitSms) * minb) / mt;  // about MINB CTAs per SM
     if (s < 1) s = 1;
     if (s > kb) s = kb;
     if (s > 32) s = 32;
     return int(s);
 }
 
-template <int N>
+// k-blocks per split, a multiple of the k-blocks per stage
+static int proj_tc_kps(int64_t K, int S, int kbs)
+{
+    const int kb_total = int((K + 63) / 64);
+    int kps = (kb_total + S - 1) / S;
+    return (kps + kbs - 1) / kbs * kbs;
+}
+
+template <int N, class P>
 static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_t C, bf16 *Whl,
                                 float *upart, float *spart, int S, int *fault, cudaStream_t s)
 {
-    using P = ProjTc<N>;
     const int64_t K = int64_t(N) * C;
     {
         MHC_PROF("k_w_split", s);
@@ -277,16 +303,16 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
         !make_map_bf16(&tmw, Whl, uint64_t(P::NB), uint64_t(K), P::NB, P::BK,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_proj_tc<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         P::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_proj_tc<N, P>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
     if (e != cudaSuccess) return e;
     const int kb_total = int((K + P::BK - 1) / P::BK);
-    const int kps = (kb_total + S - 1) / S;
+    const int kps = proj_tc_kps(K, S, P::KBS);
     const int S_used = (kb_total + kps - 1) / kps;
     dim3 grid(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used));
     {
         MHC_PROF("k_proj_tc", s);
-        k_proj_tc<N><<<grid, 192, P::SMEM, s>>>(tmx, tmw, upart, spart, T, kps, kb_total, fault);
+        k_proj_tc<N, P><<<grid, 192, P::SMEM, s>>>(tmx, tmw, upart, spart, T, kps, kb_total, fault);
     }
     return cudaGetLastError();
 }
@@ -297,12 +323,12 @@ cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n
                                  int *fault, cudaStream_t s)
 {
     const int64_t K = int64_t(n) * C;
-    const int S = proj_tc_splits(T, K);
+    const int S = proj_tc_splits(T, n, K);
     const int kb_total = int((K + 63) / 64);
-    const int kps = (kb_total + S - 1) / S;
+    const int kps = proj_tc_kps(K, S, n == 4 ? ProjTc<4>::KBS : ProjTc<8>::KBS);
     *splits_used = (kb_total + kps - 1) / kps;
-    if (n == 4) return proj_tc_impl<4>(x, W, T, C, Whl, upart, spart, S, fault, s);
-    return proj_tc_impl<8>(x, W, T, C, Whl, upart, spart, S, fault, s);
+    if (n == 4) return proj_tc_impl<4, ProjTc<4>>(x, W, T, C, Whl, upart, spart, S, fault, s);
+    return proj_tc_impl<8, ProjTc<8>>(x, W, T, C, Whl, upart, spart, S, fault, s);
 }
 
 }  // namespace mhc

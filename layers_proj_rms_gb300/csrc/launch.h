@@ -67,7 +67,7 @@ cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf1
                            int64_t rows, int64_t cols, float eps, cudaStream_t s);
 
 // k_proj_tc.cu: tensor-core projection partials of the forward
-int proj_tc_splits(int64_t T, int64_t K);
+int proj_tc_splits(int64_t T, int n, int64_t K);
 cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n, int64_t C,
                                  bf16 *Whl, float *upart, float *spart, int *splits_used,
                                  int *fault, cudaStream_t s);
