@@ -80,38 +80,6 @@ struct BwdTc {
     static_assert(SMEM <= 232448, "shared memory");
 };
 
-// W [K][O] fp32 -> Wd [planes][K][64] bf16 with row k = [W_hi | W_hi | W_lo | 0],
-// W_hi = bf16(W), W_lo = bf16(W - W_hi).
-template <int N>
-__global__ void k_w_planes(const float *__restrict__ W, bf16 *__restrict__ Wd, int64_t K)
-{
-    using P = BwdTc<N>;
-    constexpr int O = P::O;
-    const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (k >= K) return;
-    for (int p = 0; p < P::W_PLANES; ++p)
-        for (int pc = 0; pc < 64; pc += 8) {
-            uint16_t hbits[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int c = p * 64 + pc + e;
-                bf16 v = __float2bfloat16_rn(0.f);
-                if (c < 3 * O) {
-                    const float w = __ldg(W + k * O + (c % O));
-                    const bf16 hi = __float2bfloat16_rn(w);
-                    v = c < 2 * O ? hi : __float2bfloat16_rn(w - __bfloat162float(hi));
-                }
-                hbits[e] = *reinterpret_cast<uint16_t *>(&v);
-            }
-            uint4 q;
-            q.x = hbits[0] | (uint32_t(hbits[1]) << 16);
-            q.y = hbits[2] | (uint32_t(hbits[3]) << 16);
-            q.z = hbits[4] | (uint32_t(hbits[5]) << 16);
-            q.w = hbits[6] | (uint32_t(hbits[7]) << 16);
-            *reinterpret_cast<uint4 *>(Wd + (int64_t(p) * K + k) * 64 + pc) = q;
-        }
-}
-
 // Column sums over the 32 lanes of a warp: on entry every lane holds COLS
 // values, on exit lane l holds the warp total of column (l % COLS).
 template <int COLS>
@@ -135,6 +103,7 @@ __device__ __forceinline__ float warp_column_sum(float (&v)[COLS])
 }
 
 struct BwdTcArgs {
+    const float *W;    // [K][O] fp32
     const bf16 *dout, *dy;
     const float *coef, *Hpre, *Hres, *Hpost;
     bf16 *dx;
@@ -158,7 +127,7 @@ __device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
 template <int N, bool LAYER>
 __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmdu,
-             const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmg,
+             const __grid_constant__ CUtensorMap tmg,
              const __grid_constant__ CUtensorMap tmy, const BwdTcArgs a)
 {
     using P = BwdTc<N>;
@@ -189,7 +158,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
         }
-        tc::mbar_init(&wfull, 1);
+        tc::mbar_init(&wfull, P::EPI_WARPS);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&d2full[b], 1);
             tc::mbar_init(&d2empty[b], P::EPI_WARPS);
@@ -209,16 +178,10 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmx);
             tc::tma_prefetch_desc(&tmdu);
-            tc::tma_prefetch_desc(&tmw);
             if (SG) {
                 tc::tma_prefetch_desc(&tmg);
                 tc::tma_prefetch_desc(&tmy);
             }
-            tc::mbar_arrive_expect_tx(&wfull, P::W_BYTES);
-            for (int p = 0; p < P::W_PLANES; ++p)
-                for (int j = 0; j < N; ++j)
-                    tc::tma_load_2d(wtile + p * P::W_PLANE_BYTES + j * CW * 128, &tmw, 0,
-                                    int(int64_t(p) * K + int64_t(j) * C + c0), &wfull);
             int issued = 0;
             for (int i = 0; i < ntiles && !*abort_v; ++i) {
                 const int s = i % P::STAGES;
@@ -244,7 +207,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 }
                 issued = i + 1;
             }
-            tc::mbar_wait(&wfull, 0, a.fault, tc::kFaultTimeoutMisc);
             for (int i = max(0, issued - P::STAGES); i < issued; ++i)
                 tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
                               tc::kFaultTimeoutMisc);
@@ -318,6 +280,37 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
+        // The W tile of this slice, [W_hi | W_hi | W_lo | 0] per k row in
+        // 64-column planes, written in the 128-byte swizzled K-major layout
+        // of the MMA B operand (16-byte chunk q of row rr at rr*128 +
+        // ((q ^ (rr % 8)) * 16)); rows past C are zero.
+        for (int idx = threadIdx.x - 64; idx < P::W_PLANES * 128 * 8; idx += 32 * P::EPI_WARPS) {
+            const int p = idx >> 10, rr = (idx >> 3) & 127, qc = idx & 7;
+            const int col = p * 64 + qc * 8;
+            const int64_t cw = c0 + rr % CW;
+            float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (col < 3 * O && cw < C) {
+                const float4 *src = reinterpret_cast<const float4 *>(
+                    a.W + (int64_t(rr / CW) * C + cw) * O + col % O);
+                const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
+                w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+                if (col >= 2 * O)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        w[e] -= __bfloat162float(__float2bfloat16_rn(w[e]));
+            }
+            const uint4 v = pack8(w);
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                             tc::smem_u32(wtile + p * P::W_PLANE_BYTES + rr * 128 +
+                                          ((qc ^ (rr & 7)) << 4))),
+                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&wfull);
+
         const int q = warp & 3;              // TMEM lane quadrant
         const int h = (warp - 2) >> 2;       // this thread's 8-channel chunk of every stream
         const int r = q * 32 + lane;         // token row in the tile / k row of dW
@@ -531,13 +524,6 @@ static bool map2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols
 
 int bwd_tc_du_cols(int n) { return n == 4 ? BwdTc<4>::DU_COLS : BwdTc<8>::DU_COLS; }
 
-size_t bwd_tc_wb_bytes(int n, int64_t C)
-{
-    const int64_t K = int64_t(n) * C;
-    const int planes = n == 4 ? BwdTc<4>::W_PLANES : BwdTc<8>::W_PLANES;
-    return size_t(K) * planes * 64 * 2;
-}
-
 int bwd_tc_splits(int64_t T, int n, int64_t C)
 {
     const int64_t slices = (C + 128 / n - 1) / (128 / n);
@@ -550,21 +536,16 @@ int bwd_tc_splits(int64_t T, int n, int64_t C)
 }
 
 template <int N, bool LAYER>
-static cudaError_t bwd_tc_impl(const bf16 *x, const float *W, const bf16 *du_hl, bf16 *Wd,
-                               const BwdTcArgs &args, int splits, cudaStream_t s)
+static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs &args,
+                               int splits, cudaStream_t s)
 {
     using P = BwdTc<N>;
     const int64_t T = args.T, C = args.C, K = int64_t(N) * C;
-    {
-        MHC_PROF("k_w_planes", s);
-        k_w_planes<N><<<unsigned((K + 255) / 256), 256, 0, s>>>(W, Wd, K);
-    }
-    CUtensorMap tmx, tmdu, tmw, tmg, tmy;
+    CUtensorMap tmx, tmdu, tmg, tmy;
     const CUtensorMapSwizzle xsw = N == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!map2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
         !map2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
-               CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !map2d(&tmw, Wd, uint64_t(P::W_PLANES * K), 64, P::CW, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+               CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     tmg = tmx;
     tmy = tmx;
@@ -579,18 +560,19 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const float *W, const bf16 *du_hl,
     dim3 grid(unsigned((C + P::CW - 1) / P::CW), unsigned(splits));
     {
         MHC_PROF("k_bwd_tc", s);
-        k_bwd_tc<N, LAYER><<<grid, P::THREADS, P::SMEM, s>>>(tmx, tmdu, tmw, tmg, tmy, args);
+        k_bwd_tc<N, LAYER><<<grid, P::THREADS, P::SMEM, s>>>(tmx, tmdu, tmg, tmy, args);
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
-                          bf16 *Wd, int64_t T, int n, int64_t C, const bf16 *dout,
+                          int64_t T, int n, int64_t C, const bf16 *dout,
                           const bf16 *dy, const float *Hpre, const float *Hres,
                           const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
                           int splits, int *fault, cudaStream_t s)
 {
     BwdTcArgs a;
+    a.W = W;
     a.dout = dout;
     a.dy = dy;
     a.coef = coef;
@@ -607,10 +589,10 @@ cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, cons
     a.fault = fault;
     const bool layer = dout != nullptr;
     if (n == 4)
-        return layer ? bwd_tc_impl<4, true>(x, W, du_hl, Wd, a, splits, s)
-                     : bwd_tc_impl<4, false>(x, W, du_hl, Wd, a, splits, s);
-    return layer ? bwd_tc_impl<8, true>(x, W, du_hl, Wd, a, splits, s)
-                 : bwd_tc_impl<8, false>(x, W, du_hl, Wd, a, splits, s);
+        return layer ? bwd_tc_impl<4, true>(x, du_hl, a, splits, s)
+                     : bwd_tc_impl<4, false>(x, du_hl, a, splits, s);
+    return layer ? bwd_tc_impl<8, true>(x, du_hl, a, splits, s)
+                 : bwd_tc_impl<8, false>(x, du_hl, a, splits, s);
 }
 
 }  // namespace mhc

@@ -12,10 +12,12 @@
 // Forward:  k_proj_tc (k_proj_tc.cu: split-K partial u = x W and s = sum x^2
 //           on the tensor cores), k_compute_h_fwd (sum of partials, r, z,
 //           gates, Sinkhorn)
-// Backward: k_compute_h_bwd (per-token du as bf16 hi|lo, dz, dalpha terms,
-//           RMS coefficient), k_bwd_tc (k_bwd_tc.cu: du W^T + coef x [+ H_res
-//           dout + H_pre dy], dW and dbias partials on the tensor cores),
-//           fixed-order reductions for dW, dbias, dalpha, db.
+// Backward: k_compute_h_bwd (standalone op: per-token du as bf16 hi|lo, RMS
+//           coefficient, per-block sums of dz and the dalpha terms) or, in
+//           the layer, k_bwd_tok (k_bwd_tok.cu) for the same outputs; then
+//           k_bwd_tc (k_bwd_tc.cu: du W^T + coef x [+ H_res dout + H_pre dy],
+//           dW and dbias on the tensor cores) and k_bwd_finalize, the
+//           fixed-order sums for db, dalpha (and dW, dbias when split).
 #include "launch.h"
 #include "sinkhorn.cuh"
 
@@ -82,9 +84,11 @@ __global__ void __launch_bounds__(128)
 
 // ---------------------------------------------------------------------------
 // compute_h backward.  Same lane layout.  Per token writes
-//   du[t][o] = alpha_seg r dz[o],  dz[t][o],  ga[t][seg] = sum_{o in seg} dz r u,
+//   du[t][o] = alpha_seg r dz[o] (bf16 hi | lo) and
 //   coef[t] = -dr r^2 / (K q) with dr = sum_o dz alpha_seg u and q = 1/r - eps_rms
-//   (coef = 0 when q <= 0: an all-zero row has zero RMS gradient).
+//   (coef = 0 when q <= 0: an all-zero row has zero RMS gradient);
+// per block one partial row: the block's sums of dz[o] (in token order) and
+// of the dalpha terms ga[seg] = sum_{o in seg} dz r u.
 // ---------------------------------------------------------------------------
 template <int N>
 __global__ void __launch_bounds__(128)
@@ -92,14 +96,17 @@ __global__ void __launch_bounds__(128)
                     const float *__restrict__ dHres, const float *__restrict__ u_save,
                     const float *__restrict__ r_save, const float *__restrict__ alpha,
                     const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
-                    float eps_rms, bf16 *__restrict__ du_hl, int du_cols, float *__restrict__ dz,
-                    float *__restrict__ ga, float *__restrict__ coef)
+                    float eps_rms, bf16 *__restrict__ du_hl, int du_cols,
+                    float *__restrict__ coef, float *__restrict__ part)
 {
     constexpr int O = Dims<N>::O;
+    constexpr int PW = O + 4, TB = 128 / N;
     extern __shared__ float sk_store[];  // [2*iters][blockDim.x]
+    __shared__ float red[TB][PW];
     const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = gt / N;
     const int i = int(gt % N);
+    const int tb = threadIdx.x / N;
     const bool live = t < T;
     const int64_t tt = live ? t : 0;
     const float *u = u_save + tt * O;
@@ -122,25 +129,21 @@ __global__ void __launch_bounds__(128)
     const float sp = sigmoidf_(zpre), so = sigmoidf_(zpost);
     const float dzpre = (live ? __ldg(dHpre + tt * N + i) : 0.f) * sp * (1.f - sp);
     const float dzpost = (live ? __ldg(dHpost + tt * N + i) : 0.f) * 2.f * so * (1.f - so);
-    float gres = 0.f, dres_dot = 0.f;
+    float gres = 0.f;
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-        gres = fmaf(g[j], ures[j], gres);
-    }
+    for (int j = 0; j < N; ++j) gres = fmaf(g[j], ures[j], gres);
     float gpre = dzpre * upre, gpost = dzpost * upost;
-    dres_dot = gres;
     // sums over the N lanes of the group
 #pragma unroll
     for (int m = 1; m < N; m <<= 1) {
         gpre += __shfl_xor_sync(kFull, gpre, m);
         gpost += __shfl_xor_sync(kFull, gpost, m);
-        dres_dot += __shfl_xor_sync(kFull, dres_dot, m);
+        gres += __shfl_xor_sync(kFull, gres, m);
     }
     if (live) {
         // du = alpha_seg r dz, stored as bf16 hi (columns [0,O)) and the bf16
         // remainder (columns [O,2O)); zero columns pad the row to du_cols.
         bf16 *dut = du_hl + t * du_cols;
-        float *dzt = dz + t * O;
         auto put = [&](int o, float v) {
             const bf16 hi = __float2bfloat16_rn(v);
             dut[o] = hi;
@@ -148,59 +151,81 @@ __global__ void __launch_bounds__(128)
         };
         put(i, a0 * r * dzpre);
         put(N + i, a1 * r * dzpost);
-        dzt[i] = dzpre;
-        dzt[N + i] = dzpost;
 #pragma unroll
-        for (int j = 0; j < N; ++j) {
-            put(2 * N + i * N + j, a2 * r * g[j]);
-            dzt[2 * N + i * N + j] = g[j];
-        }
+        for (int j = 0; j < N; ++j) put(2 * N + i * N + j, a2 * r * g[j]);
         // columns [2O, 2O+2N): H_post[i] as bf16 hi | lo (the dbias MMA of the
         // residual-gradient pass reads them), then zeros
         const float hp = 2.0f * so;
         const bf16 hph = __float2bfloat16_rn(hp);
         dut[2 * O + i] = hph;
         dut[2 * O + N + i] = __float2bfloat16_rn(hp - __bfloat162float(hph));
-        if (i == 0)
-            for (int o = 2 * O + 2 * N; o < du_cols; ++o) dut[o] = __float2bfloat16_rn(0.f);
         if (i == 0) {
-            ga[t * 4 + 0] = gpre * r;
-            ga[t * 4 + 1] = gpost * r;
-            ga[t * 4 + 2] = dres_dot * r;
-            ga[t * 4 + 3] = 0.f;
-            const float dr = a0 * gpre + a1 * gpost + a2 * dres_dot;
+            for (int o = 2 * O + 2 * N; o < du_cols; ++o) dut[o] = __float2bfloat16_rn(0.f);
+            const float dr = a0 * gpre + a1 * gpost + a2 * gres;
             const float q = 1.0f / r - eps_rms;
             coef[t] = (q > 0.f) ? -dr * r * r / (float(K) * q) : 0.f;
         }
     }
+    // this token's row of the block partial (zeros for a dead token)
+    red[tb][i] = live ? dzpre : 0.f;
+    red[tb][N + i] = live ? dzpost : 0.f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) red[tb][2 * N + i * N + j] = live ? g[j] : 0.f;
+    if (i == 0) {
+        red[tb][O] = live ? gpre * r : 0.f;
+        red[tb][O + 1] = live ? gpost * r : 0.f;
+        red[tb][O + 2] = live ? gres * r : 0.f;
+        red[tb][O + 3] = 0.f;
+    }
+    __syncthreads();
+    if (threadIdx.x < PW) {
+        float acc = 0.f;
+        for (int k = 0; k < TB; ++k) acc += red[k][threadIdx.x];
+        part[int64_t(blockIdx.x) * PW + threadIdx.x] = acc;
+    }
 }
 
-// out[j] = sum_r part[r][j], r ascending
-__global__ void k_sum_rows_p(const float *__restrict__ part, float *__restrict__ out,
-                             int64_t rows, int64_t cols)
-{
-    const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= cols) return;
-    float acc = 0.f;
-    for (int64_t r = 0; r < rows; ++r) acc += part[r * cols + c];
-    out[c] = acc;
-}
-
-// out[j] = sum_t a[t][j] (stride lda), one block per column, fixed tree.
+// Fixed-order sums of the backward's partials.  Blocks [0, wblocks):
+// dW[j] = sum_s dWpart[s][j]; the next bblocks: dbias[j] = sum_s
+// dbiaspart[s][j] (s ascending; both only when the residual-gradient pass
+// was split); then one block per column o of the partial rows: db[o] (o < O)
+// or dalpha[o - O] = sum over rows, a fixed 256-thread tree.
 __global__ void __launch_bounds__(256)
-    k_sum_cols(const float *__restrict__ a, int64_t lda, int64_t rows, float *__restrict__ out)
+    k_bwd_finalize(const float *__restrict__ dWpart, float *__restrict__ dW, int64_t wcols,
+                   int wblocks, const float *__restrict__ dbiaspart, float *__restrict__ dbias,
+                   int64_t bcols, int bblocks, int splits, const float *__restrict__ part,
+                   int64_t prows, int O, float *__restrict__ db, float *__restrict__ dalpha)
 {
     __shared__ float red[256];
-    const int j = blockIdx.x;
+    int blk = blockIdx.x;
+    if (blk < wblocks + bblocks) {
+        const bool isw = blk < wblocks;
+        const float *src = isw ? dWpart : dbiaspart;
+        float *dst = isw ? dW : dbias;
+        const int64_t cols = isw ? wcols : bcols;
+        const int64_t c = int64_t(isw ? blk : blk - wblocks) * 256 + threadIdx.x;
+        if (c >= cols) return;
+        float acc = 0.f;
+        for (int sp = 0; sp < splits; ++sp) acc += src[int64_t(sp) * cols + c];
+        dst[c] = acc;
+        return;
+    }
+    const int o = blk - wblocks - bblocks;
+    const int PW = O + 4;
     float acc = 0.f;
-    for (int64_t r = threadIdx.x; r < rows; r += 256) acc += a[r * lda + j];
+    for (int64_t r = threadIdx.x; r < prows; r += 256) acc += part[r * PW + o];
     red[threadIdx.x] = acc;
     __syncthreads();
     for (int w = 128; w > 0; w >>= 1) {
         if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
         __syncthreads();
     }
-    if (threadIdx.x == 0) out[j] = red[0];
+    if (threadIdx.x == 0) {
+        if (o < O)
+            db[o] = red[0];
+        else
+            dalpha[o - O] = red[0];
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -257,15 +282,20 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
 }
 
 // workspace layout of the backward (each piece 256-byte aligned):
-//   du_hl [T][du_cols] bf16, dz [T][O], ga [T][4], coef [T], dHpre/dHpost [T][N],
-//   dHres [T][N][N], Wb (bf16 W for the tensor cores), dW partials [S][K][O],
-//   dbias partials [S][C]
+//   du_hl [T][du_cols] bf16, coef [T], partial rows [rows][n*n+2n+4],
+//   dbias partials [S][C], dW partials [S][K][O] (only when S > 1)
 struct BwdWs {
-    bf16 *du_hl, *Wb;
-    float *dz, *ga, *coef, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
+    bf16 *du_hl;
+    float *coef, *part, *dWpart, *dbiaspart;
     int splits;
     size_t bytes;
 };
+
+static int64_t bwd_part_rows(int64_t T, int n)
+{
+    const int64_t a = bwd_tok_blocks(T), b = (T * n + 127) / 128;
+    return a > b ? a : b;
+}
 
 static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
 {
@@ -280,15 +310,11 @@ static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
     };
     w.splits = bwd_tc_splits(T, n, C);
     w.du_hl = reinterpret_cast<bf16 *>(take(size_t(T) * bwd_tc_du_cols(n) * 2));
-    w.dz = reinterpret_cast<float *>(take(size_t(T * O) * 4));
-    w.ga = reinterpret_cast<float *>(take(size_t(T * 4) * 4));
     w.coef = reinterpret_cast<float *>(take(size_t(T) * 4));
-    w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
-    w.dHpost = reinterpret_cast<float *>(take(size_t(T * n) * 4));
-    w.dHres = reinterpret_cast<float *>(take(size_t(T * n * n) * 4));
-    w.Wb = reinterpret_cast<bf16 *>(take(bwd_tc_wb_bytes(n, C)));
-    w.dWpart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(K * O) * 4));
+    w.part = reinterpret_cast<float *>(take(size_t(bwd_part_rows(T, n)) * bwd_part_cols(n) * 4));
     w.dbiaspart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(C) * 4));
+    w.dWpart = w.splits > 1 ? reinterpret_cast<float *>(take(size_t(w.splits) * size_t(K * O) * 4))
+                            : nullptr;
     w.bytes = off;
     return w;
 }
@@ -312,55 +338,47 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
 {
     constexpr int O = Dims<N>::O;
     const int64_t K = int64_t(N) * C;
+    const int du_cols = bwd_tc_du_cols(N);
     BwdWs w = carve_bwd(ws, T, N, C);
     cudaError_t e;
+    int64_t prows;
     if (L) {
-        // pass 1: dH_res, dH_post and df from dout
-        e = launch_post_bwd_tok(L->dout, x, L->f, L->bias, L->Hres, L->Hpost, nullptr, L->df,
-                                w.dHres, w.dHpost, T, N, C, s);
+        // pass 1: per-token reductions of dout, x, f, dy; df; compute_h backward
+        prows = bwd_tok_blocks(T);
+        e = launch_bwd_tok(L->dout, x, L->f, L->bias, L->dy, L->Hpost, u_save, r_save, alpha, b,
+                           T, N, C, iters, eps_sk, eps_rms, L->df, w.du_hl, du_cols, w.coef,
+                           w.part, s);
         if (e != cudaSuccess) return e;
-        // pass 2: dH_pre = sum_c dy x
-        e = launch_aggregate_bwd(L->dy, x, L->Hpre, nullptr, w.dHpre, T, N, C, s);
+    } else {
+        prows = (T * N + 127) / 128;
+        const size_t smem = size_t(2) * iters * 128 * sizeof(float);
+        e = cudaFuncSetAttribute(k_compute_h_bwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(size_t(2) * kMaxIters * 128 * sizeof(float)));
         if (e != cudaSuccess) return e;
-        dHpre = w.dHpre;
-        dHpost = w.dHpost;
-        dHres = w.dHres;
-    }
-    const size_t smem = size_t(2) * iters * 128 * sizeof(float);
-    e = cudaFuncSetAttribute(k_compute_h_bwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(size_t(2) * kMaxIters * 128 * sizeof(float)));
-    if (e != cudaSuccess) return e;
-    {
         MHC_PROF("k_compute_h_bwd", s);
-        k_compute_h_bwd<N><<<unsigned((T * N + 127) / 128), 128, smem, s>>>(
+        k_compute_h_bwd<N><<<unsigned(prows), 128, smem, s>>>(
             dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
-            bwd_tc_du_cols(N), w.dz, w.ga, w.coef);
+            du_cols, w.coef, w.part);
     }
-    // pass 3: residual gradient, dW and dbias on the tensor cores
+    // pass 2: residual gradient, dW and dbias on the tensor cores; an unsplit
+    // pass writes dW and dbias directly
     const int tiles = int((T + 127) / 128);
     const int tps = (tiles + w.splits - 1) / w.splits;
     const int splits_used = (tiles + tps - 1) / tps;
-    e = launch_bwd_tc(x, W, w.du_hl, w.coef, w.Wb, T, N, C, L ? L->dout : nullptr,
-                      L ? L->dy : nullptr, L ? L->Hpre : nullptr, L ? L->Hres : nullptr,
-                      L ? L->Hpost : nullptr, dx, w.dWpart, w.dbiaspart, splits_used, fault, s);
+    const bool split = splits_used > 1;
+    float *dbias = L ? L->dbias : nullptr;
+    e = launch_bwd_tc(x, W, w.du_hl, w.coef, T, N, C, L ? L->dout : nullptr, L ? L->dy : nullptr,
+                      L ? L->Hpre : nullptr, L ? L->Hres : nullptr, L ? L->Hpost : nullptr, dx,
+                      split ? w.dWpart : dW, (split || !dbias) ? w.dbiaspart : dbias,
+                      splits_used, fault, s);
     if (e != cudaSuccess) return e;
+    const int wblocks = split ? int((K * O + 255) / 256) : 0;
+    const int bblocks = (split && dbias) ? int((C + 255) / 256) : 0;
     {
-        MHC_PROF("k_sum_rows_p", s);
-        k_sum_rows_p<<<unsigned((K * O + 255) / 256), 256, 0, s>>>(w.dWpart, dW, splits_used,
-                                                                   K * O);
-    }
-    if (L && L->dbias) {
-        MHC_PROF("k_sum_rows_p", s);
-        k_sum_rows_p<<<unsigned((C + 255) / 256), 256, 0, s>>>(w.dbiaspart, L->dbias,
-                                                               splits_used, C);
-    }
-    {
-        MHC_PROF("k_sum_cols", s);
-        k_sum_cols<<<3, 256, 0, s>>>(w.ga, 4, T, dalpha);
-    }
-    {
-        MHC_PROF("k_sum_cols", s);
-        k_sum_cols<<<O, 256, 0, s>>>(w.dz, O, T, db);
+        MHC_PROF("k_bwd_finalize", s);
+        k_bwd_finalize<<<unsigned(wblocks + bblocks + O + 3), 256, 0, s>>>(
+            w.dWpart, dW, K * O, wblocks, w.dbiaspart, dbias, C, bblocks, splits_used, w.part,
+            prows, O, db, dalpha);
     }
     return cudaGetLastError();
 }

@@ -72,12 +72,23 @@ cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n
                                  bf16 *Whl, float *upart, float *spart, int *splits_used,
                                  int *fault, cudaStream_t s);
 
+// Width of one partial row of the backward's token sums: dz sums over the
+// n*n+2n logits (for db), the three dalpha terms, one pad column.
+constexpr int bwd_part_cols(int n) { return n * n + 2 * n + 4; }
+
+// k_bwd_tok.cu: token pass of the layer backward (one partial row per block)
+int bwd_tok_blocks(int64_t T);
+cudaError_t launch_bwd_tok(const bf16 *dout, const bf16 *x, const bf16 *f, const bf16 *bias,
+                           const bf16 *dy, const float *Hpost, const float *u_save,
+                           const float *r_save, const float *alpha, const float *b, int64_t T,
+                           int n, int64_t C, int iters, float eps_sk, float eps_rms, bf16 *df,
+                           bf16 *du_hl, int du_cols, float *coef, float *part, cudaStream_t s);
+
 // k_bwd_tc.cu: residual-gradient pass of the backward on the tensor cores
 int bwd_tc_du_cols(int n);
-size_t bwd_tc_wb_bytes(int n, int64_t C);
 int bwd_tc_splits(int64_t T, int n, int64_t C);
 cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
-                          bf16 *Wb, int64_t T, int n, int64_t C, const bf16 *dout,
+                          int64_t T, int n, int64_t C, const bf16 *dout,
                           const bf16 *dy, const float *Hpre, const float *Hres,
                           const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
                           int splits, int *fault, cudaStream_t s);
@@ -96,9 +107,9 @@ cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float
                             int64_t C, int iters, float eps_sk, float eps_rms, bf16 *dx,
                             float *dW, float *dalpha, float *db, void *ws, int *fault,
                             cudaStream_t s);
-// Layer backward (three passes over HBM): post_bda per-token reductions and
-// df; aggregate reduction for dH_pre with the compute_h backward; the
-// residual-gradient pass dx = H_res dout + H_pre dy + du W^T + coef x, with
+// Layer backward (two passes over HBM): the token pass (post_bda and
+// aggregate reductions, df, the compute_h backward), then the
+// residual-gradient pass dx = H_res dout + H_pre dy + du W^T + coef x with
 // dW and dbias.  Workspace proj_bwd_ws_bytes.
 cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
                              const float *alpha, const float *b, const bf16 *f,
