@@ -12,10 +12,9 @@
 // Forward:  k_proj_tc (k_proj_tc.cu: split-K partial u = x W and s = sum x^2
 //           on the tensor cores), k_compute_h_fwd (sum of partials, r, z,
 //           gates, Sinkhorn)
-// Backward: k_compute_h_bwd (standalone op: per-token du as bf16 hi|lo, RMS
-//           coefficient, per-block sums of dz and the dalpha terms) or, in
-//           the layer, k_bwd_tok (k_bwd_tok.cu) for the same outputs; then
-//           k_bwd_tc (k_bwd_tc.cu: du W^T + coef x [+ H_res dout + H_pre dy],
+// Backward: [layer: k_bwd_tok (k_bwd_tok.cu), the per-token dH sums and df]
+//           k_compute_h_bwd (per-token du as bf16 hi|lo, RMS coefficient,
+//           per-block sums of dz and the dalpha terms), k_bwd_tc (k_bwd_tc.cu: du W^T + coef x [+ H_res dout + H_pre dy],
 //           dW and dbias on the tensor cores) and k_bwd_finalize, the
 //           fixed-order sums for db, dalpha (and dW, dbias when split).
 #include "launch.h"
@@ -282,20 +281,15 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
 }
 
 // workspace layout of the backward (each piece 256-byte aligned):
-//   du_hl [T][du_cols] bf16, coef [T], partial rows [rows][n*n+2n+4],
-//   dbias partials [S][C], dW partials [S][K][O] (only when S > 1)
+//   du_hl [T][du_cols] bf16, coef [T], partial rows [ceil(T n / 128)][n*n+2n+4],
+//   dH_pre, dH_post [T][n], dH_res [T][n][n] (layer), dbias partials [S][C],
+//   dW partials [S][K][O] (only when S > 1)
 struct BwdWs {
     bf16 *du_hl;
-    float *coef, *part, *dWpart, *dbiaspart;
+    float *coef, *part, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
     int splits;
     size_t bytes;
 };
-
-static int64_t bwd_part_rows(int64_t T, int n)
-{
-    const int64_t a = bwd_tok_blocks(T), b = (T * n + 127) / 128;
-    return a > b ? a : b;
-}
 
 static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
 {
@@ -311,7 +305,10 @@ static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
     w.splits = bwd_tc_splits(T, n, C);
     w.du_hl = reinterpret_cast<bf16 *>(take(size_t(T) * bwd_tc_du_cols(n) * 2));
     w.coef = reinterpret_cast<float *>(take(size_t(T) * 4));
-    w.part = reinterpret_cast<float *>(take(size_t(bwd_part_rows(T, n)) * bwd_part_cols(n) * 4));
+    w.part = reinterpret_cast<float *>(take(size_t((T * n + 127) / 128) * bwd_part_cols(n) * 4));
+    w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
+    w.dHpost = reinterpret_cast<float *>(take(size_t(T * n) * 4));
+    w.dHres = reinterpret_cast<float *>(take(size_t(T * n * n) * 4));
     w.dbiaspart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(C) * 4));
     w.dWpart = w.splits > 1 ? reinterpret_cast<float *>(take(size_t(w.splits) * size_t(K * O) * 4))
                             : nullptr;
@@ -341,16 +338,17 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     const int du_cols = bwd_tc_du_cols(N);
     BwdWs w = carve_bwd(ws, T, N, C);
     cudaError_t e;
-    int64_t prows;
     if (L) {
-        // pass 1: per-token reductions of dout, x, f, dy; df; compute_h backward
-        prows = bwd_tok_blocks(T);
-        e = launch_bwd_tok(L->dout, x, L->f, L->bias, L->dy, L->Hpost, u_save, r_save, alpha, b,
-                           T, N, C, iters, eps_sk, eps_rms, L->df, w.du_hl, du_cols, w.coef,
-                           w.part, s);
+        // pass 1: per-token sums over dout, x, f, dy and df
+        e = launch_bwd_tok(L->dout, x, L->f, L->bias, L->dy, L->Hpost, T, N, C, L->df, w.dHres,
+                           w.dHpost, w.dHpre, s);
         if (e != cudaSuccess) return e;
-    } else {
-        prows = (T * N + 127) / 128;
+        dHpre = w.dHpre;
+        dHpost = w.dHpost;
+        dHres = w.dHres;
+    }
+    const int64_t prows = (T * N + 127) / 128;
+    {
         const size_t smem = size_t(2) * iters * 128 * sizeof(float);
         e = cudaFuncSetAttribute(k_compute_h_bwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  int(size_t(2) * kMaxIters * 128 * sizeof(float)));

@@ -76,13 +76,12 @@ cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n
 // n*n+2n logits (for db), the three dalpha terms, one pad column.
 constexpr int bwd_part_cols(int n) { return n * n + 2 * n + 4; }
 
-// k_bwd_tok.cu: token pass of the layer backward (one partial row per block)
+// k_bwd_tok.cu: token pass of the layer backward: df and the per-token sums
+// dH_res [T][n][n], dH_post [T][n], dH_pre [T][n]
 int bwd_tok_blocks(int64_t T);
 cudaError_t launch_bwd_tok(const bf16 *dout, const bf16 *x, const bf16 *f, const bf16 *bias,
-                           const bf16 *dy, const float *Hpost, const float *u_save,
-                           const float *r_save, const float *alpha, const float *b, int64_t T,
-                           int n, int64_t C, int iters, float eps_sk, float eps_rms, bf16 *df,
-                           bf16 *du_hl, int du_cols, float *coef, float *part, cudaStream_t s);
+                           const bf16 *dy, const float *Hpost, int64_t T, int n, int64_t C,
+                           bf16 *df, float *dHres, float *dHpost, float *dHpre, cudaStream_t s);
 
 // k_bwd_tc.cu: residual-gradient pass of the backward on the tensor cores
 int bwd_tc_du_cols(int n);
@@ -108,7 +107,7 @@ cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float
                             float *dW, float *dalpha, float *db, void *ws, int *fault,
                             cudaStream_t s);
 // Layer backward (two passes over HBM): the token pass (post_bda and
-// aggregate reductions, df, the compute_h backward), then the
+// aggregate reductions, df), the compute_h backward, then the
 // residual-gradient pass dx = H_res dout + H_pre dy + du W^T + coef x with
 // dW and dbias.  Workspace proj_bwd_ws_bytes.
 cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
