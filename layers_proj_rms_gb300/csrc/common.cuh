@@ -76,6 +76,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr)
     return v;
 }
 
+__device__ __forceinline__ float lds32f(uint32_t saddr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(saddr));
+    return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

@@ -74,7 +74,13 @@ struct BwdTc {
     // columns 2O+i (hi) and 2O+N+i (lo) of du_hl hold H_post[t][i]
     static constexpr int D3_COL = 320, D3_N = 64;
     static constexpr int TMEM_COLS = 512;
-    static constexpr int SMEM = STAGES * STAGE + W_BYTES + 1024;
+    // n = 4: the epilogue stages the next tile's per-token inputs (H_res row,
+    // H_pre row: 20 floats per token; coef) in shared memory with cp.async
+    static constexpr bool STAGE_P = N == 4;
+    static constexpr int PAR_ROW = 20 * 4;
+    static constexpr int PAR_OFF = STAGES * STAGE + W_BYTES;
+    static constexpr int PAR_BYTES = STAGE_P ? TT * PAR_ROW + TT * 4 : 0;
+    static constexpr int SMEM = STAGES * STAGE + W_BYTES + PAR_BYTES + 1024;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
     static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0, "alignment");
     static_assert(SMEM <= 232448, "shared memory");
@@ -319,6 +325,24 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         const bool cvalid = cc < C;          // the last slice may pass C
         float bias_acc = 0.f;                // lane l: running total of channel cc + (l % 8)
         bool ok = true;
+        // The four warps of a quadrant share its 32 token rows: together they
+        // copy the rows' inputs of a tile into shared memory one tile ahead
+        // (H_res chunk h, H_pre by h = 0, coef by one warp; rows past T are
+        // zero-filled) and meet at a named barrier before and after reading.
+        const uint32_t prow = tc::smem_u32(smem + P::PAR_OFF) + r * P::PAR_ROW;
+        const uint32_t pcoef = tc::smem_u32(smem + P::PAR_OFF + P::TT * P::PAR_ROW) + r * 4;
+        auto stage_params = [&](int tile) {
+            const int64_t tp = int64_t(tile) * P::TT + r;
+            const bool v = tp < a.T;
+            const int64_t tv = v ? tp : 0;
+            if (LAYER) {
+                tc::cp_async16(prow + h * 16, a.Hres + tv * N * N + h * 4, v ? 16u : 0u);
+                if (h == 0) tc::cp_async16(prow + 64, a.Hpre + tv * N, v ? 16u : 0u);
+            }
+            if (h == (LAYER ? 1 : 0)) tc::cp_async4(pcoef, a.coef + tv, v ? 4u : 0u);
+            tc::cp_async_commit();
+        };
+        if (P::STAGE_P && ntiles > 0) stage_params(tile0);
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % P::STAGES, b = i & 1;
             const int64_t t = int64_t(tile0 + i) * P::TT + r;
@@ -332,7 +356,31 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             uint4 g[N], gy = make_uint4(0, 0, 0, 0);
 #pragma unroll
             for (int ii = 0; ii < N; ++ii) g[ii] = make_uint4(0, 0, 0, 0);
-            if (valid) {
+            if (P::STAGE_P) {
+                // every warp of the quadrant passes both barriers on every
+                // tile, also after a failure, so none of them waits alone
+                tc::cp_async_wait_all();
+                tc::named_bar_sync(1 + q, 128);
+                if (LAYER) {
+#pragma unroll
+                    for (int e = 0; e < N * N; e += 4) {
+                        const uint4 v = lds128(prow + e * 4);
+                        hres[e] = __uint_as_float(v.x);
+                        hres[e + 1] = __uint_as_float(v.y);
+                        hres[e + 2] = __uint_as_float(v.z);
+                        hres[e + 3] = __uint_as_float(v.w);
+                    }
+                    const uint4 v = lds128(prow + 64);
+                    hpre[0] = __uint_as_float(v.x);
+                    hpre[1] = __uint_as_float(v.y);
+                    hpre[2] = __uint_as_float(v.z);
+                    hpre[3] = __uint_as_float(v.w);
+                }
+                coef = lds32f(pcoef);
+                tc::named_bar_sync(1 + q, 128);
+                if (i + 1 < ntiles) stage_params(tile0 + i + 1);
+                if (!ok) continue;
+            } else if (valid) {
                 coef = __ldg(a.coef + t);
                 if (LAYER) {
 #pragma unroll
@@ -359,6 +407,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
                 !tc::mbar_wait(&d2full[b], (i >> 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
                 ok = false;
+                if (P::STAGE_P) continue;
                 break;
             }
             tc::tc_fence_after();
@@ -425,6 +474,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::mbar_arrive(&empty[s]);
             }
         }
+        if (P::STAGE_P) tc::cp_async_wait_all();
         if (!ok) *abort_v = 1;
         // dW partial of this split: D1 rows are the 128 k of the slice; the
         // chunk-0 warps write it

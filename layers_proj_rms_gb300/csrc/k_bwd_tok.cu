@@ -13,10 +13,10 @@ namespace mhc {
 
 constexpr int kTokWarps = 8;
 #ifndef MHC_TOK_U
-#define MHC_TOK_U 1
+#define MHC_TOK_U 2
 #endif
 #ifndef MHC_TOK_MINB
-#define MHC_TOK_MINB 3
+#define MHC_TOK_MINB 1
 #endif
 
 // U: 8-channel chunks per lane in flight per step
