@@ -46,6 +46,54 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
     return v;
 }
 
+// ---- packed fp32 pairs: f32x2 arithmetic, two IEEE fp32 operations (each
+// rounded as its scalar form) per instruction --------------------------------
+typedef unsigned long long f32x2;
+
+__device__ __forceinline__ f32x2 f2_make(float lo, float hi)
+{
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_split(f32x2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// 8 bf16 -> 4 pairs (elements 2q, 2q+1) and back (round to nearest even)
+__device__ __forceinline__ void unpack8x2(const uint4 v, f32x2 (&p)[4])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        p[q] = f2_make(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u));
+}
+__device__ __forceinline__ uint4 pack8x2(const f32x2 (&p)[4])
+{
+    float f[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) f2_split(p[q], f[2 * q], f[2 * q + 1]);
+    return pack8(f);
+}
+
 // Streaming 16-byte loads: read-only path, no L1 allocation for data that is
 // touched once.
 __device__ __forceinline__ uint4 ld_stream(const void *p)

@@ -418,31 +418,45 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 gy = box_chunk<N>(st + P::Y_OFF, r, h);
             }
             // mix[j][e] = H_pre[j] dy[e] + sum_i H_res[j][i] dout_i[e];  df = sum_i H_post[i] dout_i
-            float mix[LAYER ? N : 1][8];
+            // (element pairs in f32x2 arithmetic)
+            f32x2 mix[LAYER ? N : 1][4];
             if (LAYER) {
-                float gyv[8], df[8];
-                unpack8(gy, gyv);
+                f32x2 gyv[4], df[4];
+                unpack8x2(gy, gyv);
 #pragma unroll
-                for (int j = 0; j < N; ++j)
+                for (int j = 0; j < N; ++j) {
+                    const f32x2 w2 = f2_make(hpre[j], hpre[j]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) mix[j][e] = hpre[j] * gyv[e];
+                    for (int p = 0; p < 4; ++p) mix[j][p] = f2_mul(w2, gyv[p]);
+                }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) df[e] = 0.f;
+                for (int p = 0; p < 4; ++p) df[p] = 0ull;
 #pragma unroll
                 for (int ii = 0; ii < N; ++ii) {
-                    float dv[8];
-                    unpack8(g[ii], dv);
+                    f32x2 dv[4];
+                    unpack8x2(g[ii], dv);
+                    if (!SG) {
+                        const f32x2 w2 = f2_make(hpost[ii], hpost[ii]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) df[e] = fmaf(hpost[ii], dv[e], df[e]);
+                        for (int p = 0; p < 4; ++p) df[p] = f2_fma(w2, dv[p], df[p]);
+                    }
 #pragma unroll
-                    for (int j = 0; j < N; ++j)
+                    for (int j = 0; j < N; ++j) {
+                        const f32x2 w2 = f2_make(hres[j * N + ii], hres[j * N + ii]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) mix[j][e] = fmaf(hres[j * N + ii], dv[e], mix[j][e]);
+                        for (int p = 0; p < 4; ++p) mix[j][p] = f2_fma(w2, dv[p], mix[j][p]);
+                    }
                 }
-                if (!SG) bias_acc += warp_column_sum<8>(df);
+                if (!SG) {
+                    float dfs[8];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) f2_split(df[p], dfs[2 * p], dfs[2 * p + 1]);
+                    bias_acc += warp_column_sum<8>(dfs);
+                }
             }
             // dx_gemm of this chunk for every stream: all TMEM loads, one wait
-            constexpr int JB = N == 4 ? 4 : 2;  // streams per batch of TMEM loads
+            constexpr int JB = 2;  // streams per batch of TMEM loads
+            const f32x2 coef2 = f2_make(coef, coef);
 #pragma unroll
             for (int j0 = 0; j0 < N; j0 += JB) {
                 float acc[JB][8];
@@ -456,14 +470,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj) {
                     const int j = j0 + jj;
-                    float xv[8];
-                    unpack8(xr[jj], xv);
+                    f32x2 xv[4], o[4];
+                    unpack8x2(xr[jj], xv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc[jj][e] = fmaf(coef, xv[e], acc[jj][e]);
-                        if (LAYER) acc[jj][e] += mix[j][e];
+                    for (int p = 0; p < 4; ++p) {
+                        o[p] = f2_fma(coef2, xv[p], f2_make(acc[jj][2 * p], acc[jj][2 * p + 1]));
+                        if (LAYER) o[p] = f2_add(o[p], mix[j][p]);
                     }
-                    if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8(acc[jj]));
+                    if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8x2(o));
                 }
             }
             // D2 buffer b and the stage have been read: release them

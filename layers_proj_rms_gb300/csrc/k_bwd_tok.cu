@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
 int bwd_tok_blocks(int64_t T)
 {
     const int64_t want = (T + kTokWarps - 1) / kTokWarps;
-    const int64_t cap = int64_t(kSplitSms) * 8;
+    const int64_t cap = int64_t(kSplitSms) * 2;
     return int(want < cap ? (want > 0 ? want : 1) : cap);
 }
 
