@@ -14,7 +14,8 @@
 // du (fp32) arrives as bf16 hi | lo halves (du_hl[t][0..O) = bf16(du),
 // du_hl[t][O..2O) = bf16(du - hi)), which together carry du to ~2^-17; W is
 // split the same way into W_hi and W_lo.
-// Per tile of 128 tokens:
+// Per tile of 128 tokens (MMA 1 first, so the epilogue's accumulator is
+// complete before the dW and dbias MMAs of the tile run):
 //   MMA 1 (dx_gemm): D2[t][k] = du_hi.W_hi + du_lo.W_hi + du_hi.W_lo (the
 //          dropped du_lo.W_lo is ~2^-18 relative): M = 128 tokens, N = 128 k,
 //          K = 2*O against Wd = [W_hi | W_hi], then K = O against W_lo
@@ -31,7 +32,11 @@
 // slices) the epilogue reads them from global memory.
 // Warps: 0 TMA producer, 1 TMEM + MMA issue, 2.. epilogue: CW/8 warps per
 // TMEM lane quadrant, each thread one token row x one 8-channel chunk of
-// every stream (16 epilogue warps for n = 4, 8 for n = 8).
+// every stream (16 epilogue warps for n = 4, 8 for n = 8).  Before their
+// first tile the epilogue warps build the slice's W tile in shared memory
+// from fp32 W (bf16 hi/lo split, swizzled for the MMA); for n = 4 they also
+// copy each tile's per-token inputs (H_res, H_pre, coef) into shared memory
+// one tile ahead.  An unsplit pass writes dW and dbias directly.
 #include <cudaTypedefs.h>
 
 #include "launch.h"
@@ -234,6 +239,27 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::tc_fence_after();
                 const uint32_t xs = tc::smem_u32(smem + s * P::STAGE);
                 const uint32_t dus = xs + P::DU_OFF;
+                // dx accumulator b must have been drained by the epilogue (tile i-2)
+                if (i >= 2 &&
+                    !tc::mbar_wait(&d2empty[b], ((i >> 1) - 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                // K steps: du_hl[0,2O) against [W_hi | W_hi], then du_hi against W_lo
+#pragma unroll
+                for (int kk = 0; kk < P::KSTEP_A + P::KSTEP_B; ++kk) {
+                    const int acol = kk < P::KSTEP_A ? 16 * kk : 16 * (kk - P::KSTEP_A);
+                    const int bcol = 16 * kk;
+                    const uint64_t ad =
+                        tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES + (acol % 64) * 2, 16,
+                                      1024, tc::kSwz128);
+                    const uint64_t bd =
+                        tc::make_desc(wb + (bcol / 64) * P::W_PLANE_BYTES + (bcol % 64) * 2, 16,
+                                      1024, tc::kSwz128);
+                    tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
+                }
+                tc::mma_commit(&d2full[b]);
                 // dW += x^T du_hl over the tile's 128 tokens, 16 per step
 #pragma unroll
                 for (int ks = 0; ks < P::TT / 16; ++ks) {
@@ -256,27 +282,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                                      (i > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
-                // dx accumulator b must have been drained by the epilogue (tile i-2)
-                if (i >= 2 &&
-                    !tc::mbar_wait(&d2empty[b], ((i >> 1) - 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
-                    ok = false;
-                    break;
-                }
-                tc::tc_fence_after();
-                // K steps: du_hl[0,2O) against [W_hi | W_hi], then du_hi against W_lo
-#pragma unroll
-                for (int kk = 0; kk < P::KSTEP_A + P::KSTEP_B; ++kk) {
-                    const int acol = kk < P::KSTEP_A ? 16 * kk : 16 * (kk - P::KSTEP_A);
-                    const int bcol = 16 * kk;
-                    const uint64_t ad =
-                        tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES + (acol % 64) * 2, 16,
-                                      1024, tc::kSwz128);
-                    const uint64_t bd =
-                        tc::make_desc(wb + (bcol / 64) * P::W_PLANE_BYTES + (bcol % 64) * 2, 16,
-                                      1024, tc::kSwz128);
-                    tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
-                }
-                tc::mma_commit(&d2full[b]);
                 tc::mma_commit(&empty[s]);
             }
             if (!ok) *abort_v = 1;
@@ -412,6 +417,9 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             }
             tc::tc_fence_after();
             const uint8_t *st = smem + s * P::STAGE;
+            // (releasing the stage right after these reads, before the
+            // arithmetic, measured slower: the stage goes back at the end)
+            uint4 xr[N];
             if (SG) {
 #pragma unroll
                 for (int ii = 0; ii < N; ++ii) g[ii] = box_chunk<N>(st + P::G_OFF + ii * P::XBOX, r, h);
@@ -463,15 +471,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj)
                     tc::tmem_ld8(trow + P::D2_COL + b * 128 + (j0 + jj) * CW + h * 8, acc[jj]);
-                uint4 xr[JB];
 #pragma unroll
-                for (int jj = 0; jj < JB; ++jj) xr[jj] = box_chunk<N>(st + (j0 + jj) * P::XBOX, r, h);
+                for (int jj = 0; jj < JB; ++jj) xr[j0 + jj] = box_chunk<N>(st + (j0 + jj) * P::XBOX, r, h);
                 tc::tmem_ld_wait();
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj) {
                     const int j = j0 + jj;
                     f32x2 xv[4], o[4];
-                    unpack8x2(xr[jj], xv);
+                    unpack8x2(xr[j], xv);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) {
                         o[p] = f2_fma(coef2, xv[p], f2_make(acc[jj][2 * p], acc[jj][2 * p + 1]));
