@@ -177,6 +177,32 @@ class Clocks:
 
 
 # ---------------------------------------------------------------------------
+# multi-rank helpers (one process per GPU; tokens sharded, no data-path
+# collective: only the timings are reduced)
+# ---------------------------------------------------------------------------
+
+def max_over_ranks(v, world, device):
+    """The largest value of v over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return float(v)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(seed, rank):
+    """Each rank draws its own batch of the workload (weak scaling)."""
+    return seed + 1000 * rank
+
+
+def job_tokens_per_s(T, world, ms):
+    """Whole-job throughput: every rank's T tokens over the slowest rank's time."""
+    return T * world / (ms / 1e3)
+
+
+# ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
 
@@ -189,7 +215,7 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     T, n, C, w_std, seed = mi.LAYER_WORKLOADS[args.workload]
     O = n * n + 2 * n
-    inp = mi.layer_inputs(T, n, C, seed + 1000 * rank, w_std=w_std, rmsnorm=True)
+    inp = mi.layer_inputs(T, n, C, rank_seed(seed, rank), w_std=w_std, rmsnorm=True)
 
     def h2d_src(a):
         t = torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a)
@@ -264,11 +290,7 @@ def run_ours(args, rank, world):
     kernels = {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(nk)}
     launches = int(sum(v[0] for v in kernels.values()))
 
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
 
     # ---- the layer alone (fwd + bwd, no RMSNorm), for the layer byte model ----
     def layer_step():
@@ -288,11 +310,7 @@ def run_ours(args, rank, world):
     ev1.record(stream)
     barrier()
     lms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([lms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        lms = float(t.item())
+    lms = max_over_ranks(lms, world, dev)
 
     # ---- end to end: pinned host inputs -> device -> step -> host grads ----
     e2e = None
@@ -319,12 +337,8 @@ def run_ours(args, rank, world):
         ev1.record(stream)
         barrier()
         ems = ev0.elapsed_time(ev1) / args.steps
-        if world > 1:
-            import torch.distributed as dist
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": T * world / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+        ems = max_over_ranks(ems, world, dev)
+        e2e = {"value": job_tokens_per_s(T, world, ems), "unit": "tokens/s", "ms_per_step": ems,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "api": "pinned host -> cudaMemcpyAsync -> mhc_layer_fwd/bwd + rmsnorm_fwd/bwd -> "
                       "host dW, dalpha, db, dbias"}
@@ -352,7 +366,7 @@ def run_ours(args, rank, world):
                     "share_of_step": round(tot / (ms * args.steps), 4)}
     res = {
         "metric": METRIC,
-        "value": T * world / (ms / 1e3),
+        "value": job_tokens_per_s(T, world, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -375,7 +389,7 @@ def run_ours(args, rank, world):
                 "moved_bytes_per_step": int(moved_b),
                 "moved_gbs": round(moved_b / (ms / 1e3) / 1e9, 1),
                 "moved_frac_of_measured": round(moved_b / (ms / 1e3) / 1e9 / peak, 4)},
-        "layer_only": {"ms_per_step": round(lms, 4), "tokens_per_s": T * world / (lms / 1e3),
+        "layer_only": {"ms_per_step": round(lms, 4), "tokens_per_s": job_tokens_per_s(T, world, lms),
                        "model_bytes_per_step": int(mb["layer_fwd"] + mb["layer_bwd"]),
                        "achieved_gbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3) / 1e9, 1),
                        "frac_of_nominal_8tbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3)

@@ -64,6 +64,15 @@ def _L():
             "orc_h_post_bda_bwd": [P, P, P, P, P, P, i64, i32, i64, P, P, P, P, P],
             "orc_rmsnorm_fwd": [P, i64, i64, f64, P, P],
             "orc_rmsnorm_bwd": [P, P, i64, i64, f64, P],
+            "orc_h_aggregate_static_fwd": [P, P, i64, i32, i64, P],
+            "orc_h_aggregate_static_bwd": [P, P, P, i64, i32, i64, P, P],
+            "orc_rmsnorm_residual_fwd": [P, P, P, i64, i64, f64, P, P, P],
+            "orc_rmsnorm_residual_bwd": [P, P, P, P, P, i64, i64, f64, P, P],
+            "orc_proj_rms_partials": [P, P, i64, i32, i64, P, P],
+            "orc_compute_h_from_sums": [P, P, i64, P, P, i64, i32, i32, f64, f64, P, P, P, P],
+            "orc_compute_h_bwd_from_sums": [P, P, P, P, P, i64, P, P, i64, i32, i32, f64, f64,
+                                            P, P, P, P],
+            "orc_proj_rms_partial_bwd": [P, P, P, P, i64, i32, i64, P, P],
             "orc_num_threads": [],
         }
         for name, args in sig.items():
@@ -231,6 +240,124 @@ def rmsnorm_bwd(dy, x, eps):
     dx = np.empty((rows, cols))
     _check(_L().orc_rmsnorm_bwd(_p(_f64(dy)), _p(x), rows, cols, float(eps), _p(dx)), "rms_bwd")
     return dx
+
+
+# --------------------------------------------------------------------------
+# h_aggregate with a static (token-independent) H_pre [n] (rwkv
+# StreamAggregateFwd/Bwd with per_token = false)
+# --------------------------------------------------------------------------
+
+def h_aggregate_static_fwd(x, H_pre):
+    x = _f64(x)
+    T, n, C = x.shape
+    y = np.empty((T, C))
+    _check(_L().orc_h_aggregate_static_fwd(_p(x), _p(_f64(H_pre)), T, n, C, _p(y)), "aggs_fwd")
+    return y
+
+
+def h_aggregate_static_bwd(dy, x, H_pre, *, want_dx=True):
+    x = _f64(x)
+    T, n, C = x.shape
+    dx = np.empty((T, n, C)) if want_dx else None
+    dH = np.empty(n)
+    _check(_L().orc_h_aggregate_static_bwd(_p(_f64(dy)), _p(x), _p(_f64(H_pre)), T, n, C,
+                                           _p(dx), _p(dH)), "aggs_bwd")
+    return {"dx": dx, "dH_pre": dH}
+
+
+# --------------------------------------------------------------------------
+# rmsnorm_residual (RL-Kernel PR #383 task P1-5 "RMSNorm + residual fork",
+# P1-8 "cross-rank dgamma"): h = x + res, y = h rho gamma
+# --------------------------------------------------------------------------
+
+def rmsnorm_residual_fwd(x, res, gamma, eps):
+    x = _f64(x)
+    rows, cols = x.shape
+    h = np.empty((rows, cols)); y = np.empty((rows, cols)); rstd = np.empty(rows)
+    _check(_L().orc_rmsnorm_residual_fwd(_p(x), _p(None if res is None else _f64(res)),
+                                         _p(None if gamma is None else _f64(gamma)), rows, cols,
+                                         float(eps), _p(h), _p(y), _p(rstd)), "rmsr_fwd")
+    return {"h": h, "y": y, "rstd": rstd}
+
+
+def rmsnorm_residual_bwd(dy, dh, x, res, gamma, eps):
+    x = _f64(x)
+    rows, cols = x.shape
+    dx = np.empty((rows, cols)); dgamma = np.empty(cols)
+    _check(_L().orc_rmsnorm_residual_bwd(_p(_f64(dy)), _p(None if dh is None else _f64(dh)),
+                                         _p(x), _p(None if res is None else _f64(res)),
+                                         _p(None if gamma is None else _f64(gamma)), rows, cols,
+                                         float(eps), _p(dx), _p(dgamma)), "rmsr_bwd")
+    return {"dx": dx, "dgamma": dgamma}
+
+
+# --------------------------------------------------------------------------
+# h_aggregate followed by the weighted RMSNorm of its output, as one op:
+# y = sum_i H_pre[i] x_i (kept: the pre-normalization intermediate) and
+# yn = y rho gamma.  Backward: the gradient at y is dy (if y is used
+# elsewhere) plus the RMSNorm backward of dyn; then the aggregate backward.
+# --------------------------------------------------------------------------
+
+def h_aggregate_rmsnorm_fwd(x, H_pre, gamma, eps):
+    y = h_aggregate_fwd(x, H_pre)
+    r = rmsnorm_residual_fwd(y, None, gamma, eps)
+    return {"y": y, "yn": r["y"], "rstd": r["rstd"]}
+
+
+def h_aggregate_rmsnorm_bwd(dyn, dy, x, H_pre, gamma, eps):
+    y = h_aggregate_fwd(x, H_pre)
+    r = rmsnorm_residual_bwd(dyn, dy, y, None, gamma, eps)
+    a = h_aggregate_bwd(r["dx"], x, H_pre)
+    return {"dx": a["dx"], "dH_pre": a["dH_pre"], "dgamma": r["dgamma"]}
+
+
+# --------------------------------------------------------------------------
+# proj_rms_compute_h over channel shards (RL-Kernel PR #383 task P1-6, the
+# fp32_gemm_rms TP/SP contract): per-shard partial sums, compute_h on the
+# totals, per-shard backward from the per-token du and RMS coefficient.
+# --------------------------------------------------------------------------
+
+def proj_rms_partials(xs, Ws):
+    xs = _f64(xs)
+    T, n, Cs = xs.shape
+    O = controller_width(n)
+    u = np.empty((T, O)); s = np.empty(T)
+    _check(_L().orc_proj_rms_partials(_p(xs), _p(_f64(Ws)), T, n, Cs, _p(u), _p(s)), "partials")
+    return {"u": u, "s": s}
+
+
+def compute_h_from_sums(u, s, K, alpha, b, n, iters, eps_sk, eps_rms):
+    u = _f64(u)
+    T = u.shape[0]
+    H_pre = np.empty((T, n)); H_post = np.empty((T, n)); H_res = np.empty((T, n, n))
+    r = np.empty(T)
+    _check(_L().orc_compute_h_from_sums(_p(u), _p(_f64(s)), K, _p(_f64(alpha)), _p(_f64(b)), T,
+                                        n, iters, eps_sk, eps_rms, _p(H_pre), _p(H_post),
+                                        _p(H_res), _p(r)), "compute_h_sums")
+    return {"H_pre": H_pre, "H_post": H_post, "H_res": H_res, "r": r}
+
+
+def compute_h_bwd_from_sums(dH_pre, dH_post, dH_res, u, s, K, alpha, b, n, iters, eps_sk,
+                            eps_rms):
+    u = _f64(u)
+    T, O = u.shape
+    du = np.empty((T, O)); coef = np.empty(T); dalpha = np.empty(3); db = np.empty(O)
+    _check(_L().orc_compute_h_bwd_from_sums(_p(_f64(dH_pre)), _p(_f64(dH_post)),
+                                            _p(_f64(dH_res)), _p(u), _p(_f64(s)), K,
+                                            _p(_f64(alpha)), _p(_f64(b)), T, n, iters, eps_sk,
+                                            eps_rms, _p(du), _p(coef), _p(dalpha), _p(db)),
+           "compute_h_bwd_sums")
+    return {"du": du, "coef": coef, "dalpha": dalpha, "db": db}
+
+
+def proj_rms_partial_bwd(xs, Ws, du, coef):
+    xs = _f64(xs)
+    T, n, Cs = xs.shape
+    O = controller_width(n)
+    dx = np.empty((T, n, Cs)); dW = np.empty((n * Cs, O))
+    _check(_L().orc_proj_rms_partial_bwd(_p(xs), _p(_f64(Ws)), _p(_f64(du)), _p(_f64(coef)), T,
+                                         n, Cs, _p(dx), _p(dW)), "partial_bwd")
+    return {"dx": dx, "dW": dW}
 
 
 # --------------------------------------------------------------------------

@@ -471,6 +471,269 @@ int orc_rmsnorm_bwd(const double *dy, const double *x, int64_t rows, int64_t col
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* h_aggregate with one static weight vector ([rwkv] StreamAggregateFwd/Bwd  */
+/* with per_token = false: H_pre is [n] instead of [B, T, n], and d_H_pre is */
+/* [n]).                                                                     */
+/*   y[t][c] = sum_i H_pre[i] x[t][i][c]                                      */
+/*   dx[t][i][c] = H_pre[i] dy[t][c];  dH_pre[i] = sum_t sum_c dy[t][c] x[t][i][c] */
+/* ------------------------------------------------------------------------ */
+
+int orc_h_aggregate_static_fwd(const double *x, const double *Hpre, int64_t T, int n, int64_t C,
+                               double *y)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t c = 0; c < C; ++c) {
+            double acc = 0.0;
+            for (int i = 0; i < n; ++i) acc += Hpre[i] * x[(t * n + i) * C + c];
+            y[t * C + c] = acc;
+        }
+    return 0;
+}
+
+int orc_h_aggregate_static_bwd(const double *dy, const double *x, const double *Hpre, int64_t T,
+                               int n, int64_t C, double *dx, double *dHpre)
+{
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            for (int i = 0; i < n; ++i)
+                for (int64_t c = 0; c < C; ++c) dx[(t * n + i) * C + c] = Hpre[i] * dy[t * C + c];
+    }
+    if (dHpre) {
+#pragma omp parallel for schedule(static)
+        for (int i = 0; i < n; ++i) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < T; ++t)
+                for (int64_t c = 0; c < C; ++c) acc += dy[t * C + c] * x[(t * n + i) * C + c];
+            dHpre[i] = acc;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* rmsnorm_residual ([rlk] PR body task P1-5 "RMSNorm + residual fork",      */
+/* P1-8 "cross-rank dgamma"; the review notes that rmsnorm_residual_fwd      */
+/* guards its own zero row; the follow-up commit: the pre-normalization      */
+/* intermediate must be exposed).  Reading: the fork h = x + res is both    */
+/* returned (the residual that continues) and normalized with a learnable    */
+/* per-channel weight gamma:                                                 */
+/*   h = x + res;  rho = 1 / sqrt(sum_c h^2 / C + eps);  y = h rho gamma       */
+/* res and gamma may be NULL (no residual add; gamma = 1).  Backward, with   */
+/* dh the gradient that reaches the fork output h from elsewhere (NULL = 0): */
+/*   g = dy gamma;  dx = dres = dh + rho g - rho^3 h (sum_c g h) / C          */
+/*   dgamma[c] = sum_t dy[t][c] h[t][c] rho_t   (ascending t)                 */
+/* ------------------------------------------------------------------------ */
+
+static double fork_h(const double *x, const double *res, int64_t i)
+{
+    return res ? x[i] + res[i] : x[i];
+}
+
+int orc_rmsnorm_residual_fwd(const double *x, const double *res, const double *gamma,
+                             int64_t rows, int64_t cols, double eps, double *h, double *y,
+                             double *rstd)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double s = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = fork_h(x, res, r * cols + c);
+            s += v * v;
+        }
+        double rho = 1.0 / sqrt(s / (double)cols + eps);
+        if (rstd) rstd[r] = rho;
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = fork_h(x, res, r * cols + c);
+            if (h) h[r * cols + c] = v;
+            if (y) y[r * cols + c] = v * rho * (gamma ? gamma[c] : 1.0);
+        }
+    }
+    return 0;
+}
+
+int orc_rmsnorm_residual_bwd(const double *dy, const double *dh, const double *x,
+                             const double *res, const double *gamma, int64_t rows, int64_t cols,
+                             double eps, double *dx, double *dgamma)
+{
+    double *rho_all = (double *)malloc(sizeof(double) * (size_t)(rows > 0 ? rows : 1));
+    if (!rho_all) return 2;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double s = 0.0, d = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            double v = fork_h(x, res, r * cols + c);
+            s += v * v;
+            d += dy[r * cols + c] * (gamma ? gamma[c] : 1.0) * v;
+        }
+        double rho = 1.0 / sqrt(s / (double)cols + eps);
+        rho_all[r] = rho;
+        if (dx)
+            for (int64_t c = 0; c < cols; ++c) {
+                double v = fork_h(x, res, r * cols + c);
+                double g = dy[r * cols + c] * (gamma ? gamma[c] : 1.0);
+                dx[r * cols + c] = (dh ? dh[r * cols + c] : 0.0) + rho * g -
+                                   rho * rho * rho * v * d / (double)cols;
+            }
+    }
+    if (dgamma) {
+#pragma omp parallel for schedule(static)
+        for (int64_t c = 0; c < cols; ++c) {
+            double acc = 0.0;
+            for (int64_t r = 0; r < rows; ++r)
+                acc += dy[r * cols + c] * fork_h(x, res, r * cols + c) * rho_all[r];
+            dgamma[c] = acc;
+        }
+    }
+    free(rho_all);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* proj_rms_compute_h over a channel-sharded residual ([rlk] PR body task    */
+/* P1-6 "fp32_gemm_rms TP/SP contract").  Reading: a shard owns channels     */
+/* [c0, c1) of every stream, i.e. the K indices k = i*C + c; s = sum x^2 and */
+/* u = x.W are sums over K, so a shard computes its partial sums, the        */
+/* partials are summed over shards, and compute_h runs on the totals with    */
+/* the full K.  In the backward, du and the RMS coefficient are per-token    */
+/* values of the totals; each shard forms dx and dW for its own K indices.   */
+/* Here a shard's x is [T][n][Cs] and its W rows are k' = i*Cs + c'.          */
+/* ------------------------------------------------------------------------ */
+
+int orc_proj_rms_partials(const double *xs, const double *Ws, int64_t T, int n, int64_t Cs,
+                          double *u, double *s)
+{
+    const int O = n * n + 2 * n;
+    const int64_t Ks = (int64_t)n * Cs;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double acc[ORC_MAX_N * ORC_MAX_N + 2 * ORC_MAX_N];
+        double sq = 0.0;
+        for (int o = 0; o < O; ++o) acc[o] = 0.0;
+        for (int64_t k = 0; k < Ks; ++k) {
+            double xv = xs[t * Ks + k];
+            sq += xv * xv;
+            for (int o = 0; o < O; ++o) acc[o] += xv * Ws[k * O + o];
+        }
+        for (int o = 0; o < O; ++o) u[t * O + o] = acc[o];
+        s[t] = sq;
+    }
+    return 0;
+}
+
+/* compute_h from the summed partials: q = sqrt(s/K), r = 1/(q + eps_rms),
+ * z = alpha_seg r u + b, then the gates and Sinkhorn. */
+int orc_compute_h_from_sums(const double *u, const double *s, int64_t K, const double *alpha,
+                            const double *b, int64_t T, int n, int iters, double eps_sk,
+                            double eps_rms, double *Hpre, double *Hpost, double *Hres,
+                            double *r_out)
+{
+    if (n < 1 || n > ORC_MAX_N) return 1;
+    const int O = n * n + 2 * n;
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double z[ORC_MAX_N * ORC_MAX_N + 2 * ORC_MAX_N];
+        double r = 1.0 / (sqrt(s[t] / (double)K) + eps_rms);
+        for (int o = 0; o < O; ++o) z[o] = seg_alpha(alpha, n, o) * r * u[t * O + o] + b[o];
+        compute_h_token(z, n, iters, eps_sk, Hpre + t * n, Hpost + t * n, Hres + t * n * n);
+        if (r_out) r_out[t] = r;
+    }
+    return 0;
+}
+
+/* Backward of compute_h from the totals: per token du[o] = alpha_seg r dz[o]
+ * and coef = dr (-r^2 / (K q)) (0 when q == 0), so that a shard's
+ * dx[k] = sum_o du[o] W[k][o] + coef x[k]; dalpha and db as in
+ * orc_proj_rms_compute_h_bwd (ascending t).  Any output may be NULL. */
+int orc_compute_h_bwd_from_sums(const double *dHpre, const double *dHpost, const double *dHres,
+                                const double *u, const double *s, int64_t K,
+                                const double *alpha, const double *b, int64_t T, int n,
+                                int iters, double eps_sk, double eps_rms, double *du,
+                                double *coef, double *dalpha, double *db)
+{
+    if (n < 1 || n > ORC_MAX_N) return 1;
+    const int O = n * n + 2 * n;
+    double *ga_all = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * 3);
+    double *dz_all = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * O);
+    const size_t trace_len = (size_t)(2 * iters + 1) * n * n;
+    double *traces = (double *)malloc(sizeof(double) * trace_len * (size_t)(T > 0 ? T : 1));
+    if (!ga_all || !dz_all || !traces) {
+        free(ga_all); free(dz_all); free(traces);
+        return 2;
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double z[ORC_MAX_N * ORC_MAX_N + 2 * ORC_MAX_N], dz[ORC_MAX_N * ORC_MAX_N + 2 * ORC_MAX_N];
+        double g[ORC_MAX_N * ORC_MAX_N];
+        const double *ut = u + t * O;
+        double q = sqrt(s[t] / (double)K);
+        double r = 1.0 / (q + eps_rms);
+        for (int o = 0; o < O; ++o) z[o] = seg_alpha(alpha, n, o) * r * ut[o] + b[o];
+        for (int i = 0; i < n; ++i) {
+            double sp = sigmoid(z[i]);
+            double so = sigmoid(z[n + i]);
+            dz[i] = dHpre[t * n + i] * sp * (1.0 - sp);
+            dz[n + i] = dHpost[t * n + i] * 2.0 * so * (1.0 - so);
+        }
+        for (int e = 0; e < n * n; ++e) g[e] = dHres[t * n * n + e];
+        sinkhorn_bwd_one(g, z + 2 * n, n, iters, eps_sk, dz + 2 * n, traces + (size_t)t * trace_len);
+        double ga[3] = {0.0, 0.0, 0.0};
+        double dr = 0.0;
+        for (int o = 0; o < O; ++o) {
+            int sgi = (o < n) ? 0 : (o < 2 * n ? 1 : 2);
+            ga[sgi] += dz[o] * r * ut[o];
+            dr += dz[o] * seg_alpha(alpha, n, o) * ut[o];
+            if (du) du[t * O + o] = seg_alpha(alpha, n, o) * r * dz[o];
+            dz_all[t * O + o] = dz[o];
+        }
+        for (int k = 0; k < 3; ++k) ga_all[t * 3 + k] = ga[k];
+        if (coef) coef[t] = (q > 0.0) ? dr * (-(r * r) / ((double)K * q)) : 0.0;
+    }
+    if (dalpha) {
+        for (int k = 0; k < 3; ++k) dalpha[k] = 0.0;
+        for (int64_t t = 0; t < T; ++t)
+            for (int k = 0; k < 3; ++k) dalpha[k] += ga_all[t * 3 + k];
+    }
+    if (db) {
+        for (int o = 0; o < O; ++o) db[o] = 0.0;
+        for (int64_t t = 0; t < T; ++t)
+            for (int o = 0; o < O; ++o) db[o] += dz_all[t * O + o];
+    }
+    free(ga_all); free(dz_all); free(traces);
+    return 0;
+}
+
+/* A shard's part of the projection backward:
+ *   dx[t][k'] = sum_o du[t][o] W[k'][o] + coef[t] x[t][k'];  dW[k'][o] = sum_t x[t][k'] du[t][o] */
+int orc_proj_rms_partial_bwd(const double *xs, const double *Ws, const double *du,
+                             const double *coef, int64_t T, int n, int64_t Cs, double *dx,
+                             double *dW)
+{
+    const int O = n * n + 2 * n;
+    const int64_t Ks = (int64_t)n * Cs;
+    if (dx) {
+#pragma omp parallel for schedule(static)
+        for (int64_t t = 0; t < T; ++t)
+            for (int64_t k = 0; k < Ks; ++k) {
+                double acc = 0.0;
+                for (int o = 0; o < O; ++o) acc += du[t * O + o] * Ws[k * O + o];
+                dx[t * Ks + k] = acc + coef[t] * xs[t * Ks + k];
+            }
+    }
+    if (dW) {
+#pragma omp parallel for schedule(static)
+        for (int64_t k = 0; k < Ks; ++k)
+            for (int o = 0; o < O; ++o) {
+                double acc = 0.0;
+                for (int64_t t = 0; t < T; ++t) acc += xs[t * Ks + k] * du[t * O + o];
+                dW[k * O + o] = acc;
+            }
+    }
+    return 0;
+}
+
 int orc_num_threads(void)
 {
     int nt = 1;
