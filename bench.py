@@ -203,6 +203,104 @@ def job_tokens_per_s(T, world, ms):
 
 
 # ---------------------------------------------------------------------------
+# every op of the C ABI on its own, at the workload's sizes
+# ---------------------------------------------------------------------------
+
+def bench_ops(M, d, o, T, n, C, dev, reps=5):
+    """Event-timed average of each op (after 2 untimed calls) with its
+    algorithmic HBM bytes (U = one bf16 [T, C] tensor) and the GB/s that
+    gives.  Inputs reuse the step's tensors; all are larger than L2 except
+    the Sinkhorn batch (32768 matrices, latency-bound)."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    e = lambda *sh, dt=f32: torch.empty(*sh, dtype=dt, device=dev)  # noqa: E731
+    U = T * C * 2
+    O = n * n + 2 * n
+    K = n * C
+    x, f, bias, W = d["x"], d["f"], d["bias"], d["W"]
+    alpha, b, dout, dy = d["alpha"], d["b"], d["dout"], d["dy"]
+    Hp, Hq, Hr = o["H_pre"], o["H_post"], o["H_res"]
+    g = torch.ones(C, device=dev)
+    Hs = torch.full((n,), 0.5, device=dev)
+    y, dxb, dfb = e(T, C, dt=bf), e(T, n, C, dt=bf), e(T, C, dt=bf)
+    outb = e(T, n, C, dt=bf)
+    dHp, dHq, dHr = (torch.full((T, n), 0.1, device=dev), torch.full((T, n), 0.1, device=dev),
+                     torch.full((T, n, n), 0.1, device=dev))
+    y2, dx2 = e(T, C, dt=bf), e(T, C, dt=bf)
+    rstd, dg = e(T), e(C)
+    u, sq, r = e(T, O), e(T), e(T)
+    du, coef, dal, dbb, dW = e(T, O), e(T), e(3), e(O), e(K, O)
+    Cs = C // 2
+    xs = x[:, :, :Cs].contiguous()
+    Ws = torch.cat([W[i * C:i * C + Cs] for i in range(n)]).contiguous()
+    dxs, dWs = e(T, n, Cs, dt=bf), e(n * Cs, O)
+    Mm = 32768
+    lg = torch.randn(Mm, n, n, device=dev)
+    dP = torch.randn(Mm, n, n, device=dev)
+    P, dl = e(Mm, n, n), e(Mm, n, n)
+    W_ = lambda op, c=C: M.workspace(op, T, n, c, dev)  # noqa: E731
+    wsf, wsb = W_(M.OP_PROJ_RMS_COMPUTE_H_FWD), W_(M.OP_PROJ_RMS_COMPUTE_H_BWD)
+    wspb, wsas = W_(M.OP_H_POST_BDA_BWD), W_(M.OP_H_AGGREGATE_STATIC_BWD)
+    wsr, wsan = M.workspace(M.OP_RMSNORM_RESIDUAL_BWD, T, 0, C, dev), W_(M.OP_H_AGGREGATE_RMSNORM_BWD)
+    wspf, wspb2 = W_(M.OP_PROJ_RMS_PARTIAL_FWD, Cs), W_(M.OP_PROJ_RMS_PARTIAL_BWD, Cs)
+    wsch = W_(M.OP_COMPUTE_H_BWD, 8)
+    it, es, er = ITERS, EPS_SK, EPS_RMS
+    ops = {
+        "mhc_sinkhorn_fwd": (lambda: M.mhc_sinkhorn_fwd(lg, P, it, es), Mm * n * n * 8),
+        "mhc_sinkhorn_bwd": (lambda: M.mhc_sinkhorn_bwd(dP, lg, dl, it, es), Mm * n * n * 12),
+        "mhc_proj_rms_compute_h_fwd": (lambda: M.mhc_proj_rms_compute_h_fwd(
+            x, W, alpha, b, it, es, er, Hp, Hq, Hr, u, r, wsf), n * U),
+        "mhc_proj_rms_compute_h_bwd": (lambda: M.mhc_proj_rms_compute_h_bwd(
+            dHp, dHq, dHr, x, W, alpha, b, u, r, it, es, er, dxb, dW, dal, dbb, wsb), 2 * n * U),
+        "mhc_h_aggregate_fwd": (lambda: M.mhc_h_aggregate_fwd(x, Hp, y), (n + 1) * U),
+        "mhc_h_aggregate_bwd": (lambda: M.mhc_h_aggregate_bwd(dy, x, Hp, dxb, dHp),
+                                (2 * n + 1) * U),
+        "mhc_h_post_bda_fwd": (lambda: M.mhc_h_post_bda_fwd(x, f, bias, Hr, Hq, outb),
+                               (2 * n + 1) * U),
+        "mhc_h_post_bda_bwd": (lambda: M.mhc_h_post_bda_bwd(dout, x, f, bias, Hr, Hq, dxb, dfb,
+                                                            dg, dHr, dHq, wspb), (3 * n + 2) * U),
+        "rmsnorm_fwd": (lambda: M.rmsnorm_fwd(y, dfb, rstd, EPS_NORM), 2 * U),
+        "rmsnorm_bwd": (lambda: M.rmsnorm_bwd(dy, y, rstd, dfb, EPS_NORM), 3 * U),
+        "mhc_h_aggregate_static_fwd": (lambda: M.mhc_h_aggregate_static_fwd(x, Hs, y),
+                                       (n + 1) * U),
+        "mhc_h_aggregate_static_bwd": (lambda: M.mhc_h_aggregate_static_bwd(
+            dy, x, Hs, dxb, dHp[0], wsas), (2 * n + 1) * U),
+        "rmsnorm_residual_fwd": (lambda: M.rmsnorm_residual_fwd(
+            y, f, g, dfb, y2, rstd, EPS_NORM), 4 * U),
+        "rmsnorm_residual_bwd": (lambda: M.rmsnorm_residual_bwd(
+            dy, None, y, f, g, rstd, dx2, dg, EPS_NORM, wsr), 4 * U),
+        "mhc_h_aggregate_rmsnorm_fwd": (lambda: M.mhc_h_aggregate_rmsnorm_fwd(
+            x, Hp, g, y, dfb, rstd, EPS_NORM), (n + 2) * U),
+        "mhc_h_aggregate_rmsnorm_bwd": (lambda: M.mhc_h_aggregate_rmsnorm_bwd(
+            dy, None, x, Hp, g, rstd, dxb, dHp, dg, EPS_NORM, wsan), (2 * n + 1) * U),
+        "mhc_proj_rms_partial_fwd": (lambda: M.mhc_proj_rms_partial_fwd(xs, Ws, u, sq, wspf),
+                                     n * U // 2),
+        "mhc_compute_h_fwd": (lambda: M.mhc_compute_h_fwd(u, sq, K, alpha, b, it, es, er, Hp, Hq,
+                                                          Hr, r), T * (O + 1) * 4),
+        "mhc_compute_h_bwd": (lambda: M.mhc_compute_h_bwd(dHp, dHq, dHr, u, sq, K, alpha, b, it,
+                                                          es, er, du, coef, dal, dbb, wsch),
+                              T * (3 * O + 1) * 4),
+        "mhc_proj_rms_partial_bwd": (lambda: M.mhc_proj_rms_partial_bwd(xs, Ws, du, coef, dxs,
+                                                                        dWs, wspb2), n * U),
+    }
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name, (fn, nbytes) in ops.items():
+        fn(); fn()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        z.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(z) / reps
+        res[name] = {"ms": round(ms, 4), "alg_bytes": int(nbytes),
+                     "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+    return res
+
+
+# ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
 
@@ -312,6 +410,9 @@ def run_ours(args, rank, world):
     lms = ev0.elapsed_time(ev1) / args.steps
     lms = max_over_ranks(lms, world, dev)
 
+    # ---- every op on its own ----
+    ops = None if args.no_ops else bench_ops(M, d, o, T, n, C, dev)
+
     # ---- end to end: pinned host inputs -> device -> step -> host grads ----
     e2e = None
     if not args.no_e2e:
@@ -402,6 +503,7 @@ def run_ours(args, rank, world):
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
+        "ops": ops,
     }
     return res
 
@@ -484,6 +586,7 @@ def main():
                     choices=[k for k in mi.LAYER_WORKLOADS if "fwd_" not in k])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-ops", action="store_true", help="skip the per-op timings")
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--ref-tokens", type=int, default=1024)
     args = ap.parse_args()

@@ -94,11 +94,17 @@ typedef enum {
     MHC_OP_PROJ_RMS_COMPUTE_H_BWD = 2,
     MHC_OP_H_POST_BDA_BWD = 3,
     MHC_OP_LAYER_FWD = 4,
-    MHC_OP_LAYER_BWD = 5
+    MHC_OP_LAYER_BWD = 5,
+    MHC_OP_RMSNORM_RESIDUAL_BWD = 6,   /* (rows, -, cols); only when dgamma is wanted */
+    MHC_OP_H_AGGREGATE_RMSNORM_BWD = 7, /* only when dgamma is wanted */
+    MHC_OP_H_AGGREGATE_STATIC_BWD = 8,
+    MHC_OP_PROJ_RMS_PARTIAL_FWD = 9,   /* C = the shard's channels Cs */
+    MHC_OP_COMPUTE_H_BWD = 10,
+    MHC_OP_PROJ_RMS_PARTIAL_BWD = 11   /* C = the shard's channels Cs */
 } mhc_op;
 
 /* Workspace bytes an op needs for (T, n, C); 0 for a bad op or shape.
- * The other ops need none. */
+ * The other ops need none.  MHC_OP_RMSNORM_RESIDUAL_BWD ignores n. */
 MHC_API size_t mhc_workspace_bytes(mhc_op op, int64_t T, int n, int64_t C);
 
 /* ------------------------------------------------------------------ */
@@ -210,6 +216,130 @@ MHC_API mhc_status rmsnorm_fwd(const mhc_bf16 *x, mhc_bf16 *y, float *rstd, int6
  * to recompute rho from x. */
 MHC_API mhc_status rmsnorm_bwd(const mhc_bf16 *dy, const mhc_bf16 *x, const float *rstd, mhc_bf16 *dx,
                        int64_t rows, int64_t cols, float eps, mhc_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* h_aggregate with one static H_pre [n] for every token ([rwkv]        */
+/* StreamAggregateFwd/Bwd with per_token = false: H_pre [n], d_H_pre [n]).*/
+/* ------------------------------------------------------------------ */
+
+/* y[t][c] = sum_i H_pre[i] x[t][i][c].  x [T,n,C] bf16, H_pre [n] fp32,
+ * y [T,C] bf16. */
+MHC_API mhc_status mhc_h_aggregate_static_fwd(const mhc_bf16 *x, const float *H_pre, mhc_bf16 *y,
+                                              int64_t T, int n, int64_t C, mhc_stream_t stream);
+
+/* dx[t][i][c] = H_pre[i] dy[t][c] (bf16; dx may be NULL),
+ * dH_pre[i] = sum_t sum_c dy[t][c] x[t][i][c] (fp32 [n], fixed summation order).
+ * ws: mhc_workspace_bytes(MHC_OP_H_AGGREGATE_STATIC_BWD, T, n, C).  T = 0
+ * writes dH_pre = 0. */
+MHC_API mhc_status mhc_h_aggregate_static_bwd(const mhc_bf16 *dy, const mhc_bf16 *x,
+                                              const float *H_pre, mhc_bf16 *dx, float *dH_pre,
+                                              int64_t T, int n, int64_t C, void *ws,
+                                              size_t ws_bytes, mhc_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* rmsnorm_residual: RMSNorm with a residual fork and a learnable       */
+/* weight ([rlk] PR body tasks P1-5 "RMSNorm + residual fork" and P1-8  */
+/* "cross-rank dgamma"; the follow-up commit: the pre-normalization     */
+/* intermediate is exposed).                                           */
+/* ------------------------------------------------------------------ */
+
+/* h = x + res (res NULL: h = x), rho = 1/sqrt(mean_c h^2 + eps),
+ * y = h rho gamma (gamma NULL: 1).  x, res, h, y [rows, cols] bf16; gamma
+ * [cols] fp32; rstd [rows] fp32.  h (the fork) and rstd may be NULL.  The
+ * norm uses the fp32 sum; h is its bf16 rounding.  cols % 8 == 0,
+ * cols <= 32768. */
+MHC_API mhc_status rmsnorm_residual_fwd(const mhc_bf16 *x, const mhc_bf16 *res,
+                                        const float *gamma, mhc_bf16 *h, mhc_bf16 *y,
+                                        float *rstd, int64_t rows, int64_t cols, float eps,
+                                        mhc_stream_t stream);
+
+/* With g = dy gamma:
+ *   dx = dres = dh + rho g - rho^3 h (sum_c g h) / cols     (bf16; the one
+ *        gradient of both x and res; dh, the gradient reaching the fork
+ *        output h from elsewhere, may be NULL = 0)
+ *   dgamma[c] = sum_t dy h rho (fp32 [cols], fixed order; NULL to skip).
+ * rstd from the forward, or NULL to recompute rho.
+ * ws: mhc_workspace_bytes(MHC_OP_RMSNORM_RESIDUAL_BWD, rows, 0, cols), needed
+ * only with dgamma.  rows = 0 writes dgamma = 0. */
+MHC_API mhc_status rmsnorm_residual_bwd(const mhc_bf16 *dy, const mhc_bf16 *dh,
+                                        const mhc_bf16 *x, const mhc_bf16 *res,
+                                        const float *gamma, const float *rstd, mhc_bf16 *dx,
+                                        float *dgamma, int64_t rows, int64_t cols, float eps,
+                                        void *ws, size_t ws_bytes, mhc_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* h_aggregate followed by the weighted RMSNorm of its output, in one   */
+/* pass over x ([mcore] fused_h_aggregate; [rlk] rmsnorm_residual).     */
+/* ------------------------------------------------------------------ */
+
+/* y = sum_i H_pre[t][i] x_i (the pre-normalization intermediate; bf16 [T,C],
+ * may be NULL), yn = y rho gamma with rho = 1/sqrt(mean_c y^2 + eps) from
+ * the fp32 y (bf16 [T,C]); rstd [T] fp32 (may be NULL).  H_pre [T,n] fp32,
+ * gamma [C] fp32 or NULL.  C <= 32768. */
+MHC_API mhc_status mhc_h_aggregate_rmsnorm_fwd(const mhc_bf16 *x, const float *H_pre,
+                                               const float *gamma, mhc_bf16 *y, mhc_bf16 *yn,
+                                               float *rstd, int64_t T, int n, int64_t C,
+                                               float eps, mhc_stream_t stream);
+
+/* With dy_total = dy + rho g - rho^3 y (sum_c g y)/C, g = dyn gamma (dy, the
+ * gradient reaching y from elsewhere, may be NULL):
+ *   dx[t][i][c] = H_pre[t][i] dy_total (bf16), dH_pre[t][i] = sum_c dy_total x_i
+ *   (fp32), dgamma[c] = sum_t dyn y rho (fp32, fixed order; NULL to skip).
+ * rstd from the forward or NULL to recompute.  ws:
+ * mhc_workspace_bytes(MHC_OP_H_AGGREGATE_RMSNORM_BWD, T, n, C), only with dgamma. */
+MHC_API mhc_status mhc_h_aggregate_rmsnorm_bwd(const mhc_bf16 *dyn, const mhc_bf16 *dy,
+                                               const mhc_bf16 *x, const float *H_pre,
+                                               const float *gamma, const float *rstd,
+                                               mhc_bf16 *dx, float *dH_pre, float *dgamma,
+                                               int64_t T, int n, int64_t C, float eps, void *ws,
+                                               size_t ws_bytes, mhc_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* proj_rms_compute_h over channel shards ([rlk] PR body task P1-6,     */
+/* the fp32_gemm_rms TP/SP contract).  A shard owns channels [c0, c1)  */
+/* of every stream: x_shard [T, n, Cs] bf16 and W_shard [n*Cs, O] fp32 */
+/* with rows i*Cs + c' (the rows i*C + c0 + c' of W).  Each shard      */
+/* computes partial sums; the caller sums them over shards (an         */
+/* all-reduce); compute_h runs on the totals with the full K = n*C;    */
+/* each shard forms dx and dW for its own channels from the per-token  */
+/* du and RMS coefficient.                                             */
+/* ------------------------------------------------------------------ */
+
+/* u_part[t][o] = sum_{k in shard} x[t][k] W[k][o], s_part[t] = sum_{k in shard} x^2
+ * (fp32).  ws: mhc_workspace_bytes(MHC_OP_PROJ_RMS_PARTIAL_FWD, T, n, Cs). */
+MHC_API mhc_status mhc_proj_rms_partial_fwd(const mhc_bf16 *x_shard, const float *W_shard,
+                                            int64_t T, int n, int64_t Cs, float *u_part,
+                                            float *s_part, void *ws, size_t ws_bytes,
+                                            mhc_stream_t stream);
+
+/* compute_h from the totals u [T,O], s [T]: r = 1/(sqrt(s/K) + eps_rms),
+ * z = alpha_seg r u + b, gates and Sinkhorn as mhc_proj_rms_compute_h_fwd.
+ * r_save [T] may be NULL. */
+MHC_API mhc_status mhc_compute_h_fwd(const float *u, const float *s, int64_t K,
+                                     const float *alpha3, const float *b, int64_t T, int n,
+                                     int iters, float eps_sk, float eps_rms, float *H_pre,
+                                     float *H_post, float *H_res, float *r_save,
+                                     mhc_stream_t stream);
+
+/* Per-token backward coefficients from the totals: du[t][o] = alpha_seg r dz[o]
+ * ([T,O] fp32) and coef[t] = -dr r^2/(K q) ([T]; 0 for an all-zero row), so
+ * that a shard's dx = du W_shard^T + coef x_shard; dalpha3 [3], db [O] summed
+ * over tokens (fixed order).  ws: mhc_workspace_bytes(MHC_OP_COMPUTE_H_BWD, T, n, 8). */
+MHC_API mhc_status mhc_compute_h_bwd(const float *dH_pre, const float *dH_post,
+                                     const float *dH_res, const float *u, const float *s,
+                                     int64_t K, const float *alpha3, const float *b, int64_t T,
+                                     int n, int iters, float eps_sk, float eps_rms, float *du,
+                                     float *coef, float *dalpha3, float *db, void *ws,
+                                     size_t ws_bytes, mhc_stream_t stream);
+
+/* A shard's dx_shard[t][k'] = sum_o du[t][o] W_shard[k'][o] + coef[t] x_shard[t][k']
+ * (bf16) and dW_shard[k'][o] = sum_t x_shard[t][k'] du[t][o] (fp32).
+ * ws: mhc_workspace_bytes(MHC_OP_PROJ_RMS_PARTIAL_BWD, T, n, Cs). */
+MHC_API mhc_status mhc_proj_rms_partial_bwd(const mhc_bf16 *x_shard, const float *W_shard,
+                                            const float *du, const float *coef, int64_t T,
+                                            int n, int64_t Cs, mhc_bf16 *dx_shard,
+                                            float *dW_shard, void *ws, size_t ws_bytes,
+                                            mhc_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Per-kernel timing (off by default).  When enabled, every kernel the  */

@@ -22,6 +22,12 @@ __all__ = [
     "mhc_h_post_bda_fwd", "mhc_h_post_bda_bwd", "rmsnorm_fwd", "rmsnorm_bwd", "mhc_layer_fwd",
     "mhc_layer_bwd", "OP_PROJ_RMS_COMPUTE_H_FWD", "OP_PROJ_RMS_COMPUTE_H_BWD",
     "OP_H_POST_BDA_BWD", "OP_LAYER_FWD", "OP_LAYER_BWD", "mhc_proj_rms_compute_h_fwd_noalloc",
+    "mhc_h_aggregate_static_fwd", "mhc_h_aggregate_static_bwd", "rmsnorm_residual_fwd",
+    "rmsnorm_residual_bwd", "mhc_h_aggregate_rmsnorm_fwd", "mhc_h_aggregate_rmsnorm_bwd",
+    "mhc_proj_rms_partial_fwd", "mhc_compute_h_fwd", "mhc_compute_h_bwd",
+    "mhc_proj_rms_partial_bwd", "OP_RMSNORM_RESIDUAL_BWD", "OP_H_AGGREGATE_RMSNORM_BWD",
+    "OP_H_AGGREGATE_STATIC_BWD", "OP_PROJ_RMS_PARTIAL_FWD", "OP_COMPUTE_H_BWD",
+    "OP_PROJ_RMS_PARTIAL_BWD",
 ]
 
 

@@ -22,6 +22,12 @@ OP_PROJ_RMS_COMPUTE_H_BWD = 2
 OP_H_POST_BDA_BWD = 3
 OP_LAYER_FWD = 4
 OP_LAYER_BWD = 5
+OP_RMSNORM_RESIDUAL_BWD = 6
+OP_H_AGGREGATE_RMSNORM_BWD = 7
+OP_H_AGGREGATE_STATIC_BWD = 8
+OP_PROJ_RMS_PARTIAL_FWD = 9
+OP_COMPUTE_H_BWD = 10
+OP_PROJ_RMS_PARTIAL_BWD = 11
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -50,6 +56,18 @@ _SIGS = {
     "mhc_device_error": [ctypes.POINTER(ctypes.c_int), _P],
     "mhc_proj_rms_compute_h_fwd_noalloc": [_P, _P, _P, _P, _I64, _I, _I64, _I, _F, _F, _P, _P,
                                            _P, _P, _P, _P],
+    "mhc_h_aggregate_static_fwd": [_P, _P, _P, _I64, _I, _I64, _P],
+    "mhc_h_aggregate_static_bwd": [_P, _P, _P, _P, _P, _I64, _I, _I64, _P, _SZ, _P],
+    "rmsnorm_residual_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P],
+    "rmsnorm_residual_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _F, _P, _SZ, _P],
+    "mhc_h_aggregate_rmsnorm_fwd": [_P, _P, _P, _P, _P, _P, _I64, _I, _I64, _F, _P],
+    "mhc_h_aggregate_rmsnorm_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _F, _P,
+                                    _SZ, _P],
+    "mhc_proj_rms_partial_fwd": [_P, _P, _I64, _I, _I64, _P, _P, _P, _SZ, _P],
+    "mhc_compute_h_fwd": [_P, _P, _I64, _P, _P, _I64, _I, _I, _F, _F, _P, _P, _P, _P, _P],
+    "mhc_compute_h_bwd": [_P, _P, _P, _P, _P, _I64, _P, _P, _I64, _I, _I, _F, _F, _P, _P, _P, _P,
+                          _P, _SZ, _P],
+    "mhc_proj_rms_partial_bwd": [_P, _P, _P, _P, _I64, _I, _I64, _P, _P, _P, _SZ, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -272,3 +290,110 @@ def mhc_proj_rms_compute_h_fwd_noalloc(x, W, alpha3, b, iters, eps_sk, eps_rms, 
         _ptr(H_pre, _F32, (T, n), "H_pre"), _ptr(H_post, _F32, (T, n), "H_post"),
         _ptr(H_res, _F32, (T, n, n), "H_res"), _ptr(u_save, _F32, (T, O), "u_save"),
         _ptr(r_save, _F32, (T,), "r_save"), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------
+# ops beyond the layer path
+# ---------------------------------------------------------------------------
+
+def mhc_h_aggregate_static_fwd(x, H_pre, y, stream=None):
+    T, n, C = x.shape
+    _ok(lib.mhc_h_aggregate_static_fwd(_ptr(x, _BF, name="x"), _ptr(H_pre, _F32, (n,), "H_pre"),
+                                       _ptr(y, _BF, (T, C), "y"), T, n, C, _stream(stream)))
+
+
+def mhc_h_aggregate_static_bwd(dy, x, H_pre, dx, dH_pre, ws, stream=None):
+    T, n, C = x.shape
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_h_aggregate_static_bwd(
+        _ptr(dy, _BF, (T, C), "dy"), _ptr(x, _BF, name="x"), _ptr(H_pre, _F32, (n,), "H_pre"),
+        _ptr(dx, _BF, (T, n, C), "dx"), _ptr(dH_pre, _F32, (n,), "dH_pre"), T, n, C, wp, wb,
+        _stream(stream)))
+
+
+def rmsnorm_residual_fwd(x, res, gamma, h, y, rstd, eps, stream=None):
+    rows, cols = x.shape
+    _ok(lib.rmsnorm_residual_fwd(
+        _ptr(x, _BF, name="x"), _ptr(res, _BF, (rows, cols), "res"),
+        _ptr(gamma, _F32, (cols,), "gamma"), _ptr(h, _BF, (rows, cols), "h"),
+        _ptr(y, _BF, (rows, cols), "y"), _ptr(rstd, _F32, (rows,), "rstd"), rows, cols, eps,
+        _stream(stream)))
+
+
+def rmsnorm_residual_bwd(dy, dh, x, res, gamma, rstd, dx, dgamma, eps, ws=None, stream=None):
+    rows, cols = x.shape
+    wp, wb = _ws(ws)
+    _ok(lib.rmsnorm_residual_bwd(
+        _ptr(dy, _BF, (rows, cols), "dy"), _ptr(dh, _BF, (rows, cols), "dh"),
+        _ptr(x, _BF, name="x"), _ptr(res, _BF, (rows, cols), "res"),
+        _ptr(gamma, _F32, (cols,), "gamma"), _ptr(rstd, _F32, (rows,), "rstd"),
+        _ptr(dx, _BF, (rows, cols), "dx"), _ptr(dgamma, _F32, (cols,), "dgamma"), rows, cols,
+        eps, wp, wb, _stream(stream)))
+
+
+def mhc_h_aggregate_rmsnorm_fwd(x, H_pre, gamma, y, yn, rstd, eps, stream=None):
+    T, n, C = x.shape
+    _ok(lib.mhc_h_aggregate_rmsnorm_fwd(
+        _ptr(x, _BF, name="x"), _ptr(H_pre, _F32, (T, n), "H_pre"),
+        _ptr(gamma, _F32, (C,), "gamma"), _ptr(y, _BF, (T, C), "y"),
+        _ptr(yn, _BF, (T, C), "yn"), _ptr(rstd, _F32, (T,), "rstd"), T, n, C, eps,
+        _stream(stream)))
+
+
+def mhc_h_aggregate_rmsnorm_bwd(dyn, dy, x, H_pre, gamma, rstd, dx, dH_pre, dgamma, eps,
+                                ws=None, stream=None):
+    T, n, C = x.shape
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_h_aggregate_rmsnorm_bwd(
+        _ptr(dyn, _BF, (T, C), "dyn"), _ptr(dy, _BF, (T, C), "dy"), _ptr(x, _BF, name="x"),
+        _ptr(H_pre, _F32, (T, n), "H_pre"), _ptr(gamma, _F32, (C,), "gamma"),
+        _ptr(rstd, _F32, (T,), "rstd"), _ptr(dx, _BF, (T, n, C), "dx"),
+        _ptr(dH_pre, _F32, (T, n), "dH_pre"), _ptr(dgamma, _F32, (C,), "dgamma"), T, n, C, eps,
+        wp, wb, _stream(stream)))
+
+
+def mhc_proj_rms_partial_fwd(x_shard, W_shard, u_part, s_part, ws, stream=None):
+    T, n, Cs = x_shard.shape
+    O = _O(n)
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_proj_rms_partial_fwd(
+        _ptr(x_shard, _BF, name="x_shard"), _ptr(W_shard, _F32, (n * Cs, O), "W_shard"), T, n,
+        Cs, _ptr(u_part, _F32, (T, O), "u_part"), _ptr(s_part, _F32, (T,), "s_part"), wp, wb,
+        _stream(stream)))
+
+
+def mhc_compute_h_fwd(u, s, K, alpha3, b, iters, eps_sk, eps_rms, H_pre, H_post, H_res, r_save,
+                      stream=None):
+    T, O = u.shape
+    n = H_pre.shape[1]
+    _ok(lib.mhc_compute_h_fwd(
+        _ptr(u, _F32, (T, _O(n)), "u"), _ptr(s, _F32, (T,), "s"), K,
+        _ptr(alpha3, _F32, (3,), "alpha3"), _ptr(b, _F32, (O,), "b"), T, n, iters, eps_sk,
+        eps_rms, _ptr(H_pre, _F32, (T, n), "H_pre"), _ptr(H_post, _F32, (T, n), "H_post"),
+        _ptr(H_res, _F32, (T, n, n), "H_res"), _ptr(r_save, _F32, (T,), "r_save"),
+        _stream(stream)))
+
+
+def mhc_compute_h_bwd(dH_pre, dH_post, dH_res, u, s, K, alpha3, b, iters, eps_sk, eps_rms, du,
+                      coef, dalpha3, db, ws, stream=None):
+    T, n = dH_pre.shape
+    O = _O(n)
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_compute_h_bwd(
+        _ptr(dH_pre, _F32, (T, n), "dH_pre"), _ptr(dH_post, _F32, (T, n), "dH_post"),
+        _ptr(dH_res, _F32, (T, n, n), "dH_res"), _ptr(u, _F32, (T, O), "u"),
+        _ptr(s, _F32, (T,), "s"), K, _ptr(alpha3, _F32, (3,), "alpha3"),
+        _ptr(b, _F32, (O,), "b"), T, n, iters, eps_sk, eps_rms, _ptr(du, _F32, (T, O), "du"),
+        _ptr(coef, _F32, (T,), "coef"), _ptr(dalpha3, _F32, (3,), "dalpha3"),
+        _ptr(db, _F32, (O,), "db"), wp, wb, _stream(stream)))
+
+
+def mhc_proj_rms_partial_bwd(x_shard, W_shard, du, coef, dx_shard, dW_shard, ws, stream=None):
+    T, n, Cs = x_shard.shape
+    O = _O(n)
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_proj_rms_partial_bwd(
+        _ptr(x_shard, _BF, name="x_shard"), _ptr(W_shard, _F32, (n * Cs, O), "W_shard"),
+        _ptr(du, _F32, (T, O), "du"), _ptr(coef, _F32, (T,), "coef"), T, n, Cs,
+        _ptr(dx_shard, _BF, (T, n, Cs), "dx_shard"), _ptr(dW_shard, _F32, (n * Cs, O), "dW_shard"),
+        wp, wb, _stream(stream)))

@@ -192,8 +192,16 @@ mhc_status mhc_device_error(int *code, mhc_stream_t stream)
 
 size_t mhc_workspace_bytes(mhc_op op, int64_t T, int n, int64_t C)
 {
-    if (T < 0 || (n != 4 && n != 8) || C < 8 || C % 8 != 0) return 0;
+    if (T < 0 || C < 8 || C % 8 != 0) return 0;
+    if (op == MHC_OP_RMSNORM_RESIDUAL_BWD) return mhc::norm_ws_bytes(T, C);  // n unused
+    if (n != 4 && n != 8) return 0;
     switch (op) {
+    case MHC_OP_RMSNORM_RESIDUAL_BWD: return 0;
+    case MHC_OP_H_AGGREGATE_RMSNORM_BWD: return mhc::norm_ws_bytes(T, C);
+    case MHC_OP_H_AGGREGATE_STATIC_BWD: return mhc::agg_static_ws_bytes(T, n);
+    case MHC_OP_PROJ_RMS_PARTIAL_FWD: return mhc::proj_fwd_ws_bytes(T, n, C);
+    case MHC_OP_COMPUTE_H_BWD: return mhc::compute_h_bwd_ws_bytes(T, n);
+    case MHC_OP_PROJ_RMS_PARTIAL_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
     case MHC_OP_PROJ_RMS_COMPUTE_H_FWD: return mhc::proj_fwd_ws_bytes(T, n, C);
     case MHC_OP_PROJ_RMS_COMPUTE_H_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
     case MHC_OP_H_POST_BDA_BWD: return mhc::dbias_ws_bytes(T, C);
@@ -442,6 +450,219 @@ mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const mhc_bf1
                                      u_save, r_save, T, n, C, iters, eps_sk, eps_rms,
                                      reinterpret_cast<bf16 *>(dx), reinterpret_cast<bf16 *>(df),
                                      dW, dalpha3, db, dbias, ws, fault_ptr(), stream));
+}
+
+/* ---------------------------------------------------------------------- */
+/* Ops beyond the layer path                                               */
+/* ---------------------------------------------------------------------- */
+
+mhc_status mhc_h_aggregate_static_fwd(const mhc_bf16 *x, const float *H_pre, mhc_bf16 *y,
+                                      int64_t T, int n, int64_t C, mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_static_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x, "x").ptr(H_pre, "H_pre").ptr(y, "y").device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggregate_fwd(reinterpret_cast<const bf16 *>(x), H_pre,
+                                                     reinterpret_cast<bf16 *>(y), T, n, C, stream,
+                                                     false));
+}
+
+mhc_status mhc_h_aggregate_static_bwd(const mhc_bf16 *dy, const mhc_bf16 *x, const float *H_pre,
+                                      mhc_bf16 *dx, float *dH_pre, int64_t T, int n, int64_t C,
+                                      void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_static_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C");
+    ck.ptr(H_pre, "H_pre").ptr(dH_pre, "dH_pre");
+    if (ck.st) return ck.st;
+    if (T == 0) {
+        if (ck.device().st) return ck.st;
+        return launched(ck.fn, cudaMemsetAsync(dH_pre, 0, size_t(n) * sizeof(float), stream));
+    }
+    ck.ptr(dy, "dy").ptr(x, "x").opt(dx, "dx");
+    ck.ws(ws, ws_bytes, mhc::agg_static_ws_bytes(T, n)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggregate_bwd_static(
+                               reinterpret_cast<const bf16 *>(dy), reinterpret_cast<const bf16 *>(x),
+                               H_pre, reinterpret_cast<bf16 *>(dx), dH_pre, T, n, C, ws, stream));
+}
+
+mhc_status rmsnorm_residual_fwd(const mhc_bf16 *x, const mhc_bf16 *res, const float *gamma,
+                                mhc_bf16 *h, mhc_bf16 *y, float *rstd, int64_t rows,
+                                int64_t cols, float eps, mhc_stream_t stream)
+{
+    Check ck("rmsnorm_residual_fwd");
+    ck.count(rows, "rows").channels(cols, "cols").fits(rows, cols, "rows*cols").eps(eps, "eps");
+    if (ck.st == MHC_OK && cols > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "rmsnorm_residual_fwd: cols = %lld > %lld",
+                     (long long)cols, (long long)kMaxRmsCols);
+    if (ck.st || rows == 0) return ck.st;
+    ck.ptr(x, "x").opt(res, "res").opt(gamma, "gamma").opt(h, "h").ptr(y, "y").opt(rstd, "rstd");
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_rmsr_fwd(reinterpret_cast<const bf16 *>(x),
+                                                reinterpret_cast<const bf16 *>(res), gamma,
+                                                reinterpret_cast<bf16 *>(h),
+                                                reinterpret_cast<bf16 *>(y), rstd, rows, cols,
+                                                eps, stream));
+}
+
+mhc_status rmsnorm_residual_bwd(const mhc_bf16 *dy, const mhc_bf16 *dh, const mhc_bf16 *x,
+                                const mhc_bf16 *res, const float *gamma, const float *rstd,
+                                mhc_bf16 *dx, float *dgamma, int64_t rows, int64_t cols,
+                                float eps, void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("rmsnorm_residual_bwd");
+    ck.count(rows, "rows").channels(cols, "cols").fits(rows, cols, "rows*cols").eps(eps, "eps");
+    if (ck.st == MHC_OK && cols > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "rmsnorm_residual_bwd: cols = %lld > %lld",
+                     (long long)cols, (long long)kMaxRmsCols);
+    ck.opt(dgamma, "dgamma");
+    if (ck.st) return ck.st;
+    if (rows == 0) {
+        if (!dgamma || ck.device().st) return ck.st;
+        return launched(ck.fn, cudaMemsetAsync(dgamma, 0, size_t(cols) * sizeof(float), stream));
+    }
+    ck.ptr(dy, "dy").opt(dh, "dh").ptr(x, "x").opt(res, "res").opt(gamma, "gamma");
+    ck.opt(rstd, "rstd").ptr(dx, "dx");
+    if (dgamma) ck.ws(ws, ws_bytes, mhc::norm_ws_bytes(rows, cols));
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_rmsr_bwd(
+                               reinterpret_cast<const bf16 *>(dy), reinterpret_cast<const bf16 *>(dh),
+                               reinterpret_cast<const bf16 *>(x), reinterpret_cast<const bf16 *>(res),
+                               gamma, rstd, reinterpret_cast<bf16 *>(dx), dgamma, rows, cols, eps,
+                               ws, stream));
+}
+
+mhc_status mhc_h_aggregate_rmsnorm_fwd(const mhc_bf16 *x, const float *H_pre, const float *gamma,
+                                       mhc_bf16 *y, mhc_bf16 *yn, float *rstd, int64_t T, int n,
+                                       int64_t C, float eps, mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_rmsnorm_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").eps(eps, "eps");
+    if (ck.st == MHC_OK && C > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "mhc_h_aggregate_rmsnorm_fwd: C = %lld > %lld",
+                     (long long)C, (long long)kMaxRmsCols);
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x, "x").ptr(H_pre, "H_pre").opt(gamma, "gamma").opt(y, "y").ptr(yn, "yn");
+    ck.opt(rstd, "rstd");
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggn_fwd(reinterpret_cast<const bf16 *>(x), H_pre, gamma,
+                                                reinterpret_cast<bf16 *>(y),
+                                                reinterpret_cast<bf16 *>(yn), rstd, T, n, C, eps,
+                                                stream));
+}
+
+mhc_status mhc_h_aggregate_rmsnorm_bwd(const mhc_bf16 *dyn, const mhc_bf16 *dy, const mhc_bf16 *x,
+                                       const float *H_pre, const float *gamma, const float *rstd,
+                                       mhc_bf16 *dx, float *dH_pre, float *dgamma, int64_t T,
+                                       int n, int64_t C, float eps, void *ws, size_t ws_bytes,
+                                       mhc_stream_t stream)
+{
+    Check ck("mhc_h_aggregate_rmsnorm_bwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").eps(eps, "eps");
+    if (ck.st == MHC_OK && C > kMaxRmsCols)
+        ck.st = fail(MHC_ERR_BAD_SHAPE, "mhc_h_aggregate_rmsnorm_bwd: C = %lld > %lld",
+                     (long long)C, (long long)kMaxRmsCols);
+    ck.opt(dgamma, "dgamma");
+    if (ck.st) return ck.st;
+    if (T == 0) {
+        if (!dgamma || ck.device().st) return ck.st;
+        return launched(ck.fn, cudaMemsetAsync(dgamma, 0, size_t(C) * sizeof(float), stream));
+    }
+    ck.ptr(dyn, "dyn").opt(dy, "dy").ptr(x, "x").ptr(H_pre, "H_pre").opt(gamma, "gamma");
+    ck.opt(rstd, "rstd").ptr(dx, "dx").ptr(dH_pre, "dH_pre");
+    if (dgamma) ck.ws(ws, ws_bytes, mhc::norm_ws_bytes(T, C));
+    if (ck.device().st) return ck.st;
+    return launched(ck.fn, mhc::launch_aggn_bwd(
+                               reinterpret_cast<const bf16 *>(dyn), reinterpret_cast<const bf16 *>(dy),
+                               reinterpret_cast<const bf16 *>(x), H_pre, gamma, rstd,
+                               reinterpret_cast<bf16 *>(dx), dH_pre, dgamma, T, n, C, eps, ws,
+                               stream));
+}
+
+mhc_status mhc_proj_rms_partial_fwd(const mhc_bf16 *x_shard, const float *W_shard, int64_t T,
+                                    int n, int64_t Cs, float *u_part, float *s_part, void *ws,
+                                    size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_proj_rms_partial_fwd");
+    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(x_shard, "x_shard").ptr(W_shard, "W_shard").ptr(u_part, "u_part").ptr(s_part, "s_part");
+    ck.ws(ws, ws_bytes, mhc::proj_fwd_ws_bytes(T, n, Cs)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_proj_partial_sums(reinterpret_cast<const bf16 *>(x_shard),
+                                                         W_shard, T, n, Cs, u_part, s_part, ws,
+                                                         fault_ptr(), stream));
+}
+
+mhc_status mhc_compute_h_fwd(const float *u, const float *s, int64_t K, const float *alpha3,
+                             const float *b, int64_t T, int n, int iters, float eps_sk,
+                             float eps_rms, float *H_pre, float *H_post, float *H_res,
+                             float *r_save, mhc_stream_t stream)
+{
+    Check ck("mhc_compute_h_fwd");
+    ck.count(T, "T").nstreams(n).iters(iters).eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    if (ck.st == MHC_OK && K < 1) ck.st = fail(MHC_ERR_BAD_SHAPE, "mhc_compute_h_fwd: K = %lld < 1", (long long)K);
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(u, "u").ptr(s, "s").ptr(alpha3, "alpha3").ptr(b, "b").ptr(H_pre, "H_pre");
+    ck.ptr(H_post, "H_post").ptr(H_res, "H_res").opt(r_save, "r_save").device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_compute_h_fwd(u, s, K, alpha3, b, T, n, iters, eps_sk,
+                                                     eps_rms, H_pre, H_post, H_res, r_save,
+                                                     stream));
+}
+
+mhc_status mhc_compute_h_bwd(const float *dH_pre, const float *dH_post, const float *dH_res,
+                             const float *u, const float *s, int64_t K, const float *alpha3,
+                             const float *b, int64_t T, int n, int iters, float eps_sk,
+                             float eps_rms, float *du, float *coef, float *dalpha3, float *db,
+                             void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_compute_h_bwd");
+    ck.count(T, "T").nstreams(n).iters(iters).eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    if (ck.st == MHC_OK && K < 1) ck.st = fail(MHC_ERR_BAD_SHAPE, "mhc_compute_h_bwd: K = %lld < 1", (long long)K);
+    ck.ptr(dalpha3, "dalpha3").ptr(db, "db");
+    if (ck.st) return ck.st;
+    if (T == 0) {
+        if (ck.device().st) return ck.st;
+        cudaError_t e = cudaMemsetAsync(dalpha3, 0, 3 * sizeof(float), stream);
+        if (e == cudaSuccess) e = cudaMemsetAsync(db, 0, size_t(n * n + 2 * n) * sizeof(float), stream);
+        return launched(ck.fn, e);
+    }
+    ck.ptr(dH_pre, "dH_pre").ptr(dH_post, "dH_post").ptr(dH_res, "dH_res").ptr(u, "u");
+    ck.ptr(s, "s").ptr(alpha3, "alpha3").ptr(b, "b").ptr(du, "du").ptr(coef, "coef");
+    ck.ws(ws, ws_bytes, mhc::compute_h_bwd_ws_bytes(T, n)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_compute_h_bwd(dH_pre, dH_post, dH_res, u, s, K, alpha3, b,
+                                                     T, n, iters, eps_sk, eps_rms, du, coef,
+                                                     dalpha3, db, ws, stream));
+}
+
+mhc_status mhc_proj_rms_partial_bwd(const mhc_bf16 *x_shard, const float *W_shard,
+                                    const float *du, const float *coef, int64_t T, int n,
+                                    int64_t Cs, mhc_bf16 *dx_shard, float *dW_shard, void *ws,
+                                    size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_proj_rms_partial_bwd");
+    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs");
+    ck.ptr(dW_shard, "dW_shard");
+    if (ck.st) return ck.st;
+    if (T == 0) {
+        if (ck.device().st) return ck.st;
+        return launched(ck.fn, cudaMemsetAsync(dW_shard, 0,
+                                               size_t(n) * Cs * (n * n + 2 * n) * sizeof(float),
+                                               stream));
+    }
+    ck.ptr(x_shard, "x_shard").ptr(W_shard, "W_shard").ptr(du, "du").ptr(coef, "coef");
+    ck.ptr(dx_shard, "dx_shard");
+    ck.ws(ws, ws_bytes, mhc::proj_bwd_ws_bytes(T, n, Cs)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_proj_partial_bwd(
+                               reinterpret_cast<const bf16 *>(x_shard), W_shard, du, coef, T, n, Cs,
+                               reinterpret_cast<bf16 *>(dx_shard), dW_shard, ws, fault_ptr(),
+                               stream));
 }
 
 }  // extern "C"

@@ -96,7 +96,8 @@ __global__ void __launch_bounds__(128)
                     const float *__restrict__ r_save, const float *__restrict__ alpha,
                     const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
                     float eps_rms, bf16 *__restrict__ du_hl, int du_cols,
-                    float *__restrict__ coef, float *__restrict__ part)
+                    float *__restrict__ coef, float *__restrict__ part,
+                    const float *__restrict__ s_tot, float *__restrict__ du_f32)
 {
     constexpr int O = Dims<N>::O;
     constexpr int PW = O + 4, TB = 128 / N;
@@ -109,7 +110,9 @@ __global__ void __launch_bounds__(128)
     const bool live = t < T;
     const int64_t tt = live ? t : 0;
     const float *u = u_save + tt * O;
-    const float r = __ldg(r_save + tt);
+    // r from the forward, or from the summed squares of a sharded forward
+    const float r = r_save ? __ldg(r_save + tt)
+                           : 1.0f / (sqrtf(__ldg(s_tot + tt) / float(K)) + eps_rms);
     const float a0 = __ldg(alpha), a1 = __ldg(alpha + 1), a2 = __ldg(alpha + 2);
     const float upre = __ldg(u + i), upost = __ldg(u + N + i);
     const float zpre = a0 * r * upre + __ldg(b + i);
@@ -147,6 +150,7 @@ __global__ void __launch_bounds__(128)
             const bf16 hi = __float2bfloat16_rn(v);
             dut[o] = hi;
             dut[O + o] = __float2bfloat16_rn(v - __bfloat162float(hi));
+            if (du_f32) du_f32[t * O + o] = v;
         };
         put(i, a0 * r * dzpre);
         put(N + i, a1 * r * dzpost);
@@ -356,7 +360,7 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
         MHC_PROF("k_compute_h_bwd", s);
         k_compute_h_bwd<N><<<unsigned(prows), 128, smem, s>>>(
             dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
-            du_cols, w.coef, w.part);
+            du_cols, w.coef, w.part, nullptr, nullptr);
     }
     // pass 2: residual gradient, dW and dbias on the tensor cores; an unsplit
     // pass writes dW and dbias directly
@@ -409,6 +413,170 @@ cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, co
                            iters, eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, fault, s);
     return bwd_impl<8>(nullptr, nullptr, nullptr, x, W, alpha, b, u_save, r_save, T, C, iters,
                        eps_sk, eps_rms, &L, dx, dW, dalpha, db, ws, fault, s);
+}
+
+// ---------------------------------------------------------------------------
+// proj_rms_compute_h over channel shards (RL-Kernel PR #383 task P1-6, the
+// fp32_gemm_rms TP/SP contract): a shard's partial sums, compute_h on the
+// totals, the per-token backward coefficients, a shard's dx and dW.
+// ---------------------------------------------------------------------------
+// u[t][o] = sum_s upart[s][t][o], s[t] = sum_s spart[s][t] (s ascending)
+__global__ void k_sum_splits(const float *__restrict__ upart, const float *__restrict__ spart,
+                             int S, int64_t T, int O, float *__restrict__ u,
+                             float *__restrict__ s_out)
+{
+    const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t TO = T * O;
+    if (e < TO) {
+        float a = 0.f;
+        for (int sp = 0; sp < S; ++sp) a += upart[int64_t(sp) * TO + e];
+        u[e] = a;
+    } else if (e < TO + T) {
+        const int64_t t = e - TO;
+        float a = 0.f;
+        for (int sp = 0; sp < S; ++sp) a += spart[int64_t(sp) * T + t];
+        s_out[t] = a;
+    }
+}
+
+cudaError_t launch_proj_partial_sums(const bf16 *x, const float *W, int64_t T, int n, int64_t Cs,
+                                     float *u, float *s_out, void *ws, int *fault, cudaStream_t s)
+{
+    const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * Cs;
+    const int64_t S = proj_tc_splits(T, n, K);
+    char *p = static_cast<char *>(ws);
+    bf16 *Whl = reinterpret_cast<bf16 *>(p);
+    p += ws_align(size_t(2 * O * K) * 2);
+    float *upart = reinterpret_cast<float *>(p);
+    p += ws_align(size_t(S * T * O) * 4);
+    float *spart = reinterpret_cast<float *>(p);
+    int S_used = 1;
+    cudaError_t e = launch_proj_partials(x, W, T, n, Cs, Whl, upart, spart, &S_used, fault, s);
+    if (e != cudaSuccess) return e;
+    MHC_PROF("k_sum_splits", s);
+    k_sum_splits<<<unsigned((T * O + T + 255) / 256), 256, 0, s>>>(upart, spart, S_used, T,
+                                                                   int(O), u, s_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compute_h_fwd(const float *u, const float *s_tot, int64_t K,
+                                 const float *alpha, const float *b, int64_t T, int n, int iters,
+                                 float eps_sk, float eps_rms, float *Hpre, float *Hpost,
+                                 float *Hres, float *r_save, cudaStream_t s)
+{
+    const int64_t threads = T * n;
+    MHC_PROF("k_compute_h_fwd", s);
+    if (n == 4)
+        k_compute_h_fwd<4><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+            u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
+            r_save);
+    else
+        k_compute_h_fwd<8><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+            u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
+            r_save);
+    return cudaGetLastError();
+}
+
+// scratch of the sharded compute_h backward: du_hl [T][du_cols], partial rows
+size_t compute_h_bwd_ws_bytes(int64_t T, int n)
+{
+    return ws_align(size_t(T) * bwd_tc_du_cols(n) * 2) +
+           ws_align(size_t((T * n + 127) / 128) * bwd_part_cols(n) * 4);
+}
+
+template <int N>
+static cudaError_t compute_h_bwd_impl(const float *dHpre, const float *dHpost,
+                                      const float *dHres, const float *u, const float *s_tot,
+                                      int64_t K, const float *alpha, const float *b, int64_t T,
+                                      int iters, float eps_sk, float eps_rms, float *du,
+                                      float *coef, float *dalpha, float *db, void *ws,
+                                      cudaStream_t s)
+{
+    constexpr int O = Dims<N>::O;
+    char *p = static_cast<char *>(ws);
+    bf16 *du_hl = reinterpret_cast<bf16 *>(p);
+    p += ws_align(size_t(T) * bwd_tc_du_cols(N) * 2);
+    float *part = reinterpret_cast<float *>(p);
+    const int64_t prows = (T * N + 127) / 128;
+    const size_t smem = size_t(2) * iters * 128 * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(k_compute_h_bwd<N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    {
+        MHC_PROF("k_compute_h_bwd", s);
+        k_compute_h_bwd<N><<<unsigned(prows), 128, smem, s>>>(
+            dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters, eps_sk, eps_rms, du_hl,
+            bwd_tc_du_cols(N), coef, part, s_tot, du);
+    }
+    {
+        MHC_PROF("k_bwd_finalize", s);
+        k_bwd_finalize<<<unsigned(O + 3), 256, 0, s>>>(nullptr, nullptr, 0, 0, nullptr, nullptr, 0,
+                                                        0, 1, part, prows, O, db, dalpha);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_compute_h_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                                 const float *u, const float *s_tot, int64_t K,
+                                 const float *alpha, const float *b, int64_t T, int n, int iters,
+                                 float eps_sk, float eps_rms, float *du, float *coef,
+                                 float *dalpha, float *db, void *ws, cudaStream_t s)
+{
+    if (n == 4)
+        return compute_h_bwd_impl<4>(dHpre, dHpost, dHres, u, s_tot, K, alpha, b, T, iters,
+                                     eps_sk, eps_rms, du, coef, dalpha, db, ws, s);
+    return compute_h_bwd_impl<8>(dHpre, dHpost, dHres, u, s_tot, K, alpha, b, T, iters, eps_sk,
+                                 eps_rms, du, coef, dalpha, db, ws, s);
+}
+
+// du (fp32 [T][O]) -> du_hl rows: bf16 hi | lo, zeros for the rest of the row
+__global__ void k_du_split(const float *__restrict__ du, int64_t T, int O, int du_cols,
+                           bf16 *__restrict__ du_hl)
+{
+    const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= T * du_cols) return;
+    const int64_t t = e / du_cols;
+    const int c = int(e % du_cols);
+    bf16 v = __float2bfloat16_rn(0.f);
+    if (c < 2 * O) {
+        const float d = __ldg(du + t * O + (c % O));
+        const bf16 hi = __float2bfloat16_rn(d);
+        v = c < O ? hi : __float2bfloat16_rn(d - __bfloat162float(hi));
+    }
+    du_hl[e] = v;
+}
+
+size_t proj_partial_bwd_ws_bytes(int64_t T, int n, int64_t Cs) { return proj_bwd_ws_bytes(T, n, Cs); }
+
+cudaError_t launch_proj_partial_bwd(const bf16 *x, const float *W, const float *du,
+                                    const float *coef, int64_t T, int n, int64_t Cs, bf16 *dx,
+                                    float *dW, void *ws, int *fault, cudaStream_t s)
+{
+    const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * Cs;
+    BwdWs w = carve_bwd(ws, T, n, Cs);
+    const int du_cols = bwd_tc_du_cols(n);
+    {
+        MHC_PROF("k_du_split", s);
+        k_du_split<<<unsigned((T * du_cols + 255) / 256), 256, 0, s>>>(du, T, int(O), du_cols,
+                                                                       w.du_hl);
+    }
+    const int tiles = int((T + 127) / 128);
+    const int tps = (tiles + w.splits - 1) / w.splits;
+    const int splits_used = (tiles + tps - 1) / tps;
+    const bool split = splits_used > 1;
+    cudaError_t e = launch_bwd_tc(x, W, w.du_hl, coef, T, n, Cs, nullptr, nullptr, nullptr,
+                                  nullptr, nullptr, dx, split ? w.dWpart : dW, w.dbiaspart,
+                                  splits_used, fault, s);
+    if (e != cudaSuccess) return e;
+    if (split) {
+        const int wblocks = int((K * O + 255) / 256);
+        MHC_PROF("k_bwd_finalize", s);
+        k_bwd_finalize<<<unsigned(wblocks), 256, 0, s>>>(w.dWpart, dW, K * O, wblocks, nullptr,
+                                                          nullptr, 0, 0, splits_used, nullptr, 0,
+                                                          int(O), nullptr, nullptr);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace mhc

@@ -42,7 +42,7 @@ static int threads_for(int64_t C8)
 // h_aggregate forward: y[t][c] = sum_i H_pre[t][i] x[t][i][c]
 // One block walks tokens; each thread one 8-wide chunk of c at a time.
 // ---------------------------------------------------------------------------
-template <int N>
+template <int N, bool STATIC>
 __global__ void __launch_bounds__(256)
     k_agg_fwd(const bf16 *__restrict__ x, const float *__restrict__ Hpre, bf16 *__restrict__ y,
               int64_t T, int64_t C8)
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(256)
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float h[N];
 #pragma unroll
-        for (int i = 0; i < N; ++i) h[i] = __ldg(Hpre + t * N + i);
+        for (int i = 0; i < N; ++i) h[i] = __ldg(Hpre + (STATIC ? 0 : t * N) + i);
         for (int64_t c8 = threadIdx.x; c8 < C8; c8 += blockDim.x) {
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -126,6 +126,66 @@ __global__ void __launch_bounds__(256)
         if (lane == 0)
 #pragma unroll
             for (int i = 0; i < N; ++i) dHpre[t * N + i] = part[i];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// h_aggregate backward with one static H_pre [N] (rwkv-ops StreamAggregateBwd
+// with per_token = false): dx[t][i][c] = H_pre[i] dy[t][c] (if dx != null),
+// dH_pre[i] = sum_t sum_c dy x_i.  Warp per token as in k_agg_bwd; each warp
+// keeps its running sums over its tokens (ascending), the block adds its
+// warps in order and writes one partial row part[block][N]; k_col_sum adds
+// the rows in block order.
+// ---------------------------------------------------------------------------
+template <int N>
+__global__ void __launch_bounds__(256)
+    k_agg_bwd_static(const bf16 *__restrict__ dy, const bf16 *__restrict__ x,
+                     const float *__restrict__ Hpre, bf16 *__restrict__ dx,
+                     float *__restrict__ part, int64_t T, int64_t C8)
+{
+    __shared__ float red[8][N];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    float h[N], tot[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        h[i] = __ldg(Hpre + i);
+        tot[i] = 0.f;
+    }
+    for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + warp; t < T; t += warps) {
+        float p[N];
+#pragma unroll
+        for (int i = 0; i < N; ++i) p[i] = 0.f;
+        for (int64_t c8 = lane; c8 < C8; c8 += 32) {
+            float g[8];
+            unpack8(ld_stream(dy + (t * C8 + c8) * 8), g);
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                float v[8];
+                unpack8(ld_stream(x + ((t * N + i) * C8 + c8) * 8), v);
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc = fmaf(g[e], v[e], acc);
+                p[i] += acc;
+                if (dx) {
+                    float o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = h[i] * g[e];
+                    st_stream(dx + ((t * N + i) * C8 + c8) * 8, pack8(o));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < N; ++i) tot[i] += warp_sum(p[i]);
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int i = 0; i < N; ++i) red[warp][i] = tot[i];
+    __syncthreads();
+    if (threadIdx.x < N) {
+        float s = 0.f;
+        for (int w = 0; w < int(blockDim.x >> 5); ++w) s += red[w][threadIdx.x];
+        part[int64_t(blockIdx.x) * N + threadIdx.x] = s;
     }
 }
 
@@ -584,17 +644,51 @@ __global__ void __launch_bounds__(256)
 // launchers
 // ---------------------------------------------------------------------------
 cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int64_t T, int n,
-                                 int64_t C, cudaStream_t s)
+                                 int64_t C, cudaStream_t s, bool per_token)
 {
     const int64_t C8 = C / 8;
     const unsigned g = grid_for(T, 8);
     const int th = threads_for(C8);
+    MHC_PROF("k_agg_fwd", s);
     if (n == 4) {
-        MHC_PROF("k_agg_fwd", s);
-        k_agg_fwd<4><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+        if (per_token)
+            k_agg_fwd<4, false><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+        else
+            k_agg_fwd<4, true><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
     } else {
-        MHC_PROF("k_agg_fwd", s);
-        k_agg_fwd<8><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+        if (per_token)
+            k_agg_fwd<8, false><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+        else
+            k_agg_fwd<8, true><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+    }
+    return cudaGetLastError();
+}
+
+int agg_static_blocks(int64_t T)
+{
+    const int64_t want = (T + 7) / 8, cap = int64_t(kSplitSms) * 8;
+    return int(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+size_t agg_static_ws_bytes(int64_t T, int n) { return ws_align(size_t(agg_static_blocks(T)) * n * 4); }
+
+cudaError_t launch_aggregate_bwd_static(const bf16 *dy, const bf16 *x, const float *Hpre,
+                                        bf16 *dx, float *dHpre, int64_t T, int n, int64_t C,
+                                        void *ws, cudaStream_t s)
+{
+    const int64_t C8 = C / 8;
+    const int nb = agg_static_blocks(T);
+    float *part = static_cast<float *>(ws);
+    {
+        MHC_PROF("k_agg_bwd_static", s);
+        if (n == 4)
+            k_agg_bwd_static<4><<<unsigned(nb), 256, 0, s>>>(dy, x, Hpre, dx, part, T, C8);
+        else
+            k_agg_bwd_static<8><<<unsigned(nb), 256, 0, s>>>(dy, x, Hpre, dx, part, T, C8);
+    }
+    {
+        MHC_PROF("k_col_sum", s);
+        k_col_sum<<<1, dim3(32, 32), 0, s>>>(part, nb, n, dHpre);
     }
     return cudaGetLastError();
 }

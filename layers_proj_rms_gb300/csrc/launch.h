@@ -44,8 +44,14 @@ cudaError_t launch_sinkhorn_bwd(const float *dP, const float *logits, float *dlo
                                 int n, int iters, float eps, cudaStream_t s);
 
 // k_stream.cu
+// per_token: H_pre is [T][n]; else one static H_pre [n] for every token.
 cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int64_t T, int n,
-                                 int64_t C, cudaStream_t s);
+                                 int64_t C, cudaStream_t s, bool per_token = true);
+// Static-H_pre backward: dH_pre [n] summed over tokens; scratch agg_static_ws_bytes.
+size_t agg_static_ws_bytes(int64_t T, int n);
+cudaError_t launch_aggregate_bwd_static(const bf16 *dy, const bf16 *x, const float *Hpre,
+                                        bf16 *dx, float *dHpre, int64_t T, int n, int64_t C,
+                                        void *ws, cudaStream_t s);
 cudaError_t launch_aggregate_bwd(const bf16 *dy, const bf16 *x, const float *Hpre, bf16 *dx,
                                  float *dHpre, int64_t T, int n, int64_t C, cudaStream_t s);
 cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, const float *Hres,
@@ -65,6 +71,28 @@ cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, in
                            float eps, cudaStream_t s);
 cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf16 *dx,
                            int64_t rows, int64_t cols, float eps, cudaStream_t s);
+
+// k_norm.cu: rmsnorm_residual (h = x + res, y = h rho gamma) and h_aggregate
+// fused with that RMSNorm; dgamma through per-block partials (scratch
+// norm_ws_bytes(rows, cols)); k_col_sum (grid ceil(cols/32), block 32 x 32)
+// adds rows of partials in a fixed order.
+__global__ void k_col_sum(const float *__restrict__ part, int64_t nrows, int64_t cols,
+                          float *__restrict__ out);
+int norm_blocks(int64_t rows);
+size_t norm_ws_bytes(int64_t rows, int64_t cols);
+cudaError_t launch_rmsr_fwd(const bf16 *x, const bf16 *res, const float *gamma, bf16 *hout,
+                            bf16 *y, float *rstd, int64_t rows, int64_t cols, float eps,
+                            cudaStream_t s);
+cudaError_t launch_rmsr_bwd(const bf16 *dy, const bf16 *dh, const bf16 *x, const bf16 *res,
+                            const float *gamma, const float *rstd, bf16 *dx, float *dgamma,
+                            int64_t rows, int64_t cols, float eps, void *ws, cudaStream_t s);
+cudaError_t launch_aggn_fwd(const bf16 *x, const float *Hpre, const float *gamma, bf16 *y,
+                            bf16 *yn, float *rstd, int64_t T, int n, int64_t C, float eps,
+                            cudaStream_t s);
+cudaError_t launch_aggn_bwd(const bf16 *dyn, const bf16 *dy, const bf16 *x, const float *Hpre,
+                            const float *gamma, const float *rstd, bf16 *dx, float *dHpre,
+                            float *dgamma, int64_t T, int n, int64_t C, float eps, void *ws,
+                            cudaStream_t s);
 
 // k_proj_tc.cu: tensor-core projection partials of the forward
 int proj_tc_splits(int64_t T, int n, int64_t K);
@@ -110,6 +138,25 @@ cudaError_t launch_proj_bwd(const float *dHpre, const float *dHpost, const float
 // aggregate reductions, df), the compute_h backward, then the
 // residual-gradient pass dx = H_res dout + H_pre dy + du W^T + coef x with
 // dW and dbias.  Workspace proj_bwd_ws_bytes.
+// Channel-sharded proj_rms_compute_h: a shard's partial sums u [T][O], s [T]
+// (scratch proj_fwd_ws_bytes(T, n, Cs)); compute_h from the totals; the
+// per-token backward coefficients du, coef with dalpha, db (scratch
+// compute_h_bwd_ws_bytes); a shard's dx and dW (scratch proj_bwd_ws_bytes(T, n, Cs)).
+cudaError_t launch_proj_partial_sums(const bf16 *x, const float *W, int64_t T, int n, int64_t Cs,
+                                     float *u, float *s_out, void *ws, int *fault, cudaStream_t s);
+cudaError_t launch_compute_h_fwd(const float *u, const float *s_tot, int64_t K,
+                                 const float *alpha, const float *b, int64_t T, int n, int iters,
+                                 float eps_sk, float eps_rms, float *Hpre, float *Hpost,
+                                 float *Hres, float *r_save, cudaStream_t s);
+size_t compute_h_bwd_ws_bytes(int64_t T, int n);
+cudaError_t launch_compute_h_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                                 const float *u, const float *s_tot, int64_t K,
+                                 const float *alpha, const float *b, int64_t T, int n, int iters,
+                                 float eps_sk, float eps_rms, float *du, float *coef,
+                                 float *dalpha, float *db, void *ws, cudaStream_t s);
+cudaError_t launch_proj_partial_bwd(const bf16 *x, const float *W, const float *du,
+                                    const float *coef, int64_t T, int n, int64_t Cs, bf16 *dx,
+                                    float *dW, void *ws, int *fault, cudaStream_t s);
 cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
                              const float *alpha, const float *b, const bf16 *f,
                              const bf16 *bias, const float *Hpre, const float *Hpost,

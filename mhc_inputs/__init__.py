@@ -113,6 +113,23 @@ def rmsnorm_inputs(rows: int, cols: int, seed: int) -> dict:
     }
 
 
+def norm_inputs(rows: int, cols: int, seed: int, *, gamma_std: float = 0.1) -> dict:
+    """rmsnorm_residual inputs: x, res, dy, dh bf16 bits ~N(0,1) and a
+    per-channel weight gamma = 1 + N(0, gamma_std) in float32."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = {k: bf16_bits(_normal(rng, (rows, cols), 1.0)) for k in ("x", "res", "dy", "dh")}
+    out["gamma"] = (np.float32(1.0) + _normal(rng, (cols,), gamma_std)).astype(np.float32)
+    return out
+
+
+def gate_inputs(T: int, n: int, seed: int) -> dict:
+    """Aggregate weights in [0, 1): per-token H_pre [T, n] and one static
+    H_pre [n], float32 uniform draws."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return {"H_pre": rng.random((T, n), dtype=np.float32),
+            "H_static": rng.random(n, dtype=np.float32)}
+
+
 # The workloads, by what they are.  Each entry: (T, n, C, w_std, seed).
 LAYER_WORKLOADS = {
     "tiny_T256_n4_C256": (256, 4, 256, 0.02, 0),

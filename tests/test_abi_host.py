@@ -29,7 +29,11 @@ def test_header_declares_the_op_set():
     for op in ["mhc_sinkhorn_fwd", "mhc_sinkhorn_bwd", "mhc_proj_rms_compute_h_fwd",
                "mhc_proj_rms_compute_h_bwd", "mhc_h_aggregate_fwd", "mhc_h_aggregate_bwd",
                "mhc_h_post_bda_fwd", "mhc_h_post_bda_bwd", "rmsnorm_fwd", "rmsnorm_bwd",
-               "mhc_layer_fwd", "mhc_layer_bwd"]:
+               "mhc_layer_fwd", "mhc_layer_bwd", "mhc_h_aggregate_static_fwd",
+               "mhc_h_aggregate_static_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
+               "mhc_h_aggregate_rmsnorm_fwd", "mhc_h_aggregate_rmsnorm_bwd",
+               "mhc_proj_rms_partial_fwd", "mhc_compute_h_fwd", "mhc_compute_h_bwd",
+               "mhc_proj_rms_partial_bwd"]:
         assert op in names
 
 
@@ -84,8 +88,32 @@ def test_workspace_sizes(L):
         a = ws(op, 256, 4, 256)
         b = ws(op, 16384, 4, 4096)
         assert a > 0 and b >= a and a % 256 == 0
+    for op in (7, 8, 9, 10, 11):
+        a = ws(op, 256, 4, 256)
+        b = ws(op, 16384, 4, 4096)
+        assert a > 0 and b >= a and a % 256 == 0
+    # the RMSNorm op ignores n
+    assert ws(6, 256, 0, 4096) == ws(6, 256, 4, 4096) > 0
     assert ws(1, 256, 5, 256) == 0
-    assert ws(9, 256, 4, 256) == 0
+    assert ws(99, 256, 4, 256) == 0
+
+
+def test_next_ops_validation_without_gpu(L):
+    from layers_proj_rms_gb300 import _lib  # noqa: F401  (argtypes)
+    f = L.rmsnorm_residual_fwd
+    # cols not a multiple of 8; cols too large; rows = 0 is a no-op
+    assert f(A, None, None, None, A, None, 4, 60, 1e-6, None) == 2
+    assert f(A, None, None, None, A, None, 4, 65536, 1e-6, None) == 2
+    assert f(None, None, None, None, None, None, 0, 64, 1e-6, None) == 0
+    # dgamma wanted: the workspace is required
+    g = L.rmsnorm_residual_bwd
+    assert g(A, None, A, None, None, None, A, A, 4, 64, 1e-6, None, 0, None) == 5
+    # static aggregate: dH_pre is always required
+    h = L.mhc_h_aggregate_static_bwd
+    assert h(A, A, A, A, None, 16, 4, 64, A, 1 << 20, None) == 1
+    # compute_h needs K >= 1
+    c = L.mhc_compute_h_fwd
+    assert c(A, A, 0, A, A, 16, 4, 20, 1e-6, 1e-6, A, A, A, None, None) == 2
 
 
 def test_workspace_checks(L):

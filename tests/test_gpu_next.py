@@ -1,0 +1,280 @@
+"""GPU parity of the ops beyond the layer path against the fp64 oracle, on
+the same seeded inputs, with out-of-bounds canaries around the outputs:
+
+  * h_aggregate with a static H_pre [n] (rwkv-ops StreamAggregate with
+    per_token = false);
+  * rmsnorm_residual (RL-Kernel PR #383 tasks P1-5 / P1-8: residual fork,
+    learnable gamma, dgamma);
+  * h_aggregate fused with the weighted RMSNorm of its output;
+  * proj_rms_compute_h over channel shards (task P1-6): shard partial sums,
+    compute_h on the summed totals, per-token backward coefficients, a
+    shard's dx and dW; the shards assembled against the unsharded oracle.
+
+Sizes span several blocks with ragged tails; the full 7B-scale sizes are
+checked on sampled rows where the oracle would be slow.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mhc_inputs as mi
+from tests._util import dev_bf16, dev_f32, err_bf16, err_grad, err_h, host
+from tests.test_gpu_ops import EPS_RMS, EPS_SK, ITERS, canary, check_canary
+
+pytestmark = pytest.mark.gpu
+EPS_N = 1e-6
+
+
+@pytest.fixture(scope="module")
+def M():
+    import layers_proj_rms_gb300 as m
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return m
+
+
+def _f64(bits):
+    return mi.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# static H_pre
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,n,C", [(1, 4, 8), (129, 4, 264), (67, 8, 64), (300, 8, 136),
+                                   (2048, 4, 4096)])
+def test_aggregate_static(M, orc, T, n, C):
+    inp = mi.layer_inputs(T, n, C, 200 + T, grads=True)
+    H = mi.gate_inputs(T, n, 201 + T)["H_static"]
+    x, dy = dev_bf16(inp["x"]), dev_bf16(inp["dy"])
+    Hd = dev_f32(H)
+    by, y = canary((T, C), torch.bfloat16)
+    bx, dx = canary((T, n, C), torch.bfloat16)
+    bh, dH = canary((n,), torch.float32)
+    ws = M.workspace(M.OP_H_AGGREGATE_STATIC_BWD, T, n, C)
+    M.mhc_h_aggregate_static_fwd(x, Hd, y)
+    M.mhc_h_aggregate_static_bwd(dy, x, Hd, dx, dH, ws)
+    torch.cuda.synchronize()
+    for b in (by, bx, bh):
+        check_canary(b)
+    xf = _f64(inp["x"])
+    err_bf16(y, orc.h_aggregate_static_fwd(xf, H))
+    ref = orc.h_aggregate_static_bwd(_f64(inp["dy"]), xf, H)
+    err_bf16(dx, ref["dx"])
+    err_grad(dH, ref["dH_pre"])
+
+
+def test_aggregate_static_zero_tokens(M):
+    dH = torch.full((4,), 5.0, device="cuda")
+    e = torch.empty(0, dtype=torch.bfloat16, device="cuda")
+    M.mhc_h_aggregate_static_bwd(e.view(0, 64), e.view(0, 4, 64), torch.ones(4, device="cuda"),
+                                 e.view(0, 4, 64), dH, None)
+    torch.cuda.synchronize()
+    assert torch.all(dH == 0)
+
+
+# ---------------------------------------------------------------------------
+# rmsnorm_residual
+# ---------------------------------------------------------------------------
+
+NORM_SHAPES = [(1, 8), (3, 264), (200, 1024), (67, 4096), (33, 7168), (5, 32768)]
+
+
+@pytest.mark.parametrize("rows,cols", NORM_SHAPES)
+@pytest.mark.parametrize("variant", ["res_gamma", "plain", "gamma_no_rstd"])
+def test_rmsnorm_residual(M, orc, rows, cols, variant):
+    inp = mi.norm_inputs(rows, cols, 300 + rows + cols)
+    with_res = variant == "res_gamma"
+    with_gamma = variant != "plain"
+    x, dy, dh = dev_bf16(inp["x"]), dev_bf16(inp["dy"]), dev_bf16(inp["dh"])
+    res = dev_bf16(inp["res"]) if with_res else None
+    gamma = dev_f32(inp["gamma"]) if with_gamma else None
+    bh, h = canary((rows, cols), torch.bfloat16)
+    byy, y = canary((rows, cols), torch.bfloat16)
+    br, rstd = canary((rows,), torch.float32)
+    bdx, dx = canary((rows, cols), torch.bfloat16)
+    bg, dg = canary((cols,), torch.float32)
+    M.rmsnorm_residual_fwd(x, res, gamma, h, y, rstd, EPS_N)
+    ws = M.workspace(M.OP_RMSNORM_RESIDUAL_BWD, rows, 0, cols)
+    M.rmsnorm_residual_bwd(dy, dh if with_res else None, x, res, gamma,
+                           None if variant == "gamma_no_rstd" else rstd, dx, dg, EPS_N, ws)
+    torch.cuda.synchronize()
+    for b in (bh, byy, br, bdx, bg):
+        check_canary(b)
+    xf = _f64(inp["x"]); rf = _f64(inp["res"]) if with_res else None
+    gf = inp["gamma"].astype(np.float64) if with_gamma else None
+    f = orc.rmsnorm_residual_fwd(xf, rf, gf, EPS_N)
+    err_bf16(h, f["h"])
+    err_bf16(y, f["y"])
+    err_grad(rstd, f["rstd"], rel=1e-5)
+    b = orc.rmsnorm_residual_bwd(_f64(inp["dy"]), _f64(inp["dh"]) if with_res else None, xf, rf,
+                                 gf, EPS_N)
+    err_bf16(dx, b["dx"])
+    err_grad(dg, b["dgamma"])
+
+
+def test_rmsnorm_residual_zero_row(M, orc):
+    """An all-zero fork row: finite, y = 0, dx = rho g (rho = 1/sqrt(eps))."""
+    inp = mi.norm_inputs(4, 64, 7)
+    xb = inp["x"].copy(); xb[1] = 0
+    rb = np.zeros_like(inp["res"])
+    x, res = dev_bf16(xb), dev_bf16(rb)
+    gamma, dy = dev_f32(inp["gamma"]), dev_bf16(inp["dy"])
+    h = torch.empty(4, 64, dtype=torch.bfloat16, device="cuda")
+    y, dx = torch.empty_like(h), torch.empty_like(h)
+    rstd = torch.empty(4, device="cuda"); dg = torch.empty(64, device="cuda")
+    M.rmsnorm_residual_fwd(x, res, gamma, h, y, rstd, EPS_N)
+    M.rmsnorm_residual_bwd(dy, None, x, res, gamma, rstd, dx, dg, EPS_N,
+                           M.workspace(M.OP_RMSNORM_RESIDUAL_BWD, 4, 0, 64))
+    torch.cuda.synchronize()
+    f = orc.rmsnorm_residual_fwd(_f64(xb), _f64(rb), inp["gamma"].astype(np.float64), EPS_N)
+    b = orc.rmsnorm_residual_bwd(_f64(inp["dy"]), None, _f64(xb), _f64(rb),
+                                 inp["gamma"].astype(np.float64), EPS_N)
+    assert torch.all(torch.isfinite(dx.float()))
+    err_bf16(y, f["y"])
+    err_bf16(dx, b["dx"])  # rho = 1/sqrt(eps): the zero row has |dx| ~ 1e3
+    err_grad(dg, b["dgamma"])
+
+
+def test_rmsnorm_residual_7b_rows_sampled(M, orc):
+    rows, cols = 16384, 4096
+    inp = mi.norm_inputs(rows, cols, 77)
+    x, res, dy = dev_bf16(inp["x"]), dev_bf16(inp["res"]), dev_bf16(inp["dy"])
+    gamma = dev_f32(inp["gamma"])
+    h = torch.empty(rows, cols, dtype=torch.bfloat16, device="cuda")
+    y, dx = torch.empty_like(h), torch.empty_like(h)
+    rstd = torch.empty(rows, device="cuda"); dg = torch.empty(cols, device="cuda")
+    M.rmsnorm_residual_fwd(x, res, gamma, h, y, rstd, EPS_N)
+    M.rmsnorm_residual_bwd(dy, None, x, res, gamma, rstd, dx, dg, EPS_N,
+                           M.workspace(M.OP_RMSNORM_RESIDUAL_BWD, rows, 0, cols))
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([[0, rows - 1], np.random.Generator(np.random.PCG64(5)).choice(rows, 64, replace=False)]))
+    g = inp["gamma"].astype(np.float64)
+    f = orc.rmsnorm_residual_fwd(_f64(inp["x"][idx]), _f64(inp["res"][idx]), g, EPS_N)
+    b = orc.rmsnorm_residual_bwd(_f64(inp["dy"][idx]), None, _f64(inp["x"][idx]),
+                                 _f64(inp["res"][idx]), g, EPS_N)
+    ti = torch.from_numpy(idx).cuda()
+    err_bf16(y[ti], f["y"])
+    err_bf16(dx[ti], b["dx"])
+    # dgamma over all rows, checked against the oracle in full
+    full = orc.rmsnorm_residual_bwd(_f64(inp["dy"]), None, _f64(inp["x"]), _f64(inp["res"]), g,
+                                    EPS_N)
+    err_grad(dg, full["dgamma"])
+
+
+# ---------------------------------------------------------------------------
+# aggregate + weighted RMSNorm
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,n,C", [(1, 4, 8), (129, 4, 264), (67, 8, 64), (200, 8, 7168),
+                                   (300, 4, 4096)])
+@pytest.mark.parametrize("with_dy", [True, False])
+def test_aggregate_rmsnorm(M, orc, T, n, C, with_dy):
+    inp = mi.layer_inputs(T, n, C, 400 + T + C, grads=True)
+    nin = mi.norm_inputs(T, C, 401 + T)
+    H = mi.gate_inputs(T, n, 402 + T)["H_pre"]
+    x, Hd, gamma = dev_bf16(inp["x"]), dev_f32(H), dev_f32(nin["gamma"])
+    dyn, dy = dev_bf16(nin["dy"]), dev_bf16(inp["dy"]) if with_dy else None
+    by, y = canary((T, C), torch.bfloat16)
+    byn, yn = canary((T, C), torch.bfloat16)
+    br, rstd = canary((T,), torch.float32)
+    bdx, dx = canary((T, n, C), torch.bfloat16)
+    bdh, dH = canary((T, n), torch.float32)
+    bg, dg = canary((C,), torch.float32)
+    M.mhc_h_aggregate_rmsnorm_fwd(x, Hd, gamma, y, yn, rstd, EPS_N)
+    M.mhc_h_aggregate_rmsnorm_bwd(dyn, dy, x, Hd, gamma, rstd, dx, dH, dg, EPS_N,
+                                  M.workspace(M.OP_H_AGGREGATE_RMSNORM_BWD, T, n, C))
+    torch.cuda.synchronize()
+    for b in (by, byn, br, bdx, bdh, bg):
+        check_canary(b)
+    xf, g = _f64(inp["x"]), nin["gamma"].astype(np.float64)
+    f = orc.h_aggregate_rmsnorm_fwd(xf, H, g, EPS_N)
+    err_bf16(y, f["y"])
+    err_bf16(yn, f["yn"])
+    err_grad(rstd, f["rstd"], rel=1e-5)
+    b = orc.h_aggregate_rmsnorm_bwd(_f64(nin["dy"]), _f64(inp["dy"]) if with_dy else None, xf, H,
+                                    g, EPS_N)
+    err_bf16(dx, b["dx"])
+    err_grad(dH, b["dH_pre"])
+    err_grad(dg, b["dgamma"])
+
+
+# ---------------------------------------------------------------------------
+# channel-sharded proj_rms_compute_h
+# ---------------------------------------------------------------------------
+
+def _shard_np(x, W, C, c0, c1):
+    n = x.shape[1]
+    xs = np.ascontiguousarray(x[:, :, c0:c1])
+    Ws = np.ascontiguousarray(np.concatenate([W[i * C + c0:i * C + c1] for i in range(n)], 0))
+    return xs, Ws
+
+
+# "stress" draws alpha = 1, b ~ N(0, 1), W ~ N(0, 0.05), so the gates and the
+# Sinkhorn leave their near-uniform regime; at K = 4096 that makes H sensitive
+# to the ~1e-5 absolute rounding of u (alpha r du), so the 4-shard case uses
+# the workloads' alpha = 0.01, W ~ N(0, 0.02).
+@pytest.mark.parametrize("T,n,C,cuts,stress", [(256, 4, 256, [0, 128, 256], True),
+                                               (129, 4, 264, [0, 128, 264], True),
+                                               (67, 8, 136, [0, 64, 136], True),
+                                               (300, 4, 1024, [0, 256, 512, 768, 1024], False)])
+def test_sharded_proj_rms(M, orc, T, n, C, cuts, stress):
+    O = n * n + 2 * n
+    K = n * C
+    if stress:
+        inp = mi.layer_inputs(T, n, C, 500 + T, w_std=0.05, b_std=1.0, alpha=1.0)
+    else:
+        inp = mi.layer_inputs(T, n, C, 500 + T, w_std=0.02, b_std=1.0)
+    dH = mi.sinkhorn_inputs(T, n, 501 + T)
+    dHp = mi.gate_inputs(T, n, 502 + T)
+    dH_pre, dH_post = dHp["H_pre"] - 0.5, dHp["H_pre"][:, ::-1].copy() - 0.5
+    dH_res = dH["dP"]
+    alpha, b = inp["alpha"], inp["b"]
+    u = torch.zeros(T, O, device="cuda"); s = torch.zeros(T, device="cuda")
+    shards = []
+    for c0, c1 in zip(cuts[:-1], cuts[1:]):
+        Cs = c1 - c0
+        xs_b, Ws = _shard_np(inp["x"], inp["W"], C, c0, c1)
+        xs, Wd = dev_bf16(xs_b), dev_f32(Ws)
+        up = torch.empty(T, O, device="cuda"); sp = torch.empty(T, device="cuda")
+        M.mhc_proj_rms_partial_fwd(xs, Wd, up, sp, M.workspace(M.OP_PROJ_RMS_PARTIAL_FWD, T, n, Cs))
+        u += up; s += sp  # the all-reduce over shards
+        shards.append((c0, c1, xs, Wd))
+    Hpre = torch.empty(T, n, device="cuda"); Hpost = torch.empty(T, n, device="cuda")
+    Hres = torch.empty(T, n, n, device="cuda"); r = torch.empty(T, device="cuda")
+    M.mhc_compute_h_fwd(u, s, K, dev_f32(alpha), dev_f32(b), ITERS, EPS_SK, EPS_RMS, Hpre, Hpost,
+                        Hres, r)
+    du = torch.empty(T, O, device="cuda"); coef = torch.empty(T, device="cuda")
+    dalpha = torch.empty(3, device="cuda"); db = torch.empty(O, device="cuda")
+    M.mhc_compute_h_bwd(dev_f32(dH_pre), dev_f32(dH_post), dev_f32(dH_res), u, s, K,
+                        dev_f32(alpha), dev_f32(b), ITERS, EPS_SK, EPS_RMS, du, coef, dalpha, db,
+                        M.workspace(M.OP_COMPUTE_H_BWD, T, n, 8))
+    dx = torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(K, O, device="cuda")
+    for c0, c1, xs, Wd in shards:
+        Cs = c1 - c0
+        dxs = torch.empty(T, n, Cs, dtype=torch.bfloat16, device="cuda")
+        dWs = torch.empty(n * Cs, O, device="cuda")
+        M.mhc_proj_rms_partial_bwd(xs, Wd, du, coef, dxs, dWs,
+                                   M.workspace(M.OP_PROJ_RMS_PARTIAL_BWD, T, n, Cs))
+        dx[:, :, c0:c1] = dxs
+        for i in range(n):
+            dW[i * C + c0:i * C + c1] = dWs[i * Cs:(i + 1) * Cs]
+    torch.cuda.synchronize()
+    xf = _f64(inp["x"])
+    ref = orc.proj_rms_compute_h_fwd(xf, inp["W"], alpha, b, n, ITERS, EPS_SK, EPS_RMS)
+    err_h(Hpre, ref["H_pre"]); err_h(Hpost, ref["H_post"]); err_h(Hres, ref["H_res"])
+    err_grad(u, ref["u"])
+    err_grad(r, ref["r"], rel=1e-5)
+    sref = np.sum(xf.reshape(T, -1) ** 2, axis=1)
+    err_grad(s, sref, rel=1e-5)
+    cb = orc.compute_h_bwd_from_sums(dH_pre, dH_post, dH_res, ref["u"], sref, K, alpha, b, n,
+                                     ITERS, EPS_SK, EPS_RMS)
+    err_grad(du, cb["du"])
+    err_grad(coef, cb["coef"])
+    err_grad(dalpha, cb["dalpha"])
+    err_grad(db, cb["db"])
+    rb = orc.proj_rms_compute_h_bwd(dH_pre, dH_post, dH_res, xf, inp["W"], alpha, b, n, ITERS,
+                                    EPS_SK, EPS_RMS)
+    err_bf16(dx, rb["dx"])
+    err_grad(dW, rb["dW"])
