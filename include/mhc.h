@@ -84,6 +84,17 @@ MHC_API const char *mhc_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 MHC_API int mhc_version(void);
 
+/* Batch-invariant mode ([rlk] PR body: the fixed-K / batch-invariant GEMM
+ * reference of task P1-2).  Off by default.  When on, the forward
+ * projection's K splits are a function of K alone (4096-wide), so every
+ * per-token output of every op (H_*, u, r, y, out, dx, df, ...) is bitwise
+ * independent of T and of the token's position in the batch; the sums over
+ * tokens (dW, dalpha, db, dbias, dgamma) are deterministic for a given T.
+ * Process-wide; workspace sizes depend on it, so query them after setting
+ * it, and do not change it while calls are in flight. */
+MHC_API void mhc_set_batch_invariant(int on);
+MHC_API int mhc_batch_invariant(void);
+
 /* Synchronises `stream`, reads and clears the device-side fault word.
  * Returns MHC_OK if no kernel reported a fault, MHC_ERR_DEVICE_FAULT
  * otherwise (*code receives the fault code, 0 if none; code may be NULL). */

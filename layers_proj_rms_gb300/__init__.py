@@ -27,7 +27,7 @@ __all__ = [
     "mhc_proj_rms_partial_fwd", "mhc_compute_h_fwd", "mhc_compute_h_bwd",
     "mhc_proj_rms_partial_bwd", "OP_RMSNORM_RESIDUAL_BWD", "OP_H_AGGREGATE_RMSNORM_BWD",
     "OP_H_AGGREGATE_STATIC_BWD", "OP_PROJ_RMS_PARTIAL_FWD", "OP_COMPUTE_H_BWD",
-    "OP_PROJ_RMS_PARTIAL_BWD",
+    "OP_PROJ_RMS_PARTIAL_BWD", "mhc_set_batch_invariant", "mhc_batch_invariant",
 ]
 
 

@@ -79,6 +79,10 @@ lib.mhc_last_error.argtypes = []
 lib.mhc_last_error.restype = ctypes.c_char_p
 lib.mhc_version.argtypes = []
 lib.mhc_version.restype = ctypes.c_int
+lib.mhc_set_batch_invariant.argtypes = [_I]
+lib.mhc_set_batch_invariant.restype = None
+lib.mhc_batch_invariant.argtypes = []
+lib.mhc_batch_invariant.restype = ctypes.c_int
 lib.mhc_workspace_bytes.argtypes = [_I, _I64, _I, _I64]
 lib.mhc_workspace_bytes.restype = ctypes.c_size_t
 
@@ -397,3 +401,11 @@ def mhc_proj_rms_partial_bwd(x_shard, W_shard, du, coef, dx_shard, dW_shard, ws,
         _ptr(du, _F32, (T, O), "du"), _ptr(coef, _F32, (T,), "coef"), T, n, Cs,
         _ptr(dx_shard, _BF, (T, n, Cs), "dx_shard"), _ptr(dW_shard, _F32, (n * Cs, O), "dW_shard"),
         wp, wb, _stream(stream)))
+
+
+def mhc_set_batch_invariant(on: bool) -> None:
+    lib.mhc_set_batch_invariant(1 if on else 0)
+
+
+def mhc_batch_invariant() -> bool:
+    return bool(lib.mhc_batch_invariant())

@@ -170,6 +170,10 @@ const char *mhc_last_error(void) { return g_msg; }
 
 int mhc_version(void) { return 100; }
 
+void mhc_set_batch_invariant(int on) { mhc::set_batch_invariant(on); }
+
+int mhc_batch_invariant(void) { return mhc::batch_invariant(); }
+
 mhc_status mhc_device_error(int *code, mhc_stream_t stream)
 {
     Check ck("mhc_device_error");

@@ -268,12 +268,22 @@ static bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Batch-invariant mode: the K splits depend on K alone (fixed 4096-wide
+// splits), so a token's u and s, and everything computed from them, do not
+// depend on how many tokens share the call.  Otherwise the split count is
+// chosen for about MINB CTAs per SM, which depends on T.
+static int g_batch_invariant = 0;
+
+void set_batch_invariant(int on) { g_batch_invariant = on ? 1 : 0; }
+int batch_invariant() { return g_batch_invariant; }
+
 int proj_tc_splits(int64_t T, int n, int64_t K)
 {
     const int64_t mt = (T + 127) / 128;
     const int64_t kb = (K + 63) / 64;
     const int minb = n == 4 ? ProjTc<4>::MINB : ProjTc<8>::MINB;
-    int64_t s = (int64_t(kSplitSms) * minb) / mt;  // about MINB CTAs per SM
+    int64_t s = g_batch_invariant ? (kb + 63) / 64
+                                  : (int64_t(kSplitSms) * minb) / (mt > 0 ? mt : 1);
     if (s < 1) s = 1;
     if (s > kb) s = kb;
     if (s > 32) s = 32;

@@ -96,6 +96,8 @@ cudaError_t launch_aggn_bwd(const bf16 *dyn, const bf16 *dy, const bf16 *x, cons
 
 // k_proj_tc.cu: tensor-core projection partials of the forward
 int proj_tc_splits(int64_t T, int n, int64_t K);
+void set_batch_invariant(int on);
+int batch_invariant();
 cudaError_t launch_proj_partials(const bf16 *x, const float *W, int64_t T, int n, int64_t C,
                                  bf16 *Whl, float *upart, float *spart, int *splits_used,
                                  int *fault, cudaStream_t s);

@@ -149,3 +149,20 @@ def test_binding_fails_loudly_without_library(tmp_path):
     finally:
         os.rename(hidden, lib)
     assert r.returncode != 0 and "libmhc.so is missing" in r.stderr
+
+
+def test_batch_invariant_mode_flag(L):
+    from layers_proj_rms_gb300 import _lib  # noqa: F401  (argtypes)
+    assert L.mhc_batch_invariant() == 0
+    off = L.mhc_workspace_bytes(1, 256, 4, 256)
+    L.mhc_set_batch_invariant(1)
+    try:
+        assert L.mhc_batch_invariant() == 1
+        on_small = L.mhc_workspace_bytes(1, 256, 4, 256)
+        on_big = L.mhc_workspace_bytes(1, 16384, 4, 256)
+    finally:
+        L.mhc_set_batch_invariant(0)
+    # K splits fixed by K: fewer splits than the T-dependent choice at small T,
+    # and the per-token part of the scratch scales with T only
+    assert 0 < on_small < off
+    assert on_big > on_small

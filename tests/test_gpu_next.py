@@ -278,3 +278,35 @@ def test_sharded_proj_rms(M, orc, T, n, C, cuts, stress):
                                     EPS_SK, EPS_RMS)
     err_bf16(dx, rb["dx"])
     err_grad(dW, rb["dW"])
+
+
+# ---------------------------------------------------------------------------
+# batch-invariant mode (RL-Kernel PR #383: fixed-K / batch-invariant GEMM)
+# ---------------------------------------------------------------------------
+
+def _layer_on(M, t, T, n, C):
+    from tests.test_gpu_ops import run_layer
+    return run_layer(M, t, T, n, C)
+
+
+@pytest.mark.parametrize("n,C", [(4, 1024), (8, 512)])
+def test_batch_invariant_mode(M, n, C):
+    """With the mode on, the outputs of a token do not depend on the batch it
+    is in: 64 tokens alone and the same 64 tokens at offset 517 of a
+    1000-token batch give bitwise equal per-token outputs, forward and
+    backward."""
+    big = mi.layer_inputs(1000, n, C, 600, w_std=0.02, b_std=1.0, alpha=1.0)
+    off, Ts = 517, 64
+    small = dict(big)
+    for k in ("x", "f", "dout", "dy"):
+        small[k] = np.ascontiguousarray(big[k][off:off + Ts])
+    M.mhc_set_batch_invariant(True)
+    try:
+        assert M.mhc_batch_invariant()
+        ob = _layer_on(M, big, 1000, n, C)
+        os_ = _layer_on(M, small, Ts, n, C)
+    finally:
+        M.mhc_set_batch_invariant(False)
+    for k in ("H_pre", "H_post", "H_res", "u", "r", "y", "out", "dx", "df"):
+        a, b = host(ob[k][off:off + Ts]), host(os_[k])
+        assert np.array_equal(a, b), f"{k} depends on the batch"
