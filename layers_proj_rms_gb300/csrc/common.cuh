@@ -124,6 +124,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr)
     return v;
 }
 
+// Programmatic dependent launch: every kernel of the library is launched
+// with programmatic stream serialization (launch_k in launch.h), so its grid
+// may be set up while the previous kernel on the stream drains; pdl_wait()
+// at the top of each kernel then blocks until that kernel has completed and
+// its memory is visible.  Without the launch attribute it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float lds32f(uint32_t saddr)
 {
     float v;

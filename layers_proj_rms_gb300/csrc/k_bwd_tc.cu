@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
              const __grid_constant__ CUtensorMap tmg,
              const __grid_constant__ CUtensorMap tmy, const BwdTcArgs a)
 {
+    pdl_wait();
     using P = BwdTc<N>;
     constexpr int O = P::O, CW = P::CW;
     constexpr bool SG = LAYER && P::STAGE_G;
@@ -625,13 +626,12 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
             !map2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_tc<N, LAYER>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_bwd_tc<N, LAYER>), P::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(unsigned((C + P::CW - 1) / P::CW), unsigned(splits));
     {
         MHC_PROF("k_bwd_tc", s);
-        k_bwd_tc<N, LAYER><<<grid, P::THREADS, P::SMEM, s>>>(tmx, tmdu, tmg, tmy, args);
+        launch_k(k_bwd_tc<N, LAYER>, dim3(grid), dim3(P::THREADS), P::SMEM, s, tmx, tmdu, tmg, tmy, args);
     }
     return cudaGetLastError();
 }

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
               int64_t C8, bf16 *__restrict__ df, float *__restrict__ dHres,
               float *__restrict__ dHpost, float *__restrict__ dHpre)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t warps = int64_t(gridDim.x) * kTokWarps;
     for (int64_t t = int64_t(blockIdx.x) * kTokWarps + warp; t < T; t += warps) {
@@ -139,10 +140,10 @@ cudaError_t launch_bwd_tok(const bf16 *dout, const bf16 *x, const bf16 *f, const
     const unsigned g = unsigned(bwd_tok_blocks(T));
     MHC_PROF("k_bwd_tok", s);
     if (n == 4)
-        k_bwd_tok<4, MHC_TOK_U><<<g, 32 * kTokWarps, 0, s>>>(dout, x, f, bias, dy, Hpost, T, C / 8,
+        launch_k(k_bwd_tok<4, MHC_TOK_U>, dim3(g), dim3(32 * kTokWarps), 0, s, dout, x, f, bias, dy, Hpost, T, C / 8,
                                                              df, dHres, dHpost, dHpre);
     else
-        k_bwd_tok<8, 1><<<g, 32 * kTokWarps, 0, s>>>(dout, x, f, bias, dy, Hpost, T, C / 8, df,
+        launch_k(k_bwd_tok<8, 1>, dim3(g), dim3(32 * kTokWarps), 0, s, dout, x, f, bias, dy, Hpost, T, C / 8, df,
                                                      dHres, dHpost, dHpre);
     return cudaGetLastError();
 }

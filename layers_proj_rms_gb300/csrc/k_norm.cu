@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(512)
                const float *__restrict__ gamma, bf16 *__restrict__ hout, bf16 *__restrict__ y,
                float *__restrict__ rstd, int64_t rows, int64_t C8, float inv_cols, float eps)
 {
+    pdl_wait();
     __shared__ float red[32];
     const int tid = threadIdx.x, NT = blockDim.x;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(512)
                bf16 *__restrict__ dx, float *__restrict__ dgpart, int64_t rows, int64_t C8,
                float inv_cols, float eps)
 {
+    pdl_wait();
     __shared__ float red[64];
     const int tid = threadIdx.x, NT = blockDim.x;
     float acc[CPT][8];
@@ -212,6 +214,7 @@ __global__ void __launch_bounds__(512)
                const float *__restrict__ gamma, bf16 *__restrict__ y, bf16 *__restrict__ yn,
                float *__restrict__ rstd, int64_t T, int64_t C8, float inv_cols, float eps)
 {
+    pdl_wait();
     __shared__ float red[32];
     const int tid = threadIdx.x, NT = blockDim.x;
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(512)
                bf16 *__restrict__ dx, float *__restrict__ dHpre, float *__restrict__ dgpart,
                int64_t T, int64_t C8, float inv_cols, float eps)
 {
+    pdl_wait();
     // x stays in registers between the two phases when it is small enough,
     // else the second phase reads it again (an L2 hit); y is re-formed from
     // x in the second phase
@@ -377,6 +381,7 @@ __global__ void __launch_bounds__(1024)
     k_col_sum(const float *__restrict__ part, int64_t nrows, int64_t cols,
               float *__restrict__ out)
 {
+    pdl_wait();
     __shared__ float red[32][33];
     const int64_t c = int64_t(blockIdx.x) * 32 + threadIdx.x;
     float s = 0.f;
@@ -437,7 +442,7 @@ cudaError_t launch_rmsr_fwd(const bf16 *x, const bf16 *res, const float *gamma, 
     const unsigned g = unsigned(norm_blocks(rows));
     const float ic = 1.0f / float(cols);
     MHC_PROF("k_rmsr_fwd", s);
-    MHC_NORM_CPT_SWITCH(cpt, k_rmsr_fwd<CPT><<<g, nt, 0, s>>>(x, res, gamma, hout, y, rstd, rows,
+    MHC_NORM_CPT_SWITCH(cpt, launch_k(k_rmsr_fwd<CPT>, dim3(g), dim3(nt), 0, s, x, res, gamma, hout, y, rstd, rows,
                                                                C8, ic, eps));
     return cudaGetLastError();
 }
@@ -454,12 +459,12 @@ cudaError_t launch_rmsr_bwd(const bf16 *dy, const bf16 *dh, const bf16 *x, const
     float *part = dgamma ? static_cast<float *>(ws) : nullptr;
     {
         MHC_PROF("k_rmsr_bwd", s);
-        MHC_NORM_CPT_SWITCH(cpt, k_rmsr_bwd<CPT><<<unsigned(nb), nt, 0, s>>>(
+        MHC_NORM_CPT_SWITCH(cpt, launch_k(k_rmsr_bwd<CPT>, dim3(unsigned(nb)), dim3(nt), 0, s, 
                                      dy, dh, x, res, gamma, rstd, dx, part, rows, C8, ic, eps));
     }
     if (dgamma) {
         MHC_PROF("k_col_sum", s);
-        k_col_sum<<<unsigned((cols + 31) / 32), dim3(32, 32), 0, s>>>(part, nb, cols, dgamma);
+        launch_k(k_col_sum, dim3(unsigned((cols + 31) / 32)), dim3(dim3(32, 32)), 0, s, part, nb, cols, dgamma);
     }
     return cudaGetLastError();
 }
@@ -475,10 +480,10 @@ cudaError_t launch_aggn_fwd(const bf16 *x, const float *Hpre, const float *gamma
     const float ic = 1.0f / float(C);
     MHC_PROF("k_aggn_fwd", s);
     if (n == 4) {
-        MHC_NORM_CPT_SWITCH(cpt, k_aggn_fwd<4, CPT><<<g, nt, 0, s>>>(x, Hpre, gamma, y, yn, rstd,
+        MHC_NORM_CPT_SWITCH(cpt, launch_k(k_aggn_fwd<4, CPT>, dim3(g), dim3(nt), 0, s, x, Hpre, gamma, y, yn, rstd,
                                                                       T, C8, ic, eps));
     } else {
-        MHC_NORM_CPT_SWITCH(cpt, k_aggn_fwd<8, CPT><<<g, nt, 0, s>>>(x, Hpre, gamma, y, yn, rstd,
+        MHC_NORM_CPT_SWITCH(cpt, launch_k(k_aggn_fwd<8, CPT>, dim3(g), dim3(nt), 0, s, x, Hpre, gamma, y, yn, rstd,
                                                                       T, C8, ic, eps));
     }
     return cudaGetLastError();
@@ -498,18 +503,18 @@ cudaError_t launch_aggn_bwd(const bf16 *dyn, const bf16 *dy, const bf16 *x, cons
     {
         MHC_PROF("k_aggn_bwd", s);
         if (n == 4) {
-            MHC_NORM_CPT_SWITCH(cpt, k_aggn_bwd<4, CPT><<<unsigned(nb), nt, 0, s>>>(
+            MHC_NORM_CPT_SWITCH(cpt, launch_k(k_aggn_bwd<4, CPT>, dim3(unsigned(nb)), dim3(nt), 0, s, 
                                          dyn, dy, x, Hpre, gamma, rstd, dx, dHpre, part, T, C8,
                                          ic, eps));
         } else {
-            MHC_NORM_CPT_SWITCH(cpt, k_aggn_bwd<8, CPT><<<unsigned(nb), nt, 0, s>>>(
+            MHC_NORM_CPT_SWITCH(cpt, launch_k(k_aggn_bwd<8, CPT>, dim3(unsigned(nb)), dim3(nt), 0, s, 
                                          dyn, dy, x, Hpre, gamma, rstd, dx, dHpre, part, T, C8,
                                          ic, eps));
         }
     }
     if (dgamma) {
         MHC_PROF("k_col_sum", s);
-        k_col_sum<<<unsigned((C + 31) / 32), dim3(32, 32), 0, s>>>(part, nb, C, dgamma);
+        launch_k(k_col_sum, dim3(unsigned((C + 31) / 32)), dim3(dim3(32, 32)), 0, s, part, nb, C, dgamma);
     }
     return cudaGetLastError();
 }

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(128)
                     float *__restrict__ Hpost, float *__restrict__ Hres,
                     float *__restrict__ u_save, float *__restrict__ r_save)
 {
+    pdl_wait();
     constexpr int O = Dims<N>::O;
     const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = gt / N;
@@ -99,6 +100,7 @@ __global__ void __launch_bounds__(128)
                     float *__restrict__ coef, float *__restrict__ part,
                     const float *__restrict__ s_tot, float *__restrict__ du_f32)
 {
+    pdl_wait();
     constexpr int O = Dims<N>::O;
     constexpr int PW = O + 4, TB = 128 / N;
     extern __shared__ float sk_store[];  // [2*iters][blockDim.x]
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(256)
                    int64_t bcols, int bblocks, int splits, const float *__restrict__ part,
                    int64_t prows, int O, float *__restrict__ db, float *__restrict__ dalpha)
 {
+    pdl_wait();
     __shared__ float red[256];
     int blk = blockIdx.x;
     if (blk < wblocks + bblocks) {
@@ -265,7 +268,7 @@ static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alp
     const int64_t threads = T * N;
     {
         MHC_PROF("k_compute_h_fwd", s);
-        k_compute_h_fwd<N><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+        launch_k(k_compute_h_fwd<N>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
             upart, spart, S_used, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
             u_save, r_save);
     }
@@ -354,11 +357,11 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     const int64_t prows = (T * N + 127) / 128;
     {
         const size_t smem = size_t(2) * iters * 128 * sizeof(float);
-        e = cudaFuncSetAttribute(k_compute_h_bwd<N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+        e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd<N>),
+                           int(size_t(2) * kMaxIters * 128 * sizeof(float)));
         if (e != cudaSuccess) return e;
         MHC_PROF("k_compute_h_bwd", s);
-        k_compute_h_bwd<N><<<unsigned(prows), 128, smem, s>>>(
+        launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
             dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
             du_cols, w.coef, w.part, nullptr, nullptr);
     }
@@ -378,7 +381,7 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     const int bblocks = (split && dbias) ? int((C + 255) / 256) : 0;
     {
         MHC_PROF("k_bwd_finalize", s);
-        k_bwd_finalize<<<unsigned(wblocks + bblocks + O + 3), 256, 0, s>>>(
+        launch_k(k_bwd_finalize, dim3(unsigned(wblocks + bblocks + O + 3)), dim3(256), 0, s, 
             w.dWpart, dW, K * O, wblocks, w.dbiaspart, dbias, C, bblocks, splits_used, w.part,
             prows, O, db, dalpha);
     }
@@ -425,6 +428,7 @@ __global__ void k_sum_splits(const float *__restrict__ upart, const float *__res
                              int S, int64_t T, int O, float *__restrict__ u,
                              float *__restrict__ s_out)
 {
+    pdl_wait();
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t TO = T * O;
     if (e < TO) {
@@ -454,7 +458,7 @@ cudaError_t launch_proj_partial_sums(const bf16 *x, const float *W, int64_t T, i
     cudaError_t e = launch_proj_partials(x, W, T, n, Cs, Whl, upart, spart, &S_used, fault, s);
     if (e != cudaSuccess) return e;
     MHC_PROF("k_sum_splits", s);
-    k_sum_splits<<<unsigned((T * O + T + 255) / 256), 256, 0, s>>>(upart, spart, S_used, T,
+    launch_k(k_sum_splits, dim3(unsigned((T * O + T + 255) / 256)), dim3(256), 0, s, upart, spart, S_used, T,
                                                                    int(O), u, s_out);
     return cudaGetLastError();
 }
@@ -467,11 +471,11 @@ cudaError_t launch_compute_h_fwd(const float *u, const float *s_tot, int64_t K,
     const int64_t threads = T * n;
     MHC_PROF("k_compute_h_fwd", s);
     if (n == 4)
-        k_compute_h_fwd<4><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+        launch_k(k_compute_h_fwd<4>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
             u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
             r_save);
     else
-        k_compute_h_fwd<8><<<unsigned((threads + 127) / 128), 128, 0, s>>>(
+        launch_k(k_compute_h_fwd<8>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
             u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
             r_save);
     return cudaGetLastError();
@@ -499,19 +503,18 @@ static cudaError_t compute_h_bwd_impl(const float *dHpre, const float *dHpost,
     float *part = reinterpret_cast<float *>(p);
     const int64_t prows = (T * N + 127) / 128;
     const size_t smem = size_t(2) * iters * 128 * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(k_compute_h_bwd<N>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd<N>),
+                                   int(size_t(2) * kMaxIters * 128 * sizeof(float)));
     if (e != cudaSuccess) return e;
     {
         MHC_PROF("k_compute_h_bwd", s);
-        k_compute_h_bwd<N><<<unsigned(prows), 128, smem, s>>>(
+        launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
             dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters, eps_sk, eps_rms, du_hl,
             bwd_tc_du_cols(N), coef, part, s_tot, du);
     }
     {
         MHC_PROF("k_bwd_finalize", s);
-        k_bwd_finalize<<<unsigned(O + 3), 256, 0, s>>>(nullptr, nullptr, 0, 0, nullptr, nullptr, 0,
+        launch_k(k_bwd_finalize, dim3(unsigned(O + 3)), dim3(256), 0, s, nullptr, nullptr, 0, 0, nullptr, nullptr, 0,
                                                         0, 1, part, prows, O, db, dalpha);
     }
     return cudaGetLastError();
@@ -534,6 +537,7 @@ cudaError_t launch_compute_h_bwd(const float *dHpre, const float *dHpost, const 
 __global__ void k_du_split(const float *__restrict__ du, int64_t T, int O, int du_cols,
                            bf16 *__restrict__ du_hl)
 {
+    pdl_wait();
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= T * du_cols) return;
     const int64_t t = e / du_cols;
@@ -558,7 +562,7 @@ cudaError_t launch_proj_partial_bwd(const bf16 *x, const float *W, const float *
     const int du_cols = bwd_tc_du_cols(n);
     {
         MHC_PROF("k_du_split", s);
-        k_du_split<<<unsigned((T * du_cols + 255) / 256), 256, 0, s>>>(du, T, int(O), du_cols,
+        launch_k(k_du_split, dim3(unsigned((T * du_cols + 255) / 256)), dim3(256), 0, s, du, T, int(O), du_cols,
                                                                        w.du_hl);
     }
     const int tiles = int((T + 127) / 128);
@@ -572,7 +576,7 @@ cudaError_t launch_proj_partial_bwd(const bf16 *x, const float *W, const float *
     if (split) {
         const int wblocks = int((K * O + 255) / 256);
         MHC_PROF("k_bwd_finalize", s);
-        k_bwd_finalize<<<unsigned(wblocks), 256, 0, s>>>(w.dWpart, dW, K * O, wblocks, nullptr,
+        launch_k(k_bwd_finalize, dim3(unsigned(wblocks)), dim3(256), 0, s, w.dWpart, dW, K * O, wblocks, nullptr,
                                                           nullptr, 0, 0, splits_used, nullptr, 0,
                                                           int(O), nullptr, nullptr);
     }

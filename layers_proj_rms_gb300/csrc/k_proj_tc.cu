@@ -50,6 +50,7 @@ using ProjTc = typename ProjTcSel<N>::type;
 template <int N>
 __global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, int64_t K)
 {
+    pdl_wait();
     constexpr int O = N * N + 2 * N;
     const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (k >= K) return;
@@ -69,6 +70,7 @@ __global__ void __launch_bounds__(192, P::MINB)
               float *__restrict__ upart, float *__restrict__ spart, int64_t T, int kb_per_split,
               int kb_total, int *fault)
 {
+    pdl_wait();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -305,7 +307,7 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
     const int64_t K = int64_t(N) * C;
     {
         MHC_PROF("k_w_split", s);
-        k_w_split<N><<<unsigned((K + 255) / 256), 256, 0, s>>>(W, Whl, K);
+        launch_k(k_w_split<N>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
     }
     CUtensorMap tmx, tmw;
     if (!make_map_bf16(&tmx, x, uint64_t(T), uint64_t(K), P::BM, P::BK,
@@ -313,8 +315,7 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
         !make_map_bf16(&tmw, Whl, uint64_t(P::NB), uint64_t(K), P::NB, P::BK,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(k_proj_tc<N, P>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, P::SMEM);
+    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_proj_tc<N, P>), P::SMEM);
     if (e != cudaSuccess) return e;
     const int kb_total = int((K + P::BK - 1) / P::BK);
     const int kps = proj_tc_kps(K, S, P::KBS);
@@ -322,7 +323,7 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
     dim3 grid(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used));
     {
         MHC_PROF("k_proj_tc", s);
-        k_proj_tc<N, P><<<grid, 192, P::SMEM, s>>>(tmx, tmw, upart, spart, T, kps, kb_total, fault);
+        launch_k(k_proj_tc<N, P>, dim3(grid), dim3(192), P::SMEM, s, tmx, tmw, upart, spart, T, kps, kb_total, fault);
     }
     return cudaGetLastError();
 }

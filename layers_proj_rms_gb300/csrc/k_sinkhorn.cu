@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kSkThreads)
     k_sinkhorn_fwd(const float *__restrict__ logits, float *__restrict__ P, int64_t rows,
                    int iters, float eps)
 {
+    pdl_wait();
     const int64_t row = int64_t(blockIdx.x) * kSkThreads + threadIdx.x;  // = m*N + i
     const bool live = row < rows;
     float a[N];
@@ -57,6 +58,7 @@ __global__ void __launch_bounds__(kSkThreads)
     k_sinkhorn_bwd(const float *__restrict__ dP, const float *__restrict__ logits,
                    float *__restrict__ dlogits, int64_t rows, int iters, float eps)
 {
+    pdl_wait();
     extern __shared__ float sk_store[];  // [2*iters][kSkThreads]
     const int64_t row = int64_t(blockIdx.x) * kSkThreads + threadIdx.x;
     const bool live = row < rows;
@@ -90,10 +92,10 @@ cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n,
     const unsigned grid = unsigned((rows + kSkThreads - 1) / kSkThreads);
     if (n == 4) {
         MHC_PROF("k_sinkhorn_fwd", s);
-        k_sinkhorn_fwd<4><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
+        launch_k(k_sinkhorn_fwd<4>, dim3(grid), dim3(kSkThreads), 0, s, logits, P, rows, iters, eps);
     } else {
         MHC_PROF("k_sinkhorn_fwd", s);
-        k_sinkhorn_fwd<8><<<grid, kSkThreads, 0, s>>>(logits, P, rows, iters, eps);
+        launch_k(k_sinkhorn_fwd<8>, dim3(grid), dim3(kSkThreads), 0, s, logits, P, rows, iters, eps);
     }
     return cudaGetLastError();
 }
@@ -106,20 +108,18 @@ cudaError_t launch_sinkhorn_bwd(const float *dP, const float *logits, float *dlo
     const size_t smem = sk_smem(iters);
     cudaError_t e;
     if (n == 4) {
-        e = cudaFuncSetAttribute(k_sinkhorn_bwd<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sk_smem(64)));
+        e = set_smem_limit(reinterpret_cast<const void *>(k_sinkhorn_bwd<4>), int(sk_smem(64)));
         if (e != cudaSuccess) return e;
         {
             MHC_PROF("k_sinkhorn_bwd", s);
-            k_sinkhorn_bwd<4><<<grid, kSkThreads, smem, s>>>(dP, logits, dlogits, rows, iters, eps);
+            launch_k(k_sinkhorn_bwd<4>, dim3(grid), dim3(kSkThreads), smem, s, dP, logits, dlogits, rows, iters, eps);
         }
     } else {
-        e = cudaFuncSetAttribute(k_sinkhorn_bwd<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 int(sk_smem(64)));
+        e = set_smem_limit(reinterpret_cast<const void *>(k_sinkhorn_bwd<8>), int(sk_smem(64)));
         if (e != cudaSuccess) return e;
         {
             MHC_PROF("k_sinkhorn_bwd", s);
-            k_sinkhorn_bwd<8><<<grid, kSkThreads, smem, s>>>(dP, logits, dlogits, rows, iters, eps);
+            launch_k(k_sinkhorn_bwd<8>, dim3(grid), dim3(kSkThreads), smem, s, dP, logits, dlogits, rows, iters, eps);
         }
     }
     return cudaGetLastError();

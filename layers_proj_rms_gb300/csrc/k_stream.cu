@@ -7,6 +7,9 @@
 // _torch_h_aggregate_bwd, fused_h_post_bda "H_res.T @ residual + H_post *
 // (x + bias)", _torch_h_post_bda_bwd) and rwkv-ops mhu_ffi.cu
 // (StreamAggregateFwd/Bwd, MhcPostOpFwdHost/BwdHost, RMSNormFwdHost/BwdHost).
+#include <mutex>
+#include <vector>
+
 #include "launch.h"
 
 namespace mhc {
@@ -24,6 +27,26 @@ int num_sms()
         g_num_sms[dev] = v > 0 ? v : 1;
     }
     return g_num_sms[dev];
+}
+
+cudaError_t set_smem_limit(const void *kernel, int bytes)
+{
+    struct Entry {
+        int dev;
+        const void *kernel;
+        int bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    for (const Entry &d : done)
+        if (d.dev == dev && d.kernel == kernel && d.bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.push_back({dev, kernel, bytes});
+    return e;
 }
 
 static unsigned grid_for(int64_t work, int per_sm)
@@ -47,6 +70,7 @@ __global__ void __launch_bounds__(256)
     k_agg_fwd(const bf16 *__restrict__ x, const float *__restrict__ Hpre, bf16 *__restrict__ y,
               int64_t T, int64_t C8)
 {
+    pdl_wait();
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         float h[N];
 #pragma unroll
@@ -76,6 +100,7 @@ __global__ void __launch_bounds__(256)
               const float *__restrict__ Hpre, bf16 *__restrict__ dx, float *__restrict__ dHpre,
               int64_t T, int64_t C8)
 {
+    pdl_wait();
     constexpr int U = N == 4 ? 4 : 2;
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -143,6 +168,7 @@ __global__ void __launch_bounds__(256)
                      const float *__restrict__ Hpre, bf16 *__restrict__ dx,
                      float *__restrict__ part, int64_t T, int64_t C8)
 {
+    pdl_wait();
     __shared__ float red[8][N];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -200,6 +226,7 @@ __global__ void __launch_bounds__(256)
                const bf16 *__restrict__ bias, const float *__restrict__ Hres,
                const float *__restrict__ Hpost, bf16 *__restrict__ out, int64_t T, int64_t C8)
 {
+    pdl_wait();
     constexpr int U = N == 4 ? 2 : 1;
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
@@ -274,6 +301,7 @@ __global__ void __launch_bounds__(256)
                    bf16 *__restrict__ dres, bf16 *__restrict__ df, float *__restrict__ dHres,
                    float *__restrict__ dHpost, int64_t T, int64_t C8)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
     for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
@@ -378,6 +406,7 @@ __global__ void __launch_bounds__(256)
     k_dbias_partial(const bf16 *__restrict__ dout, const float *__restrict__ Hpost,
                     float *__restrict__ part, int64_t T, int64_t C8, int64_t splits)
 {
+    pdl_wait();
     const int64_t c8 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t s = blockIdx.y;
     const int64_t t0 = T * s / splits, t1 = T * (s + 1) / splits;
@@ -404,6 +433,7 @@ __global__ void __launch_bounds__(256)
 __global__ void k_sum_rows(const float *__restrict__ part, float *__restrict__ out, int64_t rows,
                            int64_t cols)
 {
+    pdl_wait();
     const int64_t c = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c >= cols) return;
     float acc = 0.f;
@@ -420,14 +450,14 @@ cudaError_t launch_dbias(const bf16 *dout, const float *Hpost, float *dbias, int
     dim3 grid(unsigned((C8 + 255) / 256), unsigned(splits));
     if (n == 4) {
         MHC_PROF("k_dbias_partial", s);
-        k_dbias_partial<4><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
+        launch_k(k_dbias_partial<4>, dim3(grid), dim3(256), 0, s, dout, Hpost, part, T, C8, splits);
     } else {
         MHC_PROF("k_dbias_partial", s);
-        k_dbias_partial<8><<<grid, 256, 0, s>>>(dout, Hpost, part, T, C8, splits);
+        launch_k(k_dbias_partial<8>, dim3(grid), dim3(256), 0, s, dout, Hpost, part, T, C8, splits);
     }
     {
         MHC_PROF("k_sum_rows", s);
-        k_sum_rows<<<unsigned((C + 255) / 256), 256, 0, s>>>(part, dbias, splits, C);
+        launch_k(k_sum_rows, dim3(unsigned((C + 255) / 256)), dim3(256), 0, s, part, dbias, splits, C);
     }
     return cudaGetLastError();
 }
@@ -457,6 +487,7 @@ __global__ void __launch_bounds__(256)
     k_rms_fwd_w(const bf16 *__restrict__ x, bf16 *__restrict__ y, float *__restrict__ rstd,
                 int64_t rows, int64_t C8, float inv_cols, float eps)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
     for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
@@ -501,6 +532,7 @@ __global__ void __launch_bounds__(256)
                 const float *__restrict__ rstd, bf16 *__restrict__ dx, int64_t rows, int64_t C8,
                 float inv_cols, float eps)
 {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
     for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
@@ -558,6 +590,7 @@ __global__ void __launch_bounds__(256)
     k_rms_fwd(const bf16 *__restrict__ x, bf16 *__restrict__ y, float *__restrict__ rstd,
               int64_t rows, int64_t C8, float inv_cols, float eps)
 {
+    pdl_wait();
     __shared__ float red[8];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         uint4 v[R];
@@ -596,6 +629,7 @@ __global__ void __launch_bounds__(256)
               const float *__restrict__ rstd, bf16 *__restrict__ dx, int64_t rows, int64_t C8,
               float inv_cols, float eps)
 {
+    pdl_wait();
     __shared__ float red[8];
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         uint4 vx[R], vg[R];
@@ -652,14 +686,14 @@ cudaError_t launch_aggregate_fwd(const bf16 *x, const float *Hpre, bf16 *y, int6
     MHC_PROF("k_agg_fwd", s);
     if (n == 4) {
         if (per_token)
-            k_agg_fwd<4, false><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+            launch_k(k_agg_fwd<4, false>, dim3(g), dim3(th), 0, s, x, Hpre, y, T, C8);
         else
-            k_agg_fwd<4, true><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+            launch_k(k_agg_fwd<4, true>, dim3(g), dim3(th), 0, s, x, Hpre, y, T, C8);
     } else {
         if (per_token)
-            k_agg_fwd<8, false><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+            launch_k(k_agg_fwd<8, false>, dim3(g), dim3(th), 0, s, x, Hpre, y, T, C8);
         else
-            k_agg_fwd<8, true><<<g, th, 0, s>>>(x, Hpre, y, T, C8);
+            launch_k(k_agg_fwd<8, true>, dim3(g), dim3(th), 0, s, x, Hpre, y, T, C8);
     }
     return cudaGetLastError();
 }
@@ -682,13 +716,13 @@ cudaError_t launch_aggregate_bwd_static(const bf16 *dy, const bf16 *x, const flo
     {
         MHC_PROF("k_agg_bwd_static", s);
         if (n == 4)
-            k_agg_bwd_static<4><<<unsigned(nb), 256, 0, s>>>(dy, x, Hpre, dx, part, T, C8);
+            launch_k(k_agg_bwd_static<4>, dim3(unsigned(nb)), dim3(256), 0, s, dy, x, Hpre, dx, part, T, C8);
         else
-            k_agg_bwd_static<8><<<unsigned(nb), 256, 0, s>>>(dy, x, Hpre, dx, part, T, C8);
+            launch_k(k_agg_bwd_static<8>, dim3(unsigned(nb)), dim3(256), 0, s, dy, x, Hpre, dx, part, T, C8);
     }
     {
         MHC_PROF("k_col_sum", s);
-        k_col_sum<<<1, dim3(32, 32), 0, s>>>(part, nb, n, dHpre);
+        launch_k(k_col_sum, dim3(1), dim3(dim3(32, 32)), 0, s, part, nb, n, dHpre);
     }
     return cudaGetLastError();
 }
@@ -700,10 +734,10 @@ cudaError_t launch_aggregate_bwd(const bf16 *dy, const bf16 *x, const float *Hpr
     const unsigned g = grid_for((T + 7) / 8, 8);
     if (n == 4) {
         MHC_PROF("k_agg_bwd", s);
-        k_agg_bwd<4><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
+        launch_k(k_agg_bwd<4>, dim3(g), dim3(256), 0, s, dy, x, Hpre, dx, dHpre, T, C8);
     } else {
         MHC_PROF("k_agg_bwd", s);
-        k_agg_bwd<8><<<g, 256, 0, s>>>(dy, x, Hpre, dx, dHpre, T, C8);
+        launch_k(k_agg_bwd<8>, dim3(g), dim3(256), 0, s, dy, x, Hpre, dx, dHpre, T, C8);
     }
     return cudaGetLastError();
 }
@@ -716,10 +750,10 @@ cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, co
     const unsigned g = grid_for((T + 7) / 8, 8);
     if (n == 4) {
         MHC_PROF("k_post_fwd", s);
-        k_post_fwd<4><<<g, 256, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+        launch_k(k_post_fwd<4>, dim3(g), dim3(256), 0, s, res, f, bias, Hres, Hpost, out, T, C8);
     } else {
         MHC_PROF("k_post_fwd", s);
-        k_post_fwd<8><<<g, 256, 0, s>>>(res, f, bias, Hres, Hpost, out, T, C8);
+        launch_k(k_post_fwd<8>, dim3(g), dim3(256), 0, s, res, f, bias, Hres, Hpost, out, T, C8);
     }
     return cudaGetLastError();
 }
@@ -733,11 +767,11 @@ cudaError_t launch_post_bwd_tok(const bf16 *dout, const bf16 *res, const bf16 *f
     const unsigned g = grid_for((T + 7) / 8, 8);
     if (n == 4) {
         MHC_PROF("k_post_bwd_tok", s);
-        k_post_bwd_tok<4><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
+        launch_k(k_post_bwd_tok<4>, dim3(g), dim3(256), 0, s, dout, res, f, bias, Hres, Hpost, dres, df, dHres,
                                             dHpost, T, C8);
     } else {
         MHC_PROF("k_post_bwd_tok", s);
-        k_post_bwd_tok<8><<<g, 256, 0, s>>>(dout, res, f, bias, Hres, Hpost, dres, df, dHres,
+        launch_k(k_post_bwd_tok<8>, dim3(g), dim3(256), 0, s, dout, res, f, bias, Hres, Hpost, dres, df, dHres,
                                             dHpost, T, C8);
     }
     return cudaGetLastError();
@@ -760,23 +794,23 @@ cudaError_t launch_rms_fwd(const bf16 *x, bf16 *y, float *rstd, int64_t rows, in
         const unsigned g = grid_for((rows + 7) / 8, 8);
         if (C8 <= 32 * 4) {
             MHC_PROF("k_rms_fwd", s);
-            k_rms_fwd_w<4><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+            launch_k(k_rms_fwd_w<4>, dim3(g), dim3(256), 0, s, x, y, rstd, rows, C8, ic, eps);
         } else if (C8 <= 32 * 8) {
             MHC_PROF("k_rms_fwd", s);
-            k_rms_fwd_w<8><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+            launch_k(k_rms_fwd_w<8>, dim3(g), dim3(256), 0, s, x, y, rstd, rows, C8, ic, eps);
         } else {
             MHC_PROF("k_rms_fwd", s);
-            k_rms_fwd_w<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+            launch_k(k_rms_fwd_w<16>, dim3(g), dim3(256), 0, s, x, y, rstd, rows, C8, ic, eps);
         }
         return cudaGetLastError();
     }
     const unsigned g = grid_for(rows, 8);
     if (rms_R(C8) == 4) {
         MHC_PROF("k_rms_fwd", s);
-        k_rms_fwd<4><<<g, threads_for((C8 + 3) / 4), 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        launch_k(k_rms_fwd<4>, dim3(g), dim3(threads_for((C8 + 3) / 4)), 0, s, x, y, rstd, rows, C8, ic, eps);
     } else {
         MHC_PROF("k_rms_fwd", s);
-        k_rms_fwd<16><<<g, 256, 0, s>>>(x, y, rstd, rows, C8, ic, eps);
+        launch_k(k_rms_fwd<16>, dim3(g), dim3(256), 0, s, x, y, rstd, rows, C8, ic, eps);
     }
     return cudaGetLastError();
 }
@@ -790,23 +824,23 @@ cudaError_t launch_rms_bwd(const bf16 *dy, const bf16 *x, const float *rstd, bf1
         const unsigned g = grid_for((rows + 7) / 8, 8);
         if (C8 <= 32 * 4) {
             MHC_PROF("k_rms_bwd", s);
-            k_rms_bwd_w<4><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+            launch_k(k_rms_bwd_w<4>, dim3(g), dim3(256), 0, s, dy, x, rstd, dx, rows, C8, ic, eps);
         } else if (C8 <= 32 * 8) {
             MHC_PROF("k_rms_bwd", s);
-            k_rms_bwd_w<8><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+            launch_k(k_rms_bwd_w<8>, dim3(g), dim3(256), 0, s, dy, x, rstd, dx, rows, C8, ic, eps);
         } else {
             MHC_PROF("k_rms_bwd", s);
-            k_rms_bwd_w<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+            launch_k(k_rms_bwd_w<16>, dim3(g), dim3(256), 0, s, dy, x, rstd, dx, rows, C8, ic, eps);
         }
         return cudaGetLastError();
     }
     const unsigned g = grid_for(rows, 8);
     if (rms_R(C8) == 4) {
         MHC_PROF("k_rms_bwd", s);
-        k_rms_bwd<4><<<g, threads_for((C8 + 3) / 4), 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        launch_k(k_rms_bwd<4>, dim3(g), dim3(threads_for((C8 + 3) / 4)), 0, s, dy, x, rstd, dx, rows, C8, ic, eps);
     } else {
         MHC_PROF("k_rms_bwd", s);
-        k_rms_bwd<16><<<g, 256, 0, s>>>(dy, x, rstd, dx, rows, C8, ic, eps);
+        launch_k(k_rms_bwd<16>, dim3(g), dim3(256), 0, s, dy, x, rstd, dx, rows, C8, ic, eps);
     }
     return cudaGetLastError();
 }

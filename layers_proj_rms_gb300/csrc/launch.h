@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "common.cuh"
 
 namespace mhc {
@@ -21,6 +23,12 @@ constexpr int kSplitSms = 152;
 
 int num_sms();
 
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per device
+// and kernel (k_stream.cu).  The attribute call is not stream-ordered, so after
+// the first call of each op nothing but launches reaches the stream (the
+// calls can be captured into a CUDA graph).
+cudaError_t set_smem_limit(const void *kernel, int bytes);
+
 // Sets the thread-local text that mhc_last_error() returns (abi.cu).
 void set_error_message(const char *msg);
 
@@ -36,6 +44,27 @@ struct ProfScope {
 #define MHC_PROF_CAT(a, b) MHC_PROF_CAT2(a, b)
 // Time the launch(es) in the rest of the enclosing scope under `name`.
 #define MHC_PROF(name, s) ::mhc::ProfScope MHC_PROF_CAT(prof_scope_, __LINE__)(name, s)
+
+// Launches `kernel` on stream s with programmatic stream serialization
+// allowed: the grid may start its setup while the previous kernel drains,
+// and waits in pdl_wait() for that kernel's completion before any memory
+// access.
+template <class... KArgs, class... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // k_sinkhorn.cu
 cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int iters,
