@@ -32,14 +32,19 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t warps = int64_t(gridDim.x) * kTokWarps;
     for (int64_t t = int64_t(blockIdx.x) * kTokWarps + warp; t < T; t += warps) {
-        float hp[N];
+        // element pairs in f32x2 arithmetic: the running sums are pairs (even
+        // and odd channels of a chunk), added together once per token
+        f32x2 hp2[N];
 #pragma unroll
-        for (int ii = 0; ii < N; ++ii) hp[ii] = __ldg(Hpost + t * N + ii);
-        float aR[N * N], aP[N], aQ[N];
+        for (int ii = 0; ii < N; ++ii) {
+            const float h = __ldg(Hpost + t * N + ii);
+            hp2[ii] = f2_make(h, h);
+        }
+        f32x2 sR[N * N], sP[N], sQ[N];
 #pragma unroll
-        for (int e = 0; e < N * N; ++e) aR[e] = 0.f;
+        for (int e = 0; e < N * N; ++e) sR[e] = 0ull;
 #pragma unroll
-        for (int j = 0; j < N; ++j) aP[j] = aQ[j] = 0.f;
+        for (int j = 0; j < N; ++j) sP[j] = sQ[j] = 0ull;
 
         for (int64_t base = lane; base < C8; base += 32 * U) {
             uint4 dr[U][N], xr[U][N], fv[U], yv[U];
@@ -60,48 +65,55 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
             for (int u = 0; u < U; ++u) {
                 const int64_t c8 = base + 32 * u;
                 if (U > 1 && c8 >= C8) continue;
-                float fb[8], gy[8];
-                unpack8(fv[u], fb);
-                unpack8(yv[u], gy);
+                f32x2 fb[4], gy[4];
+                unpack8x2(fv[u], fb);
+                unpack8x2(yv[u], gy);
                 if (bias) {
-                    float bv[8];
-                    unpack8(__ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8)), bv);
+                    f32x2 bv[4];
+                    unpack8x2(__ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8)), bv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) fb[e] += bv[e];
+                    for (int p = 0; p < 4; ++p) fb[p] = f2_add(fb[p], bv[p]);
                 }
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
-                    float v[8];
-                    unpack8(xr[u][j], v);
-                    float s = 0.f;
+                    f32x2 v[4];
+                    unpack8x2(xr[u][j], v);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) s = fmaf(gy[e], v[e], s);
-                    aQ[j] += s;
+                    for (int p = 0; p < 4; ++p) sQ[j] = f2_fma(gy[p], v[p], sQ[j]);
                 }
-                float dfv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                f32x2 dfv[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
                 for (int ii = 0; ii < N; ++ii) {
-                    float d[8];
-                    unpack8(dr[u][ii], d);
-                    float sp = 0.f;
+                    f32x2 d[4];
+                    unpack8x2(dr[u][ii], d);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        sp = fmaf(d[e], fb[e], sp);
-                        dfv[e] = fmaf(hp[ii], d[e], dfv[e]);
+                    for (int p = 0; p < 4; ++p) {
+                        sP[ii] = f2_fma(d[p], fb[p], sP[ii]);
+                        dfv[p] = f2_fma(hp2[ii], d[p], dfv[p]);
                     }
-                    aP[ii] += sp;
 #pragma unroll
                     for (int j = 0; j < N; ++j) {
-                        float v[8];
-                        unpack8(xr[u][j], v);
-                        float s = 0.f;
+                        f32x2 v[4];
+                        unpack8x2(xr[u][j], v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) s = fmaf(v[e], d[e], s);
-                        aR[j * N + ii] += s;
+                        for (int p = 0; p < 4; ++p) sR[j * N + ii] = f2_fma(v[p], d[p], sR[j * N + ii]);
                     }
                 }
-                if (df) st_stream(df + (t * C8 + c8) * 8, pack8(dfv));
+                if (df) st_stream(df + (t * C8 + c8) * 8, pack8x2(dfv));
             }
+        }
+        float aR[N * N], aP[N], aQ[N];
+        auto fold = [](f32x2 v) {
+            float lo, hi;
+            f2_split(v, lo, hi);
+            return lo + hi;
+        };
+#pragma unroll
+        for (int e = 0; e < N * N; ++e) aR[e] = fold(sR[e]);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            aP[j] = fold(sP[j]);
+            aQ[j] = fold(sQ[j]);
         }
 #pragma unroll
         for (int e = 0; e < N * N; ++e) aR[e] = warp_sum(aR[e]);
