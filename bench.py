@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 
 import mhc_inputs as mi  # noqa: E402
 
-ITERS, EPS_SK, EPS_RMS, EPS_NORM = 20, 1e-6, 1e-6, 1e-6
+ITERS, EPS_SK, EPS_RMS, EPS_NORM = mi.ITERS, mi.EPS_SK, mi.EPS_RMS, mi.EPS_NORM
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "mHC layer fwd+bwd tokens/sec on 1 GB300; achieved HBM GB/s vs ~8 TB/s peak"

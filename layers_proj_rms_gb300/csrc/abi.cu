@@ -5,6 +5,8 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/mhc.h"
 #include "launch.h"
 
@@ -41,10 +43,20 @@ int *fault_ptr()
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Host-side argument checks of one entry point.  Its lifetime is the call's:
+// it also brackets the call in an NVTX range named after the entry point (no
+// cost unless a profiler is attached).
 struct Check {
     mhc_status st = MHC_OK;
     const char *fn;
-    explicit Check(const char *f) : fn(f) { g_msg[0] = '\0'; }
+    explicit Check(const char *f) : fn(f)
+    {
+        g_msg[0] = '\0';
+        nvtxRangePushA(f);
+    }
+    ~Check() { nvtxRangePop(); }
+    Check(const Check &) = delete;
+    Check &operator=(const Check &) = delete;
 
     Check &ptr(const void *p, const char *name)
     {

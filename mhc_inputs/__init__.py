@@ -130,11 +130,22 @@ def gate_inputs(T: int, n: int, seed: int) -> dict:
             "H_static": rng.random(n, dtype=np.float32)}
 
 
+def _load_spec() -> dict:
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "configs",
+                        "spec.json")
+    with open(path) as fh:
+        return json.load(fh)
+
+
+# The fixed constants, readings, tolerances and workloads (configs/spec.json).
+SPEC = _load_spec()
+ITERS = int(SPEC["constants"]["sinkhorn_iters"])
+EPS_SK = float(SPEC["constants"]["eps_sinkhorn"])
+EPS_RMS = float(SPEC["constants"]["eps_rms"])
+EPS_NORM = float(SPEC["constants"]["eps_rmsnorm"])
+
 # The workloads, by what they are.  Each entry: (T, n, C, w_std, seed).
-LAYER_WORKLOADS = {
-    "tiny_T256_n4_C256": (256, 4, 256, 0.02, 0),
-    "mid_T4096_n4_C4096": (4096, 4, 4096, 0.02, 5),
-    "7b_fwd_T16384_n4_C4096": (16384, 4, 4096, 0.02, 2),
-    "7b_fwdbwd_T16384_n4_C4096": (16384, 4, 4096, 0.02, 3),
-    "wide_T8192_n8_C7168": (8192, 8, 7168, 0.01, 4),
-}
+LAYER_WORKLOADS = {k: (v["T"], v["n"], v["C"], v["w_std"], v["seed"])
+                   for k, v in SPEC["workloads"].items()}

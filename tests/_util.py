@@ -12,6 +12,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+import mhc_inputs as mi
+
+_TOL = mi.SPEC["tolerances"]
+
 
 def dev_bf16(bits: np.ndarray) -> torch.Tensor:
     """bf16 bit patterns (uint16) -> CUDA bf16 tensor with the same bytes."""
@@ -29,7 +33,7 @@ def host(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().astype(np.float64)
 
 
-def err_h(gpu, ref, tol=1e-5):
+def err_h(gpu, ref, tol=_TOL["H_abs"]):
     g, r = host(gpu) if isinstance(gpu, torch.Tensor) else gpu, np.asarray(ref)
     err = float(np.max(np.abs(g - r))) if r.size else 0.0
     assert np.all(np.isfinite(g)), "non-finite values"
@@ -37,7 +41,7 @@ def err_h(gpu, ref, tol=1e-5):
     return err
 
 
-def err_bf16(gpu, ref, atol=2e-2, rtol=1e-2):
+def err_bf16(gpu, ref, atol=_TOL["bf16_abs"], rtol=_TOL["bf16_rel"]):
     g, r = host(gpu) if isinstance(gpu, torch.Tensor) else gpu, np.asarray(ref)
     assert np.all(np.isfinite(g)), "non-finite values"
     if not r.size:
@@ -49,7 +53,7 @@ def err_bf16(gpu, ref, atol=2e-2, rtol=1e-2):
     return float(np.max(np.abs(g - r)))
 
 
-def err_grad(gpu, ref, rel=1e-4, atol=1e-5):
+def err_grad(gpu, ref, rel=_TOL["fp32_rel_of_max"], atol=_TOL["fp32_abs"]):
     g, r = host(gpu) if isinstance(gpu, torch.Tensor) else gpu, np.asarray(ref)
     assert np.all(np.isfinite(g)), "non-finite values"
     if not r.size:

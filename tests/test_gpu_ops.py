@@ -11,7 +11,7 @@ from tests._util import dev_bf16, dev_f32, err_bf16, err_grad, err_h, host
 
 pytestmark = pytest.mark.gpu
 
-ITERS, EPS_SK, EPS_RMS = 20, 1e-6, 1e-6
+ITERS, EPS_SK, EPS_RMS = mi.ITERS, mi.EPS_SK, mi.EPS_RMS
 SENTINEL = 7680.0  # exact in bf16 and fp32
 
 
