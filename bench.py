@@ -244,6 +244,8 @@ def bench_ops(M, d, o, T, n, C, dev, reps=5):
     wsr, wsan = M.workspace(M.OP_RMSNORM_RESIDUAL_BWD, T, 0, C, dev), W_(M.OP_H_AGGREGATE_RMSNORM_BWD)
     wspf, wspb2 = W_(M.OP_PROJ_RMS_PARTIAL_FWD, Cs), W_(M.OP_PROJ_RMS_PARTIAL_BWD, Cs)
     wsch = W_(M.OP_COMPUTE_H_BWD, 8)
+    wspp = W_(M.OP_H_POST_BDA_COMPUTE_H_FWD)
+    Hp2, Hq2, Hr2, u2, r2 = e(T, n), e(T, n), e(T, n, n), e(T, O), e(T)
     it, es, er = ITERS, EPS_SK, EPS_RMS
     ops = {
         "mhc_sinkhorn_fwd": (lambda: M.mhc_sinkhorn_fwd(lg, P, it, es), Mm * n * n * 8),
@@ -259,6 +261,11 @@ def bench_ops(M, d, o, T, n, C, dev, reps=5):
                                (2 * n + 1) * U),
         "mhc_h_post_bda_bwd": (lambda: M.mhc_h_post_bda_bwd(dout, x, f, bias, Hr, Hq, dxb, dfb,
                                                             dg, dHr, dHq, wspb), (3 * n + 2) * U),
+        # post-mix of this layer + the next layer's proj_rms pass on its output
+        # (the separate ops move (2n+1)U + nU)
+        "mhc_h_post_bda_compute_h_fwd": (lambda: M.mhc_h_post_bda_compute_h_fwd(
+            x, f, bias, Hr, Hq, W, alpha, b, it, es, er, outb, Hp2, Hq2, Hr2, u2, r2, wspp),
+            (2 * n + 1) * U),
         "rmsnorm_fwd": (lambda: M.rmsnorm_fwd(y, dfb, rstd, EPS_NORM), 2 * U),
         "rmsnorm_bwd": (lambda: M.rmsnorm_bwd(dy, y, rstd, dfb, EPS_NORM), 3 * U),
         "mhc_h_aggregate_static_fwd": (lambda: M.mhc_h_aggregate_static_fwd(x, Hs, y),

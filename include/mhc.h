@@ -111,7 +111,8 @@ typedef enum {
     MHC_OP_H_AGGREGATE_STATIC_BWD = 8,
     MHC_OP_PROJ_RMS_PARTIAL_FWD = 9,   /* C = the shard's channels Cs */
     MHC_OP_COMPUTE_H_BWD = 10,
-    MHC_OP_PROJ_RMS_PARTIAL_BWD = 11   /* C = the shard's channels Cs */
+    MHC_OP_PROJ_RMS_PARTIAL_BWD = 11,  /* C = the shard's channels Cs */
+    MHC_OP_H_POST_BDA_COMPUTE_H_FWD = 12
 } mhc_op;
 
 /* Workspace bytes an op needs for (T, n, C); 0 for a bad op or shape.
@@ -351,6 +352,29 @@ MHC_API mhc_status mhc_proj_rms_partial_bwd(const mhc_bf16 *x_shard, const float
                                             int n, int64_t Cs, mhc_bf16 *dx_shard,
                                             float *dW_shard, void *ws, size_t ws_bytes,
                                             mhc_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* Cross-layer fusion: the h_post_bda of layer l, whose output is the   */
+/* residual input of layer l+1, with the proj_rms_compute_h forward of  */
+/* layer l+1 on it ([rlk] PR body: fusing fp32_gemm_rms with the op     */
+/* that produces its input; [mcore] fused_h_post_bda followed by         */
+/* fused_proj_rms_compute_h).  The projection pass then reads no HBM of  */
+/* its own: out is summed and projected while it is written.            */
+/* ------------------------------------------------------------------ */
+
+/* out[t][i][c] = sum_j H_res[t][j][i] residual[t][j][c] + H_post[t][i] (f[t][c] + bias[c])
+ * exactly as mhc_h_post_bda_fwd (bf16, bitwise the same), and on x' = out as
+ * stored: H_pre_next, H_post_next, H_res_next (and the saves u_save_next
+ * [T,O], r_save_next [T], both nullable) exactly as mhc_proj_rms_compute_h_fwd
+ * with W_next [K,O], alpha3_next, b_next (the same values up to the order of
+ * the fp32 sums over K).  Shapes, alignment and bias as the two ops.
+ * ws: mhc_workspace_bytes(MHC_OP_H_POST_BDA_COMPUTE_H_FWD, T, n, C). */
+MHC_API mhc_status mhc_h_post_bda_compute_h_fwd(
+    const mhc_bf16 *residual, const mhc_bf16 *f, const mhc_bf16 *bias, const float *H_res,
+    const float *H_post, const float *W_next, const float *alpha3_next, const float *b_next,
+    int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms, mhc_bf16 *out,
+    float *H_pre_next, float *H_post_next, float *H_res_next, float *u_save_next,
+    float *r_save_next, void *ws, size_t ws_bytes, mhc_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* Per-kernel timing (off by default).  When enabled, every kernel the  */

@@ -28,6 +28,7 @@ OP_H_AGGREGATE_STATIC_BWD = 8
 OP_PROJ_RMS_PARTIAL_FWD = 9
 OP_COMPUTE_H_BWD = 10
 OP_PROJ_RMS_PARTIAL_BWD = 11
+OP_H_POST_BDA_COMPUTE_H_FWD = 12
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -68,6 +69,8 @@ _SIGS = {
     "mhc_compute_h_bwd": [_P, _P, _P, _P, _P, _I64, _P, _P, _I64, _I, _I, _F, _F, _P, _P, _P, _P,
                           _P, _SZ, _P],
     "mhc_proj_rms_partial_bwd": [_P, _P, _P, _P, _I64, _I, _I64, _P, _P, _P, _SZ, _P],
+    "mhc_h_post_bda_compute_h_fwd": [_P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F, _F,
+                                     _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(lib, _name)
@@ -223,6 +226,25 @@ def mhc_h_post_bda_fwd(residual, f, bias, H_res, H_post, out, stream=None):
                                _ptr(H_res, _F32, (T, n, n), "H_res"),
                                _ptr(H_post, _F32, (T, n), "H_post"),
                                _ptr(out, _BF, (T, n, C), "out"), T, n, C, _stream(stream)))
+
+
+def mhc_h_post_bda_compute_h_fwd(residual, f, bias, H_res, H_post, W_next, alpha3_next, b_next,
+                                 iters, eps_sk, eps_rms, out, H_pre_next, H_post_next,
+                                 H_res_next, u_save_next=None, r_save_next=None, ws=None,
+                                 stream=None):
+    T, n, C = residual.shape
+    O = _O(n)
+    wp, wb = _ws(ws)
+    _ok(lib.mhc_h_post_bda_compute_h_fwd(
+        _ptr(residual, _BF, name="residual"), _ptr(f, _BF, (T, C), "f"),
+        _ptr(bias, _BF, (C,), "bias"), _ptr(H_res, _F32, (T, n, n), "H_res"),
+        _ptr(H_post, _F32, (T, n), "H_post"), _ptr(W_next, _F32, (n * C, O), "W_next"),
+        _ptr(alpha3_next, _F32, (3,), "alpha3_next"), _ptr(b_next, _F32, (O,), "b_next"),
+        T, n, C, iters, eps_sk, eps_rms, _ptr(out, _BF, (T, n, C), "out"),
+        _ptr(H_pre_next, _F32, (T, n), "H_pre_next"), _ptr(H_post_next, _F32, (T, n), "H_post_next"),
+        _ptr(H_res_next, _F32, (T, n, n), "H_res_next"),
+        _ptr(u_save_next, _F32, (T, O), "u_save_next"), _ptr(r_save_next, _F32, (T,), "r_save_next"),
+        wp, wb, _stream(stream)))
 
 
 def mhc_h_post_bda_bwd(dout, residual, f, bias, H_res, H_post, dresidual, df, dbias, dH_res,

@@ -223,6 +223,7 @@ size_t mhc_workspace_bytes(mhc_op op, int64_t T, int n, int64_t C)
     case MHC_OP_H_POST_BDA_BWD: return mhc::dbias_ws_bytes(T, C);
     case MHC_OP_LAYER_FWD: return layer_fwd_ws(T, n, C);
     case MHC_OP_LAYER_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
+    case MHC_OP_H_POST_BDA_COMPUTE_H_FWD: return mhc::post_proj_ws_bytes(T, n, C);
     }
     return 0;
 }
@@ -340,6 +341,32 @@ mhc_status mhc_h_post_bda_fwd(const mhc_bf16 *residual, const mhc_bf16 *f, const
                                                 reinterpret_cast<const bf16 *>(f),
                                                 reinterpret_cast<const bf16 *>(bias), H_res, H_post,
                                                 reinterpret_cast<bf16 *>(out), T, n, C, stream));
+}
+
+mhc_status mhc_h_post_bda_compute_h_fwd(
+    const mhc_bf16 *residual, const mhc_bf16 *f, const mhc_bf16 *bias, const float *H_res,
+    const float *H_post, const float *W_next, const float *alpha3_next, const float *b_next,
+    int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms, mhc_bf16 *out,
+    float *H_pre_next, float *H_post_next, float *H_res_next, float *u_save_next,
+    float *r_save_next, void *ws, size_t ws_bytes, mhc_stream_t stream)
+{
+    Check ck("mhc_h_post_bda_compute_h_fwd");
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
+    if (ck.st || T == 0) return ck.st;
+    ck.ptr(residual, "residual").ptr(f, "f").opt(bias, "bias").ptr(H_res, "H_res");
+    ck.ptr(H_post, "H_post").ptr(W_next, "W_next").ptr(alpha3_next, "alpha3_next");
+    ck.ptr(b_next, "b_next").ptr(out, "out").ptr(H_pre_next, "H_pre_next");
+    ck.ptr(H_post_next, "H_post_next").ptr(H_res_next, "H_res_next");
+    ck.opt(u_save_next, "u_save_next").opt(r_save_next, "r_save_next");
+    ck.ws(ws, ws_bytes, mhc::post_proj_ws_bytes(T, n, C)).device();
+    if (ck.st) return ck.st;
+    return launched(ck.fn, mhc::launch_post_proj_fwd(
+                               reinterpret_cast<const bf16 *>(residual),
+                               reinterpret_cast<const bf16 *>(f), reinterpret_cast<const bf16 *>(bias),
+                               H_res, H_post, W_next, alpha3_next, b_next, T, n, C, iters, eps_sk,
+                               eps_rms, reinterpret_cast<bf16 *>(out), H_pre_next, H_post_next,
+                               H_res_next, u_save_next, r_save_next, ws, fault_ptr(), stream));
 }
 
 mhc_status mhc_h_post_bda_bwd(const mhc_bf16 *dout, const mhc_bf16 *residual, const mhc_bf16 *f,

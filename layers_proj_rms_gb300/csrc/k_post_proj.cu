@@ -1,0 +1,379 @@
+// The post-mix of one layer fused with the projection pass of the next
+// (cross-op fusion: h_post_bda of layer l, whose output is the residual
+// input of layer l+1, and the sum-of-squares / thin-projection pass of
+// proj_rms_compute_h on that input; RL-Kernel PR #383 names fusing
+// fp32_gemm_rms with its producer, Megatron-Core fused_mhc_kernels the two
+// ops).  Per token t:
+//   out[t][i][c] = sum_j H_res[t][j][i] x[t][j][c] + H_post[t][i] (f[t][c] + bias[c])   (bf16)
+//   upart[s][t][o] = sum_{k in s} out[t][k] W'[k][o],  spart[s][t] = sum_{k in s} out[t][k]^2
+// with k = i*C + c and out taken as stored (bf16), so the next layer sees
+// exactly what a separate projection pass over `out` would read.  The
+// partial sums then go through the usual compute_h (next layer's H).
+//
+// n = 4.  CTA: 128 tokens x a range of 64-channel blocks; a stage is one
+// channel block: the n residual boxes [128 x 64] and f's box (TMA, 128-byte
+// swizzle) plus the n W'_hl boxes [2O x 64] of its k-blocks.  Warps:
+//   0     TMA producer
+//   1     TMEM, then per stage: TMA store of the stage's out boxes to HBM and
+//         the MMAs u += out . [W'_hi | W'_lo] (N = 2O, one k-block per stream)
+//   2..5  token row r: out for the row's 64 channels of every stream, written
+//         over the residual boxes in place (same swizzled layout, so the
+//         boxes become both the MMA A operand and the store source); the
+//         row's sum of squares of the bf16 outputs; finally TMEM -> partials
+// A stage is free again when its MMAs have completed and the store has read
+// it.  Channels past C and rows past T load as zeros and are not stored.
+#include <cudaTypedefs.h>
+
+#include "launch.h"
+#include "tc.cuh"
+
+namespace mhc {
+
+struct PostProj {
+    static constexpr int N = 4, O = N * N + 2 * N, NB = 2 * O;  // 24 logits, 48 MMA columns
+    static constexpr int BM = 128, BC = 64;                      // tokens, channels per stage
+    static constexpr int XBOX = BM * BC * 2;                     // one stream's box: 16 KB
+    static constexpr int F_OFF = N * XBOX;
+    static constexpr int WBOX = NB * BC * 2;                     // 6 KB
+    static constexpr int W_OFF = F_OFF + XBOX;
+    static constexpr int STAGE = W_OFF + N * WBOX;               // 104 KB
+    static constexpr int STAGES = 2;
+    static constexpr int SMEM = STAGES * STAGE + 1024;
+    static constexpr int TMEM_COLS = 64;
+    static constexpr int THREADS = 192;
+    static_assert(XBOX % 1024 == 0 && WBOX % 1024 == 0 && STAGE % 1024 == 0, "alignment");
+    static_assert(SMEM <= 232448, "shared memory");
+};
+
+__global__ void __launch_bounds__(PostProj::THREADS, 1)
+    k_post_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmf,
+                   const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmo,
+                   const bf16 *__restrict__ bias, const float *__restrict__ Hres,
+                   const float *__restrict__ Hpost, float *__restrict__ upart,
+                   float *__restrict__ spart, int64_t T, int64_t C, int cb_per_split,
+                   int cb_total, int *fault)
+{
+    pdl_wait();
+    using P = PostProj;
+    constexpr int N = P::N, O = P::O;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t full[P::STAGES], ready[P::STAGES], empty[P::STAGES], acc_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int *abort_v = &abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = int(blockIdx.x) * P::BM;
+    const int split = int(blockIdx.y);
+    const int cb0 = split * cb_per_split;
+    const int ncb = min(cb_total, cb0 + cb_per_split) - cb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P::STAGES; ++s) {
+            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&ready[s], 4);
+            tc::mbar_init(&empty[s], 2);  // the MMAs' commit + the store's read
+        }
+        tc::mbar_init(&acc_bar, 1);
+        abort_flag = 0;
+        tc::fence_barrier_init();
+    }
+    if (warp == 1) tc::tmem_alloc(&tmem_slot, P::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmx);
+            tc::tma_prefetch_desc(&tmf);
+            tc::tma_prefetch_desc(&tmw);
+            int issued = 0;
+            for (int i = 0; i < ncb && !*abort_v; ++i) {
+                const int s = i % P::STAGES;
+                if (i >= P::STAGES &&
+                    !tc::mbar_wait(&empty[s], ((i / P::STAGES) & 1) ^ 1, fault,
+                                   tc::kFaultTimeoutEmpty)) {
+                    *abort_v = 1;
+                    break;
+                }
+                uint8_t *st = smem + s * P::STAGE;
+                const int c0 = (cb0 + i) * P::BC;
+                tc::mbar_arrive_expect_tx(&full[s], P::STAGE);
+                for (int j = 0; j < N; ++j) tc::tma_load_3d(st + j * P::XBOX, &tmx, c0, j, m0, &full[s]);
+                tc::tma_load_2d(st + P::F_OFF, &tmf, c0, m0, &full[s]);
+                for (int j = 0; j < N; ++j)
+                    tc::tma_load_2d(st + P::W_OFF + j * P::WBOX, &tmw, int(int64_t(j) * C + c0), 0,
+                                    &full[s]);
+                issued = i + 1;
+            }
+            // do not leave while copies into this CTA's shared memory are in flight
+            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
+                tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, fault,
+                              tc::kFaultTimeoutMisc);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- out store + MMA issue
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmo);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(P::BM, P::NB);
+            bool ok = true;
+            for (int i = 0; i < ncb; ++i) {
+                const int s = i % P::STAGES;
+                if (*abort_v ||
+                    !tc::mbar_wait(&ready[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                uint8_t *st = smem + s * P::STAGE;
+                const int c0 = (cb0 + i) * P::BC;
+                for (int j = 0; j < N; ++j) tc::tma_store_3d(&tmo, st + j * P::XBOX, c0, j, m0);
+                tc::bulk_commit_group();
+                const uint32_t a0 = tc::smem_u32(st);
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    const uint32_t a = a0 + j * P::XBOX, b = a0 + P::W_OFF + j * P::WBOX;
+#pragma unroll
+                    for (int kk = 0; kk < P::BC / 16; ++kk)
+                        tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
+                                     tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                                     (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(&empty[s]);
+                tc::bulk_wait_read_all();
+                tc::mbar_arrive(&empty[s]);
+            }
+            if (!ok) *abort_v = 1;
+            tc::mma_commit(&acc_bar);
+            tc::mbar_wait(&acc_bar, 0, fault, tc::kFaultTimeoutAcc);
+            tc::bulk_wait_all();
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ workers
+        const int q = warp & 3;
+        const int r = q * 32 + lane;  // token row of the tile = TMEM lane
+        const int64_t t = int64_t(m0) + r;
+        const bool live = t < T;
+        float hr[N * N], hp[N];
+#pragma unroll
+        for (int e = 0; e < N * N; e += 4) {
+            const float4 v = live ? __ldg(reinterpret_cast<const float4 *>(Hres + t * N * N + e))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            hr[e] = v.x;
+            hr[e + 1] = v.y;
+            hr[e + 2] = v.z;
+            hr[e + 3] = v.w;
+        }
+        {
+            const float4 v = live ? __ldg(reinterpret_cast<const float4 *>(Hpost + t * N))
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            hp[0] = v.x;
+            hp[1] = v.y;
+            hp[2] = v.z;
+            hp[3] = v.w;
+        }
+        float ssq = 0.f;
+        bool ok = true;
+        for (int i = 0; i < ncb; ++i) {
+            const int s = i % P::STAGES;
+            if (*abort_v ||
+                !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
+                *abort_v = 1;
+                ok = false;
+                break;
+            }
+            const uint32_t st = tc::smem_u32(smem + s * P::STAGE);
+            const int c0 = (cb0 + i) * P::BC;
+#pragma unroll 2
+            for (int cc = 0; cc < P::BC / 8; ++cc) {
+                // 16-byte chunk cc of row r sits at r*128 + ((cc ^ (r % 8)) * 16)
+                const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
+                const int64_t c = int64_t(c0) + cc * 8;
+                float fb[8], bb[8];
+                unpack8(lds128(st + P::F_OFF + off), fb);
+                unpack8((bias && c < C) ? __ldg(reinterpret_cast<const uint4 *>(bias + c))
+                                        : make_uint4(0, 0, 0, 0),
+                        bb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) fb[e] += bb[e];
+                float acc[N][8];
+#pragma unroll
+                for (int ii = 0; ii < N; ++ii)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[ii][e] = hp[ii] * fb[e];
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    float v[8];
+                    unpack8(lds128(st + j * P::XBOX + off), v);
+#pragma unroll
+                    for (int ii = 0; ii < N; ++ii)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[ii][e] = fmaf(hr[j * N + ii], v[e], acc[ii][e]);
+                }
+                // out stream ii replaces residual stream ii in place
+#pragma unroll
+                for (int ii = 0; ii < N; ++ii) {
+                    const uint4 o = pack8(acc[ii]);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + ii * P::XBOX + off),
+                                 "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                                 : "memory");
+                    float rv[8];
+                    unpack8(o, rv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ssq = fmaf(rv[e], rv[e], ssq);
+                }
+            }
+            // the out boxes are read by the tensor cores and the TMA store
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&ready[s]);
+        }
+        if (ok && !tc::mbar_wait(&acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
+        tc::tc_fence_after();
+        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+        float v[2 * O];
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+            float w[16];
+            tc::tmem_ld16(trow + c * 16, w);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
+        }
+        if (ok && !*abort_v && live) {
+            float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
+#pragma unroll
+            for (int o4 = 0; o4 < O / 4; ++o4)
+                dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
+                                      v[4 * o4 + 2] + v[O + 4 * o4 + 2], v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
+            spart[int64_t(split) * T + t] = ssq;
+        }
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tc::tmem_dealloc(tmem, P::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_pp()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle
+static bool map_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
+                     const cuuint64_t *strides_bytes, const cuuint32_t *box)
+{
+    auto fn = encode_fn_pp();
+    if (!fn) return false;
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
+              dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Channel-block splits: about one CTA per SM (the CTA fills most of shared
+// memory); in batch-invariant mode fixed 16-block (1024-channel) splits, so a
+// token's sums do not depend on T.
+static int post_proj_splits(int64_t T, int64_t C)
+{
+    const int64_t mt = (T + 127) / 128, cb = (C + 63) / 64;
+    int64_t s = batch_invariant() ? (cb + 15) / 16 : int64_t(kSplitSms) / (mt > 0 ? mt : 1);
+    if (s < 1) s = 1;
+    if (s > cb) s = cb;
+    return int(s);
+}
+
+// workspace: W'_hl [2O][K] bf16, partials upart [S][T][O], spart [S][T]
+size_t post_proj_ws_bytes(int64_t T, int n, int64_t C)
+{
+    if (n != 4) return proj_fwd_ws_bytes(T, n, C);
+    const int64_t O = PostProj::O, K = int64_t(n) * C;
+    const int64_t S = post_proj_splits(T, C);
+    return ws_align(size_t(2 * O * K) * 2) + ws_align(size_t(S * T * O) * 4) +
+           ws_align(size_t(S * T) * 4);
+}
+
+cudaError_t launch_post_proj_fwd(const bf16 *res, const bf16 *f, const bf16 *bias,
+                                 const float *Hres, const float *Hpost, const float *Wn,
+                                 const float *alphan, const float *bn, int64_t T, int n,
+                                 int64_t C, int iters, float eps_sk, float eps_rms, bf16 *out,
+                                 float *Hpre_n, float *Hpost_n, float *Hres_n, float *u_save_n,
+                                 float *r_save_n, void *ws, int *fault, cudaStream_t s)
+{
+    if (n != 4) {
+        // n = 8: the n boxes and W'_hl tiles of a channel block do not fit
+        // twice in shared memory; the two passes run one after the other
+        cudaError_t e = launch_post_fwd(res, f, bias, Hres, Hpost, out, T, n, C, s);
+        if (e != cudaSuccess) return e;
+        return launch_proj_fwd(out, Wn, alphan, bn, T, n, C, iters, eps_sk, eps_rms, Hpre_n,
+                               Hpost_n, Hres_n, u_save_n, r_save_n, ws, fault, s);
+    }
+    using P = PostProj;
+    const int64_t O = P::O, K = int64_t(n) * C;
+    const int S = post_proj_splits(T, C);
+    char *p = static_cast<char *>(ws);
+    bf16 *Whl = reinterpret_cast<bf16 *>(p);
+    p += ws_align(size_t(2 * O * K) * 2);
+    float *upart = reinterpret_cast<float *>(p);
+    p += ws_align(size_t(int64_t(S) * T * O) * 4);
+    float *spart = reinterpret_cast<float *>(p);
+    cudaError_t e = launch_w_split(Wn, Whl, n, K, s);
+    if (e != cudaSuccess) return e;
+    const uint64_t uC = uint64_t(C), uT = uint64_t(T);
+    CUtensorMap tmx, tmf, tmw, tmo;
+    {
+        const cuuint64_t dims[3] = {uC, cuuint64_t(n), uT};
+        const cuuint64_t strides[2] = {uC * 2, uC * 2 * n};
+        const cuuint32_t box[3] = {P::BC, 1, P::BM};
+        if (!map_bf16(&tmx, res, 3, dims, strides, box) || !map_bf16(&tmo, out, 3, dims, strides, box))
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {uC, uT};
+        const cuuint64_t strides[1] = {uC * 2};
+        const cuuint32_t box[2] = {P::BC, P::BM};
+        if (!map_bf16(&tmf, f, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[2] = {uint64_t(K), uint64_t(P::NB)};
+        const cuuint64_t strides[1] = {uint64_t(K) * 2};
+        const cuuint32_t box[2] = {P::BC, P::NB};
+        if (!map_bf16(&tmw, Whl, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    e = set_smem_limit(reinterpret_cast<const void *>(k_post_proj_tc), P::SMEM);
+    if (e != cudaSuccess) return e;
+    const int cb_total = int((C + P::BC - 1) / P::BC);
+    const int cps = (cb_total + S - 1) / S;
+    const int S_used = (cb_total + cps - 1) / cps;
+    {
+        MHC_PROF("k_post_proj_tc", s);
+        launch_k(k_post_proj_tc, dim3(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used)),
+                 dim3(P::THREADS), P::SMEM, s, tmx, tmf, tmw, tmo, bias, Hres, Hpost, upart, spart,
+                 T, C, cps, cb_total, fault);
+    }
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_compute_h_parts(upart, spart, S_used, alphan, bn, T, n, C, iters, eps_sk,
+                                  eps_rms, Hpre_n, Hpost_n, Hres_n, u_save_n, r_save_n, s);
+}
+
+}  // namespace mhc

@@ -275,6 +275,25 @@ static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alp
     return cudaGetLastError();
 }
 
+cudaError_t launch_compute_h_parts(const float *upart, const float *spart, int S,
+                                   const float *alpha, const float *b, int64_t T, int n,
+                                   int64_t C, int iters, float eps_sk, float eps_rms, float *Hpre,
+                                   float *Hpost, float *Hres, float *u_save, float *r_save,
+                                   cudaStream_t s)
+{
+    const int64_t threads = T * n, K = int64_t(n) * C;
+    MHC_PROF("k_compute_h_fwd", s);
+    if (n == 4)
+        launch_k(k_compute_h_fwd<4>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s,
+                 upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                 u_save, r_save);
+    else
+        launch_k(k_compute_h_fwd<8>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s,
+                 upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                 u_save, r_save);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,
                             int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms,
                             float *Hpre, float *Hpost, float *Hres, float *u_save, float *r_save,

@@ -300,6 +300,16 @@ static int proj_tc_kps(int64_t K, int S, int kbs)
     return (kps + kbs - 1) / kbs * kbs;
 }
 
+cudaError_t launch_w_split(const float *W, bf16 *Whl, int n, int64_t K, cudaStream_t s)
+{
+    MHC_PROF("k_w_split", s);
+    if (n == 4)
+        launch_k(k_w_split<4>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
+    else
+        launch_k(k_w_split<8>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
+    return cudaGetLastError();
+}
+
 template <int N, class P>
 static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_t C, bf16 *Whl,
                                 float *upart, float *spart, int S, int *fault, cudaStream_t s)

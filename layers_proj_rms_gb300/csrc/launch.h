@@ -153,6 +153,23 @@ cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, cons
 
 // k_proj.cu
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C);
+// W [K][O] fp32 -> W_hl [2O][K] bf16 (hi rows, then remainder rows)
+cudaError_t launch_w_split(const float *W, bf16 *Whl, int n, int64_t K, cudaStream_t s);
+// compute_h forward from S split partials upart [S][T][O], spart [S][T]
+cudaError_t launch_compute_h_parts(const float *upart, const float *spart, int S,
+                                   const float *alpha, const float *b, int64_t T, int n,
+                                   int64_t C, int iters, float eps_sk, float eps_rms, float *Hpre,
+                                   float *Hpost, float *Hres, float *u_save, float *r_save,
+                                   cudaStream_t s);
+// k_post_proj.cu: the post-mix of a layer fused with the next layer's
+// proj_rms_compute_h forward on its output (workspace post_proj_ws_bytes).
+size_t post_proj_ws_bytes(int64_t T, int n, int64_t C);
+cudaError_t launch_post_proj_fwd(const bf16 *res, const bf16 *f, const bf16 *bias,
+                                 const float *Hres, const float *Hpost, const float *Wn,
+                                 const float *alphan, const float *bn, int64_t T, int n,
+                                 int64_t C, int iters, float eps_sk, float eps_rms, bf16 *out,
+                                 float *Hpre_n, float *Hpost_n, float *Hres_n, float *u_save_n,
+                                 float *r_save_n, void *ws, int *fault, cudaStream_t s);
 cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,
                             int64_t T, int n, int64_t C, int iters, float eps_sk, float eps_rms,
                             float *Hpre, float *Hpost, float *Hres, float *u_save, float *r_save,

@@ -101,6 +101,34 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// 3D tiled load: box at (x, y, z) (x innermost) into smem, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m, int x, int y,
+                                            int z, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 3D tiled store of a box from smem to (x, y, z); elements outside the
+// tensor are not written.  Completion is tracked by bulk async-groups.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *m, const void *smem_src, int x,
+                                             int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::
+                     "l"(reinterpret_cast<uint64_t>(m)),
+                 "r"(x), "r"(y), "r"(z), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the stores of every committed group have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// the stores of every committed group are complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // ---- cp.async (global -> shared, per thread) ------------------------------
 
 // Copies src_bytes (0..16) from global to shared and zero-fills the rest of

@@ -394,3 +394,36 @@ def layer_bwd(inp, fwd, n, iters, eps_sk, eps_rms, *, want_dx=True):
         res["dx"] = pb["dres"] + ab["dx"] + prb["dx"]
         res["df"] = pb["df"]
     return res
+
+
+# --------------------------------------------------------------------------
+# Cross-layer fusion (second half): the post-mix of layer l feeds
+# layer l+1's proj_rms_compute_h.  Layer l+1 reads layer l's output as it is
+# stored, i.e. after the single bf16 round-to-nearest-even of the post-mix
+# (the only rounding of a bf16 output); its H follows from that input.
+# --------------------------------------------------------------------------
+
+def bf16_rne(a):
+    """Round fp64 values to the nearest bf16 value, ties to even (8
+    significant bits; exponent range of fp32, subnormal spacing 2^-133);
+    returned as fp64.  Written from the definition: with e = floor(log2|v|)
+    (at least -126), the bf16 values near v are the multiples of 2^(e-7)."""
+    v = np.asarray(a, dtype=np.float64)
+    out = np.zeros_like(v)
+    nz = v != 0
+    e = np.floor(np.log2(np.abs(v[nz])))
+    # log2 may land one off next to a power of two; fix e so 2^e <= |v| < 2^(e+1)
+    e = np.where(np.abs(v[nz]) < np.exp2(e), e - 1, e)
+    e = np.where(np.abs(v[nz]) >= np.exp2(e + 1), e + 1, e)
+    e = np.maximum(e, -126.0)
+    ulp = np.exp2(e - 7)
+    out[nz] = np.rint(v[nz] / ulp) * ulp  # np.rint: round half to even
+    return out
+
+
+def h_post_bda_compute_h_fwd(res, f, bias, H_res, H_post, W_next, alpha_next, b_next, n, iters,
+                             eps_sk, eps_rms):
+    out = h_post_bda_fwd(res, f, bias, H_res, H_post)
+    x_next = bf16_rne(out)
+    h = proj_rms_compute_h_fwd(x_next, W_next, alpha_next, b_next, n, iters, eps_sk, eps_rms)
+    return dict(h, out=out, x_next=x_next)

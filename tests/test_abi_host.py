@@ -88,10 +88,14 @@ def test_workspace_sizes(L):
         a = ws(op, 256, 4, 256)
         b = ws(op, 16384, 4, 4096)
         assert a > 0 and b >= a and a % 256 == 0
-    for op in (7, 8, 9, 10, 11):
+    for op in (7, 8, 9, 10, 11, 12):
         a = ws(op, 256, 4, 256)
         b = ws(op, 16384, 4, 4096)
         assert a > 0 and b >= a and a % 256 == 0
+    # the fused post-mix + next projection needs at least the projection's W_hl
+    O, K = 24, 4 * 4096
+    assert ws(12, 16384, 4, 4096) >= 2 * O * K * 2
+    assert ws(12, 300, 8, 136) == ws(1, 300, 8, 136)
     # the RMSNorm op ignores n
     assert ws(6, 256, 0, 4096) == ws(6, 256, 4, 4096) > 0
     assert ws(1, 256, 5, 256) == 0
@@ -111,6 +115,15 @@ def test_next_ops_validation_without_gpu(L):
     # static aggregate: dH_pre is always required
     h = L.mhc_h_aggregate_static_bwd
     assert h(A, A, A, A, None, 16, 4, 64, A, 1 << 20, None) == 1
+    # fused post-mix + next projection: T = 0 is a no-op; C not a multiple
+    # of 8 and a missing W_next are refused before any launch
+    pp = L.mhc_h_post_bda_compute_h_fwd
+    assert pp(None, None, None, None, None, None, None, None, 0, 4, 64, 20, 1e-6, 1e-6,
+              None, None, None, None, None, None, None, 0, None) == 0
+    assert pp(A, A, None, A, A, A, A, A, 16, 4, 60, 20, 1e-6, 1e-6,
+              A, A, A, A, None, None, A, 1 << 20, None) == 2
+    assert pp(A, A, None, A, A, None, A, A, 16, 4, 64, 20, 1e-6, 1e-6,
+              A, A, A, A, None, None, A, 1 << 20, None) == 1
     # compute_h needs K >= 1
     c = L.mhc_compute_h_fwd
     assert c(A, A, 0, A, A, 16, 4, 20, 1e-6, 1e-6, A, A, A, None, None) == 2

@@ -243,3 +243,93 @@ def test_compute_h_bwd_du_coef_match_autograd(orc):
     cb = orc.compute_h_bwd_from_sums(dHp, dHq, dHr, u, s, K, alpha, b, n, iters, eps_sk, eps_rms)
     np.testing.assert_allclose(cb["du"], tu.grad.numpy(), rtol=1e-10, atol=1e-12)
     np.testing.assert_allclose(cb["coef"], 2.0 * ts.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------
+# cross-layer fusion: post-mix of layer l -> proj_rms_compute_h of layer l+1
+# ----------------------------------------------------------------------------
+
+def test_bf16_rne_ties_and_subnormals(orc):
+    """Round-to-nearest-even at 8 significant bits, from worked cases: a tie
+    at 1 + 2^-8 goes down to the even 1, 1 + 3*2^-8 up to 1 + 2^-6; 255.5 and
+    257 are ties that go to 256; in the subnormal range the spacing is
+    2^-133, so 1.5 * 2^-133 rounds to 2^-132."""
+    v = np.array([1.0, 1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, -(1 + 2.0 ** -8 + 2.0 ** -12), 255.5,
+                  257.0, 1.5 * 2.0 ** -133, 0.0, 2.0 ** -126 * (1 + 2.0 ** -7)])
+    want = np.array([1.0, 1.0, 1 + 2.0 ** -6, -(1 + 2.0 ** -7), 256.0, 256.0, 2.0 ** -132, 0.0,
+                     2.0 ** -126 * (1 + 2.0 ** -7)])
+    np.testing.assert_array_equal(orc.bf16_rne(v), want)
+
+
+def test_bf16_rne_matches_bit_rounding(orc):
+    """The arithmetic rounding agrees with the bit-level rounding of fp32
+    (add 0x7FFF plus the kept lsb, truncate) on values of every magnitude."""
+    import mhc_inputs as mi
+    g = _rng(77)
+    x = (g.standard_normal(50000) * 10.0 ** g.integers(-35, 35, 50000)).astype(np.float32)
+    x = x[np.isfinite(x)]
+    want = mi.bf16_bits_to_f32(mi.bf16_bits(x)).astype(np.float64)
+    np.testing.assert_array_equal(orc.bf16_rne(x.astype(np.float64)), want)
+
+
+def _fused_inputs(g, T, n, C):
+    res = orc_bf16(g.standard_normal((T, n, C)))
+    f = orc_bf16(g.standard_normal((T, C)))
+    bias = orc_bf16(0.02 * g.standard_normal(C))
+    W = 0.05 * g.standard_normal((n * C, n * n + 2 * n))
+    alpha = np.array([0.7, 0.9, 1.1])
+    b = g.standard_normal(n * n + 2 * n)
+    return res, f, bias, W, alpha, b
+
+
+def orc_bf16(a):
+    import mhc_inputs as mi
+    return mi.bf16_bits_to_f32(mi.bf16_bits(np.asarray(a, dtype=np.float32))).astype(np.float64)
+
+
+@pytest.mark.parametrize("n", [4, 8])
+def test_fused_next_layer_sees_permuted_residual(orc, n):
+    """H_res a permutation per token and H_post = 0: layer l's output is the
+    residual with its streams permuted (exact in bf16), so layer l+1's H must
+    be the plain proj_rms_compute_h of that permuted tensor, and not of the
+    residual itself."""
+    g = _rng(90 + n)
+    T, C = 6, 16
+    res, f, bias, W, alpha, b = _fused_inputs(g, T, n, C)
+    Hres = np.zeros((T, n, n))
+    perms = [g.permutation(n) for _ in range(T)]
+    for t, p in enumerate(perms):
+        Hres[t, np.arange(n), p] = 1.0  # stream j goes to output stream p[j]
+    Hpost = np.zeros((T, n))
+    got = orc.h_post_bda_compute_h_fwd(res, f, bias, Hres, Hpost, W, alpha, b, n, 20, 1e-6, 1e-6)
+    moved = np.empty_like(res)
+    for t, p in enumerate(perms):
+        moved[t, p] = res[t]
+    np.testing.assert_array_equal(got["x_next"], moved)
+    want = orc.proj_rms_compute_h_fwd(moved, W, alpha, b, n, 20, 1e-6, 1e-6)
+    for k in ("H_pre", "H_post", "H_res", "u", "r"):
+        np.testing.assert_array_equal(got[k], want[k])
+    other = orc.proj_rms_compute_h_fwd(res, W, alpha, b, n, 20, 1e-6, 1e-6)
+    assert np.max(np.abs(other["u"] - got["u"])) > 1e-3
+
+
+def test_fused_next_layer_reads_rounded_output(orc):
+    """Layer l+1's sum of squares is that of the bf16-rounded output, the
+    tensor it would read back: r = 1/(sqrt(sum bf16(out)^2 / K) + eps), and u
+    is bf16(out) . W, both checked with numpy; the unrounded output gives a
+    different r."""
+    g = _rng(95)
+    T, n, C = 5, 4, 24
+    res, f, bias, W, alpha, b = _fused_inputs(g, T, n, C)
+    Hres = g.random((T, n, n))
+    Hpost = 2 * g.random((T, n))
+    got = orc.h_post_bda_compute_h_fwd(res, f, bias, Hres, Hpost, W, alpha, b, n, 20, 1e-6, 1e-6)
+    out = np.einsum("tji,tjc->tic", Hres, res) + Hpost[:, :, None] * (f + bias)[:, None, :]
+    np.testing.assert_allclose(got["out"], out, rtol=1e-13, atol=1e-13)
+    xr = orc.bf16_rne(out).reshape(T, n * C)
+    K = n * C
+    r = 1.0 / (np.sqrt(np.sum(xr * xr, axis=1) / K) + 1e-6)
+    np.testing.assert_allclose(got["r"], r, rtol=1e-13)
+    np.testing.assert_allclose(got["u"], xr @ W, rtol=1e-12, atol=1e-12)
+    r_exact = 1.0 / (np.sqrt(np.sum(out.reshape(T, K) ** 2, axis=1) / K) + 1e-6)
+    assert np.max(np.abs(r_exact - got["r"])) > 1e-7
