@@ -10,16 +10,17 @@
 // exactly what a separate projection pass over `out` would read.  The
 // partial sums then go through the usual compute_h (next layer's H).
 //
-// n = 4.  CTA: 128 tokens x a range of 64-channel blocks; a stage is one
-// channel block: the n residual boxes [128 x 64] and f's box (TMA, 128-byte
-// swizzle) plus the n W'_hl boxes [2O x 64] of its k-blocks.  Warps:
+// n = 4.  CTA: 128 tokens x a range of channel blocks; a stage is one
+// channel block of BC channels: the n residual boxes [128 x BC] and f's box
+// (TMA, swizzled) plus the n W'_hl boxes [2O x BC] of its k-blocks.  Warps:
 //   0     TMA producer
 //   1     TMEM, then per stage: TMA store of the stage's out boxes to HBM and
 //         the MMAs u += out . [W'_hi | W'_lo] (N = 2O, one k-block per stream)
-//   2..5  token row r: out for the row's 64 channels of every stream, written
-//         over the residual boxes in place (same swizzled layout, so the
-//         boxes become both the MMA A operand and the store source); the
-//         row's sum of squares of the bf16 outputs; finally TMEM -> partials
+//   2..9  two warps per token row r (half the block's channels each): out for the row's
+//         channels of every stream, written over the residual boxes in place
+//         (same swizzled layout, so the boxes become both the MMA A operand
+//         and the store source); the row's sum of squares of the bf16
+//         outputs; finally TMEM -> partials
 // A stage is free again when its MMAs have completed and the store has read
 // it.  Channels past C and rows past T load as zeros and are not stored.
 #include <cudaTypedefs.h>
@@ -29,23 +30,45 @@
 
 namespace mhc {
 
-struct PostProj {
+// BC channels per stage (64: 128-byte rows and swizzle; 32: 64-byte rows
+// and swizzle), STAGES stages, MINB CTAs per SM.
+template <int BC_, int STAGES_, int MINB_>
+struct PostProjCfg {
     static constexpr int N = 4, O = N * N + 2 * N, NB = 2 * O;  // 24 logits, 48 MMA columns
-    static constexpr int BM = 128, BC = 64;                      // tokens, channels per stage
-    static constexpr int XBOX = BM * BC * 2;                     // one stream's box: 16 KB
+    static constexpr int BM = 128, BC = BC_;                     // tokens, channels per stage
+    static constexpr int RB = BC * 2;                            // bytes of a box row
+    static constexpr int CH = BC / 8;                            // 16-byte chunks per row
+    static constexpr int XBOX = BM * RB;                         // one stream's box
     static constexpr int F_OFF = N * XBOX;
-    static constexpr int WBOX = NB * BC * 2;                     // 6 KB
+    static constexpr int WBOX = NB * RB;
     static constexpr int W_OFF = F_OFF + XBOX;
-    static constexpr int STAGE = W_OFF + N * WBOX;               // 104 KB
-    static constexpr int STAGES = 2;
+    static constexpr int STAGE = W_OFF + N * WBOX;
+    static constexpr int STAGES = STAGES_, MINB = MINB_;
     static constexpr int SMEM = STAGES * STAGE + 1024;
     static constexpr int TMEM_COLS = 64;
-    static constexpr int THREADS = 192;
-    static_assert(XBOX % 1024 == 0 && WBOX % 1024 == 0 && STAGE % 1024 == 0, "alignment");
-    static_assert(SMEM <= 232448, "shared memory");
+    static constexpr int WORKERS = 8;  // warps 2..9
+    static constexpr int THREADS = 64 + 32 * WORKERS;
+    static constexpr int ATOM = BC == 64 ? 1024 : 512;  // swizzle pattern repeat
+    static_assert(BC == 64 || BC == 32, "box width");
+    static_assert(XBOX % ATOM == 0 && WBOX % ATOM == 0 && STAGE % 1024 == 0, "alignment");
+    static_assert((SMEM + 1024) * MINB <= 233472, "shared memory");
+    // 16-byte chunk cc of row r in the swizzled box
+    __device__ static uint32_t chunk_off(int r, int cc)
+    {
+        return uint32_t(r * RB + ((BC == 64 ? (cc ^ (r & 7)) : (cc ^ ((r >> 1) & 3))) << 4));
+    }
+    __device__ static uint64_t desc(uint32_t addr)
+    {
+        return BC == 64 ? tc::desc_kmajor_sw128(addr) : tc::make_desc(addr, 16, 512, tc::kSwz64);
+    }
 };
+// Four 52 KB stages of 32 channels, one CTA per SM (T=16384, n=4, C=4096:
+// 0.217 ms; two 104 KB stages of 64 channels: 0.244 ms; two 52 KB stages at
+// two CTAs per SM: 0.248 ms).
+using PostProj = PostProjCfg<32, 4, 1>;
 
-__global__ void __launch_bounds__(PostProj::THREADS, 1)
+template <class P>
+__global__ void __launch_bounds__(P::THREADS, P::MINB)
     k_post_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmf,
                    const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmo,
                    const bf16 *__restrict__ bias, const float *__restrict__ Hres,
@@ -54,12 +77,12 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
                    int cb_total, int *fault)
 {
     pdl_wait();
-    using P = PostProj;
     constexpr int N = P::N, O = P::O;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[P::STAGES], ready[P::STAGES], empty[P::STAGES], acc_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ float ssq_red[P::BM];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     volatile int *abort_v = &abort_flag;
@@ -73,7 +96,7 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&ready[s], 4);
+            tc::mbar_init(&ready[s], P::WORKERS);
             tc::mbar_init(&empty[s], 2);  // the MMAs' commit + the store's read
         }
         tc::mbar_init(&acc_bar, 1);
@@ -140,8 +163,7 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
                     const uint32_t a = a0 + j * P::XBOX, b = a0 + P::W_OFF + j * P::WBOX;
 #pragma unroll
                     for (int kk = 0; kk < P::BC / 16; ++kk)
-                        tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
-                                     tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                        tc::mma_bf16(tmem, P::desc(a + kk * 32), P::desc(b + kk * 32), idesc,
                                      (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(&empty[s]);
@@ -156,29 +178,33 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ workers
+        // two warps per TMEM lane quadrant; warp half `hf` takes half of the
+        // 16-byte chunks of every row of the quadrant
         const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int r = q * 32 + lane;  // token row of the tile = TMEM lane
         const int64_t t = int64_t(m0) + r;
         const bool live = t < T;
-        float hr[N * N], hp[N];
+        // the row's H_res and H_post as f32x2 pairs (the same value twice)
+        f32x2 hr2[N * N], hp2[N];
 #pragma unroll
         for (int e = 0; e < N * N; e += 4) {
             const float4 v = live ? __ldg(reinterpret_cast<const float4 *>(Hres + t * N * N + e))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            hr[e] = v.x;
-            hr[e + 1] = v.y;
-            hr[e + 2] = v.z;
-            hr[e + 3] = v.w;
+            hr2[e] = f2_make(v.x, v.x);
+            hr2[e + 1] = f2_make(v.y, v.y);
+            hr2[e + 2] = f2_make(v.z, v.z);
+            hr2[e + 3] = f2_make(v.w, v.w);
         }
         {
             const float4 v = live ? __ldg(reinterpret_cast<const float4 *>(Hpost + t * N))
                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-            hp[0] = v.x;
-            hp[1] = v.y;
-            hp[2] = v.z;
-            hp[3] = v.w;
+            hp2[0] = f2_make(v.x, v.x);
+            hp2[1] = f2_make(v.y, v.y);
+            hp2[2] = f2_make(v.z, v.z);
+            hp2[3] = f2_make(v.w, v.w);
         }
-        float ssq = 0.f;
+        f32x2 ssq2 = 0ull;
         bool ok = true;
         for (int i = 0; i < ncb; ++i) {
             const int s = i % P::STAGES;
@@ -191,42 +217,44 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
             const uint32_t st = tc::smem_u32(smem + s * P::STAGE);
             const int c0 = (cb0 + i) * P::BC;
 #pragma unroll 2
-            for (int cc = 0; cc < P::BC / 8; ++cc) {
-                // 16-byte chunk cc of row r sits at r*128 + ((cc ^ (r % 8)) * 16)
-                const uint32_t off = r * 128 + ((cc ^ (r & 7)) << 4);
+            for (int c4 = 0; c4 < P::CH / 2; ++c4) {
+                const int cc = (P::CH / 2) * hf + c4;
+                const uint32_t off = P::chunk_off(r, cc);
                 const int64_t c = int64_t(c0) + cc * 8;
-                float fb[8], bb[8];
-                unpack8(lds128(st + P::F_OFF + off), fb);
-                unpack8((bias && c < C) ? __ldg(reinterpret_cast<const uint4 *>(bias + c))
-                                        : make_uint4(0, 0, 0, 0),
-                        bb);
+                f32x2 fb[4], bb[4];
+                unpack8x2(lds128(st + P::F_OFF + off), fb);
+                unpack8x2((bias && c < C) ? __ldg(reinterpret_cast<const uint4 *>(bias + c))
+                                          : make_uint4(0, 0, 0, 0),
+                          bb);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) fb[e] += bb[e];
-                float acc[N][8];
+                for (int e = 0; e < 4; ++e) fb[e] = f2_add(fb[e], bb[e]);
+                // the same fp32 operations per element as the separate
+                // post-mix: H_post (f + bias), then H_res[j][i] x_j for j ascending
+                f32x2 acc[N][4];
 #pragma unroll
                 for (int ii = 0; ii < N; ++ii)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[ii][e] = hp[ii] * fb[e];
+                    for (int e = 0; e < 4; ++e) acc[ii][e] = f2_mul(hp2[ii], fb[e]);
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
-                    float v[8];
-                    unpack8(lds128(st + j * P::XBOX + off), v);
+                    f32x2 v[4];
+                    unpack8x2(lds128(st + j * P::XBOX + off), v);
 #pragma unroll
                     for (int ii = 0; ii < N; ++ii)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[ii][e] = fmaf(hr[j * N + ii], v[e], acc[ii][e]);
+                        for (int e = 0; e < 4; ++e) acc[ii][e] = f2_fma(hr2[j * N + ii], v[e], acc[ii][e]);
                 }
                 // out stream ii replaces residual stream ii in place
 #pragma unroll
                 for (int ii = 0; ii < N; ++ii) {
-                    const uint4 o = pack8(acc[ii]);
+                    const uint4 o = pack8x2(acc[ii]);
                     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(st + ii * P::XBOX + off),
                                  "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
                                  : "memory");
-                    float rv[8];
-                    unpack8(o, rv);
+                    f32x2 rv[4];
+                    unpack8x2(o, rv);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ssq = fmaf(rv[e], rv[e], ssq);
+                    for (int e = 0; e < 4; ++e) ssq2 = f2_fma(rv[e], rv[e], ssq2);
                 }
             }
             // the out boxes are read by the tensor cores and the TMA store
@@ -234,25 +262,35 @@ __global__ void __launch_bounds__(PostProj::THREADS, 1)
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&ready[s]);
         }
-        if (ok && !tc::mbar_wait(&acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
-        tc::tc_fence_after();
-        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-        float v[2 * O];
+        float s_lo, s_hi;
+        f2_split(ssq2, s_lo, s_hi);
+        const float ssq = s_lo + s_hi;
+        // the row's sum of squares: half 1 hands its part to half 0
+        if (hf == 1) ssq_red[r] = ssq;
+        tc::named_bar_sync(1 + q, 64);
+        if (hf == 0) {
+            const float ssq_row = ssq + ssq_red[r];
+            if (ok && !tc::mbar_wait(&acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
+            tc::tc_fence_after();
+            const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+            float v[2 * O];
 #pragma unroll
-        for (int c = 0; c < 3; ++c) {
-            float w[16];
-            tc::tmem_ld16(trow + c * 16, w);
-            tc::tmem_ld_wait();
+            for (int c = 0; c < 3; ++c) {
+                float w[16];
+                tc::tmem_ld16(trow + c * 16, w);
+                tc::tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
-        }
-        if (ok && !*abort_v && live) {
-            float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
+                for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
+            }
+            if (ok && !*abort_v && live) {
+                float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
 #pragma unroll
-            for (int o4 = 0; o4 < O / 4; ++o4)
-                dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
-                                      v[4 * o4 + 2] + v[O + 4 * o4 + 2], v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
-            spart[int64_t(split) * T + t] = ssq;
+                for (int o4 = 0; o4 < O / 4; ++o4)
+                    dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
+                                          v[4 * o4 + 2] + v[O + 4 * o4 + 2],
+                                          v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
+                spart[int64_t(split) * T + t] = ssq_row;
+            }
         }
     }
     tc::tc_fence_before();
@@ -277,26 +315,29 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_pp()
     return fn;
 }
 
-// bf16 tensor of `rank` dims (innermost first), 128-byte swizzle
+// bf16 tensor of `rank` dims (innermost first) in the stage's swizzle
 static bool map_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
                      const cuuint64_t *strides_bytes, const cuuint32_t *box)
 {
+    const CUtensorMapSwizzle sw =
+        PostProj::BC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     auto fn = encode_fn_pp();
     if (!fn) return false;
     cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
               dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Channel-block splits: about one CTA per SM (the CTA fills most of shared
-// memory); in batch-invariant mode fixed 16-block (1024-channel) splits, so a
+// memory); in batch-invariant mode fixed 1024-channel splits, so a
 // token's sums do not depend on T.
 static int post_proj_splits(int64_t T, int64_t C)
 {
-    const int64_t mt = (T + 127) / 128, cb = (C + 63) / 64;
-    int64_t s = batch_invariant() ? (cb + 15) / 16 : int64_t(kSplitSms) / (mt > 0 ? mt : 1);
+    const int64_t mt = (T + 127) / 128, cb = (C + PostProj::BC - 1) / PostProj::BC;
+    int64_t s = batch_invariant() ? (cb * PostProj::BC + 1023) / 1024
+                                  : int64_t(kSplitSms) * PostProj::MINB / (mt > 0 ? mt : 1);
     if (s < 1) s = 1;
     if (s > cb) s = cb;
     return int(s);
@@ -359,14 +400,14 @@ cudaError_t launch_post_proj_fwd(const bf16 *res, const bf16 *f, const bf16 *bia
         const cuuint32_t box[2] = {P::BC, P::NB};
         if (!map_bf16(&tmw, Whl, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
-    e = set_smem_limit(reinterpret_cast<const void *>(k_post_proj_tc), P::SMEM);
+    e = set_smem_limit(reinterpret_cast<const void *>(k_post_proj_tc<PostProj>), P::SMEM);
     if (e != cudaSuccess) return e;
     const int cb_total = int((C + P::BC - 1) / P::BC);
     const int cps = (cb_total + S - 1) / S;
     const int S_used = (cb_total + cps - 1) / cps;
     {
         MHC_PROF("k_post_proj_tc", s);
-        launch_k(k_post_proj_tc, dim3(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used)),
+        launch_k(k_post_proj_tc<PostProj>, dim3(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used)),
                  dim3(P::THREADS), P::SMEM, s, tmx, tmf, tmw, tmo, bias, Hres, Hpost, upart, spart,
                  T, C, cps, cb_total, fault);
     }
