@@ -100,6 +100,14 @@ MHC_API int mhc_batch_invariant(void);
  * otherwise (*code receives the fault code, 0 if none; code may be NULL). */
 MHC_API mhc_status mhc_device_error(int *code, mhc_stream_t stream);
 
+/* Self-test of that path: launches one kernel whose bounded wait, the same
+ * wait the tensor-core kernels use, is on an mbarrier that nothing arrives
+ * at; after about wait_us microseconds of SM clock (1 <= wait_us <= 1e6) it
+ * gives up, records fault code 105 in the device error word and returns.
+ * Nothing faults or hangs, and the context stays usable; a following
+ * mhc_device_error() returns MHC_ERR_DEVICE_FAULT with code 105. */
+MHC_API mhc_status mhc_selftest_wait_timeout(int wait_us, mhc_stream_t stream);
+
 typedef enum {
     MHC_OP_PROJ_RMS_COMPUTE_H_FWD = 1,
     MHC_OP_PROJ_RMS_COMPUTE_H_BWD = 2,

@@ -55,6 +55,7 @@ _SIGS = {
     "mhc_layer_bwd": [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I, _I64, _I, _F,
                       _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "mhc_device_error": [ctypes.POINTER(ctypes.c_int), _P],
+    "mhc_selftest_wait_timeout": [_I, _P],
     "mhc_proj_rms_compute_h_fwd_noalloc": [_P, _P, _P, _P, _I64, _I, _I64, _I, _F, _F, _P, _P,
                                            _P, _P, _P, _P],
     "mhc_h_aggregate_static_fwd": [_P, _P, _P, _I64, _I, _I64, _P],
@@ -157,6 +158,10 @@ def mhc_device_error(stream=None) -> int:
     if st not in (0, 9):
         _ok(st)
     return code.value
+
+
+def mhc_selftest_wait_timeout(wait_us, stream=None):
+    _ok(lib.mhc_selftest_wait_timeout(int(wait_us), _stream(stream)))
 
 
 def mhc_sinkhorn_fwd(logits, P, iters, eps, stream=None):

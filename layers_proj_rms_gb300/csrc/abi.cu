@@ -186,6 +186,20 @@ void mhc_set_batch_invariant(int on) { mhc::set_batch_invariant(on); }
 
 int mhc_batch_invariant(void) { return mhc::batch_invariant(); }
 
+mhc_status mhc_selftest_wait_timeout(int wait_us, mhc_stream_t stream)
+{
+    Check ck("mhc_selftest_wait_timeout");
+    if (wait_us < 1 || wait_us > 1000000)
+        return fail(MHC_ERR_BAD_SHAPE, "mhc_selftest_wait_timeout: wait_us must be in [1, 1e6]");
+    if (ck.device().st) return ck.st;
+    int dev = 0, khz = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev);
+    if (e != cudaSuccess) return launched(ck.fn, e);
+    const long long cycles = (long long)wait_us * (khz > 0 ? khz : 2000000) / 1000;
+    return launched(ck.fn, mhc::launch_selftest_wait(cycles, fault_ptr(), stream));
+}
+
 mhc_status mhc_device_error(int *code, mhc_stream_t stream)
 {
     Check ck("mhc_device_error");

@@ -161,6 +161,8 @@ cudaError_t launch_compute_h_parts(const float *upart, const float *spart, int S
                                    int64_t C, int iters, float eps_sk, float eps_rms, float *Hpre,
                                    float *Hpost, float *Hres, float *u_save, float *r_save,
                                    cudaStream_t s);
+// selftest.cu: a bounded wait that runs out after `limit` cycles
+cudaError_t launch_selftest_wait(long long limit, int *fault, cudaStream_t s);
 // k_post_proj.cu: the post-mix of a layer fused with the next layer's
 // proj_rms_compute_h forward on its output (workspace post_proj_ws_bytes).
 size_t post_proj_ws_bytes(int64_t T, int n, int64_t C);

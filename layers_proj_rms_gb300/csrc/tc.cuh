@@ -17,6 +17,7 @@ enum : int {
     kFaultTimeoutEmpty = 102,  // the producer waited too long for a free stage
     kFaultTimeoutAcc = 103,    // the epilogue waited too long for the accumulator
     kFaultTimeoutMisc = 104,
+    kFaultSelfTest = 105,      // the self-test's wait ran out, as it must
 };
 
 // Spin limit of every wait: about a second of SM clock.
@@ -69,12 +70,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 
 // Waits for the phase with the given parity to complete.  Returns false
 // (after reporting `code`) if it did not within kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *fault, int code)
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *fault, int code,
+                                          long long limit = kWaitCycles)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) {
+        if (clock64() - t0 > limit) {
             report_fault(fault, code);
             return false;
         }

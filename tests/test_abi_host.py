@@ -124,6 +124,9 @@ def test_next_ops_validation_without_gpu(L):
               A, A, A, A, None, None, A, 1 << 20, None) == 2
     assert pp(A, A, None, A, A, None, A, A, 16, 4, 64, 20, 1e-6, 1e-6,
               A, A, A, A, None, None, A, 1 << 20, None) == 1
+    # the fault-path self-test takes 1 <= wait_us <= 1e6
+    st = L.mhc_selftest_wait_timeout
+    assert st(0, None) == 2 and st(2000000, None) == 2
     # compute_h needs K >= 1
     c = L.mhc_compute_h_fwd
     assert c(A, A, 0, A, A, 16, 4, 20, 1e-6, 1e-6, A, A, A, None, None) == 2

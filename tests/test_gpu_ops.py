@@ -356,3 +356,21 @@ def test_empty_token_count(M):
 
 def test_no_device_fault_reported(M):
     assert M.mhc_device_error() == 0
+
+
+def test_bounded_wait_reports_fault_and_context_survives(M, orc):
+    """The fault path, exercised without a fault: a kernel's bounded wait on
+    an mbarrier that nothing arrives at runs out after ~20 ms, the kernel
+    records fault code 105 and returns; the host reads (and clears) it, and
+    the context still runs kernels correctly afterwards."""
+    assert M.mhc_device_error() == 0
+    M.mhc_selftest_wait_timeout(20000)
+    assert M.mhc_device_error() == 105
+    assert M.mhc_device_error() == 0
+    inp = mi.sinkhorn_inputs(33, 4, seed=7)
+    lg = dev_f32(inp["logits"])
+    P = torch.empty_like(lg)
+    M.mhc_sinkhorn_fwd(lg, P, ITERS, EPS_SK)
+    torch.cuda.synchronize()
+    err_h(P, orc.sinkhorn_fwd(inp["logits"], ITERS, EPS_SK))
+    assert M.mhc_device_error() == 0
