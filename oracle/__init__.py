@@ -397,10 +397,11 @@ def layer_bwd(inp, fwd, n, iters, eps_sk, eps_rms, *, want_dx=True):
 
 
 # --------------------------------------------------------------------------
-# Cross-layer fusion (second half): the post-mix of layer l feeds
-# layer l+1's proj_rms_compute_h.  Layer l+1 reads layer l's output as it is
-# stored, i.e. after the single bf16 round-to-nearest-even of the post-mix
-# (the only rounding of a bf16 output); its H follows from that input.
+# Cross-layer fusion (RL-Kernel PR #383 body: fuse fp32_gemm_rms with the op
+# that produces its input): the post-mix of layer l feeds layer l+1's
+# proj_rms_compute_h.  Layer l+1 reads layer l's output as it is stored, i.e.
+# after the single bf16 round-to-nearest-even of the post-mix (the only
+# rounding of a bf16 output); its H follows from that input.
 # --------------------------------------------------------------------------
 
 def bf16_rne(a):
