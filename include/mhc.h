@@ -32,8 +32,9 @@
  *  - Arguments are validated on the host before any launch.  A failed check
  *    returns a nonzero mhc_status, launches nothing and writes nothing;
  *    mhc_last_error() then describes it (thread-local).
- *  - bf16 pointers must be 16-byte aligned and C a multiple of 8; fp32
- *    pointers 4-byte aligned.  n must be 4 or 8; 0 <= iters <= 64.
+ *  - Every pointer must be 16-byte aligned and C a multiple of 8.  n must be
+ *    4 or 8; 0 <= iters <= 64.  The ops that take W (they run on the tensor
+ *    cores with 32-bit TMA coordinates) need T < 2^31 and n*C < 2^31.
  *  - T (or M, rows) may be 0: the call then returns MHC_OK and does nothing.
  *  - Results are deterministic: no atomics, fixed reduction order; the same
  *    inputs give bitwise identical outputs run to run.

@@ -91,6 +91,15 @@ struct Check {
             st = fail(MHC_ERR_BAD_SHAPE, "%s: %s = %lld too large", fn, name, (long long)C);
         return *this;
     }
+    // the tensor-core kernels address rows and the flattened k = i*C + c with
+    // 32-bit TMA coordinates
+    Check &tma(int64_t T, int64_t K)
+    {
+        if (st == MHC_OK && (T > INT32_MAX || K > INT32_MAX))
+            st = fail(MHC_ERR_BAD_SHAPE, "%s: T = %lld and n*C = %lld must be below 2^31", fn,
+                      (long long)T, (long long)K);
+        return *this;
+    }
     Check &fits(int64_t a, int64_t b, const char *what)  // a*b elements must fit in int64 / 2^62
     {
         if (st == MHC_OK && a > 0 && b > 0 && a > (int64_t(1) << 62) / b)
@@ -273,7 +282,7 @@ mhc_status mhc_proj_rms_compute_h_fwd(const mhc_bf16 *x, const float *W, const f
                                       size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_proj_rms_compute_h_fwd");
-    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").tma(T, n * C).iters(iters);
     ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
     if (ck.st || T == 0) return ck.st;
     ck.ptr(x, "x").ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(H_pre, "H_pre");
@@ -294,7 +303,7 @@ mhc_status mhc_proj_rms_compute_h_bwd(const float *dH_pre, const float *dH_post,
                                       size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_proj_rms_compute_h_bwd");
-    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").tma(T, n * C).iters(iters);
     ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
     ck.ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(dW, "dW").ptr(dalpha3, "dalpha3");
     ck.ptr(db, "db");
@@ -365,7 +374,7 @@ mhc_status mhc_h_post_bda_compute_h_fwd(
     float *r_save_next, void *ws, size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_h_post_bda_compute_h_fwd");
-    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").tma(T, n * C).iters(iters);
     ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
     if (ck.st || T == 0) return ck.st;
     ck.ptr(residual, "residual").ptr(f, "f").opt(bias, "bias").ptr(H_res, "H_res");
@@ -455,7 +464,7 @@ mhc_status mhc_layer_fwd(const mhc_bf16 *x, const float *W, const float *alpha3,
                          mhc_bf16 *out, void *ws, size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_layer_fwd");
-    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").tma(T, n * C).iters(iters);
     ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
     if (ck.st || T == 0) return ck.st;
     ck.ptr(x, "x").ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").ptr(f, "f").opt(bias, "bias");
@@ -484,7 +493,7 @@ mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const mhc_bf1
                          float *dbias, void *ws, size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_layer_bwd");
-    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").iters(iters);
+    ck.count(T, "T").nstreams(n).channels(C).fits(T, n * C, "T*n*C").tma(T, n * C).iters(iters);
     ck.eps(eps_sk, "eps_sk").eps(eps_rms, "eps_rms");
     ck.ptr(W, "W").ptr(alpha3, "alpha3").ptr(b, "b").opt(bias, "bias").ptr(dW, "dW");
     ck.ptr(dalpha3, "dalpha3").ptr(db, "db").opt(dbias, "dbias");
@@ -644,7 +653,7 @@ mhc_status mhc_proj_rms_partial_fwd(const mhc_bf16 *x_shard, const float *W_shar
                                     size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_proj_rms_partial_fwd");
-    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs");
+    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs").tma(T, n * Cs);
     if (ck.st || T == 0) return ck.st;
     ck.ptr(x_shard, "x_shard").ptr(W_shard, "W_shard").ptr(u_part, "u_part").ptr(s_part, "s_part");
     ck.ws(ws, ws_bytes, mhc::proj_fwd_ws_bytes(T, n, Cs)).device();
@@ -703,7 +712,7 @@ mhc_status mhc_proj_rms_partial_bwd(const mhc_bf16 *x_shard, const float *W_shar
                                     size_t ws_bytes, mhc_stream_t stream)
 {
     Check ck("mhc_proj_rms_partial_bwd");
-    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs");
+    ck.count(T, "T").nstreams(n).channels(Cs, "Cs").fits(T, n * Cs, "T*n*Cs").tma(T, n * Cs);
     ck.ptr(dW_shard, "dW_shard");
     if (ck.st) return ck.st;
     if (T == 0) {

@@ -124,6 +124,13 @@ def test_next_ops_validation_without_gpu(L):
               A, A, A, A, None, None, A, 1 << 20, None) == 2
     assert pp(A, A, None, A, A, None, A, A, 16, 4, 64, 20, 1e-6, 1e-6,
               A, A, A, A, None, None, A, 1 << 20, None) == 1
+    # the tensor-core ops address rows and k = i*C + c with 32-bit TMA
+    # coordinates: T or n*C of 2^31 is refused on the host
+    pf = L.mhc_proj_rms_compute_h_fwd
+    assert pf(A, A, A, A, 1 << 31, 4, 8, 20, 1e-6, 1e-6, A, A, A, None, None, A, 1 << 20,
+              None) == 2
+    assert pf(A, A, A, A, 1, 8, 1 << 28, 20, 1e-6, 1e-6, A, A, A, None, None, A, 1 << 20,
+              None) == 2
     # the fault-path self-test takes 1 <= wait_us <= 1e6
     st = L.mhc_selftest_wait_timeout
     assert st(0, None) == 2 and st(2000000, None) == 2
