@@ -37,10 +37,9 @@
 // from fp32 W (bf16 hi/lo split, swizzled for the MMA); for n = 4 they also
 // copy each tile's per-token inputs (H_res, H_pre, coef) into shared memory
 // one tile ahead.  An unsplit pass writes dW and dbias directly.
-#include <cudaTypedefs.h>
-
 #include "launch.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace mhc {
 
@@ -566,34 +565,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_bwd()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-static bool map2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
-                  uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn_bwd();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int bwd_tc_du_cols(int n) { return n == 4 ? BwdTc<4>::DU_COLS : BwdTc<8>::DU_COLS; }
 
 int bwd_tc_splits(int64_t T, int n, int64_t C)
@@ -615,15 +586,15 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
     const int64_t T = args.T, C = args.C, K = int64_t(N) * C;
     CUtensorMap tmx, tmdu, tmg, tmy;
     const CUtensorMapSwizzle xsw = N == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
-    if (!map2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
-        !map2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
+    if (!tmap_bf16_2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
+        !tmap_bf16_2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
                CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     tmg = tmx;
     tmy = tmx;
     if (LAYER && P::STAGE_G) {
-        if (!map2d(&tmg, args.dout, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
-            !map2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
+        if (!tmap_bf16_2d(&tmg, args.dout, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
+            !tmap_bf16_2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_bwd_tc<N, LAYER>), P::SMEM);

@@ -23,10 +23,9 @@
 //         outputs; finally TMEM -> partials
 // A stage is free again when its MMAs have completed and the store has read
 // it.  Channels past C and rows past T load as zeros and are not stored.
-#include <cudaTypedefs.h>
-
 #include "launch.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace mhc {
 
@@ -301,33 +300,12 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_pp()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // bf16 tensor of `rank` dims (innermost first) in the stage's swizzle
-static bool map_bf16(CUtensorMap *m, const void *base, int rank, const cuuint64_t *dims,
-                     const cuuint64_t *strides_bytes, const cuuint32_t *box)
+static bool map_bf16(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+                     const uint64_t *strides_bytes, const uint32_t *box)
 {
-    const CUtensorMapSwizzle sw =
-        PostProj::BC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    auto fn = encode_fn_pp();
-    if (!fn) return false;
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cuuint32_t(rank), const_cast<void *>(base),
-              dims, strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return tmap_bf16(m, base, rank, dims, strides_bytes, box,
+                     PostProj::BC == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Channel-block splits: about one CTA per SM (the CTA fills most of shared
@@ -382,22 +360,22 @@ cudaError_t launch_post_proj_fwd(const bf16 *res, const bf16 *f, const bf16 *bia
     const uint64_t uC = uint64_t(C), uT = uint64_t(T);
     CUtensorMap tmx, tmf, tmw, tmo;
     {
-        const cuuint64_t dims[3] = {uC, cuuint64_t(n), uT};
-        const cuuint64_t strides[2] = {uC * 2, uC * 2 * n};
-        const cuuint32_t box[3] = {P::BC, 1, P::BM};
+        const uint64_t dims[3] = {uC, uint64_t(n), uT};
+        const uint64_t strides[2] = {uC * 2, uC * 2 * n};
+        const uint32_t box[3] = {P::BC, 1, P::BM};
         if (!map_bf16(&tmx, res, 3, dims, strides, box) || !map_bf16(&tmo, out, 3, dims, strides, box))
             return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[2] = {uC, uT};
-        const cuuint64_t strides[1] = {uC * 2};
-        const cuuint32_t box[2] = {P::BC, P::BM};
+        const uint64_t dims[2] = {uC, uT};
+        const uint64_t strides[1] = {uC * 2};
+        const uint32_t box[2] = {P::BC, P::BM};
         if (!map_bf16(&tmf, f, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[2] = {uint64_t(K), uint64_t(P::NB)};
-        const cuuint64_t strides[1] = {uint64_t(K) * 2};
-        const cuuint32_t box[2] = {P::BC, P::NB};
+        const uint64_t dims[2] = {uint64_t(K), uint64_t(P::NB)};
+        const uint64_t strides[1] = {uint64_t(K) * 2};
+        const uint32_t box[2] = {P::BC, P::NB};
         if (!map_bf16(&tmw, Whl, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     e = set_smem_limit(reinterpret_cast<const void *>(k_post_proj_tc<PostProj>), P::SMEM);

@@ -16,10 +16,9 @@
 //   warps 2..5  sum of squares of their token rows from the same smem tiles
 //               while the MMAs run; then the epilogue (TMEM -> partials)
 // Every wait is bounded; a timeout reports a fault code and the CTA unwinds.
-#include <cudaTypedefs.h>
-
 #include "launch.h"
 #include "tc.cuh"
+#include "tmap.h"
 
 namespace mhc {
 
@@ -241,35 +240,6 @@ __global__ void __launch_bounds__(192, P::MINB)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
-{
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
-// 2D bf16 tensor [rows][cols] (row pitch cols*2 bytes), box [box_rows][box_cols].
-static bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle sw)
-{
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Batch-invariant mode: the K splits depend on K alone (fixed 4096-wide
 // splits), so a token's u and s, and everything computed from them, do not
 // depend on how many tokens share the call.  Otherwise the split count is
@@ -320,9 +290,9 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
         launch_k(k_w_split<N>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
     }
     CUtensorMap tmx, tmw;
-    if (!make_map_bf16(&tmx, x, uint64_t(T), uint64_t(K), P::BM, P::BK,
+    if (!tmap_bf16_2d(&tmx, x, uint64_t(T), uint64_t(K), P::BM, P::BK,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_bf16(&tmw, Whl, uint64_t(P::NB), uint64_t(K), P::NB, P::BK,
+        !tmap_bf16_2d(&tmw, Whl, uint64_t(P::NB), uint64_t(K), P::NB, P::BK,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_proj_tc<N, P>), P::SMEM);
