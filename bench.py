@@ -432,6 +432,22 @@ def run_ours(args, rank, world):
     lms = ev0.elapsed_time(ev1) / args.steps
     lms = max_over_ranks(lms, world, dev)
 
+    # ---- the layer forward alone ----
+    def fwd_step():
+        M.mhc_layer_fwd(d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"], ITERS, EPS_SK,
+                        EPS_RMS, o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"],
+                        o["out"], wsf)
+
+    for _ in range(3):
+        fwd_step()
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        fwd_step()
+    ev1.record(stream)
+    barrier()
+    fms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
+
     # ---- the same step captured once into a CUDA graph and replayed ----
     graph = None
     if not args.no_graph:
@@ -590,6 +606,12 @@ def run_ours(args, rank, world):
                        "frac_of_nominal_8tbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3)
                                                      / 1e9 / NOMINAL_HBM_GBS, 4),
                        "what": "mhc_layer_fwd + mhc_layer_bwd only, timed separately (same inputs)"},
+        "forward_only": {"ms_per_step": round(fms, 4), "tokens_per_s": job_tokens_per_s(T, world, fms),
+                         "model_bytes_per_step": int(mb["layer_fwd"]),
+                         "achieved_gbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9, 1),
+                         "frac_of_nominal_8tbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9
+                                                       / NOMINAL_HBM_GBS, 4),
+                         "what": "mhc_layer_fwd only, timed separately (same inputs)"},
         "roofline": roof,
         "kernels": {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
                         "share": round(v[1] / (ms_prof * args.steps), 4)} for k, v in
