@@ -432,6 +432,20 @@ def run_ours(args, rank, world):
     lms = ev0.elapsed_time(ev1) / args.steps
     lms = max_over_ranks(lms, world, dev)
 
+    # ---- per-step times: the same steps with an event after each ----
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step()
+        evs[i + 1].record(stream)
+    barrier()
+    per = sorted(evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps))
+    per_step = {"median_ms": round(max_over_ranks(per[len(per) // 2], world, dev), 4),
+                "min_ms": round(max_over_ranks(per[0], world, dev), 4),
+                "max_ms": round(max_over_ranks(per[-1], world, dev), 4),
+                "what": "the bench step timed one by one (an event after each), median over the "
+                        "K steps"}
+
     # ---- the layer forward alone ----
     def fwd_step():
         M.mhc_layer_fwd(d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"], ITERS, EPS_SK,
@@ -606,6 +620,7 @@ def run_ours(args, rank, world):
                        "frac_of_nominal_8tbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3)
                                                      / 1e9 / NOMINAL_HBM_GBS, 4),
                        "what": "mhc_layer_fwd + mhc_layer_bwd only, timed separately (same inputs)"},
+        "per_step": per_step,
         "forward_only": {"ms_per_step": round(fms, 4), "tokens_per_s": job_tokens_per_s(T, world, fms),
                          "model_bytes_per_step": int(mb["layer_fwd"]),
                          "achieved_gbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9, 1),
