@@ -228,6 +228,28 @@ def test_post_bda_identity_is_exact_copy(M):
     assert torch.equal(out.view(torch.int16), x.view(torch.int16))
 
 
+@pytest.mark.parametrize("n", [4, 8])
+def test_post_bda_permutation_is_exact_permuted_copy(M, n):
+    """H_res a per-token permutation (stream j -> output stream p[j]) and
+    H_post = 0: the output is the residual with its streams permuted, bit for
+    bit.  Unlike the identity, this tells H_res from its transpose."""
+    T, C = 37, 72
+    inp = mi.layer_inputs(T, n, C, 11)
+    rng = np.random.Generator(np.random.PCG64(12))
+    perms = np.stack([rng.permutation(n) for _ in range(T)])
+    Hres = np.zeros((T, n, n), np.float32)
+    Hres[np.arange(T)[:, None], np.arange(n)[None, :], perms] = 1.0
+    out = torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda")
+    M.mhc_h_post_bda_fwd(dev_bf16(inp["x"]), dev_bf16(inp["f"]), dev_bf16(inp["bias"]),
+                         dev_f32(Hres), torch.zeros(T, n, device="cuda"), out)
+    torch.cuda.synchronize()
+    want = np.empty_like(inp["x"])
+    for t in range(T):
+        want[t, perms[t]] = inp["x"][t]
+    got = out.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
 def test_aggregate_one_hot_is_exact_select(M):
     T, n, C = 31, 8, 40
     inp = mi.layer_inputs(T, n, C, 10)
@@ -318,6 +340,99 @@ def test_layer(M, orc, T, n, C, seed, stress):
     ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
     ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
     check_layer(o, ref_f, ref_b)
+
+
+@pytest.mark.parametrize("n,C", [(4, 264), (8, 136)])
+def test_layer_zero_rows(M, orc, n, C):
+    """Tokens whose residual rows are all zero (the first token, one inside a
+    128-token tile, the last): r = 1/eps_rms and z = b in the forward, the RMS
+    term of the backward is zero, and the projection term is alpha r dz W
+    (large, finite); everything else as usual."""
+    T = 200
+    inp = mi.layer_inputs(T, n, C, 21)
+    for t in (0, 77, T - 1):
+        inp["x"][t] = 0
+    o = run_layer(M, inp, T, n, C)
+    ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
+    for k in ("H_pre", "H_post", "H_res"):
+        err_h(o[k], ref_f[k])
+    for k in ("y", "out"):
+        err_bf16(o[k], ref_f[k])
+    err_bf16(o["df"], ref_b["df"])
+    for k in ("dW", "dalpha", "db", "dbias"):
+        err_grad(o[k], ref_b[k])
+    # dx: at a zero row r = 1/eps, so du = alpha r dz is ~1e4 and the terms
+    # du[o] W[k][o] of dx cancel to values ~1e-1.  The kernel carries du and W
+    # as bf16 hi + lo (each to ~2^-17 relative; the dropped lo*lo term is
+    # ~2^-18), so its error is bounded by ~2^-16 * sum_o |du[o] W[k][o]|; the
+    # test allows 2^-15 times that sum on top of the bf16 tolerance (for the
+    # other rows the sum is ~1 and the term negligible).
+    K = n * C
+    xs = mi.bf16_bits_to_f32(inp["x"]).astype(np.float64).reshape(T, K)
+    du = orc.compute_h_bwd_from_sums(ref_b["dH_pre"], ref_b["dH_post"], ref_b["dH_res"],
+                                     ref_f["u"], np.sum(xs * xs, axis=1), K, inp["alpha"],
+                                     inp["b"], n, ITERS, EPS_SK, EPS_RMS)["du"]
+    scale = (np.abs(du) @ np.abs(inp["W"].astype(np.float64)).T).reshape(T, n, C)
+    g = host(o["dx"])
+    r = ref_b["dx"]
+    tol = mi.SPEC["tolerances"]
+    excess = np.abs(g - r) - (tol["bf16_abs"] + tol["bf16_rel"] * np.abs(r) + 2.0 ** -15 * scale)
+    assert np.all(np.isfinite(g)) and float(np.max(excess)) <= 0.0, \
+        f"dx beyond the derived bound at {np.unravel_index(np.argmax(excess), r.shape)}"
+    assert float(np.max(scale[0])) > 1e3  # the zero rows do carry the large terms
+
+
+@pytest.mark.parametrize("n,C", [(4, 256), (8, 64)])
+def test_layer_alpha_zero(M, orc, n, C):
+    """alpha = 0: H no longer depends on x, so du = 0, the projection adds
+    nothing to dx and dW is exactly zero; dalpha (sum of dz r u) is not."""
+    T = 129
+    inp = mi.layer_inputs(T, n, C, 22, alpha=0.0, b_std=1.0)
+    o = run_layer(M, inp, T, n, C)
+    ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
+    check_layer(o, ref_f, ref_b)
+    assert float(o["dW"].abs().max()) == 0.0
+    assert float(o["dalpha"].abs().max()) > 0.0
+
+
+@pytest.mark.parametrize("n,C", [(4, 264), (8, 64)])
+def test_layer_without_bias(M, orc, n, C):
+    """bias = NULL (zero) and dbias = NULL: the layer runs without them."""
+    T = 67
+    inp = mi.layer_inputs(T, n, C, 23)
+    inp["bias"] = None
+    O = n * n + 2 * n
+    t = {k: (dev_bf16(v) if v.dtype == np.uint16 else dev_f32(v)) for k, v in inp.items()
+         if v is not None}
+    o = {"H_pre": torch.empty(T, n, device="cuda"), "H_post": torch.empty(T, n, device="cuda"),
+         "H_res": torch.empty(T, n, n, device="cuda"), "u": torch.empty(T, O, device="cuda"),
+         "r": torch.empty(T, device="cuda"),
+         "y": torch.empty(T, C, dtype=torch.bfloat16, device="cuda"),
+         "out": torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda"),
+         "dx": torch.empty(T, n, C, dtype=torch.bfloat16, device="cuda"),
+         "df": torch.empty(T, C, dtype=torch.bfloat16, device="cuda"),
+         "dW": torch.empty(n * C, O, device="cuda"), "dalpha": torch.empty(3, device="cuda"),
+         "db": torch.empty(O, device="cuda")}
+    M.mhc_layer_fwd(t["x"], t["W"], t["alpha"], t["b"], t["f"], None, ITERS, EPS_SK, EPS_RMS,
+                    o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"], o["out"],
+                    M.workspace(M.OP_LAYER_FWD, T, n, C))
+    M.mhc_layer_bwd(t["dout"], t["dy"], t["x"], t["W"], t["alpha"], t["b"], t["f"], None,
+                    o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], ITERS, EPS_SK, EPS_RMS,
+                    o["dx"], o["df"], o["dW"], o["dalpha"], o["db"], None,
+                    M.workspace(M.OP_LAYER_BWD, T, n, C))
+    torch.cuda.synchronize()
+    ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
+    for k in ("H_pre", "H_post", "H_res"):
+        err_h(o[k], ref_f[k])
+    for k in ("y", "out"):
+        err_bf16(o[k], ref_f[k])
+    for k in ("dx", "df"):
+        err_bf16(o[k], ref_b[k])
+    for k in ("dW", "dalpha", "db"):
+        err_grad(o[k], ref_b[k])
 
 
 def test_layer_is_deterministic(M):
