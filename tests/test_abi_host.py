@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(L):
     assert not missing, missing
 
 
+def test_header_compiles_as_c_and_cpp():
+    """include/mhc.h is a plain C header (C99) that C++ can include too."""
+    import shutil
+    import subprocess
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = os.path.join(root, "include", "mhc.h")
+    for cc, lang, std in (("gcc", "c", "-std=c99"), ("g++", "c++", "-std=c++11")):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} missing")
+        r = subprocess.run([cc, std, "-Wall", "-Wextra", "-Werror", "-pedantic", "-fsyntax-only",
+                            "-x", lang, hdr], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
+
+
 def test_status_strings_and_version(L):
     for s in range(10):
         assert L.mhc_status_string(s)
