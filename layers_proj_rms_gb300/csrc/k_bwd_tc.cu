@@ -19,24 +19,31 @@
 //   MMA 1 (dx_gemm): D2[t][k] = du_hi.W_hi + du_lo.W_hi + du_hi.W_lo (the
 //          dropped du_lo.W_lo is ~2^-18 relative): M = 128 tokens, N = 128 k,
 //          K = 2*O against Wd = [W_hi | W_hi], then K = O against W_lo
+//          (n = 8: the du_lo steps reuse the W_hi steps' operand)
 //   MMA 2 (dW):      D1[k][o'] += sum_t x[t][k] du_hl[t][o'], M = 128 k,
-//          N = 2*O, K = tokens; hi and lo columns of D1 are summed at the end.
+//          N = 2*O (n = 8: 128 + 32, one MMA per du_hl swizzle box),
+//          K = tokens; hi and lo columns of D1 are summed at the end.
 //          Both operands are read MN-major straight from the TMA tiles.
 //   MMA 3 (n = 4, dbias): D3[k][o'] += sum_t dout[t][k] du_hl[t][o'] with
 //          H_post hi | lo stored in du_hl columns [2O, 2O+2n)
 //   epilogue: D2 + the elementwise terms -> dx (bf16).
 // D2 is double-buffered in TMEM so the next tile's MMAs overlap the
 // epilogue; D1 accumulates over the whole token range and is written as this
-// split's dW partial.  For n = 4 the producer also stages dout and dy through
-// shared memory (every DRAM access a whole 64-byte row); for n = 8 (16-channel
-// slices) the epilogue reads them from global memory.
+// split's dW partial.  Every input of a tile arrives by TMA ahead of its use:
+// n = 4, x, dout, dy and du_hl in a ring of two stages (every DRAM access a
+// whole 64-byte row), the per-token inputs copied by the epilogue with
+// cp.async one tile ahead; n = 8 (16-channel slices, a 40 KB W tile), x in a
+// ring of two stages and single buffers refilled a tile ahead: du_hl
+// (released by the MMAs), the per-token inputs H_res, H_pre, H_post and dout
+// and dy (released once the epilogue has read them).  Per-lane global loads
+// of these inputs (each warp load touching 32 token rows) cost 2.8x the
+// time at n = 8.
 // Warps: 0 TMA producer, 1 TMEM + MMA issue, 2.. epilogue: CW/8 warps per
 // TMEM lane quadrant, each thread one token row x one 8-channel chunk of
 // every stream (16 epilogue warps for n = 4, 8 for n = 8).  Before their
 // first tile the epilogue warps build the slice's W tile in shared memory
-// from fp32 W (bf16 hi/lo split, swizzled for the MMA); for n = 4 they also
-// copy each tile's per-token inputs (H_res, H_pre, coef) into shared memory
-// one tile ahead.  An unsplit pass writes dW and dbias directly.
+// from fp32 W (bf16 hi/lo split, swizzled for the MMA).  An unsplit pass
+// writes dW and dbias directly.
 #include "launch.h"
 #include "tc.cuh"
 #include "tmap.h"
@@ -54,40 +61,67 @@ struct BwdTc {
     static constexpr uint32_t XSWZ = N == 4 ? tc::kSwz64 : tc::kSwz32;
     static constexpr int XBOX = TT * XROW;      // bytes of one stream box
     static constexpr int X_BYTES = N * XBOX;    // 32 KB
-    static constexpr bool STAGE_G = N == 4;     // dout and dy through shared memory
+    // n = 4: one ring of stages holds x, dout, dy and du_hl of a tile.
+    // n = 8: the ring holds x only; du_hl has one buffer that the MMAs release
+    // as soon as they complete, and dout and dy one buffer (G) that the
+    // epilogue releases once it has read them: both are refilled a tile ahead
+    // in the shared memory that a second du_hl stage would take.
+    static constexpr bool STAGE_G = N == 4;     // dout and dy in the ring
     static constexpr int G_BYTES = STAGE_G ? N * XBOX : 0;
     static constexpr int Y_BYTES = STAGE_G ? XBOX : 0;
-    static constexpr int DU_ATOMS = N == 4 ? 1 : 3;
-    static constexpr int DU_COLS = 64 * DU_ATOMS;       // hi [0,O) | lo [O,2O) | zeros
+    // du_hl tile: n = 4, one 128-byte-swizzled atom of 64 columns (hi [0,24) |
+    // lo [24,48) | H_post hi, lo | zeros); n = 8, two such atoms (hi [0,80) |
+    // lo [80,128)) and a 64-byte-swizzled tail box of columns [128,160)
+    static constexpr int DU_ATOMS = N == 4 ? 1 : 2;
+    static constexpr int DU_COLS = N == 4 ? 64 : 192;   // columns of du_hl in memory
     static constexpr int DU_ATOM_BYTES = TT * 128;
-    static constexpr int DU_BYTES = DU_ATOMS * DU_ATOM_BYTES;
+    static constexpr int DU_TAIL = DU_ATOMS * DU_ATOM_BYTES;
+    static constexpr int DU_TAIL_BYTES = N == 4 ? 0 : TT * 64;
+    static constexpr int DU_BYTES = DU_TAIL + DU_TAIL_BYTES;   // 16 KB / 40 KB
     static constexpr int G_OFF = X_BYTES, Y_OFF = G_OFF + G_BYTES, DU_OFF = Y_OFF + Y_BYTES;
-    static constexpr int STAGE = DU_OFF + DU_BYTES;     // 88 KB / 80 KB
+    static constexpr int STAGE = N == 4 ? DU_OFF + DU_BYTES : X_BYTES;   // 88 KB / 32 KB
     static constexpr int STAGES = 2;
-    // Wd = [W_hi | W_hi | W_lo | 0] in bf16, planes of 64 columns (128-byte
-    // rows, 128-byte swizzle); the W_lo block is padded to whole K steps.
+    // B operand of the dx GEMM.  n = 4: Wd = [W_hi | W_hi | W_lo | 0] in bf16,
+    // planes of 64 columns (128-byte rows, 128-byte swizzle).  n = 8: a W_hi
+    // plane (columns [0,64)), a W_lo plane, and a 64-byte-swizzled tail of
+    // [W_hi [64,80) | W_lo [64,80)]; du_lo steps reuse the W_hi steps.
     static constexpr int NW = 2 * O;                    // 48 / 160
     static constexpr int KSTEP_A = NW / 16;             // du_hl . [W_hi | W_hi]: 3 / 10
     static constexpr int KSTEP_B = (O + 15) / 16;       // du_hi . W_lo: 2 / 5
-    static constexpr int W_COLS = NW + 16 * KSTEP_B;    // 80 / 240
-    static constexpr int W_PLANES = (W_COLS + 63) / 64; // 2 / 4
+    static constexpr int W_COLS = NW + 16 * KSTEP_B;    // 80 (n = 4)
+    static constexpr int W_PLANES = N == 4 ? (W_COLS + 63) / 64 : 2;
     static constexpr int W_PLANE_BYTES = 128 * 128;
-    static constexpr int W_BYTES = W_PLANES * W_PLANE_BYTES;
+    static constexpr int W_TAIL = W_PLANES * W_PLANE_BYTES;
+    static constexpr int W_BYTES = W_TAIL + (N == 4 ? 0 : 128 * 64);   // 32 KB / 40 KB
+    static constexpr int DU1_OFF = STAGES * STAGE;      // n = 8: the du_hl buffer
+    static constexpr int DU1_BYTES = N == 4 ? 0 : DU_BYTES;
+    static constexpr int W_OFF = DU1_OFF + DU1_BYTES;
     static constexpr int D2_COL = 0, D1_COL = 256;      // D2 buffers at 0 and 128
     // n = 4: dbias on the tensor cores, D3[k][o'] += sum_t dout[t][k] du_hl[t][o'];
     // columns 2O+i (hi) and 2O+N+i (lo) of du_hl hold H_post[t][i]
     static constexpr int D3_COL = 320, D3_N = 64;
     static constexpr int TMEM_COLS = 512;
-    // n = 4: the epilogue stages the next tile's per-token inputs (H_res row,
-    // H_pre row: 20 floats per token; coef) in shared memory with cp.async
+    // Per-token inputs of a tile in shared memory, one tile ahead.  n = 4:
+    // the epilogue copies them with cp.async (H_res row, H_pre row: 20 floats
+    // per token; coef).  n = 8 (layer): the producer loads them by TMA, H_res
+    // as two 128-byte-swizzled boxes of 32 floats per token, H_pre and H_post
+    // as 32-byte-swizzled boxes of 8 floats (conflict-free row reads).
     static constexpr bool STAGE_P = N == 4;
+    static constexpr bool TMA_P = N == 8;
     static constexpr int PAR_ROW = 20 * 4;
-    static constexpr int PAR_OFF = STAGES * STAGE + W_BYTES;
-    static constexpr int PAR_BYTES = STAGE_P ? TT * PAR_ROW + TT * 4 : 0;
-    static constexpr int SMEM = STAGES * STAGE + W_BYTES + PAR_BYTES + 1024;
+    static constexpr int PAR_OFF = W_OFF + W_BYTES;
+    static constexpr int PH_PRE = 2 * TT * 128, PH_POST = PH_PRE + TT * 32;
+    static constexpr int PAR_BYTES =
+        STAGE_P ? TT * PAR_ROW + TT * 4 : (TMA_P ? PH_POST + TT * 32 : 0);   // 10.5 KB / 40 KB
+    // n = 8 (layer): the G buffer, dout boxes of the n streams then the dy box
+    static constexpr int G1_OFF = PAR_OFF + PAR_BYTES;
+    static constexpr int G1_BYTES = N == 4 ? 0 : (N + 1) * XBOX;       // 36 KB
+    static constexpr int SMEM = G1_OFF + G1_BYTES + 1024;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
-    static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0, "alignment");
-    static_assert(SMEM <= 232448, "shared memory");
+    static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0 && PAR_OFF % 1024 == 0 &&
+                      W_OFF % 1024 == 0 && (N == 4 || G1_OFF % 1024 == 0),
+                  "alignment");
+    static_assert(SMEM + 512 <= 232448, "shared memory");
 };
 
 // Column sums over the 32 lanes of a warp: on entry every lane holds COLS
@@ -138,22 +172,27 @@ template <int N, bool LAYER>
 __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     k_bwd_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmdu,
              const __grid_constant__ CUtensorMap tmg,
-             const __grid_constant__ CUtensorMap tmy, const BwdTcArgs a)
+             const __grid_constant__ CUtensorMap tmy, const __grid_constant__ CUtensorMap tmdu2,
+             const __grid_constant__ CUtensorMap tmhres, const __grid_constant__ CUtensorMap tmhpre,
+             const __grid_constant__ CUtensorMap tmhpost, const BwdTcArgs a)
 {
     pdl_wait();
     using P = BwdTc<N>;
     constexpr int O = P::O, CW = P::CW;
     constexpr bool SG = LAYER && P::STAGE_G;
+    constexpr bool TP = LAYER && P::TMA_P;    // per-token inputs by TMA (n = 8)
+    constexpr bool G1 = LAYER && N == 8;      // dout and dy in the G buffer
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[P::STAGES], empty[P::STAGES];
-    __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full;
+    __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full, pfull, pempty, dufull, duempty,
+        gfull, gempty;
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float bias_red[4][CW];
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *wtile = smem + P::STAGES * P::STAGE;
+    uint8_t *wtile = smem + P::W_OFF;
     volatile int *abort_v = &abort_flag;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,7 +201,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     const int split = blockIdx.y;
     const int tile0 = split * a.tiles_per_split;
     const int ntiles = min(a.tiles_total, tile0 + a.tiles_per_split) - tile0;
-    constexpr uint32_t stage_tx = SG ? P::STAGE : P::X_BYTES + P::DU_BYTES;
+    constexpr uint32_t stage_tx = SG || N == 8 ? P::STAGE : P::X_BYTES + P::DU_BYTES;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
@@ -175,6 +214,12 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             tc::mbar_init(&d2empty[b], P::EPI_WARPS);
         }
         tc::mbar_init(&d1full, 1);
+        tc::mbar_init(&pfull, 1);
+        tc::mbar_init(&pempty, P::EPI_WARPS);
+        tc::mbar_init(&dufull, 1);
+        tc::mbar_init(&duempty, 1);
+        tc::mbar_init(&gfull, 1);
+        tc::mbar_init(&gempty, P::EPI_WARPS);
         abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -193,7 +238,21 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::tma_prefetch_desc(&tmg);
                 tc::tma_prefetch_desc(&tmy);
             }
-            int issued = 0;
+            if (N == 8) tc::tma_prefetch_desc(&tmdu2);
+            if (TP) {
+                tc::tma_prefetch_desc(&tmhres);
+                tc::tma_prefetch_desc(&tmhpre);
+                tc::tma_prefetch_desc(&tmhpost);
+            }
+            if (G1) {
+                tc::tma_prefetch_desc(&tmg);
+                tc::tma_prefetch_desc(&tmy);
+            }
+            uint8_t *par = smem + P::PAR_OFF;
+            uint8_t *du1 = smem + P::DU1_OFF;
+            uint8_t *g1 = smem + P::G1_OFF;
+            // issued: ring stages; n1: tiles whose single-buffer loads were issued
+            int issued = 0, n1 = 0;
             for (int i = 0; i < ntiles && !*abort_v; ++i) {
                 const int s = i % P::STAGES;
                 if (i >= P::STAGES &&
@@ -207,9 +266,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::mbar_arrive_expect_tx(&full[s], stage_tx);
                 for (int j = 0; j < N; ++j)
                     tc::tma_load_2d(st + j * P::XBOX, &tmx, int(int64_t(j) * C + c0), t0, &full[s]);
-                for (int u = 0; u < P::DU_ATOMS; ++u)
-                    tc::tma_load_2d(st + P::DU_OFF + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0,
-                                    &full[s]);
+                if (N == 4)
+                    tc::tma_load_2d(st + P::DU_OFF, &tmdu, 0, t0, &full[s]);
                 if (SG) {
                     for (int j = 0; j < N; ++j)
                         tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
@@ -217,10 +275,49 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &full[s]);
                 }
                 issued = i + 1;
+                if (N == 8) {
+                    // single buffers, each refilled once the previous tile is
+                    // done with it: du_hl after the tile's MMAs, the per-token
+                    // inputs and dout/dy after the epilogue has read them
+                    if (i >= 1 && (!tc::mbar_wait(&duempty, (i - 1) & 1, a.fault,
+                                                  tc::kFaultTimeoutEmpty) ||
+                                   (TP && !tc::mbar_wait(&pempty, (i - 1) & 1, a.fault,
+                                                         tc::kFaultTimeoutEmpty)) ||
+                                   (G1 && !tc::mbar_wait(&gempty, (i - 1) & 1, a.fault,
+                                                         tc::kFaultTimeoutEmpty)))) {
+                        *abort_v = 1;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&dufull, P::DU_BYTES);
+                    for (int u = 0; u < P::DU_ATOMS; ++u)
+                        tc::tma_load_2d(du1 + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0, &dufull);
+                    tc::tma_load_2d(du1 + P::DU_TAIL, &tmdu2, 128, t0, &dufull);
+                    if (TP) {
+                        tc::mbar_arrive_expect_tx(&pfull, P::PAR_BYTES);
+                        tc::tma_load_2d(par, &tmhres, 0, t0, &pfull);
+                        tc::tma_load_2d(par + P::TT * 128, &tmhres, 32, t0, &pfull);
+                        tc::tma_load_2d(par + P::PH_PRE, &tmhpre, 0, t0, &pfull);
+                        tc::tma_load_2d(par + P::PH_POST, &tmhpost, 0, t0, &pfull);
+                    }
+                    if (G1) {
+                        tc::mbar_arrive_expect_tx(&gfull, P::G1_BYTES);
+                        for (int j = 0; j < N; ++j)
+                            tc::tma_load_2d(g1 + j * P::XBOX, &tmg, int(int64_t(j) * C + c0), t0,
+                                            &gfull);
+                        tc::tma_load_2d(g1 + N * P::XBOX, &tmy, int(c0), t0, &gfull);
+                    }
+                    n1 = i + 1;
+                }
             }
+            // nothing may still be landing in shared memory when the CTA exits
             for (int i = max(0, issued - P::STAGES); i < issued; ++i)
                 tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
                               tc::kFaultTimeoutMisc);
+            if (n1 > 0) {
+                tc::mbar_wait(&dufull, (n1 - 1) & 1, a.fault, tc::kFaultTimeoutMisc);
+                if (TP) tc::mbar_wait(&pfull, (n1 - 1) & 1, a.fault, tc::kFaultTimeoutMisc);
+                if (G1) tc::mbar_wait(&gfull, (n1 - 1) & 1, a.fault, tc::kFaultTimeoutMisc);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
@@ -232,13 +329,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % P::STAGES, b = i & 1;
                 if (*abort_v ||
-                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) {
+                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
+                    (N == 8 && !tc::mbar_wait(&dufull, i & 1, a.fault, tc::kFaultTimeoutFull))) {
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
                 const uint32_t xs = tc::smem_u32(smem + s * P::STAGE);
-                const uint32_t dus = xs + P::DU_OFF;
+                const uint32_t dus = N == 4 ? xs + P::DU_OFF : tc::smem_u32(smem + P::DU1_OFF);
                 // dx accumulator b must have been drained by the epilogue (tile i-2)
                 if (i >= 2 &&
                     !tc::mbar_wait(&d2empty[b], ((i >> 1) - 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
@@ -250,13 +348,27 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < P::KSTEP_A + P::KSTEP_B; ++kk) {
                     const int acol = kk < P::KSTEP_A ? 16 * kk : 16 * (kk - P::KSTEP_A);
-                    const int bcol = 16 * kk;
-                    const uint64_t ad =
-                        tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES + (acol % 64) * 2, 16,
-                                      1024, tc::kSwz128);
-                    const uint64_t bd =
-                        tc::make_desc(wb + (bcol / 64) * P::W_PLANE_BYTES + (bcol % 64) * 2, 16,
-                                      1024, tc::kSwz128);
+                    uint64_t ad, bd;
+                    if (N == 4) {
+                        const int bcol = 16 * kk;
+                        ad = tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES + (acol % 64) * 2, 16,
+                                           1024, tc::kSwz128);
+                        bd = tc::make_desc(wb + (bcol / 64) * P::W_PLANE_BYTES + (bcol % 64) * 2, 16,
+                                           1024, tc::kSwz128);
+                    } else {
+                        // du columns [0,128) in the two atoms, [128,160) in the tail
+                        ad = acol < 128 ? tc::make_desc(dus + (acol / 64) * P::DU_ATOM_BYTES +
+                                                            (acol % 64) * 2,
+                                                        16, 1024, tc::kSwz128)
+                                        : tc::make_desc(dus + P::DU_TAIL + (acol - 128) * 2, 16,
+                                                        512, tc::kSwz64);
+                        // W step m of W_hi (kk < KSTEP_A) or W_lo
+                        const int lo = kk < P::KSTEP_A ? 0 : 1;
+                        const int m = kk < P::KSTEP_A ? kk % P::KSTEP_B : kk - P::KSTEP_A;
+                        bd = m < 4 ? tc::make_desc(wb + lo * P::W_PLANE_BYTES + m * 32, 16, 1024,
+                                                   tc::kSwz128)
+                                   : tc::make_desc(wb + P::W_TAIL + lo * 32, 16, 512, tc::kSwz64);
+                    }
                     tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&d2full[b]);
@@ -265,9 +377,22 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 for (int ks = 0; ks < P::TT / 16; ++ks) {
                     const uint64_t ad =
                         tc::make_desc(xs + ks * 16 * P::XROW, P::XBOX, 8 * P::XROW, P::XSWZ);
-                    const uint64_t bd =
-                        tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES, 1024, tc::kSwz128);
-                    tc::mma_bf16(tmem + P::D1_COL, ad, bd, idesc_dw, (i > 0 || ks > 0) ? 1u : 0u);
+                    const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+                    if (N == 4) {
+                        const uint64_t bd =
+                            tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES, 1024, tc::kSwz128);
+                        tc::mma_bf16(tmem + P::D1_COL, ad, bd, idesc_dw, acc);
+                    } else {
+                        // du columns [0,128) (N = 128) and the tail [128,160) (N = 32)
+                        constexpr uint32_t idesc_dw1 = tc::idesc_bf16_f32(128, 128, 1, 1);
+                        constexpr uint32_t idesc_dw2 = tc::idesc_bf16_f32(128, 32, 1, 1);
+                        const uint64_t bd1 =
+                            tc::make_desc(dus + ks * 16 * 128, P::DU_ATOM_BYTES, 1024, tc::kSwz128);
+                        const uint64_t bd2 = tc::make_desc(dus + P::DU_TAIL + ks * 16 * 64,
+                                                           P::DU_TAIL_BYTES, 512, tc::kSwz64);
+                        tc::mma_bf16(tmem + P::D1_COL, ad, bd1, idesc_dw1, acc);
+                        tc::mma_bf16(tmem + P::D1_COL + 128, ad, bd2, idesc_dw2, acc);
+                    }
                 }
                 if (SG) {
                     // dbias: dout^T [du_hl | H_post hi | H_post lo] over the tile
@@ -283,6 +408,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(&empty[s]);
+                if (N == 8) tc::mma_commit(&duempty);
             }
             if (!ok) *abort_v = 1;
             tc::mma_commit(&d1full);
@@ -291,31 +417,46 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        // The W tile of this slice, [W_hi | W_hi | W_lo | 0] per k row in
-        // 64-column planes, written in the 128-byte swizzled K-major layout
-        // of the MMA B operand (16-byte chunk q of row rr at rr*128 +
-        // ((q ^ (rr % 8)) * 16)); rows past C are zero.
-        for (int idx = threadIdx.x - 64; idx < P::W_PLANES * 128 * 8; idx += 32 * P::EPI_WARPS) {
-            const int p = idx >> 10, rr = (idx >> 3) & 127, qc = idx & 7;
-            const int col = p * 64 + qc * 8;
+        // The W tile of this slice in the swizzled K-major layout of the MMA B
+        // operand (16-byte chunk q of row rr at rr*128 + ((q ^ (rr % 8)) * 16)
+        // in a 128-byte plane, at rr*64 + ((q ^ ((rr / 2) % 4)) * 16) in the
+        // 64-byte tail); rows past C are zero.  n = 4: [W_hi | W_hi | W_lo | 0]
+        // in 64-column planes.  n = 8: W_hi [0,64), W_lo [0,64), and the tail
+        // [W_hi [64,80) | W_lo [64,80)].
+        constexpr int W_CHUNKS = P::W_PLANES * 128 * 8 + (N == 8 ? 128 * 4 : 0);
+        for (int idx = threadIdx.x - 64; idx < W_CHUNKS; idx += 32 * P::EPI_WARPS) {
+            int rr, col;
+            bool lo;
+            uint32_t dst;
+            if (idx < P::W_PLANES * 128 * 8) {
+                const int p = idx >> 10, qc = idx & 7;
+                rr = (idx >> 3) & 127;
+                col = N == 4 ? p * 64 + qc * 8 : qc * 8;
+                lo = N == 4 ? col >= 2 * O : p == 1;
+                dst = tc::smem_u32(wtile + p * P::W_PLANE_BYTES + rr * 128 + ((qc ^ (rr & 7)) << 4));
+            } else {
+                const int j = idx - P::W_PLANES * 128 * 8, qc = j & 3;
+                rr = j >> 2;
+                col = 64 + (qc & 1) * 8;
+                lo = qc >= 2;
+                dst = tc::smem_u32(wtile + P::W_TAIL + rr * 64 + ((qc ^ ((rr >> 1) & 3)) << 4));
+            }
             const int64_t cw = c0 + rr % CW;
             float w[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            if (col < 3 * O && cw < C) {
+            if ((N == 8 || col < 3 * O) && cw < C) {
                 const float4 *src = reinterpret_cast<const float4 *>(
                     a.W + (int64_t(rr / CW) * C + cw) * O + col % O);
                 const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
                 w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
                 w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
-                if (col >= 2 * O)
+                if (lo)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         w[e] -= __bfloat162float(__float2bfloat16_rn(w[e]));
             }
             const uint4 v = pack8(w);
-            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                             tc::smem_u32(wtile + p * P::W_PLANE_BYTES + rr * 128 +
-                                          ((qc ^ (rr & 7)) << 4))),
-                         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+            asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(v.x), "r"(v.y),
+                         "r"(v.z), "r"(v.w)
                          : "memory");
         }
         tc::fence_proxy_async_smem();
@@ -385,27 +526,74 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::named_bar_sync(1 + q, 128);
                 if (i + 1 < ntiles) stage_params(tile0 + i + 1);
                 if (!ok) continue;
-            } else if (valid) {
-                coef = __ldg(a.coef + t);
-                if (LAYER) {
+            } else {
+                if (valid) {
+                    coef = __ldg(a.coef + t);
+                    if (LAYER && !TP) {
 #pragma unroll
-                    for (int j = 0; j < N; ++j) {
-                        hpre[j] = __ldg(a.Hpre + t * N + j);
-                        hpost[j] = __ldg(a.Hpost + t * N + j);
+                        for (int j = 0; j < N; ++j) {
+                            hpre[j] = __ldg(a.Hpre + t * N + j);
+                            hpost[j] = __ldg(a.Hpost + t * N + j);
+                        }
+#pragma unroll
+                        for (int e = 0; e < N * N; e += 4) {
+                            const float4 v =
+                                __ldg(reinterpret_cast<const float4 *>(a.Hres + t * N * N + e));
+                            hres[e] = v.x;
+                            hres[e + 1] = v.y;
+                            hres[e + 2] = v.z;
+                            hres[e + 3] = v.w;
+                        }
+                    }
+                }
+                if (TP) {
+                    // this tile's H_res, H_pre and H_post rows from the TMA
+                    // boxes (rows past T read as zero), then the buffer goes
+                    // back to the producer for the next tile
+                    if (*abort_v || !tc::mbar_wait(&pfull, i & 1, a.fault, tc::kFaultTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t pb = tc::smem_u32(smem + P::PAR_OFF);
+#pragma unroll
+                    for (int e4 = 0; e4 < N * N / 4; ++e4) {
+                        const uint4 v = lds128(pb + (e4 >> 3) * (P::TT * 128) + r * 128 +
+                                               (((e4 & 7) ^ (r & 7)) << 4));
+                        hres[4 * e4] = __uint_as_float(v.x);
+                        hres[4 * e4 + 1] = __uint_as_float(v.y);
+                        hres[4 * e4 + 2] = __uint_as_float(v.z);
+                        hres[4 * e4 + 3] = __uint_as_float(v.w);
                     }
 #pragma unroll
-                    for (int e = 0; e < N * N; e += 4) {
-                        const float4 v = __ldg(reinterpret_cast<const float4 *>(a.Hres + t * N * N + e));
-                        hres[e] = v.x;
-                        hres[e + 1] = v.y;
-                        hres[e + 2] = v.z;
-                        hres[e + 3] = v.w;
+                    for (int c4 = 0; c4 < N / 4; ++c4) {
+                        const uint32_t off = r * 32 + ((c4 ^ ((r >> 2) & 1)) << 4);
+                        const uint4 vp = lds128(pb + P::PH_PRE + off);
+                        const uint4 vq = lds128(pb + P::PH_POST + off);
+                        hpre[4 * c4] = __uint_as_float(vp.x);
+                        hpre[4 * c4 + 1] = __uint_as_float(vp.y);
+                        hpre[4 * c4 + 2] = __uint_as_float(vp.z);
+                        hpre[4 * c4 + 3] = __uint_as_float(vp.w);
+                        hpost[4 * c4] = __uint_as_float(vq.x);
+                        hpost[4 * c4 + 1] = __uint_as_float(vq.y);
+                        hpost[4 * c4 + 2] = __uint_as_float(vq.z);
+                        hpost[4 * c4 + 3] = __uint_as_float(vq.w);
                     }
-                    if (!SG && cvalid) {
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&pempty);
+                }
+                if (G1) {
+                    // dout and dy of this tile (rows past T read as zero;
+                    // chunks past C are read but never stored)
+                    if (*abort_v || !tc::mbar_wait(&gfull, i & 1, a.fault, tc::kFaultTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint8_t *gb = smem + P::G1_OFF;
 #pragma unroll
-                        for (int ii = 0; ii < N; ++ii) g[ii] = ld_stream(a.dout + ((t * N + ii) * C + cc));
-                        gy = ld_stream(a.dy + (t * C + cc));
-                    }
+                    for (int ii = 0; ii < N; ++ii) g[ii] = box_chunk<N>(gb + ii * P::XBOX, r, h);
+                    gy = box_chunk<N>(gb + N * P::XBOX, r, h);
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&gempty);
                 }
             }
             if (*abort_v ||
@@ -584,17 +772,28 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
 {
     using P = BwdTc<N>;
     const int64_t T = args.T, C = args.C, K = int64_t(N) * C;
-    CUtensorMap tmx, tmdu, tmg, tmy;
+    CUtensorMap tmx, tmdu, tmg, tmy, tmdu2, tmhres, tmhpre, tmhpost;
     const CUtensorMapSwizzle xsw = N == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!tmap_bf16_2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
         !tmap_bf16_2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
                CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    tmg = tmx;
-    tmy = tmx;
-    if (LAYER && P::STAGE_G) {
+    tmg = tmy = tmdu2 = tmhres = tmhpre = tmhpost = tmx;
+    if (LAYER) {
         if (!tmap_bf16_2d(&tmg, args.dout, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
             !tmap_bf16_2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
+            return cudaErrorInvalidValue;
+    }
+    if (N == 8 && !tmap_bf16_2d(&tmdu2, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 32,
+                                CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    if (LAYER && P::TMA_P) {
+        if (!tmap_f32_2d(&tmhres, args.Hres, uint64_t(T), uint64_t(N * N), P::TT, 32,
+                         CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !tmap_f32_2d(&tmhpre, args.Hpre, uint64_t(T), uint64_t(N), P::TT, 8,
+                         CU_TENSOR_MAP_SWIZZLE_32B) ||
+            !tmap_f32_2d(&tmhpost, args.Hpost, uint64_t(T), uint64_t(N), P::TT, 8,
+                         CU_TENSOR_MAP_SWIZZLE_32B))
             return cudaErrorInvalidValue;
     }
     cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_bwd_tc<N, LAYER>), P::SMEM);
@@ -602,7 +801,8 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
     dim3 grid(unsigned((C + P::CW - 1) / P::CW), unsigned(splits));
     {
         MHC_PROF("k_bwd_tc", s);
-        launch_k(k_bwd_tc<N, LAYER>, dim3(grid), dim3(P::THREADS), P::SMEM, s, tmx, tmdu, tmg, tmy, args);
+        launch_k(k_bwd_tc<N, LAYER>, dim3(grid), dim3(P::THREADS), P::SMEM, s, tmx, tmdu, tmg, tmy,
+                 tmdu2, tmhres, tmhpre, tmhpost, args);
     }
     return cudaGetLastError();
 }

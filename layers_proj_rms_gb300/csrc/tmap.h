@@ -1,4 +1,4 @@
-// TMA tensor maps of bf16 tensors for the tensor-core kernels (the driver's
+// TMA tensor maps of bf16 and fp32 tensors for the tensor-core kernels (the driver's
 // cuTensorMapEncodeTiled, looked up once through the runtime).
 #pragma once
 
@@ -22,5 +22,9 @@ inline bool tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64
     const uint32_t box[2] = {box_cols, box_rows};
     return tmap_bf16(m, base, 2, dims, strides, box, sw);
 }
+
+// A row-major [rows][cols] fp32 matrix, box [box_rows][box_cols].
+bool tmap_f32_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols, CUtensorMapSwizzle sw);
 
 }  // namespace mhc
