@@ -286,6 +286,81 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// n = 8: the eight 8-channel accumulators and the 8x8 H_res in registers
+// (170 per thread) left one 256-thread block per SM and ~37 KB of loads in
+// flight.  Here the warp's H_res and H_post rows sit in shared memory (read
+// at uniform addresses), the outputs are formed in two halves of four (the
+// same operations in the same order per output), each lane keeps U chunks in
+// flight, and blocks are 4 warps.
+template <int U>
+__global__ void __launch_bounds__(128, 4)
+    k_post_fwd8(const bf16 *__restrict__ res, const bf16 *__restrict__ f,
+                const bf16 *__restrict__ bias, const float *__restrict__ Hres,
+                const float *__restrict__ Hpost, bf16 *__restrict__ out, int64_t T, int64_t C8)
+{
+    constexpr int N = 8;
+    pdl_wait();
+    __shared__ float4 hsm[4][18];   // per warp: H_res[t] (16 float4), H_post[t] (2 float4)
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = int64_t(blockIdx.x) * (blockDim.x >> 5) + w; t < T; t += warps) {
+        __syncwarp();
+        if (lane < 16)
+            hsm[w][lane] = __ldg(reinterpret_cast<const float4 *>(Hres + t * N * N) + lane);
+        else if (lane < 18)
+            hsm[w][lane] = __ldg(reinterpret_cast<const float4 *>(Hpost + t * N) + (lane - 16));
+        __syncwarp();
+        for (int64_t base = lane; base < C8; base += 32 * U) {
+            uint4 fv[U], bv[U], xr[U][N];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 < C8) {
+                    fv[u] = ld_stream(f + (t * C8 + c8) * 8);
+                    bv[u] = bias ? __ldg(reinterpret_cast<const uint4 *>(bias + c8 * 8))
+                                 : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                    for (int j = 0; j < N; ++j) xr[u][j] = ld_stream(res + ((t * N + j) * C8 + c8) * 8);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c8 = base + 32 * u;
+                if (c8 >= C8) continue;
+                float fb[8], bb[8];
+                unpack8(fv[u], fb);
+                unpack8(bv[u], bb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) fb[e] += bb[e];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const float4 hp4 = hsm[w][16 + half];
+                    const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
+                    float acc[4][8];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[i][e] = hp[i] * fb[e];
+#pragma unroll
+                    for (int j = 0; j < N; ++j) {
+                        float v[8];
+                        unpack8(xr[u][j], v);
+                        const float4 h4 = hsm[w][2 * j + half];   // H_res[t][j][4 half .. 4 half + 3]
+                        const float hr[4] = {h4.x, h4.y, h4.z, h4.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(hr[i], v[e], acc[i][e]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        st_stream(out + ((t * N + 4 * half + i) * C8 + c8) * 8, pack8(acc[i]));
+                }
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // h_post_bda backward, per-token part.  One warp per token:
 //   dres[t][j][c]  = sum_i H_res[t][j][i] dout[t][i][c]     (if dres != null)
@@ -753,7 +828,8 @@ cudaError_t launch_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias, co
         launch_k(k_post_fwd<4>, dim3(g), dim3(256), 0, s, res, f, bias, Hres, Hpost, out, T, C8);
     } else {
         MHC_PROF("k_post_fwd", s);
-        launch_k(k_post_fwd<8>, dim3(g), dim3(256), 0, s, res, f, bias, Hres, Hpost, out, T, C8);
+        launch_k(k_post_fwd8<1>, dim3(grid_for((T + 3) / 4, 16)), dim3(128), 0, s, res, f, bias,
+                 Hres, Hpost, out, T, C8);
     }
     return cudaGetLastError();
 }
