@@ -279,12 +279,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     // single buffers, each refilled once the previous tile is
                     // done with it: du_hl after the tile's MMAs, the per-token
                     // inputs and dout/dy after the epilogue has read them
-                    if (i >= 1 && (!tc::mbar_wait(&duempty, (i - 1) & 1, a.fault,
-                                                  tc::kFaultTimeoutEmpty) ||
-                                   (TP && !tc::mbar_wait(&pempty, (i - 1) & 1, a.fault,
-                                                         tc::kFaultTimeoutEmpty)) ||
-                                   (G1 && !tc::mbar_wait(&gempty, (i - 1) & 1, a.fault,
-                                                         tc::kFaultTimeoutEmpty)))) {
+                    if (i >= 1 && !tc::mbar_wait(&duempty, (i - 1) & 1, a.fault,
+                                                 tc::kFaultTimeoutEmpty)) {
                         *abort_v = 1;
                         break;
                     }
@@ -292,19 +288,29 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     for (int u = 0; u < P::DU_ATOMS; ++u)
                         tc::tma_load_2d(du1 + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0, &dufull);
                     tc::tma_load_2d(du1 + P::DU_TAIL, &tmdu2, 128, t0, &dufull);
-                    if (TP) {
-                        tc::mbar_arrive_expect_tx(&pfull, P::PAR_BYTES);
-                        tc::tma_load_2d(par, &tmhres, 0, t0, &pfull);
-                        tc::tma_load_2d(par + P::TT * 128, &tmhres, 32, t0, &pfull);
-                        tc::tma_load_2d(par + P::PH_PRE, &tmhpre, 0, t0, &pfull);
-                        tc::tma_load_2d(par + P::PH_POST, &tmhpost, 0, t0, &pfull);
-                    }
                     if (G1) {
+                        if (i >= 1 && !tc::mbar_wait(&gempty, (i - 1) & 1, a.fault,
+                                                     tc::kFaultTimeoutEmpty)) {
+                            *abort_v = 1;
+                            break;
+                        }
                         tc::mbar_arrive_expect_tx(&gfull, P::G1_BYTES);
                         for (int j = 0; j < N; ++j)
                             tc::tma_load_2d(g1 + j * P::XBOX, &tmg, int(int64_t(j) * C + c0), t0,
                                             &gfull);
                         tc::tma_load_2d(g1 + N * P::XBOX, &tmy, int(c0), t0, &gfull);
+                    }
+                    if (TP) {
+                        if (i >= 1 && !tc::mbar_wait(&pempty, (i - 1) & 1, a.fault,
+                                                     tc::kFaultTimeoutEmpty)) {
+                            *abort_v = 1;
+                            break;
+                        }
+                        tc::mbar_arrive_expect_tx(&pfull, P::PAR_BYTES);
+                        tc::tma_load_2d(par, &tmhres, 0, t0, &pfull);
+                        tc::tma_load_2d(par + P::TT * 128, &tmhres, 32, t0, &pfull);
+                        tc::tma_load_2d(par + P::PH_PRE, &tmhpre, 0, t0, &pfull);
+                        tc::tma_load_2d(par + P::PH_POST, &tmhpost, 0, t0, &pfull);
                     }
                     n1 = i + 1;
                 }
@@ -556,15 +562,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
                     const uint32_t pb = tc::smem_u32(smem + P::PAR_OFF);
 #pragma unroll
-                    for (int e4 = 0; e4 < N * N / 4; ++e4) {
-                        const uint4 v = lds128(pb + (e4 >> 3) * (P::TT * 128) + r * 128 +
-                                               (((e4 & 7) ^ (r & 7)) << 4));
-                        hres[4 * e4] = __uint_as_float(v.x);
-                        hres[4 * e4 + 1] = __uint_as_float(v.y);
-                        hres[4 * e4 + 2] = __uint_as_float(v.z);
-                        hres[4 * e4 + 3] = __uint_as_float(v.w);
-                    }
-#pragma unroll
                     for (int c4 = 0; c4 < N / 4; ++c4) {
                         const uint32_t off = r * 32 + ((c4 ^ ((r >> 2) & 1)) << 4);
                         const uint4 vp = lds128(pb + P::PH_PRE + off);
@@ -578,8 +575,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         hpost[4 * c4 + 2] = __uint_as_float(vq.z);
                         hpost[4 * c4 + 3] = __uint_as_float(vq.w);
                     }
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&pempty);
                 }
                 if (G1) {
                     // dout and dy of this tile (rows past T read as zero;
@@ -638,10 +633,22 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < N; ++j) {
-                        const f32x2 w2 = f2_make(hres[j * N + ii], hres[j * N + ii]);
+                        // n = 8: H_res[t][j][ii] read where it is used from the
+                        // 128-byte-swizzled rows of the parameter buffer
+                        const int e = j * N + ii;
+                        const float hw =
+                            TP ? lds32f(tc::smem_u32(smem + P::PAR_OFF) + (e >> 5) * (P::TT * 128) +
+                                        r * 128 + ((((e & 31) >> 2) ^ (r & 7)) << 4) + (e & 3) * 4)
+                               : hres[e];
+                        const f32x2 w2 = f2_make(hw, hw);
 #pragma unroll
                         for (int p = 0; p < 4; ++p) mix[j][p] = f2_fma(w2, dv[p], mix[j][p]);
                     }
+                }
+                if (TP) {
+                    // the parameter buffer has been read: refill it
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&pempty);
                 }
                 if (!SG) {
                     float dfs[8];
