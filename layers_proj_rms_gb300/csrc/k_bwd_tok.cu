@@ -40,9 +40,16 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
             const float h = __ldg(Hpost + t * N + ii);
             hp2[ii] = f2_make(h, h);
         }
-        f32x2 sR[N * N], sP[N], sQ[N];
+        // n = 8: the dH_res sums are scalars, each chunk's four channel pairs
+        // folded into them (as pairs they take 128 registers and the kernel
+        // spills)
+        constexpr bool SR1 = N == 8;
+        f32x2 sR[SR1 ? 1 : N * N], sP[N], sQ[N];
+        float sR1[SR1 ? N * N : 1];
 #pragma unroll
-        for (int e = 0; e < N * N; ++e) sR[e] = 0ull;
+        for (int e = 0; e < (SR1 ? 1 : N * N); ++e) sR[e] = 0ull;
+#pragma unroll
+        for (int e = 0; e < (SR1 ? N * N : 1); ++e) sR1[e] = 0.f;
 #pragma unroll
         for (int j = 0; j < N; ++j) sP[j] = sQ[j] = 0ull;
 
@@ -95,8 +102,18 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
                     for (int j = 0; j < N; ++j) {
                         f32x2 v[4];
                         unpack8x2(xr[u][j], v);
+                        if (SR1) {
+                            f32x2 c = f2_mul(v[0], d[0]);
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) sR[j * N + ii] = f2_fma(v[p], d[p], sR[j * N + ii]);
+                            for (int p = 1; p < 4; ++p) c = f2_fma(v[p], d[p], c);
+                            float lo, hi;
+                            f2_split(c, lo, hi);
+                            sR1[j * N + ii] += lo + hi;
+                        } else {
+#pragma unroll
+                            for (int p = 0; p < 4; ++p)
+                                sR[j * N + ii] = f2_fma(v[p], d[p], sR[j * N + ii]);
+                        }
                     }
                 }
                 if (df) st_stream(df + (t * C8 + c8) * 8, pack8x2(dfv));
@@ -109,7 +126,7 @@ __global__ void __launch_bounds__(32 * kTokWarps, N == 4 ? MHC_TOK_MINB : 1)
             return lo + hi;
         };
 #pragma unroll
-        for (int e = 0; e < N * N; ++e) aR[e] = fold(sR[e]);
+        for (int e = 0; e < N * N; ++e) aR[e] = SR1 ? sR1[e] : fold(sR[SR1 ? 0 : e]);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             aP[j] = fold(sP[j]);
