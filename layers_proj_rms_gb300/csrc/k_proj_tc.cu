@@ -9,11 +9,13 @@
 // N = 2*O gives x.W_hi and x.W_lo and their fp32 sum carries W to ~2^-17
 // relative error (x.W in fp32 semantics, well inside the 1e-5 bound on H).
 //
-// CTA: 128 tokens x one K split (K splits chosen for about two CTAs per SM); 6 warps:
-//   warp 0      TMA producer: x tile [128 x 64] and W_hl tile [2O x 64] per
+// CTA: BM tokens (128 at n = 4, 256 at n = 8) x one K split (K splits chosen
+// for about MINB CTAs per SM); 2 + BM/32 warps:
+//   warp 0      TMA producer: x tile [BM x 64] and W_hl tile [2O x 64] per
 //               stage, both in the 128-byte swizzle layout
-//   warp 1      TMEM allocation, MMA issue (one thread), commits
-//   warps 2..5  sum of squares of their token rows from the same smem tiles
+//   warp 1      TMEM allocation, MMA issue (one thread, BM/128 MMAs per k
+//               step sharing the W_hl operand), commits
+//   warps 2..   sum of squares of their token rows from the same smem tiles
 //               while the MMAs run; then the epilogue (TMEM -> partials)
 // Every wait is bounded; a timeout reports a fault code and the CTA unwinds.
 #include "launch.h"
@@ -24,33 +26,41 @@ namespace mhc {
 
 // A stage holds KBS consecutive 64-wide k-blocks (KBS boxes issued back to
 // back, so each token row is read in KBS*128 contiguous bytes); STG stages;
-// MINB CTAs per SM.
-template <int N, int KBS_, int STG_, int MINB_>
+// MINB CTAs per SM; BM tokens per CTA, in MMAs of 128 rows that share the
+// stage's W_hl tile (BM = 256 at n = 8, where the W_hl tile of a k-block,
+// 2O = 160 rows, is larger than 128 rows of x).
+template <int N, int KBS_, int STG_, int MINB_, int BM_ = 128>
 struct ProjTcCfg {
     static constexpr int O = N * N + 2 * N;
     static constexpr int NB = 2 * O;  // MMA N: hi rows then lo rows (48 or 160)
-    static constexpr int BM = 128, BK = 64, KBS = KBS_, STAGES = STG_, MINB = MINB_;
+    static constexpr int BM = BM_, BK = 64, KBS = KBS_, STAGES = STG_, MINB = MINB_;
+    static constexpr int MH = BM / 128;               // MMAs of 128 rows per k step
     static constexpr int A_SUB = BM * BK * 2;
     static constexpr int B_SUB = NB * BK * 2;
     static constexpr int A_BYTES = KBS * A_SUB;
     static constexpr int STAGE = KBS * (A_SUB + B_SUB);  // multiple of 1024
-    static constexpr int TMEM_COLS = NB <= 64 ? 64 : 256;
+    static constexpr int ACC_COLS = NB <= 64 ? 64 : 256;  // TMEM columns per accumulator
+    static constexpr int TMEM_COLS = MH * ACC_COLS;
+    static constexpr int EPI_WARPS = 4 * MH;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
     static_assert(A_SUB % 1024 == 0 && B_SUB % 1024 == 0, "sub-tiles keep 1024-byte alignment");
+    static_assert(BM == 128 || BM == 256, "tile rows");
     static_assert(SMEM * MINB <= 232448, "shared memory");
 };
 template <int N> struct ProjTcSel;
 template <> struct ProjTcSel<4> { using type = ProjTcCfg<4, 1, 4, 2>; };
-template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 2, 2, 1>; };
+template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 2, 2, 1, 256>; };
 template <int N>
 using ProjTc = typename ProjTcSel<N>::type;
 
-// W [K][O] fp32 -> W_hl [2O][K] bf16 (rows o: bf16(W[:,o]); rows O+o: the remainder)
-template <int N>
-__global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, int64_t K)
+// W [K][O] fp32 -> W_hl [2O][K] bf16 (rows o: bf16(W[:,o]); rows O+o: the
+// remainder).  n = 4: one thread per k (8.3 us at K = 16384; the tiled form
+// below, with 256 blocks, took 9.6).
+__global__ void k_w_split4(const float *__restrict__ W, bf16 *__restrict__ Whl, int64_t K)
 {
     pdl_wait();
-    constexpr int O = N * N + 2 * N;
+    constexpr int O = 24;
     const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (k >= K) return;
 #pragma unroll 4
@@ -63,8 +73,42 @@ __global__ void k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl, i
     }
 }
 
+// n = 8: a block transposes a tile of 64 k rows through shared memory:
+// the tile's 64*O floats are one contiguous, coalesced read, and each thread
+// writes 8 consecutive k of one output row (16 bytes); the tile's rows are
+// padded to O + 1 floats against bank conflicts.  Reading W[k][o] with one
+// thread per k (a 4*O-byte stride across the lanes) took 23 us at n = 8.
+constexpr int kWsplitK = 64;
+template <int N>
+__global__ void __launch_bounds__(256) k_w_split(const float *__restrict__ W, bf16 *__restrict__ Whl,
+                                                 int64_t K)
+{
+    pdl_wait();
+    constexpr int O = N * N + 2 * N;
+    constexpr int OP = O + 1;   // padded row: the 8 lanes of one output row, 8 rows apart, use 4 banks
+    __shared__ float ws[kWsplitK * OP];
+    const int64_t k0 = int64_t(blockIdx.x) * kWsplitK;
+    const int kn = int(K - k0 < kWsplitK ? K - k0 : kWsplitK);   // a multiple of 8
+    for (int i = threadIdx.x; i < kn * O; i += blockDim.x) ws[(i / O) * OP + i % O] = __ldg(W + k0 * O + i);
+    __syncthreads();
+    // item: output row ro (o, hi or lo) and 8-wide group kg of the tile's k
+    for (int it = threadIdx.x; it < 2 * O * (kWsplitK / 8); it += blockDim.x) {
+        const int ro = it / (kWsplitK / 8), kg = it % (kWsplitK / 8);
+        if (kg * 8 >= kn) continue;
+        const int o = ro < O ? ro : ro - O;
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float w = ws[(kg * 8 + e) * OP + o];
+            const bf16 hi = __float2bfloat16_rn(w);
+            v[e] = ro < O ? w : w - __bfloat162float(hi);
+        }
+        *reinterpret_cast<uint4 *>(Whl + int64_t(ro) * K + k0 + kg * 8) = pack8(v);
+    }
+}
+
 template <int N, class P>
-__global__ void __launch_bounds__(192, P::MINB)
+__global__ void __launch_bounds__(P::THREADS, P::MINB)
     k_proj_tc(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
               float *__restrict__ upart, float *__restrict__ spart, int64_t T, int kb_per_split,
               int kb_total, int *fault)
@@ -89,7 +133,7 @@ __global__ void __launch_bounds__(192, P::MINB)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1 + 4);
+            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
         }
         tc::mbar_init(acc_bar, 1);
         *abort_flag = 0;
@@ -131,7 +175,7 @@ __global__ void __launch_bounds__(192, P::MINB)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(P::BM, P::NB);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(128, P::NB);
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % P::STAGES;
                 if (*abort_flag ||
@@ -146,9 +190,12 @@ __global__ void __launch_bounds__(192, P::MINB)
                     const uint32_t a = a0 + j * P::A_SUB, b = a0 + P::A_BYTES + j * P::B_SUB;
 #pragma unroll
                     for (int kk = 0; kk < P::BK / 16; ++kk)
-                        tc::mma_bf16(tmem, tc::desc_kmajor_sw128(a + kk * 32),
-                                     tc::desc_kmajor_sw128(b + kk * 32), idesc,
-                                     (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                        for (int h = 0; h < P::MH; ++h)
+                            tc::mma_bf16(tmem + h * P::ACC_COLS,
+                                         tc::desc_kmajor_sw128(a + h * 128 * 128 + kk * 32),
+                                         tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                                         (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(&empty[s]);
             }
@@ -157,9 +204,10 @@ __global__ void __launch_bounds__(192, P::MINB)
         }
         __syncwarp();
     } else {
-        // warps 2..5: token row r of the tile = TMEM lane r
+        // warps 2..: token row r of the tile; TMEM lane r % 128 of accumulator r / 128
         const int q = warp & 3;
-        const int r = q * 32 + lane;
+        const int hh = (warp - 2) >> 2;
+        const int r = hh * 128 + q * 32 + lane;
         float ssq = 0.f;
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
@@ -191,7 +239,7 @@ __global__ void __launch_bounds__(192, P::MINB)
         if (ok && !tc::mbar_wait(acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
         tc::tc_fence_after();
         const int64_t t = m0 + r;
-        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+        const uint32_t trow = tmem + hh * P::ACC_COLS + (uint32_t(q * 32) << 16);
         constexpr int O = P::O;
         if (N == 4) {
             float v[48];
@@ -251,7 +299,8 @@ int batch_invariant() { return g_batch_invariant; }
 
 int proj_tc_splits(int64_t T, int n, int64_t K)
 {
-    const int64_t mt = (T + 127) / 128;
+    const int bm = n == 4 ? ProjTc<4>::BM : ProjTc<8>::BM;
+    const int64_t mt = (T + bm - 1) / bm;
     const int64_t kb = (K + 63) / 64;
     const int minb = n == 4 ? ProjTc<4>::MINB : ProjTc<8>::MINB;
     int64_t s = g_batch_invariant ? (kb + 63) / 64
@@ -274,9 +323,10 @@ cudaError_t launch_w_split(const float *W, bf16 *Whl, int n, int64_t K, cudaStre
 {
     MHC_PROF("k_w_split", s);
     if (n == 4)
-        launch_k(k_w_split<4>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
+        launch_k(k_w_split4, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
     else
-        launch_k(k_w_split<8>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
+        launch_k(k_w_split<8>, dim3(unsigned((K + kWsplitK - 1) / kWsplitK)), dim3(256), 0, s, W,
+                 Whl, K);
     return cudaGetLastError();
 }
 
@@ -286,8 +336,8 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
 {
     const int64_t K = int64_t(N) * C;
     {
-        MHC_PROF("k_w_split", s);
-        launch_k(k_w_split<N>, dim3(unsigned((K + 255) / 256)), dim3(256), 0, s, W, Whl, K);
+        cudaError_t e = launch_w_split(W, Whl, N, K, s);
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap tmx, tmw;
     if (!tmap_bf16_2d(&tmx, x, uint64_t(T), uint64_t(K), P::BM, P::BK,
@@ -303,7 +353,8 @@ static cudaError_t proj_tc_impl(const bf16 *x, const float *W, int64_t T, int64_
     dim3 grid(unsigned((T + P::BM - 1) / P::BM), unsigned(S_used));
     {
         MHC_PROF("k_proj_tc", s);
-        launch_k(k_proj_tc<N, P>, dim3(grid), dim3(192), P::SMEM, s, tmx, tmw, upart, spart, T, kps, kb_total, fault);
+        launch_k(k_proj_tc<N, P>, dim3(grid), dim3(P::THREADS), P::SMEM, s, tmx, tmw, upart, spart,
+                 T, kps, kb_total, fault);
     }
     return cudaGetLastError();
 }
