@@ -342,6 +342,22 @@ def test_layer(M, orc, T, n, C, seed, stress):
     check_layer(o, ref_f, ref_b)
 
 
+# Several 128-token tiles per residual-gradient CTA, element by element: the
+# single buffers that the n = 8 pass refills a tile ahead cycle through more
+# than one phase, with a ragged last tile and a ragged last channel slice
+# (C = 2056: 129 slices of 16 channels, one CTA per slice, six tiles each;
+# C = 64, T = 3000: 8 token splits of 3 tiles; n = 4, C = 1032: 33 slices of
+# 32 channels, 3 token splits of 2 tiles).
+@pytest.mark.parametrize("T,n,C,seed", [(700, 8, 2056, 11), (3000, 8, 64, 12),
+                                        (700, 4, 1032, 13)])
+def test_layer_multi_tile(M, orc, T, n, C, seed):
+    inp = _proj_inputs(T, n, C, seed, False)
+    o = run_layer(M, inp, T, n, C)
+    ref_f = orc.layer_fwd(inp, n, ITERS, EPS_SK, EPS_RMS)
+    ref_b = orc.layer_bwd(inp, ref_f, n, ITERS, EPS_SK, EPS_RMS)
+    check_layer(o, ref_f, ref_b)
+
+
 @pytest.mark.parametrize("n,C", [(4, 264), (8, 136)])
 def test_layer_zero_rows(M, orc, n, C):
     """Tokens whose residual rows are all zero (the first token, one inside a
