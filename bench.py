@@ -71,7 +71,7 @@ def kernel_bytes(name, T, n, C):
     K = n * C
     small = T * O * 4
     table = {
-        "k_w_split": 2 * K * O * 4,
+        "k_w_split": K * O * 4 + (3 * O + 15) // 16 * 16 * K * 2,
         "k_proj_tc": n * U + K * O * 4,
         "k_compute_h_fwd": small,
         "k_agg_fwd": (n + 1) * U,
@@ -311,6 +311,98 @@ def bench_ops(M, d, o, T, n, C, dev, reps=5):
 # our implementation
 # ---------------------------------------------------------------------------
 
+def collect_kernel_times(M):
+    """The library profiler's per-kernel totals since it was last collected:
+    {name: (launches, total ms)}."""
+    import ctypes
+
+    class KT(ctypes.Structure):
+        _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
+                    ("total_ms", ctypes.c_double)]
+
+    buf = (KT * 64)()
+    M.lib.mhc_profiler_collect.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    nk = M.lib.mhc_profiler_collect(ctypes.cast(buf, ctypes.c_void_p), 64)
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(nk)}
+
+
+def top_kernel_roofline(kernels, T, n, C, peak, workload):
+    """Roofline of the kernel with the largest total time: its algorithmic
+    bytes per launch over its average event-timed launch duration."""
+    if not kernels:
+        return None
+    name, (nl, tot) = max(kernels.items(), key=lambda kv: kv[1][1])
+    avg_ms = tot / nl
+    kb = kernel_bytes(name, T, n, C)
+    if kb is None:
+        return None
+    ach = kb / (avg_ms / 1e3) / 1e9
+    return {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(ach / peak, 4),
+            "traffic": ncu_traffic(name, workload),
+            "algorithmic_bytes_per_launch": int(kb), "avg_launch_ms": round(avg_ms, 4)}
+
+
+def run_wide(M, dev, steps, warmup, peak, barrier, world):
+    """The wide-stream workload (T=8192, n=8, C=7168, seed 4): the layer
+    forward + backward, timed as the main step is (events on the launching
+    stream, inputs larger than L2), then once more under the library's event
+    profiler for the per-kernel times and the dominant kernel's roofline."""
+    import torch
+    wl = "wide_T8192_n8_C7168"
+    T, n, C, w_std, seed = mi.LAYER_WORKLOADS[wl]
+    O = n * n + 2 * n
+    inp = mi.layer_inputs(T, n, C, seed, w_std=w_std)
+    bf = torch.bfloat16
+    d = {k: (torch.from_numpy(v.view(np.int16)).to(dev).view(bf) if v.dtype == np.uint16
+             else torch.from_numpy(v).to(dev)) for k, v in inp.items()}
+    del inp
+    e = lambda *s, dt=torch.float32: torch.empty(*s, dtype=dt, device=dev)  # noqa: E731
+    o = {"H_pre": e(T, n), "H_post": e(T, n), "H_res": e(T, n, n), "u": e(T, O), "r": e(T),
+         "y": e(T, C, dt=bf), "out": e(T, n, C, dt=bf), "dx": e(T, n, C, dt=bf),
+         "df": e(T, C, dt=bf), "dW": e(n * C, O), "dalpha": e(3), "db": e(O), "dbias": e(C)}
+    wsf = M.workspace(M.OP_LAYER_FWD, T, n, C, dev)
+    wsb = M.workspace(M.OP_LAYER_BWD, T, n, C, dev)
+
+    def step():
+        M.mhc_layer_fwd(d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"], ITERS, EPS_SK,
+                        EPS_RMS, o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"],
+                        o["out"], wsf)
+        M.mhc_layer_bwd(d["dout"], d["dy"], d["x"], d["W"], d["alpha"], d["b"], d["f"], d["bias"],
+                        o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], ITERS, EPS_SK,
+                        EPS_RMS, o["dx"], o["df"], o["dW"], o["dalpha"], o["db"], o["dbias"], wsb)
+
+    for _ in range(warmup):
+        step()
+    barrier()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world, dev)
+    collect_kernel_times(M)  # drop anything recorded before
+    M.lib.mhc_profiler_enable(1)
+    for _ in range(steps):
+        step()
+    barrier()
+    M.lib.mhc_profiler_enable(0)
+    kernels = collect_kernel_times(M)
+    assert M.mhc_device_error() == 0, "a kernel reported a device fault"
+    mb = model_bytes(T, n, C)
+    lb = mb["layer_fwd"] + mb["layer_bwd"]
+    gbs = lb / (ms / 1e3) / 1e9
+    return {"workload": wl, "step": "mhc_layer_fwd + mhc_layer_bwd", "ms_per_step": round(ms, 4),
+            "tokens_per_s": round(job_tokens_per_s(T, world, ms)),
+            "model_bytes_per_step": int(lb), "achieved_gbs": round(gbs, 1),
+            "frac_of_nominal_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+            "frac_of_measured": round(gbs / peak, 4),
+            "roofline": top_kernel_roofline(kernels, T, n, C, peak, wl),
+            "kernels_ms": {k: round(v[1] / v[0], 4) for k, v in
+                           sorted(kernels.items(), key=lambda kv: -kv[1][1])}}
+
 def run_ours(args, rank, world):
     import torch
 
@@ -375,7 +467,6 @@ def run_ours(args, rank, world):
     barrier()
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    import ctypes
 
     # The timed region: K steps as a user runs them.  Every library kernel is
     # launched with programmatic stream serialization, so a kernel's launch
@@ -400,14 +491,7 @@ def run_ours(args, rank, world):
     ms_prof = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world, dev)
     assert M.mhc_device_error() == 0, "a kernel reported a device fault"
 
-    class KT(ctypes.Structure):
-        _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
-                    ("total_ms", ctypes.c_double)]
-
-    buf = (KT * 64)()
-    M.lib.mhc_profiler_collect.argtypes = [ctypes.c_void_p, ctypes.c_int]
-    nk = M.lib.mhc_profiler_collect(ctypes.cast(buf, ctypes.c_void_p), 64)
-    kernels = {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(nk)}
+    kernels = collect_kernel_times(M)
     launches = int(sum(v[0] for v in kernels.values()))
 
     ms = max_over_ranks(ms, world, dev)
@@ -564,6 +648,12 @@ def run_ours(args, rank, world):
                       "step i+1's inputs copied while step i computes; two input sets) -> "
                       "mhc_layer_fwd/bwd + rmsnorm_fwd/bwd -> host dW, dalpha, db, dbias"}
 
+    # ---- the wide-stream workload (n = 8), its own step ----
+    wide = None
+    if not args.no_wide and args.workload != "wide_T8192_n8_C7168":
+        pk, _ = measured_hbm_peak()
+        wide = run_wide(M, dev, args.steps, args.warmup, pk, barrier, world)
+
     if rank != 0:
         return None
     mb = model_bytes(T, n, C)
@@ -571,20 +661,11 @@ def run_ours(args, rank, world):
     moved_b = sum(moved_bytes(T, n, C).values())
     peak, peak_kind = measured_hbm_peak()
     # dominant kernel
-    top = max(kernels.items(), key=lambda kv: kv[1][1]) if kernels else None
-    roof = None
-    if top:
-        name, (nl, tot) = top
-        avg_ms = tot / nl
-        kb = kernel_bytes(name, T, n, C)
-        if kb is not None:
-            ach = kb / (avg_ms / 1e3) / 1e9
-            roof = {"kernel": name, "bound": "hbm", "achieved": round(ach, 1), "peak": peak,
-                    "unit": "GB/s", "frac": round(ach / peak, 4),
-                    "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback 6.8 TB/s",
-                    "traffic": ncu_traffic(name, args.workload),
-                    "algorithmic_bytes_per_launch": int(kb), "avg_launch_ms": round(avg_ms, 4),
-                    "share_of_step": round(tot / (ms_prof * args.steps), 4)}
+    roof = top_kernel_roofline(kernels, T, n, C, peak, args.workload)
+    if roof:
+        roof["peak_source"] = ("measured (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                               else "fallback 6.8 TB/s")
+        roof["share_of_step"] = round(kernels[roof["kernel"]][1] / (ms_prof * args.steps), 4)
     res = {
         "metric": METRIC,
         "value": job_tokens_per_s(T, world, ms),
@@ -614,19 +695,7 @@ def run_ours(args, rank, world):
                 "moved_bytes_per_step": int(moved_b),
                 "moved_gbs": round(moved_b / (ms / 1e3) / 1e9, 1),
                 "moved_frac_of_measured": round(moved_b / (ms / 1e3) / 1e9 / peak, 4)},
-        "layer_only": {"ms_per_step": round(lms, 4), "tokens_per_s": job_tokens_per_s(T, world, lms),
-                       "model_bytes_per_step": int(mb["layer_fwd"] + mb["layer_bwd"]),
-                       "achieved_gbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3) / 1e9, 1),
-                       "frac_of_nominal_8tbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3)
-                                                     / 1e9 / NOMINAL_HBM_GBS, 4),
-                       "what": "mhc_layer_fwd + mhc_layer_bwd only, timed separately (same inputs)"},
         "per_step": per_step,
-        "forward_only": {"ms_per_step": round(fms, 4), "tokens_per_s": job_tokens_per_s(T, world, fms),
-                         "model_bytes_per_step": int(mb["layer_fwd"]),
-                         "achieved_gbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9, 1),
-                         "frac_of_nominal_8tbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9
-                                                       / NOMINAL_HBM_GBS, 4),
-                         "what": "mhc_layer_fwd only, timed separately (same inputs)"},
         "roofline": roof,
         "kernels": {k: {"launches": v[0], "avg_ms": round(v[1] / v[0], 4),
                         "share": round(v[1] / (ms_prof * args.steps), 4)} for k, v in
@@ -636,6 +705,21 @@ def run_ours(args, rank, world):
         "e2e": e2e,
         "graph": graph,
         "ops": ops,
+        # last, so that they stay in the tail of the line
+        "layer_only": {"step": "mhc_layer_fwd + mhc_layer_bwd", "ms_per_step": round(lms, 4),
+                       "tokens_per_s": round(job_tokens_per_s(T, world, lms)),
+                       "model_bytes_per_step": int(mb["layer_fwd"] + mb["layer_bwd"]),
+                       "achieved_gbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3) / 1e9, 1),
+                       "frac_of_nominal_8tbs": round((mb["layer_fwd"] + mb["layer_bwd"]) / (lms / 1e3)
+                                                     / 1e9 / NOMINAL_HBM_GBS, 4)},
+        "forward_only": {"step": "mhc_layer_fwd (the 7B-scale forward's shapes)",
+                         "ms_per_step": round(fms, 4),
+                         "tokens_per_s": round(job_tokens_per_s(T, world, fms)),
+                         "model_bytes_per_step": int(mb["layer_fwd"]),
+                         "achieved_gbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9, 1),
+                         "frac_of_nominal_8tbs": round(mb["layer_fwd"] / (fms / 1e3) / 1e9
+                                                       / NOMINAL_HBM_GBS, 4)},
+        "wide": wide,
     }
     return res
 
@@ -722,6 +806,8 @@ def main():
                     help="streams the e2e host-to-device copies are spread over")
     ap.add_argument("--no-ops", action="store_true", help="skip the per-op timings")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--no-wide", action="store_true",
+                    help="skip the wide-stream (n = 8) workload's step")
     ap.add_argument("--cpu-tokens", type=int, default=4096)
     ap.add_argument("--ref-tokens", type=int, default=1024)
     args = ap.parse_args()
@@ -742,9 +828,13 @@ def main():
     res = run_ours(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args, args.cpu_tokens)
+            cb = cpu_baseline(args, args.cpu_tokens)
         else:
-            res["cpu_baseline"] = None
+            cb = None
+        # the line ends with the layer-only, forward-only and wide numbers
+        tail = {k: res.pop(k) for k in ("layer_only", "forward_only", "wide")}
+        res["cpu_baseline"] = cb
+        res.update(tail)
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

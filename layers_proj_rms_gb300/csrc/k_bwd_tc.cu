@@ -13,7 +13,13 @@
 //
 // du (fp32) arrives as bf16 hi | lo halves (du_hl[t][0..O) = bf16(du),
 // du_hl[t][O..2O) = bf16(du - hi)), which together carry du to ~2^-17; W is
-// split the same way into W_hi and W_lo.
+// split the same way into W_hi and W_lo.  The product below then differs from
+// du.W^T by at most kSplitBound * sum_o |du_o| * max_ko |W_ko| (the dropped
+// du_lo.W_lo, the remainders of du and W, the fp32 accumulation).  A token
+// for which that bound exceeds kExactAbove (rows of near-zero RMS, where
+// r = 1/(q + eps) makes du ~1e5 while dx stays O(1) through cancellation)
+// takes the exact path instead: its du.W^T is recomputed in fp64 from the
+// fp32 du and W, so dx meets the bf16 gradient tolerance on every token.
 // Per tile of 128 tokens (MMA 1 first, so the epilogue's accumulator is
 // complete before the dW and dbias MMAs of the tile run):
 //   MMA 1 (dx_gemm): D2[t][k] = du_hi.W_hi + du_lo.W_hi + du_hi.W_lo (the
@@ -49,6 +55,33 @@
 #include "tmap.h"
 
 namespace mhc {
+
+// Error bound factor of the two-term bf16 product (see above): the three
+// dropped terms are each at most 2^-16 |du_o W_ko|, the fp32 accumulation
+// over at most 16 K steps 2^-20.
+constexpr float kSplitBound = 3.25f / 65536.f;
+// Above this bound on |dx_gemm error| (a fifth of the 2e-2 absolute
+// tolerance of the bf16 gradients) a token takes the exact path.
+constexpr float kExactAbove = 4e-3f;
+
+// The exact path's dot product of a token's fp32 du row with a row of W, in
+// fp64: each product of two fp32 values is exact in fp64 and the O terms
+// accumulate with ~2^-53 relative rounding.
+__device__ __forceinline__ float exact_du_w(const float *__restrict__ du,
+                                           const float *__restrict__ w, int O)
+{
+    double acc = 0.0;
+#pragma unroll 1
+    for (int o = 0; o < O; o += 4) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(du + o));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(w + o));
+        acc = fma(double(a.x), double(b.x), acc);
+        acc = fma(double(a.y), double(b.y), acc);
+        acc = fma(double(a.z), double(b.z), acc);
+        acc = fma(double(a.w), double(b.w), acc);
+    }
+    return float(acc);
+}
 
 template <int N>
 struct BwdTc {
@@ -112,7 +145,7 @@ struct BwdTc {
     static constexpr int PAR_OFF = W_OFF + W_BYTES;
     static constexpr int PH_PRE = 2 * TT * 128, PH_POST = PH_PRE + TT * 32;
     static constexpr int PAR_BYTES =
-        STAGE_P ? TT * PAR_ROW + TT * 4 : (TMA_P ? PH_POST + TT * 32 : 0);   // 10.5 KB / 40 KB
+        STAGE_P ? TT * PAR_ROW + 2 * TT * 4 : (TMA_P ? PH_POST + TT * 32 : 0);   // 11 KB / 40 KB
     // n = 8 (layer): the G buffer, dout boxes of the n streams then the dy box
     static constexpr int G1_OFF = PAR_OFF + PAR_BYTES;
     static constexpr int G1_BYTES = N == 4 ? 0 : (N + 1) * XBOX;       // 36 KB
@@ -148,6 +181,8 @@ __device__ __forceinline__ float warp_column_sum(float (&v)[COLS])
 
 struct BwdTcArgs {
     const float *W;    // [K][O] fp32
+    const float *du32; // [T][O] fp32 du (the exact path)
+    const float *dub;  // [T] sum_o |du[t][o]|
     const bf16 *dout, *dy;
     const float *coef, *Hpre, *Hres, *Hpost;
     bf16 *dx;
@@ -189,6 +224,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float bias_red[4][CW];
+    __shared__ uint32_t wmax_bits;   // max |W| over the slice (bits of a nonnegative float)
 
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -206,21 +242,24 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
+            // the MMAs' commit + every epilogue thread: each thread releases a
+            // buffer after its own reads of it (tc::mbar_release)
+            tc::mbar_init(&empty[s], 1 + 32 * P::EPI_WARPS);
         }
-        tc::mbar_init(&wfull, P::EPI_WARPS);
+        tc::mbar_init(&wfull, 32 * P::EPI_WARPS);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(&d2full[b], 1);
             tc::mbar_init(&d2empty[b], P::EPI_WARPS);
         }
         tc::mbar_init(&d1full, 1);
         tc::mbar_init(&pfull, 1);
-        tc::mbar_init(&pempty, P::EPI_WARPS);
+        tc::mbar_init(&pempty, 32 * P::EPI_WARPS);
         tc::mbar_init(&dufull, 1);
         tc::mbar_init(&duempty, 1);
         tc::mbar_init(&gfull, 1);
-        tc::mbar_init(&gempty, P::EPI_WARPS);
+        tc::mbar_init(&gempty, 32 * P::EPI_WARPS);
         abort_flag = 0;
+        wmax_bits = 0;
         tc::fence_barrier_init();
     }
     if (warp == 1) tc::tmem_alloc(&tmem_slot, P::TMEM_COLS);
@@ -430,6 +469,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         // in 64-column planes.  n = 8: W_hi [0,64), W_lo [0,64), and the tail
         // [W_hi [64,80) | W_lo [64,80)].
         constexpr int W_CHUNKS = P::W_PLANES * 128 * 8 + (N == 8 ? 128 * 4 : 0);
+        float wmax = 0.f;   // max |W| of the values this thread loads
         for (int idx = threadIdx.x - 64; idx < W_CHUNKS; idx += 32 * P::EPI_WARPS) {
             int rr, col;
             bool lo;
@@ -455,6 +495,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 const float4 v0 = __ldg(src), v1 = __ldg(src + 1);
                 w[0] = v0.x; w[1] = v0.y; w[2] = v0.z; w[3] = v0.w;
                 w[4] = v1.x; w[5] = v1.y; w[6] = v1.z; w[7] = v1.w;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) wmax = fmaxf(wmax, fabsf(w[e]));
                 if (lo)
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -466,8 +508,17 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                          : "memory");
         }
         tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&wfull);
+        // the slice's max |W|: each warp folds its maximum in before its
+        // threads report their part of the W tile on the W barrier, and every
+        // epilogue thread reads the total once that barrier has completed
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(kFull, wmax, m));
+        if (lane == 0) atomicMax(&wmax_bits, __float_as_uint(wmax));
+        tc::mbar_release(&wfull);
+        if (!tc::mbar_wait(&wfull, 0, a.fault, tc::kFaultTimeoutMisc)) *abort_v = 1;
+        // a token whose sum_o |du_o| times this bound factor exceeds
+        // kExactAbove takes the exact path
+        const float wbound = __uint_as_float(wmax_bits) * kSplitBound;
 
         const int q = warp & 3;              // TMEM lane quadrant
         const int h = (warp - 2) >> 2;       // this thread's 8-channel chunk of every stream
@@ -483,6 +534,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         // zero-filled) and meet at a named barrier before and after reading.
         const uint32_t prow = tc::smem_u32(smem + P::PAR_OFF) + r * P::PAR_ROW;
         const uint32_t pcoef = tc::smem_u32(smem + P::PAR_OFF + P::TT * P::PAR_ROW) + r * 4;
+        const uint32_t pdub = pcoef + P::TT * 4;
         auto stage_params = [&](int tile) {
             const int64_t tp = int64_t(tile) * P::TT + r;
             const bool v = tp < a.T;
@@ -491,7 +543,10 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 tc::cp_async16(prow + h * 16, a.Hres + tv * N * N + h * 4, v ? 16u : 0u);
                 if (h == 0) tc::cp_async16(prow + 64, a.Hpre + tv * N, v ? 16u : 0u);
             }
-            if (h == (LAYER ? 1 : 0)) tc::cp_async4(pcoef, a.coef + tv, v ? 4u : 0u);
+            if (h == (LAYER ? 1 : 0)) {
+                tc::cp_async4(pcoef, a.coef + tv, v ? 4u : 0u);
+                tc::cp_async4(pdub, a.dub + tv, v ? 4u : 0u);
+            }
             tc::cp_async_commit();
         };
         if (P::STAGE_P && ntiles > 0) stage_params(tile0);
@@ -500,7 +555,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             const int64_t t = int64_t(tile0 + i) * P::TT + r;
             const bool valid = t < a.T;
             // per-token inputs, fetched before waiting on the tensor cores
-            float coef = 0.f, hpre[N], hpost[N], hres[LAYER ? N * N : 1];
+            float coef = 0.f, dub = 0.f, hpre[N], hpost[N], hres[LAYER ? N * N : 1];
 #pragma unroll
             for (int j = 0; j < N; ++j) hpre[j] = hpost[j] = 0.f;
 #pragma unroll
@@ -529,12 +584,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     hpre[3] = __uint_as_float(v.w);
                 }
                 coef = lds32f(pcoef);
+                dub = lds32f(pdub);
                 tc::named_bar_sync(1 + q, 128);
                 if (i + 1 < ntiles) stage_params(tile0 + i + 1);
                 if (!ok) continue;
             } else {
                 if (valid) {
                     coef = __ldg(a.coef + t);
+                    dub = __ldg(a.dub + t);
                     if (LAYER && !TP) {
 #pragma unroll
                         for (int j = 0; j < N; ++j) {
@@ -587,8 +644,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                     for (int ii = 0; ii < N; ++ii) g[ii] = box_chunk<N>(gb + ii * P::XBOX, r, h);
                     gy = box_chunk<N>(gb + N * P::XBOX, r, h);
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&gempty);
+                    tc::mbar_release(&gempty);
                 }
             }
             if (*abort_v ||
@@ -599,6 +655,25 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 break;
             }
             tc::tc_fence_after();
+            // The exact path (rare: rows of near-zero RMS): a warp with such a
+            // token rewrites that token's dx_gemm values in TMEM with du.W^T
+            // from the fp32 values before the usual reads below.
+            const bool exact = valid && cvalid && dub * wbound > kExactAbove;
+            if (__any_sync(kFull, exact)) {
+                const uint32_t tb = trow + P::D2_COL + b * 128 + h * 8;
+#pragma unroll 1
+                for (int j = 0; j < N; ++j) {
+                    float v[8];
+                    tc::tmem_ld8_wait(tb + j * CW, v);
+                    if (exact) {
+                        const float *wrow = a.W + (int64_t(j) * C + cc) * O;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = exact_du_w(a.du32 + t * O, wrow + e * O, O);
+                    }
+                    __syncwarp();
+                    tc::tmem_st8_wait(tb + j * CW, v);
+                }
+            }
             const uint8_t *st = smem + s * P::STAGE;
             // (releasing the stage right after these reads, before the
             // arithmetic, measured slower: the stage goes back at the end)
@@ -646,9 +721,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
                 }
                 if (TP) {
-                    // the parameter buffer has been read: refill it
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&pempty);
+                    // this thread has read the parameter buffer
+                    tc::mbar_release(&pempty);
                 }
                 if (!SG) {
                     float dfs[8];
@@ -663,12 +737,11 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
             for (int j0 = 0; j0 < N; j0 += JB) {
                 float acc[JB][8];
-#pragma unroll
-                for (int jj = 0; jj < JB; ++jj)
-                    tc::tmem_ld8(trow + P::D2_COL + b * 128 + (j0 + jj) * CW + h * 8, acc[jj]);
+                static_assert(JB == 2, "two TMEM loads per batch");
+                const uint32_t ta = trow + P::D2_COL + b * 128 + j0 * CW + h * 8;
+                tc::tmem_ld8x2_wait(ta, ta + CW, acc[0], acc[1]);
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj) xr[j0 + jj] = box_chunk<N>(st + (j0 + jj) * P::XBOX, r, h);
-                tc::tmem_ld_wait();
 #pragma unroll
                 for (int jj = 0; jj < JB; ++jj) {
                     const int j = j0 + jj;
@@ -684,11 +757,9 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             }
             // D2 buffer b and the stage have been read: release them
             tc::tc_fence_before();
+            tc::mbar_release(&empty[s]);
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&d2empty[b]);
-                tc::mbar_arrive(&empty[s]);
-            }
+            if (lane == 0) tc::mbar_arrive(&d2empty[b]);
         }
         if (P::STAGE_P) tc::cp_async_wait_all();
         if (!ok) *abort_v = 1;
@@ -704,8 +775,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                 for (int m = 0; m < 3; ++m) {
                     float w16[16];
-                    tc::tmem_ld16(trow + P::D1_COL + m * 16, w16);
-                    tc::tmem_ld_wait();
+                    tc::tmem_ld16_wait(trow + P::D1_COL + m * 16, w16);
 #pragma unroll
                     for (int e = 0; e < 16; ++e) v[m * 16 + e] = w16[e];
                 }
@@ -719,9 +789,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll 1
                 for (int m = 0; m < O / 16; ++m) {
                     float hi[16], lo[16];
-                    tc::tmem_ld16(trow + P::D1_COL + m * 16, hi);
-                    tc::tmem_ld16(trow + P::D1_COL + O + m * 16, lo);
-                    tc::tmem_ld_wait();
+                    tc::tmem_ld16x2_wait(trow + P::D1_COL + m * 16, trow + P::D1_COL + O + m * 16,
+                                         hi, lo);
 #pragma unroll
                     for (int o4 = 0; o4 < 4; ++o4)
                         if (krow)
@@ -738,8 +807,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             float v = 0.f;
             if (ok) {
                 float d3[16];
-                tc::tmem_ld16(trow + P::D3_COL + 2 * O, d3);
-                tc::tmem_ld_wait();
+                tc::tmem_ld16_wait(trow + P::D3_COL + 2 * O, d3);
 #pragma unroll
                 for (int e = 0; e < N; ++e)
                     if (e == q) v = d3[e] + d3[N + e];
@@ -814,14 +882,16 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
-                          int64_t T, int n, int64_t C, const bf16 *dout,
-                          const bf16 *dy, const float *Hpre, const float *Hres,
+cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *du32,
+                          const float *dub, const float *coef, int64_t T, int n, int64_t C,
+                          const bf16 *dout, const bf16 *dy, const float *Hpre, const float *Hres,
                           const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
                           int splits, int *fault, cudaStream_t s)
 {
     BwdTcArgs a;
     a.W = W;
+    a.du32 = du32;
+    a.dub = dub;
     a.dout = dout;
     a.dy = dy;
     a.coef = coef;

@@ -12,15 +12,21 @@
 //
 // n = 4.  CTA: 128 tokens x a range of channel blocks; a stage is one
 // channel block of BC channels: the n residual boxes [128 x BC] and f's box
-// (TMA, swizzled) plus the n W'_hl boxes [2O x BC] of its k-blocks.  Warps:
+// (TMA, swizzled) plus the n W'_hl boxes [NB x BC] of its k-blocks (W' as
+// three bf16 terms hi | lo | lo2 and zero rows, NB = 80).  Warps:
 //   0     TMA producer
 //   1     TMEM, then per stage: TMA store of the stage's out boxes to HBM and
-//         the MMAs u += out . [W'_hi | W'_lo] (N = 2O, one k-block per stream)
+//         the MMAs out . [W'_lo | W'_lo2] (N = 48, accumulated over the split)
+//         and out . W'_hi (N = 32) into one of two buffers per group of G
+//         stages, which the epilogue warps drain into fp32 registers (the
+//         tensor core's accumulator loses about an ulp of the running sum per
+//         K step, so the large term is not accumulated over the split)
 //   2..9  two warps per token row r (half the block's channels each): out for the row's
 //         channels of every stream, written over the residual boxes in place
 //         (same swizzled layout, so the boxes become both the MMA A operand
 //         and the store source); the row's sum of squares of the bf16
-//         outputs; finally TMEM -> partials
+//         outputs; at the end of each group the first warp of a quadrant
+//         drains its out . W'_hi buffer; finally TMEM -> partials
 // A stage is free again when its MMAs have completed and the store has read
 // it.  Channels past C and rows past T load as zeros and are not stored.
 #include "launch.h"
@@ -33,7 +39,7 @@ namespace mhc {
 // and swizzle), STAGES stages, MINB CTAs per SM.
 template <int BC_, int STAGES_, int MINB_>
 struct PostProjCfg {
-    static constexpr int N = 4, O = N * N + 2 * N, NB = 2 * O;  // 24 logits, 48 MMA columns
+    static constexpr int N = 4, O = N * N + 2 * N, NB = w_split_rows(4);  // 24 logits, 80 MMA columns
     static constexpr int BM = 128, BC = BC_;                     // tokens, channels per stage
     static constexpr int RB = BC * 2;                            // bytes of a box row
     static constexpr int CH = BC / 8;                            // 16-byte chunks per row
@@ -44,7 +50,11 @@ struct PostProjCfg {
     static constexpr int STAGE = W_OFF + N * WBOX;
     static constexpr int STAGES = STAGES_, MINB = MINB_;
     static constexpr int SMEM = STAGES * STAGE + 1024;
-    static constexpr int TMEM_COLS = 64;
+    // TMEM: two out.W'_hi buffers (NH = 32 columns, 24 used) and the
+    // [out.W'_lo | out.W'_lo2] accumulator (NL = 48), drained every G stages
+    static constexpr int NH = 32, NL = 2 * O, HI0 = 0, HI1 = NH, LO = 2 * NH, G = 2;
+    static constexpr int TMEM_COLS = 128;
+    static_assert(LO + NL <= TMEM_COLS && 3 * O <= NB, "accumulators");
     static constexpr int WORKERS = 8;  // warps 2..9
     static constexpr int THREADS = 64 + 32 * WORKERS;
     static constexpr int ATOM = BC == 64 ? 1024 : 512;  // swizzle pattern repeat
@@ -61,10 +71,10 @@ struct PostProjCfg {
         return BC == 64 ? tc::desc_kmajor_sw128(addr) : tc::make_desc(addr, 16, 512, tc::kSwz64);
     }
 };
-// Four 52 KB stages of 32 channels, one CTA per SM (T=16384, n=4, C=4096:
-// 0.217 ms; two 104 KB stages of 64 channels: 0.244 ms; two 52 KB stages at
-// two CTAs per SM: 0.248 ms).
-using PostProj = PostProjCfg<32, 4, 1>;
+// Three 60 KB stages of 32 channels, one CTA per SM.  (With W' in two terms,
+// 52 KB stages: four stages 0.217 ms at T=16384, n=4, C=4096; two 104 KB
+// stages of 64 channels 0.244 ms; two stages at two CTAs per SM 0.248 ms.)
+using PostProj = PostProjCfg<32, 3, 1>;
 
 template <class P>
 __global__ void __launch_bounds__(P::THREADS, P::MINB)
@@ -78,7 +88,8 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
     pdl_wait();
     constexpr int N = P::N, O = P::O;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[P::STAGES], ready[P::STAGES], empty[P::STAGES], acc_bar;
+    __shared__ uint64_t full[P::STAGES], ready[P::STAGES], empty[P::STAGES], acc_bar, hifull[2],
+        hiempty[2];
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
     __shared__ float ssq_red[P::BM];
@@ -95,10 +106,14 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&ready[s], P::WORKERS);
+            tc::mbar_init(&ready[s], 32 * P::WORKERS);  // every worker thread
             tc::mbar_init(&empty[s], 2);  // the MMAs' commit + the store's read
         }
         tc::mbar_init(&acc_bar, 1);
+        for (int hb = 0; hb < 2; ++hb) {
+            tc::mbar_init(&hifull[hb], 1);
+            tc::mbar_init(&hiempty[hb], 4);   // the first worker warp of each quadrant
+        }
         abort_flag = 0;
         tc::fence_barrier_init();
     }
@@ -142,10 +157,12 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
         // ------------------------------------------------- out store + MMA issue
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmo);
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(P::BM, P::NB);
+            constexpr uint32_t idesc_hi = tc::idesc_bf16_f32(P::BM, P::NH);
+            constexpr uint32_t idesc_lo = tc::idesc_bf16_f32(P::BM, P::NL);
             bool ok = true;
             for (int i = 0; i < ncb; ++i) {
-                const int s = i % P::STAGES;
+                const int s = i % P::STAGES, g = i / P::G, hb = g & 1;
+                const bool first = i % P::G == 0, last = i % P::G == P::G - 1 || i == ncb - 1;
                 if (*abort_v ||
                     !tc::mbar_wait(&ready[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
                     ok = false;
@@ -157,15 +174,34 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
                 for (int j = 0; j < N; ++j) tc::tma_store_3d(&tmo, st + j * P::XBOX, c0, j, m0);
                 tc::bulk_commit_group();
                 const uint32_t a0 = tc::smem_u32(st);
+                // W'_hl rows [O, 3O) (lo | lo2) start on an 8-row swizzle group
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
                     const uint32_t a = a0 + j * P::XBOX, b = a0 + P::W_OFF + j * P::WBOX;
 #pragma unroll
                     for (int kk = 0; kk < P::BC / 16; ++kk)
-                        tc::mma_bf16(tmem, P::desc(a + kk * 32), P::desc(b + kk * 32), idesc,
+                        tc::mma_bf16(tmem + P::LO, P::desc(a + kk * 32),
+                                     P::desc(b + O * P::RB + kk * 32), idesc_lo,
                                      (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
                 }
+                // the out.W'_hi buffer must have been drained (group g - 2)
+                if (first && g >= 2 &&
+                    !tc::mbar_wait(&hiempty[hb], ((g >> 1) - 1) & 1, fault, tc::kFaultTimeoutAcc)) {
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < N; ++j) {
+                    const uint32_t a = a0 + j * P::XBOX, b = a0 + P::W_OFF + j * P::WBOX;
+#pragma unroll
+                    for (int kk = 0; kk < P::BC / 16; ++kk)
+                        tc::mma_bf16(tmem + (hb ? P::HI1 : P::HI0), P::desc(a + kk * 32),
+                                     P::desc(b + kk * 32), idesc_hi,
+                                     (!first || j > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc::mma_commit(&empty[s]);
+                if (last) tc::mma_commit(&hifull[hb]);
                 tc::bulk_wait_read_all();
                 tc::mbar_arrive(&empty[s]);
             }
@@ -204,6 +240,10 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
             hp2[3] = f2_make(v.w, v.w);
         }
         f32x2 ssq2 = 0ull;
+        const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
+        float uhi[O];   // (hf = 0) sum over the groups of out.W'_hi, fp32 round to nearest
+#pragma unroll
+        for (int o = 0; o < O; ++o) uhi[o] = 0.f;
         bool ok = true;
         for (int i = 0; i < ncb; ++i) {
             const int s = i % P::STAGES;
@@ -256,10 +296,32 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
                     for (int e = 0; e < 4; ++e) ssq2 = f2_fma(rv[e], rv[e], ssq2);
                 }
             }
-            // the out boxes are read by the tensor cores and the TMA store
+            // the out boxes are read by the tensor cores and the TMA store:
+            // each thread's writes are complete before its arrival
             tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&ready[s]);
+            tc::mbar_release(&ready[s]);
+            // end of a group: the first warp of the quadrant drains its rows'
+            // out.W'_hi buffer into registers and hands it back
+            const int g = i / P::G, hb = g & 1;
+            if (hf == 0 && (i % P::G == P::G - 1 || i == ncb - 1)) {
+                if (*abort_v ||
+                    !tc::mbar_wait(&hifull[hb], (g >> 1) & 1, fault, tc::kFaultTimeoutAcc)) {
+                    *abort_v = 1;
+                    ok = false;
+                    break;
+                }
+                tc::tc_fence_after();
+                float w0[16], w1[16];
+                tc::tmem_ld16x2_wait(trow + (hb ? P::HI1 : P::HI0), trow + (hb ? P::HI1 : P::HI0) + 16,
+                                     w0, w1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) uhi[e] += w0[e];
+#pragma unroll
+                for (int e = 0; e < O - 16; ++e) uhi[16 + e] += w1[e];
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&hiempty[hb]);
+            }
         }
         float s_lo, s_hi;
         f2_split(ssq2, s_lo, s_hi);
@@ -271,23 +333,19 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
             const float ssq_row = ssq + ssq_red[r];
             if (ok && !tc::mbar_wait(&acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
             tc::tc_fence_after();
-            const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
-            float v[2 * O];
+            // u = sum over groups of out.W'_hi + (out.W'_lo + out.W'_lo2)
 #pragma unroll
-            for (int c = 0; c < 3; ++c) {
-                float w[16];
-                tc::tmem_ld16(trow + c * 16, w);
-                tc::tmem_ld_wait();
+            for (int c = 0; c < O / 8; ++c) {
+                float w[8], w2[8];
+                tc::tmem_ld8x2_wait(trow + P::LO + c * 8, trow + P::LO + O + c * 8, w, w2);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
+                for (int e = 0; e < 8; ++e) uhi[c * 8 + e] += w[e] + w2[e];
             }
             if (ok && !*abort_v && live) {
                 float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
 #pragma unroll
                 for (int o4 = 0; o4 < O / 4; ++o4)
-                    dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
-                                          v[4 * o4 + 2] + v[O + 4 * o4 + 2],
-                                          v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
+                    dst[o4] = make_float4(uhi[4 * o4], uhi[4 * o4 + 1], uhi[4 * o4 + 2], uhi[4 * o4 + 3]);
                 spart[int64_t(split) * T + t] = ssq_row;
             }
         }
@@ -321,13 +379,13 @@ static int post_proj_splits(int64_t T, int64_t C)
     return int(s);
 }
 
-// workspace: W'_hl [2O][K] bf16, partials upart [S][T][O], spart [S][T]
+// workspace: W'_hl [NB][K] bf16, partials upart [S][T][O], spart [S][T]
 size_t post_proj_ws_bytes(int64_t T, int n, int64_t C)
 {
     if (n != 4) return proj_fwd_ws_bytes(T, n, C);
     const int64_t O = PostProj::O, K = int64_t(n) * C;
     const int64_t S = post_proj_splits(T, C);
-    return ws_align(size_t(2 * O * K) * 2) + ws_align(size_t(S * T * O) * 4) +
+    return ws_align(size_t(PostProj::NB * K) * 2) + ws_align(size_t(S * T * O) * 4) +
            ws_align(size_t(S * T) * 4);
 }
 
@@ -351,7 +409,7 @@ cudaError_t launch_post_proj_fwd(const bf16 *res, const bf16 *f, const bf16 *bia
     const int S = post_proj_splits(T, C);
     char *p = static_cast<char *>(ws);
     bf16 *Whl = reinterpret_cast<bf16 *>(p);
-    p += ws_align(size_t(2 * O * K) * 2);
+    p += ws_align(size_t(P::NB * K) * 2);
     float *upart = reinterpret_cast<float *>(p);
     p += ws_align(size_t(int64_t(S) * T * O) * 4);
     float *spart = reinterpret_cast<float *>(p);

@@ -84,7 +84,9 @@ __global__ void __launch_bounds__(128)
 
 // ---------------------------------------------------------------------------
 // compute_h backward.  Same lane layout.  Per token writes
-//   du[t][o] = alpha_seg r dz[o] (bf16 hi | lo) and
+//   du[t][o] = alpha_seg r dz[o] (bf16 hi | lo; fp32 when du_f32 is given),
+//   dub[t] = sum_o |du[t][o]| (when given: the residual-gradient pass bounds
+//   the error of its bf16 product with it) and
 //   coef[t] = -dr r^2 / (K q) with dr = sum_o dz alpha_seg u and q = 1/r - eps_rms
 //   (coef = 0 when q <= 0: an all-zero row has zero RMS gradient);
 // per block one partial row: the block's sums of dz[o] (in token order) and
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(128)
                     const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
                     float eps_rms, bf16 *__restrict__ du_hl, int du_cols,
                     float *__restrict__ coef, float *__restrict__ part,
-                    const float *__restrict__ s_tot, float *__restrict__ du_f32)
+                    const float *__restrict__ s_tot, float *__restrict__ du_f32,
+                    float *__restrict__ dub)
 {
     pdl_wait();
     constexpr int O = Dims<N>::O;
@@ -137,12 +140,22 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int j = 0; j < N; ++j) gres = fmaf(g[j], ures[j], gres);
     float gpre = dzpre * upre, gpost = dzpost * upost;
+    // this lane's du terms and the sum of their magnitudes
+    const float dupre = a0 * r * dzpre, dupost = a1 * r * dzpost;
+    float dures[N];
+    float sabs = fabsf(dupre) + fabsf(dupost);
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        dures[j] = a2 * r * g[j];
+        sabs += fabsf(dures[j]);
+    }
     // sums over the N lanes of the group
 #pragma unroll
     for (int m = 1; m < N; m <<= 1) {
         gpre += __shfl_xor_sync(kFull, gpre, m);
         gpost += __shfl_xor_sync(kFull, gpost, m);
         gres += __shfl_xor_sync(kFull, gres, m);
+        sabs += __shfl_xor_sync(kFull, sabs, m);
     }
     if (live) {
         // du = alpha_seg r dz, stored as bf16 hi (columns [0,O)) and the bf16
@@ -154,10 +167,10 @@ __global__ void __launch_bounds__(128)
             dut[O + o] = __float2bfloat16_rn(v - __bfloat162float(hi));
             if (du_f32) du_f32[t * O + o] = v;
         };
-        put(i, a0 * r * dzpre);
-        put(N + i, a1 * r * dzpost);
+        put(i, dupre);
+        put(N + i, dupost);
 #pragma unroll
-        for (int j = 0; j < N; ++j) put(2 * N + i * N + j, a2 * r * g[j]);
+        for (int j = 0; j < N; ++j) put(2 * N + i * N + j, dures[j]);
         // columns [2O, 2O+2N): H_post[i] as bf16 hi | lo (the dbias MMA of the
         // residual-gradient pass reads them), then zeros
         const float hp = 2.0f * so;
@@ -169,6 +182,7 @@ __global__ void __launch_bounds__(128)
             const float dr = a0 * gpre + a1 * gpost + a2 * gres;
             const float q = 1.0f / r - eps_rms;
             coef[t] = (q > 0.f) ? -dr * r * r / (float(K) * q) : 0.f;
+            if (dub) dub[t] = sabs;
         }
     }
     // this token's row of the block partial (zeros for a dead token)
@@ -237,12 +251,12 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-// forward workspace: W_hl [2O][K] bf16, partials upart [S][T][O], spart [S][T]
+// forward workspace: W_hl [w_split_rows(n)][K] bf16, partials upart [S][T][O], spart [S][T]
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C)
 {
     const int64_t O = int64_t(n) * n + 2 * n, K = int64_t(n) * C;
     const int64_t S = proj_tc_splits(T, n, K);
-    return ws_align(size_t(2 * O * K) * 2) + ws_align(size_t(S * T * O) * 4) +
+    return ws_align(size_t(w_split_rows(n) * K) * 2) + ws_align(size_t(S * T * O) * 4) +
            ws_align(size_t(S * T) * 4);
 }
 
@@ -258,7 +272,7 @@ static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alp
     const int64_t S = proj_tc_splits(T, N, K);
     char *p = static_cast<char *>(ws);
     bf16 *Whl = reinterpret_cast<bf16 *>(p);
-    p += ws_align(size_t(2 * O * K) * 2);
+    p += ws_align(size_t(w_split_rows(N) * K) * 2);
     float *upart = reinterpret_cast<float *>(p);
     p += ws_align(size_t(S * T * O) * 4);
     float *spart = reinterpret_cast<float *>(p);
@@ -307,12 +321,12 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
 }
 
 // workspace layout of the backward (each piece 256-byte aligned):
-//   du_hl [T][du_cols] bf16, coef [T], partial rows [ceil(T n / 128)][n*n+2n+4],
-//   dH_pre, dH_post [T][n], dH_res [T][n][n] (layer), dbias partials [S][C],
-//   dW partials [S][K][O] (only when S > 1)
+//   du_hl [T][du_cols] bf16, du [T][O] fp32, dub [T], coef [T], partial rows
+//   [ceil(T n / 128)][n*n+2n+4], dH_pre, dH_post [T][n], dH_res [T][n][n]
+//   (layer), dbias partials [S][C], dW partials [S][K][O] (only when S > 1)
 struct BwdWs {
     bf16 *du_hl;
-    float *coef, *part, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
+    float *du32, *dub, *coef, *part, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
     int splits;
     size_t bytes;
 };
@@ -330,6 +344,8 @@ static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
     };
     w.splits = bwd_tc_splits(T, n, C);
     w.du_hl = reinterpret_cast<bf16 *>(take(size_t(T) * bwd_tc_du_cols(n) * 2));
+    w.du32 = reinterpret_cast<float *>(take(size_t(T * O) * 4));
+    w.dub = reinterpret_cast<float *>(take(size_t(T) * 4));
     w.coef = reinterpret_cast<float *>(take(size_t(T) * 4));
     w.part = reinterpret_cast<float *>(take(size_t((T * n + 127) / 128) * bwd_part_cols(n) * 4));
     w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
@@ -382,7 +398,7 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
         MHC_PROF("k_compute_h_bwd", s);
         launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
             dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
-            du_cols, w.coef, w.part, nullptr, nullptr);
+            du_cols, w.coef, w.part, nullptr, w.du32, w.dub);
     }
     // pass 2: residual gradient, dW and dbias on the tensor cores; an unsplit
     // pass writes dW and dbias directly
@@ -391,7 +407,8 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     const int splits_used = (tiles + tps - 1) / tps;
     const bool split = splits_used > 1;
     float *dbias = L ? L->dbias : nullptr;
-    e = launch_bwd_tc(x, W, w.du_hl, w.coef, T, N, C, L ? L->dout : nullptr, L ? L->dy : nullptr,
+    e = launch_bwd_tc(x, W, w.du_hl, w.du32, w.dub, w.coef, T, N, C, L ? L->dout : nullptr,
+                      L ? L->dy : nullptr,
                       L ? L->Hpre : nullptr, L ? L->Hres : nullptr, L ? L->Hpost : nullptr, dx,
                       split ? w.dWpart : dW, (split || !dbias) ? w.dbiaspart : dbias,
                       splits_used, fault, s);
@@ -469,7 +486,7 @@ cudaError_t launch_proj_partial_sums(const bf16 *x, const float *W, int64_t T, i
     const int64_t S = proj_tc_splits(T, n, K);
     char *p = static_cast<char *>(ws);
     bf16 *Whl = reinterpret_cast<bf16 *>(p);
-    p += ws_align(size_t(2 * O * K) * 2);
+    p += ws_align(size_t(w_split_rows(n) * K) * 2);
     float *upart = reinterpret_cast<float *>(p);
     p += ws_align(size_t(S * T * O) * 4);
     float *spart = reinterpret_cast<float *>(p);
@@ -529,7 +546,7 @@ static cudaError_t compute_h_bwd_impl(const float *dHpre, const float *dHpost,
         MHC_PROF("k_compute_h_bwd", s);
         launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
             dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters, eps_sk, eps_rms, du_hl,
-            bwd_tc_du_cols(N), coef, part, s_tot, du);
+            bwd_tc_du_cols(N), coef, part, s_tot, du, nullptr);
     }
     {
         MHC_PROF("k_bwd_finalize", s);
@@ -552,15 +569,21 @@ cudaError_t launch_compute_h_bwd(const float *dHpre, const float *dHpost, const 
                                  eps_rms, du, coef, dalpha, db, ws, s);
 }
 
-// du (fp32 [T][O]) -> du_hl rows: bf16 hi | lo, zeros for the rest of the row
+// du (fp32 [T][O]) -> du_hl rows: bf16 hi | lo, zeros for the rest of the
+// row; the element at column 0 also writes dub[t] = sum_o |du[t][o]|
 __global__ void k_du_split(const float *__restrict__ du, int64_t T, int O, int du_cols,
-                           bf16 *__restrict__ du_hl)
+                           bf16 *__restrict__ du_hl, float *__restrict__ dub)
 {
     pdl_wait();
     const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= T * du_cols) return;
     const int64_t t = e / du_cols;
     const int c = int(e % du_cols);
+    if (c == 0) {
+        float sabs = 0.f;
+        for (int o = 0; o < O; ++o) sabs += fabsf(__ldg(du + t * O + o));
+        dub[t] = sabs;
+    }
     bf16 v = __float2bfloat16_rn(0.f);
     if (c < 2 * O) {
         const float d = __ldg(du + t * O + (c % O));
@@ -581,14 +604,14 @@ cudaError_t launch_proj_partial_bwd(const bf16 *x, const float *W, const float *
     const int du_cols = bwd_tc_du_cols(n);
     {
         MHC_PROF("k_du_split", s);
-        launch_k(k_du_split, dim3(unsigned((T * du_cols + 255) / 256)), dim3(256), 0, s, du, T, int(O), du_cols,
-                                                                       w.du_hl);
+        launch_k(k_du_split, dim3(unsigned((T * du_cols + 255) / 256)), dim3(256), 0, s, du, T,
+                 int(O), du_cols, w.du_hl, w.dub);
     }
     const int tiles = int((T + 127) / 128);
     const int tps = (tiles + w.splits - 1) / w.splits;
     const int splits_used = (tiles + tps - 1) / tps;
     const bool split = splits_used > 1;
-    cudaError_t e = launch_bwd_tc(x, W, w.du_hl, coef, T, n, Cs, nullptr, nullptr, nullptr,
+    cudaError_t e = launch_bwd_tc(x, W, w.du_hl, du, w.dub, coef, T, n, Cs, nullptr, nullptr, nullptr,
                                   nullptr, nullptr, dx, split ? w.dWpart : dW, w.dbiaspart,
                                   splits_used, fault, s);
     if (e != cudaSuccess) return e;

@@ -4,19 +4,34 @@
 //
 // Megatron's fused projection runs this on TF32 MMA with split-K (RL-Kernel
 // PR #383, follow-up commit on the Megatron mHC source).  Here the operands
-// are bf16: x is already bf16, and W (fp32) is split into W_hi = bf16(W) and
-// W_lo = bf16(W - W_hi), stacked as 2*O rows of one B operand, so one MMA of
-// N = 2*O gives x.W_hi and x.W_lo and their fp32 sum carries W to ~2^-17
-// relative error (x.W in fp32 semantics, well inside the 1e-5 bound on H).
+// are bf16: x is already bf16, and W (fp32, 24 significant bits) is split
+// into three bf16 terms W_hi = bf16(W), W_lo = bf16(W - W_hi), W_lo2 =
+// bf16(W - W_hi - W_lo), stacked as 3*O rows (zero-padded to a multiple of
+// 16) of one B operand.  One MMA gives x.W_hi, x.W_lo and x.W_lo2; every
+// product of bf16 values is exact in the fp32 accumulator and the three
+// terms carry W to ~2^-24 relative.  (Two terms leave ~2^-17 of W per
+// product, which at alpha = 1 and K = 57344 moves H by ~3e-5.)
+//
+// What remains is the accumulation.  The tensor core's fp32 accumulator
+// loses about an ulp of the running sum per K step (measured on GB300: u's
+// error grows with the number of K steps a split accumulates, ~1e-4 after
+// 112 steps at |u| ~ 50), so the large x.W_hi term is never accumulated
+// across k-blocks in TMEM: each 64-wide k-block's x.W_hi goes to one of two
+// TMEM buffers and the epilogue warps add it into fp32 registers (round to
+// nearest) while the MMAs fill the other buffer.  x.W_lo and x.W_lo2 (2^-8
+// and 2^-16 of the sum) accumulate over the whole split in a third
+// accumulator, whose accumulation error is that much smaller.
 //
 // CTA: BM tokens (128 at n = 4, 256 at n = 8) x one K split (K splits chosen
 // for about MINB CTAs per SM); 2 + BM/32 warps:
-//   warp 0      TMA producer: x tile [BM x 64] and W_hl tile [2O x 64] per
+//   warp 0      TMA producer: x tile [BM x 64] and W_hl tile [NB x 64] per
 //               stage, both in the 128-byte swizzle layout
-//   warp 1      TMEM allocation, MMA issue (one thread, BM/128 MMAs per k
-//               step sharing the W_hl operand), commits
-//   warps 2..   sum of squares of their token rows from the same smem tiles
-//               while the MMAs run; then the epilogue (TMEM -> partials)
+//   warp 1      TMEM allocation, MMA issue (one thread; per k step and
+//               128-row half: x.W_hi, x.W_lo, x.W_lo2 as three MMAs of N = NH
+//               sharing the stage's W_hl operand), commits
+//   warps 2..   per k-block: the sum of squares of their token rows from the
+//               same smem tiles, then the k-block's x.W_hi from TMEM into
+//               registers; finally the epilogue (TMEM -> partials)
 // Every wait is bounded; a timeout reports a fault code and the CTA unwinds.
 #include "launch.h"
 #include "tc.cuh"
@@ -28,49 +43,77 @@ namespace mhc {
 // back, so each token row is read in KBS*128 contiguous bytes); STG stages;
 // MINB CTAs per SM; BM tokens per CTA, in MMAs of 128 rows that share the
 // stage's W_hl tile (BM = 256 at n = 8, where the W_hl tile of a k-block,
-// 2O = 160 rows, is larger than 128 rows of x).
-template <int N, int KBS_, int STG_, int MINB_, int BM_ = 128>
+// 240 rows, is larger than 128 rows of x).
+template <int N, int KBS_, int STG_, int MINB_, int BM_ = 128, int G_ = 1>
 struct ProjTcCfg {
+    static constexpr int G = G_;   // stages per x.W_hi buffer (drained every G stages)
     static constexpr int O = N * N + 2 * N;
-    static constexpr int NB = 2 * O;  // MMA N: hi rows then lo rows (48 or 160)
+    static constexpr int NB = w_split_rows(N);  // MMA N: hi, lo, lo2 rows, zero rows (80 or 240)
     static constexpr int BM = BM_, BK = 64, KBS = KBS_, STAGES = STG_, MINB = MINB_;
     static constexpr int MH = BM / 128;               // MMAs of 128 rows per k step
     static constexpr int A_SUB = BM * BK * 2;
     static constexpr int B_SUB = NB * BK * 2;
     static constexpr int A_BYTES = KBS * A_SUB;
     static constexpr int STAGE = KBS * (A_SUB + B_SUB);  // multiple of 1024
-    static constexpr int ACC_COLS = NB <= 64 ? 64 : 256;  // TMEM columns per accumulator
+    // TMEM per 128-row half: HB x.W_hi buffers of NH columns (NH = O
+    // rounded up to 16: 32 / 80) and the accumulator of [x.W_lo | x.W_lo2]
+    // (NL = 2O columns: W_hl rows [O, 3O) in one MMA).  n = 4: two x.W_hi
+    // buffers; n = 8 (two halves of 240 columns in 512): one.
+    static constexpr int NH = (O + 15) / 16 * 16, NL = 2 * O;
+    static constexpr int HB = 3 * NH + NL <= 256 / MH ? 2 : 1;
+    static constexpr int HI0 = 0, HI1 = NH, LO = HB * NH;
+    static constexpr int ACC_COLS = LO + NL <= 128 ? 128 : 256;   // TMEM columns per half
     static constexpr int TMEM_COLS = MH * ACC_COLS;
+    static_assert(LO + NL <= ACC_COLS && NH <= NB && 3 * O <= NB && NL % 16 == 0, "accumulators");
     static constexpr int EPI_WARPS = 4 * MH;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 512 /*barriers*/;
     static_assert(A_SUB % 1024 == 0 && B_SUB % 1024 == 0, "sub-tiles keep 1024-byte alignment");
     static_assert(BM == 128 || BM == 256, "tile rows");
     static_assert(SMEM * MINB <= 232448, "shared memory");
 };
 template <int N> struct ProjTcSel;
-template <> struct ProjTcSel<4> { using type = ProjTcCfg<4, 1, 4, 2>; };
-template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 2, 2, 1, 256>; };
+// x.W_hi drained every 4 stages (16 K steps): at n = 8 draining every stage
+// took 0.244 ms for the op at T=8192, C=7168, every 4 stages 0.232, every 8
+// 0.230, with the error on u growing from 1.0e-5 to 2.3e-5 (alpha = 1,
+// K = 57344); three separate MMAs of N = 80 for hi, lo and lo2 (x read from
+// shared memory three times) took 0.29.
+template <> struct ProjTcSel<4> { using type = ProjTcCfg<4, 1, 4, 2, 128, 4>; };
+template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 1, 3, 1, 256, 4>; };
 template <int N>
 using ProjTc = typename ProjTcSel<N>::type;
 
-// W [K][O] fp32 -> W_hl [2O][K] bf16 (rows o: bf16(W[:,o]); rows O+o: the
-// remainder).  n = 4: one thread per k (8.3 us at K = 16384; the tiled form
-// below, with 256 blocks, took 9.6).
+// The three bf16 terms of one fp32 weight: hi = bf16(w), lo = bf16(w - hi),
+// lo2 = bf16(w - hi - lo).  Both differences are exact in fp32 (each is a
+// rounding error of a value that fits in 24 bits), so hi + lo + lo2 equals w
+// to within 2^-24 relative.
+__device__ __forceinline__ void w_terms(float w, float &hi, float &lo, float &lo2)
+{
+    hi = __bfloat162float(__float2bfloat16_rn(w));
+    const float r1 = w - hi;
+    lo = __bfloat162float(__float2bfloat16_rn(r1));
+    lo2 = __bfloat162float(__float2bfloat16_rn(r1 - lo));
+}
+
+// W [K][O] fp32 -> W_hl [NB][K] bf16 (rows o: hi; rows O+o: lo; rows 2O+o:
+// lo2; rows 3O..NB: zero).  n = 4: one thread per k (the tiled form below,
+// with 256 blocks, was slower at n = 4).
 __global__ void k_w_split4(const float *__restrict__ W, bf16 *__restrict__ Whl, int64_t K)
 {
     pdl_wait();
-    constexpr int O = 24;
+    constexpr int O = 24, NB = w_split_rows(4);
     const int64_t k = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     if (k >= K) return;
 #pragma unroll 4
     for (int o = 0; o < O; ++o) {
-        const float w = __ldg(W + k * O + o);
-        const bf16 hi = __float2bfloat16_rn(w);
-        const bf16 lo = __float2bfloat16_rn(w - __bfloat162float(hi));
-        Whl[int64_t(o) * K + k] = hi;
-        Whl[int64_t(O + o) * K + k] = lo;
+        float hi, lo, lo2;
+        w_terms(__ldg(W + k * O + o), hi, lo, lo2);
+        Whl[int64_t(o) * K + k] = __float2bfloat16_rn(hi);
+        Whl[int64_t(O + o) * K + k] = __float2bfloat16_rn(lo);
+        Whl[int64_t(2 * O + o) * K + k] = __float2bfloat16_rn(lo2);
     }
+#pragma unroll
+    for (int o = 3 * O; o < NB; ++o) Whl[int64_t(o) * K + k] = __float2bfloat16_rn(0.f);
 }
 
 // n = 8: a block transposes a tile of 64 k rows through shared memory:
@@ -91,17 +134,19 @@ __global__ void __launch_bounds__(256) k_w_split(const float *__restrict__ W, bf
     const int kn = int(K - k0 < kWsplitK ? K - k0 : kWsplitK);   // a multiple of 8
     for (int i = threadIdx.x; i < kn * O; i += blockDim.x) ws[(i / O) * OP + i % O] = __ldg(W + k0 * O + i);
     __syncthreads();
-    // item: output row ro (o, hi or lo) and 8-wide group kg of the tile's k
-    for (int it = threadIdx.x; it < 2 * O * (kWsplitK / 8); it += blockDim.x) {
+    // item: output row ro (o of the hi, lo or lo2 rows; zero rows past 3O)
+    // and 8-wide group kg of the tile's k
+    constexpr int NB = w_split_rows(N);
+    for (int it = threadIdx.x; it < NB * (kWsplitK / 8); it += blockDim.x) {
         const int ro = it / (kWsplitK / 8), kg = it % (kWsplitK / 8);
         if (kg * 8 >= kn) continue;
-        const int o = ro < O ? ro : ro - O;
+        const int part = ro / O, o = ro % O;
         float v[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const float w = ws[(kg * 8 + e) * OP + o];
-            const bf16 hi = __float2bfloat16_rn(w);
-            v[e] = ro < O ? w : w - __bfloat162float(hi);
+            float hi = 0.f, lo = 0.f, lo2 = 0.f;
+            if (part < 3) w_terms(ws[(kg * 8 + e) * OP + o], hi, lo, lo2);
+            v[e] = part == 0 ? hi : part == 1 ? lo : lo2;
         }
         *reinterpret_cast<uint4 *>(Whl + int64_t(ro) * K + k0 + kg * 8) = pack8(v);
     }
@@ -120,7 +165,9 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + P::STAGES * P::STAGE);
     uint64_t *empty = full + P::STAGES;
     uint64_t *acc_bar = empty + P::STAGES;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_bar + 1);
+    uint64_t *hifull = acc_bar + 1;     // [HB] a group's x.W_hi is in buffer b
+    uint64_t *hiempty = hifull + 2;     // [HB] the epilogue has drained buffer b
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(hiempty + 2);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -133,9 +180,15 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
+            // the MMAs' commit + every epilogue thread once it has read the
+            // stage (tc::mbar_release)
+            tc::mbar_init(&empty[s], 1 + 32 * P::EPI_WARPS);
         }
         tc::mbar_init(acc_bar, 1);
+        for (int hb = 0; hb < 2; ++hb) {
+            tc::mbar_init(&hifull[hb], 1);
+            tc::mbar_init(&hiempty[hb], P::EPI_WARPS);
+        }
         *abort_flag = 0;
         tc::fence_barrier_init();
         tc::tma_prefetch_desc(&tmx);
@@ -175,9 +228,13 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(128, P::NB);
+            constexpr uint32_t idesc_hi = tc::idesc_bf16_f32(128, P::NH);
+            constexpr uint32_t idesc_lo = tc::idesc_bf16_f32(128, P::NL);
+            constexpr int O = P::O;
             for (int i = 0; i < nkb; ++i) {
-                const int s = i % P::STAGES;
+                // stage i belongs to group g = i / G, whose x.W_hi goes to buffer hb
+                const int s = i % P::STAGES, g = i / P::G, hb = g % P::HB;
+                const bool first = i % P::G == 0, last = i % P::G == P::G - 1 || i == nkb - 1;
                 if (*abort_flag ||
                     !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, fault, tc::kFaultTimeoutFull)) {
                     *abort_flag = 1;
@@ -185,6 +242,10 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
                 }
                 tc::tc_fence_after();
                 const uint32_t a0 = tc::smem_u32(smem + s * P::STAGE);
+                // [x.W_lo | x.W_lo2] first (W_hl rows [O, 3O): a multiple of 8
+                // rows, so the operand starts on a 1024-byte swizzle group),
+                // which keeps the tensor cores busy while the epilogue drains
+                // the x.W_hi buffer
 #pragma unroll
                 for (int j = 0; j < P::KBS; ++j) {
                     const uint32_t a = a0 + j * P::A_SUB, b = a0 + P::A_BYTES + j * P::B_SUB;
@@ -192,12 +253,33 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
                     for (int kk = 0; kk < P::BK / 16; ++kk)
 #pragma unroll
                         for (int h = 0; h < P::MH; ++h)
-                            tc::mma_bf16(tmem + h * P::ACC_COLS,
+                            tc::mma_bf16(tmem + h * P::ACC_COLS + P::LO,
                                          tc::desc_kmajor_sw128(a + h * 128 * 128 + kk * 32),
-                                         tc::desc_kmajor_sw128(b + kk * 32), idesc,
+                                         tc::desc_kmajor_sw128(b + O * 128 + kk * 32), idesc_lo,
                                          (i > 0 || j > 0 || kk > 0) ? 1u : 0u);
                 }
+                // x.W_hi buffer hb must have been drained (group g - HB)
+                if (first && g >= P::HB &&
+                    !tc::mbar_wait(&hiempty[hb], ((g / P::HB) - 1) & 1, fault,
+                                   tc::kFaultTimeoutAcc)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < P::KBS; ++j) {
+                    const uint32_t a = a0 + j * P::A_SUB, b = a0 + P::A_BYTES + j * P::B_SUB;
+#pragma unroll
+                    for (int kk = 0; kk < P::BK / 16; ++kk)
+#pragma unroll
+                        for (int h = 0; h < P::MH; ++h)
+                            tc::mma_bf16(tmem + h * P::ACC_COLS + (hb ? P::HI1 : P::HI0),
+                                         tc::desc_kmajor_sw128(a + h * 128 * 128 + kk * 32),
+                                         tc::desc_kmajor_sw128(b + kk * 32), idesc_hi,
+                                         (!first || j > 0 || kk > 0) ? 1u : 0u);
+                }
                 tc::mma_commit(&empty[s]);
+                if (last) tc::mma_commit(&hifull[hb]);
             }
             tc::mma_commit(acc_bar);
             tc::mbar_wait(acc_bar, 0, fault, tc::kFaultTimeoutAcc);
@@ -208,7 +290,12 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
         const int q = warp & 3;
         const int hh = (warp - 2) >> 2;
         const int r = hh * 128 + q * 32 + lane;
+        const uint32_t trow = tmem + hh * P::ACC_COLS + (uint32_t(q * 32) << 16);
+        constexpr int O = P::O;
         float ssq = 0.f;
+        float uhi[O];   // sum over this split's k-blocks of x.W_hi, in fp32 (round to nearest)
+#pragma unroll
+        for (int o = 0; o < O; ++o) uhi[o] = 0.f;
         bool ok = true;
         for (int i = 0; i < nkb; ++i) {
             const int s = i % P::STAGES;
@@ -233,51 +320,52 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
                     for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
                 }
             }
+            tc::mbar_release(&empty[s]);
+            // at the end of a group: its x.W_hi into the registers, then the
+            // buffer goes back
+            const int g = i / P::G, hb = g % P::HB;
+            if (i % P::G != P::G - 1 && i != nkb - 1) continue;
+            if (*abort_flag ||
+                !tc::mbar_wait(&hifull[hb], (g / P::HB) & 1, fault, tc::kFaultTimeoutAcc)) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            tc::tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < P::NH / 16; ++c) {
+                float w[16];
+                tc::tmem_ld16_wait(trow + (hb ? P::HI1 : P::HI0) + c * 16, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (c * 16 + e < O) uhi[c * 16 + e] += w[e];
+            }
+            tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[s]);
+            if (lane == 0) tc::mbar_arrive(&hiempty[hb]);
         }
         if (ok && !tc::mbar_wait(acc_bar, 0, fault, tc::kFaultTimeoutAcc)) ok = false;
         tc::tc_fence_after();
         const int64_t t = m0 + r;
-        const uint32_t trow = tmem + hh * P::ACC_COLS + (uint32_t(q * 32) << 16);
-        constexpr int O = P::O;
-        if (N == 4) {
-            float v[48];
+        // u = sum over groups of x.W_hi + (x.W_lo + x.W_lo2)
+        {
+            float lo[O];
 #pragma unroll
-            for (int c = 0; c < 3; ++c) {
-                float w[16];
-                tc::tmem_ld16(trow + c * 16, w);
-                tc::tmem_ld_wait();
+            for (int c = 0; c < O / 8; ++c) {
+                float w[8], w2[8];
+                tc::tmem_ld8x2_wait(trow + P::LO + c * 8, trow + P::LO + O + c * 8, w, w2);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) v[c * 16 + e] = w[e];
+                for (int e = 0; e < 8; ++e) lo[c * 8 + e] = w[e] + w2[e];
             }
-            if (ok && t < T) {
-                float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
 #pragma unroll
-                for (int o4 = 0; o4 < O / 4; ++o4)
-                    dst[o4] = make_float4(v[4 * o4] + v[O + 4 * o4], v[4 * o4 + 1] + v[O + 4 * o4 + 1],
-                                          v[4 * o4 + 2] + v[O + 4 * o4 + 2],
-                                          v[4 * o4 + 3] + v[O + 4 * o4 + 3]);
-                spart[int64_t(split) * T + t] = ssq;
-            }
-        } else {
-#pragma unroll 1
-            for (int c = 0; c < O / 16; ++c) {
-                float hi[16], lo[16];
-                tc::tmem_ld16(trow + c * 16, hi);
-                tc::tmem_ld16(trow + O + c * 16, lo);
-                tc::tmem_ld_wait();
-                if (ok && t < T) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        upart + (int64_t(split) * T + t) * O + c * 16);
+            for (int o = 0; o < O; ++o) uhi[o] += lo[o];
+        }
+        if (ok && t < T) {
+            float4 *dst = reinterpret_cast<float4 *>(upart + (int64_t(split) * T + t) * O);
 #pragma unroll
-                    for (int o4 = 0; o4 < 4; ++o4)
-                        dst[o4] = make_float4(hi[4 * o4] + lo[4 * o4], hi[4 * o4 + 1] + lo[4 * o4 + 1],
-                                              hi[4 * o4 + 2] + lo[4 * o4 + 2],
-                                              hi[4 * o4 + 3] + lo[4 * o4 + 3]);
-                }
-            }
-            if (ok && t < T) spart[int64_t(split) * T + t] = ssq;
+            for (int o4 = 0; o4 < O / 4; ++o4)
+                dst[o4] = make_float4(uhi[4 * o4], uhi[4 * o4 + 1], uhi[4 * o4 + 2], uhi[4 * o4 + 3]);
+            spart[int64_t(split) * T + t] = ssq;
         }
     }
     tc::tc_fence_before();

@@ -145,15 +145,23 @@ cudaError_t launch_bwd_tok(const bf16 *dout, const bf16 *x, const bf16 *f, const
 // k_bwd_tc.cu: residual-gradient pass of the backward on the tensor cores
 int bwd_tc_du_cols(int n);
 int bwd_tc_splits(int64_t T, int n, int64_t C);
-cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *coef,
-                          int64_t T, int n, int64_t C, const bf16 *dout,
+// du32 [T][O] fp32 and dub [T] = sum_o |du| serve the exact path of tokens
+// whose bf16 product would be too coarse (see k_bwd_tc.cu).
+cudaError_t launch_bwd_tc(const bf16 *x, const float *W, const bf16 *du_hl, const float *du32,
+                          const float *dub, const float *coef, int64_t T, int n, int64_t C,
+                          const bf16 *dout,
                           const bf16 *dy, const float *Hpre, const float *Hres,
                           const float *Hpost, bf16 *dx, float *dWpart, float *dbiaspart,
                           int splits, int *fault, cudaStream_t s);
 
 // k_proj.cu
 size_t proj_fwd_ws_bytes(int64_t T, int n, int64_t C);
-// W [K][O] fp32 -> W_hl [2O][K] bf16 (hi rows, then remainder rows)
+// Rows of W_hl: W as three bf16 terms (hi, lo, lo2: 3O rows), padded with
+// zero rows to the MMA's N granularity of 16 (80 at n = 4, 240 at n = 8).
+__host__ __device__ constexpr int w_split_rows(int n) { return (3 * (n * n + 2 * n) + 15) / 16 * 16; }
+// W [K][O] fp32 -> W_hl [w_split_rows(n)][K] bf16: rows o = bf16(W[:,o]),
+// rows O+o = bf16 of the remainder, rows 2O+o = bf16 of what is left, then
+// zero rows
 cudaError_t launch_w_split(const float *W, bf16 *Whl, int n, int64_t K, cudaStream_t s);
 // compute_h forward from S split partials upart [S][T][O], spart [S][T]
 cudaError_t launch_compute_h_parts(const float *upart, const float *spart, int S,

@@ -211,12 +211,12 @@ def _shard_np(x, W, C, c0, c1):
 
 
 # "stress" draws alpha = 1, b ~ N(0, 1), W ~ N(0, 0.05), so the gates and the
-# Sinkhorn leave their near-uniform regime; at K = 4096 that makes H sensitive
-# to the ~1e-5 absolute rounding of u (alpha r du), so the 4-shard case uses
-# the workloads' alpha = 0.01, W ~ N(0, 0.02).
+# Sinkhorn leave their near-uniform regime and H is sensitive to the rounding
+# of u; the 4-shard case reaches the 7B-scale K = 4096 under it.
 @pytest.mark.parametrize("T,n,C,cuts,stress", [(256, 4, 256, [0, 128, 256], True),
                                                (129, 4, 264, [0, 128, 264], True),
                                                (67, 8, 136, [0, 64, 136], True),
+                                               (300, 4, 1024, [0, 256, 512, 768, 1024], True),
                                                (300, 4, 1024, [0, 256, 512, 768, 1024], False)])
 def test_sharded_proj_rms(M, orc, T, n, C, cuts, stress):
     O = n * n + 2 * n
@@ -369,19 +369,51 @@ def test_post_bda_compute_h_fused(M, orc, T, n, C):
 
 
 def _check_post_proj(orc, p, o, n, idx):
-    """out against the oracle's post-mix; the next layer's H against the
-    oracle's proj_rms_compute_h of the out the kernel stored.  The bf16
-    rounding of out is a quantisation decision: an fp32 sum next to a
-    rounding midpoint may round the other way than the exact value (one bf16
-    ulp), and with alpha near 1 that moves H by ~1e-4, so the oracle's second
-    stage takes the kernel's decision, as the next layer would."""
+    """Two checks.
+
+    1. Against the oracle's own composition (h_post_bda_compute_h_fwd: the
+       fp64 post-mix, rounded by the oracle's bf16_rne, then the next
+       layer's proj_rms_compute_h).  The bf16 rounding of out is a
+       quantisation decision: where the exact sum lies next to a rounding
+       midpoint the kernel's fp32 sum may round the other way (one bf16 ulp),
+       and with alpha near 1 that moves that token's H by ~1e-4.  So: the
+       elements of the stored out that differ from the oracle's rounded out
+       are counted (a small fraction: an fp32 sum lands that close to a
+       midpoint about once in 1e4 elements; each at most one bf16 ulp
+       apart), and H, u, r meet their tolerances on every token without
+       such an element.
+    2. The next layer's H, u, r against the oracle's proj_rms_compute_h of
+       the out the kernel stored (the decision taken in the kernel's
+       precision, as the next layer sees it), on every token."""
     ti = torch.from_numpy(np.arange(o["out"].shape[0])[idx]).cuda()
+    Tn = int(ti.numel())
     res = p["res"][idx]
-    out_ref = orc.h_post_bda_fwd(_f64(res), _f64(p["f"][idx]), _f64(p["bias"]), p["Hres"][idx],
-                                 p["Hpost"][idx])
-    err_bf16(o["out"][ti], out_ref)
-    h = orc.proj_rms_compute_h_fwd(host(o["out"][ti]), p["W2"], p["a2"], p["b2"], n, ITERS,
-                                   EPS_SK, EPS_RMS)
+    comp = orc.h_post_bda_compute_h_fwd(_f64(res), _f64(p["f"][idx]), _f64(p["bias"]),
+                                        p["Hres"][idx], p["Hpost"][idx], p["W2"], p["a2"],
+                                        p["b2"], n, ITERS, EPS_SK, EPS_RMS)
+    out_k = host(o["out"][ti])
+    err_bf16(out_k, comp["out"])
+    # 1: the oracle's composition
+    xr = comp["x_next"].reshape(Tn, -1)
+    diff = out_k.reshape(Tn, -1) != xr
+    flipped = np.any(diff, axis=1)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(xr), 2.0 ** -126))) - 7)
+    # where the post-mix cancels, the fp32 sum's own rounding (a few 2^-24 of
+    # the sum of the terms' magnitudes) can exceed one ulp of the result
+    terms = (np.abs(p["Hpost"][idx])[:, :, None] * np.abs(_f64(p["f"][idx]) + _f64(p["bias"]))[:, None, :]
+             + np.einsum("tji,tjc->tic", np.abs(p["Hres"][idx]).astype(np.float64), np.abs(_f64(res))))
+    slack = np.maximum(ulp, 2.0 ** -20 * terms.reshape(Tn, -1))
+    assert np.all(np.abs(out_k.reshape(Tn, -1) - xr)[diff] <= slack[diff]), \
+        "stored out differs from the oracle's rounding by more than one bf16 ulp"
+    nflip = int(diff.sum())
+    assert nflip <= max(4, diff.size // 1000), f"{nflip} of {diff.size} elements rounded apart"
+    keep = ~flipped
+    for k in ("H_pre", "H_post", "H_res"):
+        err_h(host(o[k][ti])[keep], comp[k][keep])
+    err_grad(host(o["u"][ti])[keep], comp["u"][keep])
+    err_grad(host(o["r"][ti])[keep], comp["r"][keep])
+    # 2: the oracle's second stage on the out the kernel stored
+    h = orc.proj_rms_compute_h_fwd(out_k, p["W2"], p["a2"], p["b2"], n, ITERS, EPS_SK, EPS_RMS)
     for k in ("H_pre", "H_post", "H_res"):
         err_h(o[k][ti], h[k])
     err_grad(o["u"][ti], h["u"])

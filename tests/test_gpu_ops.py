@@ -77,8 +77,12 @@ def test_sinkhorn_batched_8x4096(M, orc):
 # proj_rms_compute_h
 # ---------------------------------------------------------------------------
 
+# Every shape runs with the workload draw and with the "stress" draw (alpha =
+# 1, b ~ N(0, 1), W ~ N(0, 0.05)); the last two reach the 7B-scale K = 4096
+# and the wide K = 57344, where the projection's accuracy decides whether H
+# meets 1e-5 off the near-uniform regime.
 SHAPES = [(256, 4, 256, 0), (1, 4, 8, 1), (3, 8, 8, 2), (129, 4, 264, 3), (67, 8, 64, 4),
-          (200, 8, 136, 5)]
+          (200, 8, 136, 5), (300, 4, 1024, 6), (160, 8, 7168, 7)]
 
 
 def _proj_inputs(T, n, C, seed, stress):
@@ -358,7 +362,7 @@ def test_layer_multi_tile(M, orc, T, n, C, seed):
     check_layer(o, ref_f, ref_b)
 
 
-@pytest.mark.parametrize("n,C", [(4, 264), (8, 136)])
+@pytest.mark.parametrize("n,C", [(4, 264), (8, 136), (4, 1024), (8, 1032)])
 def test_layer_zero_rows(M, orc, n, C):
     """Tokens whose residual rows are all zero (the first token, one inside a
     128-token tile, the last): r = 1/eps_rms and z = b in the forward, the RMS
@@ -378,25 +382,15 @@ def test_layer_zero_rows(M, orc, n, C):
     err_bf16(o["df"], ref_b["df"])
     for k in ("dW", "dalpha", "db", "dbias"):
         err_grad(o[k], ref_b[k])
-    # dx: at a zero row r = 1/eps, so du = alpha r dz is ~1e4 and the terms
-    # du[o] W[k][o] of dx cancel to values ~1e-1.  The kernel carries du and W
-    # as bf16 hi + lo (each to ~2^-17 relative; the dropped lo*lo term is
-    # ~2^-18), so its error is bounded by ~2^-16 * sum_o |du[o] W[k][o]|; the
-    # test allows 2^-15 times that sum on top of the bf16 tolerance (for the
-    # other rows the sum is ~1 and the term negligible).
-    K = n * C
-    xs = mi.bf16_bits_to_f32(inp["x"]).astype(np.float64).reshape(T, K)
-    du = orc.compute_h_bwd_from_sums(ref_b["dH_pre"], ref_b["dH_post"], ref_b["dH_res"],
-                                     ref_f["u"], np.sum(xs * xs, axis=1), K, inp["alpha"],
-                                     inp["b"], n, ITERS, EPS_SK, EPS_RMS)["du"]
-    scale = (np.abs(du) @ np.abs(inp["W"].astype(np.float64)).T).reshape(T, n, C)
-    g = host(o["dx"])
+    # dx at the plain bf16 tolerance on every row.  At a zero row r = 1/eps,
+    # so du = alpha r dz is ~1e5 and dx_proj = du W^T reaches ~1e4 while many
+    # of its elements cancel to O(1): a bf16 two-term product would be off by
+    # ~0.1 there, so these tokens take the kernel's exact path.
+    err_bf16(o["dx"], ref_b["dx"])
     r = ref_b["dx"]
-    tol = mi.SPEC["tolerances"]
-    excess = np.abs(g - r) - (tol["bf16_abs"] + tol["bf16_rel"] * np.abs(r) + 2.0 ** -15 * scale)
-    assert np.all(np.isfinite(g)) and float(np.max(excess)) <= 0.0, \
-        f"dx beyond the derived bound at {np.unravel_index(np.argmax(excess), r.shape)}"
-    assert float(np.max(scale[0])) > 1e3  # the zero rows do carry the large terms
+    big = float(np.max(np.abs(r[0])))
+    assert big > 1e3  # the zero rows do carry the large terms
+    assert float(np.min(np.abs(r[0]))) < 1e-3 * big  # and elements that cancel
 
 
 @pytest.mark.parametrize("n,C", [(4, 256), (8, 64)])
