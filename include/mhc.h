@@ -449,11 +449,19 @@ MHC_API mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const
  * computation and outputs, with the scratch taken from the library's fixed
  * array.  Calls that would need more scratch than MHC_NOALLOC_SCRATCH_BYTES
  * (mhc_workspace_bytes(MHC_OP_PROJ_RMS_COMPUTE_H_FWD, T, n, C)) return
- * MHC_ERR_WORKSPACE_TOO_SMALL without launching anything.  Allocates no
- * memory.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) for that device; make it before any stream
- * capture.  All calls share the one array: calls that overlap on the GPU
- * race on it and must be ordered by the caller (same stream, or events). */
+ * MHC_ERR_WORKSPACE_TOO_SMALL without launching anything.  The size needed
+ * grows with T and C and depends on mhc_set_batch_invariant (which fixes the
+ * number of K splits): T = 16384, n = 4, C = 4096 needs about 5.9 MB by
+ * default, 8.75 MB (rejected) in batch-invariant mode; at n = 8 only small
+ * T and C fit (the split copy of W takes 3840 * C bytes, the partial sums up
+ * to 32 * T * 320 bytes).  Allocates no memory.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) for that device and caches it; make it before any
+ * stream capture.  The cached address belongs to the context current at
+ * that first call (the primary context, for CUDA-runtime users) and is not
+ * valid after cudaDeviceReset.  All calls share the one array: calls that
+ * overlap on the GPU race on it and must be ordered by the caller (same
+ * stream, or events). */
 MHC_API mhc_status mhc_proj_rms_compute_h_fwd_noalloc(const mhc_bf16 *x, const float *W,
                                                       const float *alpha3, const float *b,
                                                       int64_t T, int n, int64_t C, int iters,

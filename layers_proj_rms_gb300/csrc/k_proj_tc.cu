@@ -33,6 +33,8 @@
 //               same smem tiles, then the k-block's x.W_hi from TMEM into
 //               registers; finally the epilogue (TMEM -> partials)
 // Every wait is bounded; a timeout reports a fault code and the CTA unwinds.
+#include <atomic>
+
 #include "launch.h"
 #include "tc.cuh"
 #include "tmap.h"
@@ -380,10 +382,13 @@ __global__ void __launch_bounds__(P::THREADS, P::MINB)
 // splits), so a token's u and s, and everything computed from them, do not
 // depend on how many tokens share the call.  Otherwise the split count is
 // chosen for about MINB CTAs per SM, which depends on T.
-static int g_batch_invariant = 0;
+// The flag is process-wide and atomic: a thread that sets it while another
+// launches reads either value, never a torn one (calls that must see the new
+// mode should be ordered after the setter by the caller).
+static std::atomic<int> g_batch_invariant{0};
 
-void set_batch_invariant(int on) { g_batch_invariant = on ? 1 : 0; }
-int batch_invariant() { return g_batch_invariant; }
+void set_batch_invariant(int on) { g_batch_invariant.store(on ? 1 : 0, std::memory_order_relaxed); }
+int batch_invariant() { return g_batch_invariant.load(std::memory_order_relaxed); }
 
 int proj_tc_splits(int64_t T, int n, int64_t K)
 {
@@ -391,7 +396,7 @@ int proj_tc_splits(int64_t T, int n, int64_t K)
     const int64_t mt = (T + bm - 1) / bm;
     const int64_t kb = (K + 63) / 64;
     const int minb = n == 4 ? ProjTc<4>::MINB : ProjTc<8>::MINB;
-    int64_t s = g_batch_invariant ? (kb + 63) / 64
+    int64_t s = batch_invariant() ? (kb + 63) / 64
                                   : (int64_t(kSplitSms) * minb) / (mt > 0 ? mt : 1);
     if (s < 1) s = 1;
     if (s > kb) s = kb;

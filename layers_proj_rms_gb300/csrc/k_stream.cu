@@ -7,6 +7,7 @@
 // _torch_h_aggregate_bwd, fused_h_post_bda "H_res.T @ residual + H_post *
 // (x + bias)", _torch_h_post_bda_bwd) and rwkv-ops mhu_ffi.cu
 // (StreamAggregateFwd/Bwd, MhcPostOpFwdHost/BwdHost, RMSNormFwdHost/BwdHost).
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -14,19 +15,23 @@
 
 namespace mhc {
 
-static int g_num_sms[64];
+// SM count per device, looked up once; relaxed atomics so that threads
+// calling concurrently race on nothing (two first calls may both look it up
+// and store the same value).
+static std::atomic<int> g_num_sms[64];
 
 int num_sms()
 {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (g_num_sms[dev] == 0) {
-        int v = 0;
+    int v = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
         cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
-        g_num_sms[dev] = v > 0 ? v : 1;
+        if (v <= 0) v = 1;
+        g_num_sms[dev].store(v, std::memory_order_relaxed);
     }
-    return g_num_sms[dev];
+    return v;
 }
 
 cudaError_t set_smem_limit(const void *kernel, int bytes)

@@ -13,12 +13,19 @@
 // address, so its device address is looked up with cudaGetSymbolAddress
 // once per device (with that device current) and cached.  The first call on
 // a device does that lookup; make that first call before any stream capture.
+// The cache is per device index and holds the address in the context that
+// was current at that first call (the device's primary context, for CUDA
+// runtime users): it is not valid after cudaDeviceReset or in another
+// context on the same device.  Threads may make their first calls
+// concurrently (the slots are atomic; both lookups give the same address).
 //
 // Every call on a device uses the same array.  The kernels overwrite each
 // scratch element before they read it, so nothing needs clearing between
 // calls, but two calls whose work overlaps on the GPU (different streams,
 // no ordering between them) race on the array and give wrong results.
 #include <stdio.h>
+
+#include <atomic>
 
 #include "../../include/mhc.h"
 #include "launch.h"
@@ -31,7 +38,7 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 void *scratch_for_current_device(cudaError_t *err)
 {
-    static void *ptrs[64];
+    static std::atomic<void *> ptrs[64];
     int dev = 0;
     *err = cudaGetDevice(&dev);
     if (*err != cudaSuccess) return nullptr;
@@ -39,13 +46,13 @@ void *scratch_for_current_device(cudaError_t *err)
         *err = cudaErrorInvalidDevice;
         return nullptr;
     }
-    if (!ptrs[dev]) {
-        void *p = nullptr;
+    void *p = ptrs[dev].load(std::memory_order_acquire);
+    if (!p) {
         *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (*err != cudaSuccess) return nullptr;
-        ptrs[dev] = p;
+        ptrs[dev].store(p, std::memory_order_release);
     }
-    return ptrs[dev];
+    return p;
 }
 
 }  // namespace
