@@ -96,6 +96,25 @@ MHC_API int mhc_version(void);
 MHC_API void mhc_set_batch_invariant(int on);
 MHC_API int mhc_batch_invariant(void);
 
+/* Bit-reproducible mode (RL-Align/RL-Kernel PR #383, PR body, "Numerical
+ * contract": fp32 arithmetic and only two reduction trees, a serial
+ * ascending left fold for long reductions and (a0 + a1) + (a2 + a3) over the
+ * four streams).  When on, mhc_sinkhorn_fwd/bwd, mhc_proj_rms_compute_h_fwd/
+ * bwd, mhc_h_aggregate_fwd/bwd, mhc_h_post_bda_fwd/bwd and mhc_layer_fwd/bwd
+ * compute every result in that order: each stream sum is the four-stream
+ * tree, each sum over channels, over K, over the controller logits or over
+ * tokens (dH_*, u, sum x^2, dx_proj, dW, dalpha, db, dbias) is a serial fold
+ * in ascending index order, every product is rounded before it is added, and
+ * exp is the library's own (Cody-Waite reduction, Taylor polynomial), so the
+ * results are the same bits on every device and in any program that
+ * performs those fp32 operations in that order.  Defined for n = 4: with the
+ * mode on these calls return MHC_ERR_UNSUPPORTED_N for n = 8.  The mode uses
+ * plain (slow) kernels; the backward recomputes u, r from x and ignores
+ * u_save, r_save.  Process-wide; do not change it while calls are in flight.
+ * The other entry points (RMSNorm, the next-row ops) are not affected. */
+MHC_API void mhc_set_pinned_reductions(int on);
+MHC_API int mhc_pinned_reductions(void);
+
 /* Synchronises `stream`, reads and clears the device-side fault word.
  * Returns MHC_OK if no kernel reported a fault, MHC_ERR_DEVICE_FAULT
  * otherwise (*code receives the fault code, 0 if none; code may be NULL). */

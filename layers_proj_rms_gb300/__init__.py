@@ -28,6 +28,7 @@ __all__ = [
     "mhc_proj_rms_partial_bwd", "OP_RMSNORM_RESIDUAL_BWD", "OP_H_AGGREGATE_RMSNORM_BWD",
     "OP_H_AGGREGATE_STATIC_BWD", "OP_PROJ_RMS_PARTIAL_FWD", "OP_COMPUTE_H_BWD",
     "OP_PROJ_RMS_PARTIAL_BWD", "mhc_set_batch_invariant", "mhc_batch_invariant",
+    "mhc_set_pinned_reductions", "mhc_pinned_reductions",
     "mhc_h_post_bda_compute_h_fwd", "OP_H_POST_BDA_COMPUTE_H_FWD", "mhc_selftest_wait_timeout",
 ]
 

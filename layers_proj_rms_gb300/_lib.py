@@ -87,6 +87,10 @@ lib.mhc_set_batch_invariant.argtypes = [_I]
 lib.mhc_set_batch_invariant.restype = None
 lib.mhc_batch_invariant.argtypes = []
 lib.mhc_batch_invariant.restype = ctypes.c_int
+lib.mhc_set_pinned_reductions.argtypes = [_I]
+lib.mhc_set_pinned_reductions.restype = None
+lib.mhc_pinned_reductions.argtypes = []
+lib.mhc_pinned_reductions.restype = ctypes.c_int
 lib.mhc_workspace_bytes.argtypes = [_I, _I64, _I, _I64]
 lib.mhc_workspace_bytes.restype = ctypes.c_size_t
 
@@ -436,3 +440,11 @@ def mhc_set_batch_invariant(on: bool) -> None:
 
 def mhc_batch_invariant() -> bool:
     return bool(lib.mhc_batch_invariant())
+
+
+def mhc_set_pinned_reductions(on: bool) -> None:
+    lib.mhc_set_pinned_reductions(1 if on else 0)
+
+
+def mhc_pinned_reductions() -> bool:
+    return bool(lib.mhc_pinned_reductions())

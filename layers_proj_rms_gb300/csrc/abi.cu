@@ -164,6 +164,22 @@ mhc_status zero_param_grads(Check &ck, float *dW, int64_t nW, float *dalpha, flo
     return launched(ck.fn, e);
 }
 
+// Bit-reproducible mode: its reduction trees are defined for four streams.
+mhc_status pinned_n4(Check &ck, int n)
+{
+    if (ck.st == MHC_OK && n != 4)
+        ck.st = fail(MHC_ERR_UNSUPPORTED_N,
+                     "%s: the pinned-reduction mode is defined for n = 4 (got n = %d)", ck.fn, n);
+    return ck.st;
+}
+
+// backward workspaces cover the pinned mode's per-token scratch too
+size_t proj_bwd_ws(int64_t T, int n, int64_t C)
+{
+    const size_t a = mhc::proj_bwd_ws_bytes(T, n, C), b = n == 4 ? mhc::pin_bwd_ws_bytes(T) : 0;
+    return a > b ? a : b;
+}
+
 }  // namespace
 
 void mhc::set_error_message(const char *msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
@@ -192,6 +208,10 @@ const char *mhc_last_error(void) { return g_msg; }
 int mhc_version(void) { return 100; }
 
 void mhc_set_batch_invariant(int on) { mhc::set_batch_invariant(on); }
+
+void mhc_set_pinned_reductions(int on) { mhc::set_pinned(on); }
+
+int mhc_pinned_reductions(void) { return mhc::pinned(); }
 
 int mhc_batch_invariant(void) { return mhc::batch_invariant(); }
 
@@ -242,10 +262,10 @@ size_t mhc_workspace_bytes(mhc_op op, int64_t T, int n, int64_t C)
     case MHC_OP_COMPUTE_H_BWD: return mhc::compute_h_bwd_ws_bytes(T, n);
     case MHC_OP_PROJ_RMS_PARTIAL_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
     case MHC_OP_PROJ_RMS_COMPUTE_H_FWD: return mhc::proj_fwd_ws_bytes(T, n, C);
-    case MHC_OP_PROJ_RMS_COMPUTE_H_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
+    case MHC_OP_PROJ_RMS_COMPUTE_H_BWD: return proj_bwd_ws(T, n, C);
     case MHC_OP_H_POST_BDA_BWD: return mhc::dbias_ws_bytes(T, C);
     case MHC_OP_LAYER_FWD: return layer_fwd_ws(T, n, C);
-    case MHC_OP_LAYER_BWD: return mhc::proj_bwd_ws_bytes(T, n, C);
+    case MHC_OP_LAYER_BWD: return proj_bwd_ws(T, n, C);
     case MHC_OP_H_POST_BDA_COMPUTE_H_FWD: return mhc::post_proj_ws_bytes(T, n, C);
     }
     return 0;
@@ -260,6 +280,10 @@ mhc_status mhc_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int
     ck.ptr(logits, "logits").ptr(P, "P");
     if (ck.st) return ck.st;
     if (ck.device().st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_sinkhorn_fwd(logits, P, M, iters,
+                                                                               eps, stream));
     return launched(ck.fn, mhc::launch_sinkhorn_fwd(logits, P, M, n, iters, eps, stream));
 }
 
@@ -272,6 +296,10 @@ mhc_status mhc_sinkhorn_bwd(const float *dP, const float *logits, float *dlogits
     ck.ptr(dP, "dP").ptr(logits, "logits").ptr(dlogits, "dlogits");
     if (ck.st) return ck.st;
     if (ck.device().st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_sinkhorn_bwd(dP, logits, dlogits,
+                                                                               M, iters, eps, stream));
     return launched(ck.fn, mhc::launch_sinkhorn_bwd(dP, logits, dlogits, M, n, iters, eps, stream));
 }
 
@@ -289,6 +317,12 @@ mhc_status mhc_proj_rms_compute_h_fwd(const mhc_bf16 *x, const float *W, const f
     ck.ptr(H_post, "H_post").ptr(H_res, "H_res").opt(u_save, "u_save").opt(r_save, "r_save");
     ck.ws(ws, ws_bytes, mhc::proj_fwd_ws_bytes(T, n, C)).device();
     if (ck.st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_proj_fwd(
+                                                      reinterpret_cast<const bf16 *>(x), W, alpha3,
+                                                      b, T, C, iters, eps_sk, eps_rms, H_pre,
+                                                      H_post, H_res, u_save, r_save, stream));
     return launched(ck.fn, mhc::launch_proj_fwd(reinterpret_cast<const bf16 *>(x), W, alpha3, b,
                                                 T, n, C, iters, eps_sk, eps_rms, H_pre, H_post,
                                                 H_res, u_save, r_save, ws, fault_ptr(), stream));
@@ -312,8 +346,16 @@ mhc_status mhc_proj_rms_compute_h_bwd(const float *dH_pre, const float *dH_post,
                                         n * n + 2 * n, nullptr, 0, stream);
     ck.ptr(dH_pre, "dH_pre").ptr(dH_post, "dH_post").ptr(dH_res, "dH_res").ptr(x, "x");
     ck.ptr(u_save, "u_save").ptr(r_save, "r_save").ptr(dx, "dx");
-    ck.ws(ws, ws_bytes, mhc::proj_bwd_ws_bytes(T, n, C)).device();
+    ck.ws(ws, ws_bytes, proj_bwd_ws(T, n, C)).device();
     if (ck.st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_proj_bwd(
+                                                      dH_pre, dH_post, dH_res,
+                                                      reinterpret_cast<const bf16 *>(x), W, alpha3,
+                                                      b, T, C, iters, eps_sk, eps_rms,
+                                                      reinterpret_cast<bf16 *>(dx), dW, dalpha3, db,
+                                                      ws, stream));
     return launched(ck.fn, mhc::launch_proj_bwd(dH_pre, dH_post, dH_res,
                                                 reinterpret_cast<const bf16 *>(x), W, alpha3, b,
                                                 u_save, r_save, T, n, C, iters, eps_sk, eps_rms,
@@ -330,6 +372,11 @@ mhc_status mhc_h_aggregate_fwd(const mhc_bf16 *x, const float *H_pre, mhc_bf16 *
     ck.ptr(x, "x").ptr(H_pre, "H_pre").ptr(y, "y");
     if (ck.st) return ck.st;
     if (ck.device().st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_agg_fwd(
+                                                      reinterpret_cast<const bf16 *>(x), H_pre,
+                                                      reinterpret_cast<bf16 *>(y), T, C, stream));
     return launched(ck.fn, mhc::launch_aggregate_fwd(reinterpret_cast<const bf16 *>(x), H_pre,
                                                      reinterpret_cast<bf16 *>(y), T, n, C, stream));
 }
@@ -344,6 +391,13 @@ mhc_status mhc_h_aggregate_bwd(const mhc_bf16 *dy, const mhc_bf16 *x, const floa
     ck.ptr(dy, "dy").ptr(x, "x").ptr(H_pre, "H_pre").ptr(dx, "dx").ptr(dH_pre, "dH_pre");
     if (ck.st) return ck.st;
     if (ck.device().st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_agg_bwd(
+                                                      reinterpret_cast<const bf16 *>(dy),
+                                                      reinterpret_cast<const bf16 *>(x), H_pre,
+                                                      reinterpret_cast<bf16 *>(dx), dH_pre, T, C,
+                                                      stream));
     return launched(ck.fn, mhc::launch_aggregate_bwd(
                                reinterpret_cast<const bf16 *>(dy), reinterpret_cast<const bf16 *>(x),
                                H_pre, reinterpret_cast<bf16 *>(dx), dH_pre, T, n, C, stream));
@@ -360,6 +414,14 @@ mhc_status mhc_h_post_bda_fwd(const mhc_bf16 *residual, const mhc_bf16 *f, const
     ck.ptr(H_post, "H_post").ptr(out, "out");
     if (ck.st) return ck.st;
     if (ck.device().st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_post_fwd(
+                                                      reinterpret_cast<const bf16 *>(residual),
+                                                      reinterpret_cast<const bf16 *>(f),
+                                                      reinterpret_cast<const bf16 *>(bias), H_res,
+                                                      H_post, reinterpret_cast<bf16 *>(out), T, C,
+                                                      stream));
     return launched(ck.fn, mhc::launch_post_fwd(reinterpret_cast<const bf16 *>(residual),
                                                 reinterpret_cast<const bf16 *>(f),
                                                 reinterpret_cast<const bf16 *>(bias), H_res, H_post,
@@ -414,6 +476,15 @@ mhc_status mhc_h_post_bda_bwd(const mhc_bf16 *dout, const mhc_bf16 *residual, co
     ck.ws(ws, ws_bytes, dbias ? mhc::dbias_ws_bytes(T, C) : 0).device();
     if (ck.st) return ck.st;
     const bf16 *g = reinterpret_cast<const bf16 *>(dout);
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_post_bwd(
+                                                      g, reinterpret_cast<const bf16 *>(residual),
+                                                      reinterpret_cast<const bf16 *>(f),
+                                                      reinterpret_cast<const bf16 *>(bias), H_res,
+                                                      H_post, reinterpret_cast<bf16 *>(dresidual),
+                                                      reinterpret_cast<bf16 *>(df), dbias, dH_res,
+                                                      dH_post, T, C, stream));
     cudaError_t e = mhc::launch_post_bwd_tok(
         g, reinterpret_cast<const bf16 *>(residual), reinterpret_cast<const bf16 *>(f),
         reinterpret_cast<const bf16 *>(bias), H_res, H_post, reinterpret_cast<bf16 *>(dresidual),
@@ -473,6 +544,15 @@ mhc_status mhc_layer_fwd(const mhc_bf16 *x, const float *W, const float *alpha3,
     ck.ws(ws, ws_bytes, layer_fwd_ws(T, n, C)).device();
     if (ck.st) return ck.st;
     const bf16 *xb = reinterpret_cast<const bf16 *>(x);
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_layer_fwd(
+                                                      xb, W, alpha3, b,
+                                                      reinterpret_cast<const bf16 *>(f),
+                                                      reinterpret_cast<const bf16 *>(bias), T, C,
+                                                      iters, eps_sk, eps_rms, H_pre, H_post, H_res,
+                                                      u_save, r_save, reinterpret_cast<bf16 *>(y),
+                                                      reinterpret_cast<bf16 *>(out), stream));
     cudaError_t e = mhc::launch_proj_fwd(xb, W, alpha3, b, T, n, C, iters, eps_sk, eps_rms, H_pre,
                                          H_post, H_res, u_save, r_save, ws, fault_ptr(), stream);
     if (e == cudaSuccess)
@@ -505,8 +585,20 @@ mhc_status mhc_layer_bwd(const mhc_bf16 *dout, const mhc_bf16 *dy, const mhc_bf1
     ck.ptr(dout, "dout").ptr(dy, "dy").ptr(x, "x").ptr(f, "f").ptr(H_pre, "H_pre");
     ck.ptr(H_post, "H_post").ptr(H_res, "H_res").ptr(u_save, "u_save").ptr(r_save, "r_save");
     ck.ptr(dx, "dx").ptr(df, "df");
-    ck.ws(ws, ws_bytes, mhc::proj_bwd_ws_bytes(T, n, C)).device();
+    ck.ws(ws, ws_bytes, proj_bwd_ws(T, n, C)).device();
     if (ck.st) return ck.st;
+    if (mhc::pinned())
+        return pinned_n4(ck, n) ? ck.st
+                                : launched(ck.fn, mhc::launch_pin_layer_bwd(
+                                                      reinterpret_cast<const bf16 *>(dout),
+                                                      reinterpret_cast<const bf16 *>(dy),
+                                                      reinterpret_cast<const bf16 *>(x), W, alpha3,
+                                                      b, reinterpret_cast<const bf16 *>(f),
+                                                      reinterpret_cast<const bf16 *>(bias), H_pre,
+                                                      H_post, H_res, T, C, iters, eps_sk, eps_rms,
+                                                      reinterpret_cast<bf16 *>(dx),
+                                                      reinterpret_cast<bf16 *>(df), dW, dalpha3, db,
+                                                      dbias, ws, stream));
     return launched(
         ck.fn, mhc::launch_layer_bwd(reinterpret_cast<const bf16 *>(dout),
                                      reinterpret_cast<const bf16 *>(dy),

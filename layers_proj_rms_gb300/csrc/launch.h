@@ -223,4 +223,44 @@ cudaError_t launch_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, co
                              float eps_rms, bf16 *dx, bf16 *df, float *dW, float *dalpha,
                              float *db, float *dbias, void *ws, int *fault, cudaStream_t s);
 
+// k_pinned.cu: the bit-reproducible mode (pinned reduction trees, n = 4)
+void set_pinned(int on);
+int pinned();
+size_t pin_bwd_ws_bytes(int64_t T);
+cudaError_t launch_pin_sinkhorn_fwd(const float *lg, float *P, int64_t M, int iters, float eps,
+                                    cudaStream_t s);
+cudaError_t launch_pin_sinkhorn_bwd(const float *dP, const float *lg, float *dl, int64_t M,
+                                    int iters, float eps, cudaStream_t s);
+cudaError_t launch_pin_proj_fwd(const bf16 *x, const float *W, const float *alpha, const float *b,
+                                int64_t T, int64_t C, int iters, float eps_sk, float eps_rms,
+                                float *Hpre, float *Hpost, float *Hres, float *u_save,
+                                float *r_save, cudaStream_t s);
+cudaError_t launch_pin_proj_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                                const bf16 *x, const float *W, const float *alpha, const float *b,
+                                int64_t T, int64_t C, int iters, float eps_sk, float eps_rms,
+                                bf16 *dx, float *dW, float *dalpha, float *db, void *ws,
+                                cudaStream_t s);
+cudaError_t launch_pin_agg_fwd(const bf16 *x, const float *Hpre, bf16 *y, int64_t T, int64_t C,
+                               cudaStream_t s);
+cudaError_t launch_pin_agg_bwd(const bf16 *dy, const bf16 *x, const float *Hpre, bf16 *dx,
+                               float *dHpre, int64_t T, int64_t C, cudaStream_t s);
+cudaError_t launch_pin_post_fwd(const bf16 *res, const bf16 *f, const bf16 *bias,
+                                const float *Hres, const float *Hpost, bf16 *out, int64_t T,
+                                int64_t C, cudaStream_t s);
+cudaError_t launch_pin_post_bwd(const bf16 *dout, const bf16 *res, const bf16 *f,
+                                const bf16 *bias, const float *Hres, const float *Hpost,
+                                bf16 *dres, bf16 *df, float *dbias, float *dHres, float *dHpost,
+                                int64_t T, int64_t C, cudaStream_t s);
+cudaError_t launch_pin_layer_fwd(const bf16 *x, const float *W, const float *alpha,
+                                 const float *b, const bf16 *f, const bf16 *bias, int64_t T,
+                                 int64_t C, int iters, float eps_sk, float eps_rms, float *Hpre,
+                                 float *Hpost, float *Hres, float *u_save, float *r_save, bf16 *y,
+                                 bf16 *out, cudaStream_t s);
+cudaError_t launch_pin_layer_bwd(const bf16 *dout, const bf16 *dy, const bf16 *x, const float *W,
+                                 const float *alpha, const float *b, const bf16 *f,
+                                 const bf16 *bias, const float *Hpre, const float *Hpost,
+                                 const float *Hres, int64_t T, int64_t C, int iters, float eps_sk,
+                                 float eps_rms, bf16 *dx, bf16 *df, float *dW, float *dalpha,
+                                 float *db, float *dbias, void *ws, cudaStream_t s);
+
 }  // namespace mhc

@@ -26,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mhc_oracle.c")
+_SRC_PINNED = os.path.join(_HERE, "mhc_oracle_pinned.c")
 _OUT_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_OUT_DIR, "liboracle_mhc.so")
 _lib = None
@@ -35,11 +36,12 @@ def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no -ffast-math, no FMA contraction)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and os.path.getmtime(_LIB_PATH) >= max(os.path.getmtime(_SRC),
+                                                    os.path.getmtime(_SRC_PINNED))):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
     cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC",
-           "-shared", "-Wall", "-o", tmp, _SRC, "-lm"]
+           "-shared", "-Wall", "-o", tmp, _SRC, _SRC_PINNED, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -49,7 +51,7 @@ def _L():
     global _lib
     if _lib is None:
         _lib = ctypes.CDLL(build())
-        i64, i32, f64 = ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        i64, i32, f64, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_double, ctypes.c_float
         P = ctypes.c_void_p
         sig = {
             "orc_sinkhorn_fwd": [P, P, i64, i32, i32, f64],
@@ -74,11 +76,24 @@ def _L():
                                             P, P, P, P],
             "orc_proj_rms_partial_bwd": [P, P, P, P, i64, i32, i64, P, P],
             "orc_num_threads": [],
+            "orc_pin_sinkhorn_fwd": [P, P, i64, i32, f32],
+            "orc_pin_sinkhorn_bwd": [P, P, P, i64, i32, f32, P],
+            "orc_pin_proj_rms_compute_h_fwd": [P, P, P, P, i64, i64, i32, f32, f32, P, P, P, P, P],
+            "orc_pin_proj_rms_compute_h_bwd": [P, P, P, P, P, P, P, i64, i64, i32, f32, f32,
+                                               P, P, P, P, P, P],
+            "orc_pin_h_aggregate_fwd": [P, P, i64, i64, P],
+            "orc_pin_h_aggregate_bwd": [P, P, P, i64, i64, P, P],
+            "orc_pin_h_post_bda_fwd": [P, P, P, P, P, i64, i64, P],
+            "orc_pin_h_post_bda_bwd": [P, P, P, P, P, P, i64, i64, P, P, P, P, P],
+            "orc_pin_layer_bwd": [P, P, P, P, P, P, P, P, P, P, P, i64, i64, i32, f32, f32, P, P,
+                                  P, P, P, P, P, P],
         }
         for name, args in sig.items():
             fn = getattr(_lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        _lib.orc_pin_exp.argtypes = [f32]
+        _lib.orc_pin_exp.restype = f32
     return _lib
 
 
@@ -428,3 +443,141 @@ def h_post_bda_compute_h_fwd(res, f, bias, H_res, H_post, W_next, alpha_next, b_
     x_next = bf16_rne(out)
     h = proj_rms_compute_h_fwd(x_next, W_next, alpha_next, b_next, n, iters, eps_sk, eps_rms)
     return dict(h, out=out, x_next=x_next)
+
+
+# --------------------------------------------------------------------------
+# fp32, pinned reduction order (mhc_oracle_pinned.c): the reference of the
+# library's bit-reproducible mode, n = 4.  RL-Kernel PR #383, PR body,
+# "Numerical contract": a serial ascending left fold for long reductions,
+# (a0 + a1) + (a2 + a3) over the four streams, fp32 arithmetic.
+# Inputs are the exact fp32 values (bf16 bit patterns are widened); bf16
+# outputs come back as their fp32 values.
+# --------------------------------------------------------------------------
+
+def _f32(a):
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        a = (a.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def pin_exp(x):
+    """The exp of the pinned mode (Cody-Waite reduction, Taylor degree 7), elementwise."""
+    L = _L()
+    return np.array([L.orc_pin_exp(float(v)) for v in np.asarray(x, dtype=np.float32).ravel()],
+                    dtype=np.float32).reshape(np.shape(x))
+
+
+def pin_sinkhorn_fwd(logits, iters, eps):
+    lg = _f32(logits)
+    M = lg.size // 16
+    P = np.empty_like(lg)
+    _check(_L().orc_pin_sinkhorn_fwd(_p(lg), _p(P), M, iters, eps), "pin_sinkhorn_fwd")
+    return P
+
+
+def pin_sinkhorn_bwd(dP, logits, iters, eps):
+    lg, g = _f32(logits), _f32(dP)
+    M = lg.size // 16
+    dl = np.empty_like(lg)
+    trace = np.empty((2 * iters + 1) * 16, dtype=np.float32)
+    _check(_L().orc_pin_sinkhorn_bwd(_p(g), _p(lg), _p(dl), M, iters, eps, _p(trace)),
+           "pin_sinkhorn_bwd")
+    return dl
+
+
+def pin_proj_rms_compute_h_fwd(x, W, alpha, b, iters, eps_sk, eps_rms):
+    xs, Ws, a, bb = _f32(x), _f32(W), _f32(alpha), _f32(b)
+    T, n, C = xs.shape
+    assert n == 4
+    out = {"H_pre": np.empty((T, 4), np.float32), "H_post": np.empty((T, 4), np.float32),
+           "H_res": np.empty((T, 4, 4), np.float32), "u": np.empty((T, 24), np.float32),
+           "r": np.empty(T, np.float32)}
+    _check(_L().orc_pin_proj_rms_compute_h_fwd(
+        _p(xs), _p(Ws), _p(a), _p(bb), T, C, iters, eps_sk, eps_rms, _p(out["H_pre"]),
+        _p(out["H_post"]), _p(out["H_res"]), _p(out["u"]), _p(out["r"])), "pin_proj_fwd")
+    return out
+
+
+def pin_proj_rms_compute_h_bwd(dHpre, dHpost, dHres, x, W, alpha, b, iters, eps_sk, eps_rms):
+    xs, Ws, a, bb = _f32(x), _f32(W), _f32(alpha), _f32(b)
+    T, n, C = xs.shape
+    out = {"dx": np.empty((T, 4, C), np.float32), "dW": np.empty((4 * C, 24), np.float32),
+           "dalpha": np.empty(3, np.float32), "db": np.empty(24, np.float32)}
+    scratch = np.empty(max(T, 1) * (2 * 24 + 4), np.float32)
+    trace = np.empty((2 * iters + 1) * 16, np.float32)
+    _check(_L().orc_pin_proj_rms_compute_h_bwd(
+        _p(_f32(dHpre)), _p(_f32(dHpost)), _p(_f32(dHres)), _p(xs), _p(Ws), _p(a), _p(bb), T, C,
+        iters, eps_sk, eps_rms, _p(out["dx"]), _p(out["dW"]), _p(out["dalpha"]), _p(out["db"]),
+        _p(scratch), _p(trace)), "pin_proj_bwd")
+    return out
+
+
+def pin_h_aggregate_fwd(x, H_pre):
+    xs = _f32(x)
+    T, n, C = xs.shape
+    y = np.empty((T, C), np.float32)
+    _check(_L().orc_pin_h_aggregate_fwd(_p(xs), _p(_f32(H_pre)), T, C, _p(y)), "pin_agg_fwd")
+    return y
+
+
+def pin_h_aggregate_bwd(dy, x, H_pre):
+    xs = _f32(x)
+    T, n, C = xs.shape
+    dx = np.empty((T, 4, C), np.float32)
+    dH = np.empty((T, 4), np.float32)
+    _check(_L().orc_pin_h_aggregate_bwd(_p(_f32(dy)), _p(xs), _p(_f32(H_pre)), T, C, _p(dx),
+                                        _p(dH)), "pin_agg_bwd")
+    return dx, dH
+
+
+def pin_h_post_bda_fwd(res, f, bias, H_res, H_post):
+    rs = _f32(res)
+    T, n, C = rs.shape
+    out = np.empty((T, 4, C), np.float32)
+    _check(_L().orc_pin_h_post_bda_fwd(_p(rs), _p(_f32(f)), _p(None if bias is None else _f32(bias)),
+                                       _p(_f32(H_res)), _p(_f32(H_post)), T, C, _p(out)),
+           "pin_post_fwd")
+    return out
+
+
+def pin_h_post_bda_bwd(dout, res, f, bias, H_res, H_post):
+    rs = _f32(res)
+    T, n, C = rs.shape
+    o = {"dres": np.empty((T, 4, C), np.float32), "df": np.empty((T, C), np.float32),
+         "dbias": np.empty(C, np.float32), "dH_res": np.empty((T, 4, 4), np.float32),
+         "dH_post": np.empty((T, 4), np.float32)}
+    _check(_L().orc_pin_h_post_bda_bwd(
+        _p(_f32(dout)), _p(rs), _p(_f32(f)), _p(None if bias is None else _f32(bias)),
+        _p(_f32(H_res)), _p(_f32(H_post)), T, C, _p(o["dres"]), _p(o["df"]), _p(o["dbias"]),
+        _p(o["dH_res"]), _p(o["dH_post"])), "pin_post_bwd")
+    return o
+
+
+def pin_layer_fwd(inp, iters, eps_sk, eps_rms):
+    """The layer forward in the pinned order: proj_rms_compute_h, then
+    h_aggregate and h_post_bda with its H."""
+    h = pin_proj_rms_compute_h_fwd(inp["x"], inp["W"], inp["alpha"], inp["b"], iters, eps_sk,
+                                   eps_rms)
+    h["y"] = pin_h_aggregate_fwd(inp["x"], h["H_pre"])
+    h["out"] = pin_h_post_bda_fwd(inp["x"], inp["f"], inp.get("bias"), h["H_res"], h["H_post"])
+    return h
+
+
+def pin_layer_bwd(inp, fwd, iters, eps_sk, eps_rms):
+    xs = _f32(inp["x"])
+    T, n, C = xs.shape
+    o = {"dx": np.empty((T, 4, C), np.float32), "df": np.empty((T, C), np.float32),
+         "dW": np.empty((4 * C, 24), np.float32), "dalpha": np.empty(3, np.float32),
+         "db": np.empty(24, np.float32), "dbias": np.empty(C, np.float32)}
+    scratch = np.empty(max(T, 1) * (2 * 24 + 4 + 8 + 16), np.float32)
+    trace = np.empty((2 * iters + 1) * 16, np.float32)
+    bias = inp.get("bias")
+    _check(_L().orc_pin_layer_bwd(
+        _p(_f32(inp["dout"])), _p(_f32(inp["dy"])), _p(xs), _p(_f32(inp["W"])),
+        _p(_f32(inp["alpha"])), _p(_f32(inp["b"])), _p(_f32(inp["f"])),
+        _p(None if bias is None else _f32(bias)), _p(_f32(fwd["H_pre"])), _p(_f32(fwd["H_post"])),
+        _p(_f32(fwd["H_res"])), T, C, iters, eps_sk, eps_rms, _p(o["dx"]), _p(o["df"]),
+        _p(o["dW"]), _p(o["dalpha"]), _p(o["db"]), _p(o["dbias"]), _p(scratch), _p(trace)),
+        "pin_layer_bwd")
+    return o
