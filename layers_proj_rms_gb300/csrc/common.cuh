@@ -46,6 +46,18 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8])
     return v;
 }
 
+// The three bf16 terms of one fp32 weight: hi = bf16(w), lo = bf16(w - hi),
+// lo2 = bf16(w - hi - lo).  Both differences are exact in fp32 (each is a
+// rounding error of a value that fits in 24 bits), so hi + lo + lo2 equals w
+// to within 2^-24 relative.
+__device__ __forceinline__ void w_terms(float w, float &hi, float &lo, float &lo2)
+{
+    hi = __bfloat162float(__float2bfloat16_rn(w));
+    const float r1 = w - hi;
+    lo = __bfloat162float(__float2bfloat16_rn(r1));
+    lo2 = __bfloat162float(__float2bfloat16_rn(r1 - lo));
+}
+
 // ---- packed fp32 pairs: f32x2 arithmetic, two IEEE fp32 operations (each
 // rounded as its scalar form) per instruction --------------------------------
 typedef unsigned long long f32x2;
@@ -110,6 +122,14 @@ __device__ __forceinline__ void st_stream(void *p, uint4 v)
     asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x),
                  "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// 8-byte load from shared memory by 32-bit shared address
+__device__ __forceinline__ uint2 lds64(uint32_t saddr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr));
+    return v;
 }
 
 // 16-byte load from shared memory by 32-bit shared address (an explicit

@@ -85,18 +85,6 @@ template <> struct ProjTcSel<8> { using type = ProjTcCfg<8, 1, 3, 1, 256, 4>; };
 template <int N>
 using ProjTc = typename ProjTcSel<N>::type;
 
-// The three bf16 terms of one fp32 weight: hi = bf16(w), lo = bf16(w - hi),
-// lo2 = bf16(w - hi - lo).  Both differences are exact in fp32 (each is a
-// rounding error of a value that fits in 24 bits), so hi + lo + lo2 equals w
-// to within 2^-24 relative.
-__device__ __forceinline__ void w_terms(float w, float &hi, float &lo, float &lo2)
-{
-    hi = __bfloat162float(__float2bfloat16_rn(w));
-    const float r1 = w - hi;
-    lo = __bfloat162float(__float2bfloat16_rn(r1));
-    lo2 = __bfloat162float(__float2bfloat16_rn(r1 - lo));
-}
-
 // W [K][O] fp32 -> W_hl [NB][K] bf16 (rows o: hi; rows O+o: lo; rows 2O+o:
 // lo2; rows 3O..NB: zero).  n = 4: one thread per k (the tiled form below,
 // with 256 blocks, was slower at n = 4).

@@ -109,7 +109,9 @@ def test_workspace_sizes(L):
     # the fused post-mix + next projection needs at least the projection's W_hl
     O, K = 24, 4 * 4096
     assert ws(12, 16384, 4, 4096) >= 2 * O * K * 2
-    assert ws(12, 300, 8, 136) == ws(1, 300, 8, 136)
+    # n = 8 is fused too: its W'_hl has 3 x 80 rows of 8 C bf16
+    assert ws(12, 8192, 8, 7168) >= 3 * 80 * 8 * 7168 * 2
+    assert ws(12, 300, 8, 136) % 256 == 0
     # the RMSNorm op ignores n
     assert ws(6, 256, 0, 4096) == ws(6, 256, 4, 4096) > 0
     assert ws(1, 256, 5, 256) == 0

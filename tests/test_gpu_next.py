@@ -345,8 +345,11 @@ def _run_post_proj(M, p, T, n, C):
     return d, bufs, o
 
 
+# (2500, 8, 1032): 20 token tiles x 7 splits of ten 16-channel stages (ragged
+# last split, last stage half past C), so both x-stage and W-stage rings wrap
+# and the out.W'_hi buffers are drained five times per CTA
 @pytest.mark.parametrize("T,n,C", [(1, 4, 64), (256, 4, 256), (300, 4, 264), (129, 4, 520),
-                                   (67, 8, 64), (200, 8, 136)])
+                                   (67, 8, 64), (200, 8, 136), (2500, 8, 1032)])
 def test_post_bda_compute_h_fused(M, orc, T, n, C):
     """The fused op against the two ops run one after the other (out bitwise
     equal; the next layer's H from the same bf16 out, equal up to the order of
@@ -434,10 +437,25 @@ def test_post_bda_compute_h_fused_7b_sampled(M, orc):
     _check_post_proj(orc, p, o, n, idx)
 
 
-def test_post_bda_compute_h_fused_batch_invariant(M):
+def test_post_bda_compute_h_fused_n8_sampled(M, orc):
+    """n = 8 at C = 7168 (448 channel blocks; 32 token tiles x 4 splits of 112
+    stages each); the oracle recomputes a sample of tokens."""
+    T, n, C = 4096, 8, 7168
+    p = _post_proj_inputs(T, n, C, 5, alpha=(0.01, 0.01, 0.01))
+    _, bufs, o = _run_post_proj(M, p, T, n, C)
+    torch.cuda.synchronize()
+    for b in bufs.values():
+        check_canary(b)
+    g = np.random.Generator(np.random.PCG64(11))
+    idx = np.unique(np.concatenate([[0, 127, 128, T - 1], g.choice(T, 24, replace=False)]))
+    _check_post_proj(orc, p, o, n, idx)
+
+
+@pytest.mark.parametrize("n", [4, 8])
+def test_post_bda_compute_h_fused_batch_invariant(M, n):
     """Batch-invariant mode covers the fused op: 64 tokens alone and at
     offset 517 of a 1000-token batch give bitwise equal outputs."""
-    n, C = 4, 1024
+    C = 1024
     big = _post_proj_inputs(1000, n, C, 640)
     off, Ts = 517, 64
     small = dict(big)
