@@ -207,10 +207,13 @@ def job_tokens_per_s(T, world, ms):
 # ---------------------------------------------------------------------------
 
 def bench_ops(M, d, o, T, n, C, dev, reps=5):
-    """Event-timed average of each op (after 2 untimed calls) with its
-    algorithmic HBM bytes (U = one bf16 [T, C] tensor) and the GB/s that
-    gives.  Inputs reuse the step's tensors; all are larger than L2 except
-    the Sinkhorn batch (32768 matrices, latency-bound)."""
+    """Per op: `ms` the device time per call (reps calls replayed as one
+    CUDA graph), `ms_eager` the event-timed average of reps back-to-back
+    calls through the binding (includes the host's per-call overhead, which
+    exceeds the kernels of the small ops), its algorithmic HBM bytes (U = one
+    bf16 [T, C] tensor) and the GB/s `ms` gives.  Inputs reuse the step's
+    tensors; all are larger than L2 except the Sinkhorn batch (32768
+    matrices, latency-bound)."""
     import torch
     bf, f32 = torch.bfloat16, torch.float32
     e = lambda *sh, dt=f32: torch.empty(*sh, dtype=dt, device=dev)  # noqa: E731
@@ -291,6 +294,30 @@ def bench_ops(M, d, o, T, n, C, dev, reps=5):
                                                                         dWs, wspb2), n * U),
     }
     stream = torch.cuda.current_stream()
+
+    def graph_ms(fn):
+        """Device time per call: `reps` calls captured into one CUDA graph,
+        replayed (no host call overhead between the launches)."""
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            fn()
+        stream.wait_stream(side)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg):
+            for _ in range(reps):
+                fn()
+        cg.replay()
+        torch.cuda.synchronize()
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            cg.replay()
+        z.record(stream)
+        torch.cuda.synchronize()
+        del cg
+        return a.elapsed_time(z) / (3 * reps)
+
     res = {}
     for name, (fn, nbytes) in ops.items():
         fn(); fn()
@@ -301,9 +328,14 @@ def bench_ops(M, d, o, T, n, C, dev, reps=5):
             fn()
         z.record(stream)
         torch.cuda.synchronize()
-        ms = a.elapsed_time(z) / reps
-        res[name] = {"ms": round(ms, 4), "alg_bytes": int(nbytes),
-                     "gbs": round(nbytes / (ms / 1e3) / 1e9, 1)}
+        eager = a.elapsed_time(z) / reps
+        try:
+            ms = graph_ms(fn)
+        except Exception:  # noqa: BLE001  (capture refused: keep the eager number)
+            ms = None
+        dev_ms = ms if ms is not None else eager
+        res[name] = {"ms": round(dev_ms, 4), "ms_eager": round(eager, 4), "alg_bytes": int(nbytes),
+                     "gbs": round(nbytes / (dev_ms / 1e3) / 1e9, 1)}
     return res
 
 

@@ -58,6 +58,16 @@ __device__ __forceinline__ void w_terms(float w, float &hi, float &lo, float &lo
     lo2 = __bfloat162float(__float2bfloat16_rn(r1 - lo));
 }
 
+// The hardware's approximate reciprocal (rcp.approx: at most 1 ulp from
+// 1/x, denormal inputs flushed): one instruction where 1.0f / x is a
+// correctly rounded inline sequence with a slow-path branch.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ---- packed fp32 pairs: f32x2 arithmetic, two IEEE fp32 operations (each
 // rounded as its scalar form) per instruction --------------------------------
 typedef unsigned long long f32x2;

@@ -204,6 +204,259 @@ __global__ void __launch_bounds__(128)
     }
 }
 
+// ---------------------------------------------------------------------------
+// n = 4: one thread per token, the 4 x 4 Sinkhorn in its registers
+// (sk4_forward / sk4_backward).  The same formulas as above; the n lanes'
+// butterfly sums become (v0 + v1) + (v2 + v3) over the rows.  The backward
+// keeps 32 tokens per block, so its partial rows are those of the lane form.
+// ---------------------------------------------------------------------------
+constexpr int kCh4Fwd = 64;
+
+__global__ void __launch_bounds__(kCh4Fwd)
+    k_compute_h_fwd4(const float *__restrict__ upart, const float *__restrict__ spart, int splits,
+                     const float *__restrict__ alpha, const float *__restrict__ b, int64_t T,
+                     int64_t K, int iters, float eps_sk, float eps_rms, float *__restrict__ Hpre,
+                     float *__restrict__ Hpost, float *__restrict__ Hres,
+                     float *__restrict__ u_save, float *__restrict__ r_save)
+{
+    pdl_wait();
+    constexpr int N = 4, O = Dims<4>::O;
+    const int64_t t = int64_t(blockIdx.x) * kCh4Fwd + threadIdx.x;
+    if (t >= T) return;
+    float u[O], s = 0.f;
+#pragma unroll
+    for (int o = 0; o < O; ++o) u[o] = 0.f;
+    for (int sp = 0; sp < splits; ++sp) {
+        s += __ldg(spart + int64_t(sp) * T + t);
+        const float4 *up = reinterpret_cast<const float4 *>(upart + (int64_t(sp) * T + t) * O);
+#pragma unroll
+        for (int q4 = 0; q4 < O / 4; ++q4) {
+            const float4 v = __ldg(up + q4);
+            u[4 * q4] += v.x;
+            u[4 * q4 + 1] += v.y;
+            u[4 * q4 + 2] += v.z;
+            u[4 * q4 + 3] += v.w;
+        }
+    }
+    const float q = sqrtf(s / float(K));
+    const float r = 1.0f / (q + eps_rms);
+    const float a0 = __ldg(alpha), a1 = __ldg(alpha + 1), a2 = __ldg(alpha + 2);
+    float hp[N], hq[N], a[N][N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float zpre = a0 * r * u[i] + __ldg(b + i);
+        const float zpost = a1 * r * u[N + i] + __ldg(b + N + i);
+        hp[i] = sigmoidf_(zpre);
+        hq[i] = 2.0f * sigmoidf_(zpost);
+#pragma unroll
+        for (int j = 0; j < N; ++j)
+            a[i][j] = expf(a2 * r * u[2 * N + i * N + j] + __ldg(b + 2 * N + i * N + j));
+    }
+    sk4_forward(a, iters, eps_sk, nullptr, 0);
+    reinterpret_cast<float4 *>(Hpre)[t] = make_float4(hp[0], hp[1], hp[2], hp[3]);
+    reinterpret_cast<float4 *>(Hpost)[t] = make_float4(hq[0], hq[1], hq[2], hq[3]);
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        reinterpret_cast<float4 *>(Hres)[t * N + i] = make_float4(a[i][0], a[i][1], a[i][2], a[i][3]);
+    if (u_save) {
+        float4 *us = reinterpret_cast<float4 *>(u_save + t * O);
+#pragma unroll
+        for (int q4 = 0; q4 < O / 4; ++q4)
+            us[q4] = make_float4(u[4 * q4], u[4 * q4 + 1], u[4 * q4 + 2], u[4 * q4 + 3]);
+    }
+    if (r_save) r_save[t] = r;
+}
+
+constexpr int kCh4Bwd = 32;
+constexpr int kCh4DuCols = 64;   // du_hl columns at n = 4
+
+__global__ void __launch_bounds__(kCh4Bwd)
+    k_compute_h_bwd4(const float *__restrict__ dHpre, const float *__restrict__ dHpost,
+                     const float *__restrict__ dHres, const float *__restrict__ u_save,
+                     const float *__restrict__ r_save, const float *__restrict__ alpha,
+                     const float *__restrict__ b, int64_t T, int64_t K, int iters, float eps_sk,
+                     float eps_rms, bf16 *__restrict__ du_hl, float *__restrict__ coef,
+                     float *__restrict__ part, const float *__restrict__ s_tot,
+                     float *__restrict__ du_f32, float *__restrict__ dub)
+{
+    pdl_wait();
+    constexpr int N = 4, O = Dims<4>::O, PW = O + 4;
+    extern __shared__ float sk_store[];   // [8 iters][kCh4Bwd]
+    __shared__ float red[kCh4Bwd][PW + 1];
+    const int tid = threadIdx.x;
+    const int64_t t = int64_t(blockIdx.x) * kCh4Bwd + tid;
+    const bool live = t < T;
+    const int64_t tt = live ? t : 0;
+    float u[O];
+#pragma unroll
+    for (int q4 = 0; q4 < O / 4; ++q4) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(u_save + tt * O) + q4);
+        u[4 * q4] = v.x;
+        u[4 * q4 + 1] = v.y;
+        u[4 * q4 + 2] = v.z;
+        u[4 * q4 + 3] = v.w;
+    }
+    // r from the forward, or from the summed squares of a sharded forward
+    const float r = r_save ? __ldg(r_save + tt)
+                           : 1.0f / (sqrtf(__ldg(s_tot + tt) / float(K)) + eps_rms);
+    const float a0 = __ldg(alpha), a1 = __ldg(alpha + 1), a2 = __ldg(alpha + 2);
+    float e[N][N], a[N][N], g[N][N];
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float4 gv = live ? __ldg(reinterpret_cast<const float4 *>(dHres + tt * N * N) + i)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        g[i][0] = gv.x;
+        g[i][1] = gv.y;
+        g[i][2] = gv.z;
+        g[i][3] = gv.w;
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            e[i][j] = expf(a2 * r * u[2 * N + i * N + j] + __ldg(b + 2 * N + i * N + j));
+            a[i][j] = e[i][j];
+        }
+    }
+    float *store = sk_store + tid;
+    sk4_forward(a, iters, eps_sk, store, kCh4Bwd);
+    sk4_backward(g, a, e, iters, store, kCh4Bwd);   // g = dz_res
+    const float4 dhp = live ? __ldg(reinterpret_cast<const float4 *>(dHpre) + tt) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 dhq = live ? __ldg(reinterpret_cast<const float4 *>(dHpost) + tt) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float dhpv[N] = {dhp.x, dhp.y, dhp.z, dhp.w}, dhqv[N] = {dhq.x, dhq.y, dhq.z, dhq.w};
+    float dzpre[N], dzpost[N], hq[N], gr[N], pr[N], po[N], sb[N];
+    float dv[O];   // du in column order
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const float sp = sigmoidf_(a0 * r * u[i] + __ldg(b + i));
+        const float so = sigmoidf_(a1 * r * u[N + i] + __ldg(b + N + i));
+        hq[i] = 2.0f * so;
+        dzpre[i] = dhpv[i] * sp * (1.f - sp);
+        dzpost[i] = dhqv[i] * 2.f * so * (1.f - so);
+        pr[i] = dzpre[i] * u[i];
+        po[i] = dzpost[i] * u[N + i];
+        float gi = 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) gi = fmaf(g[i][j], u[2 * N + i * N + j], gi);
+        gr[i] = gi;
+        dv[i] = a0 * r * dzpre[i];
+        dv[N + i] = a1 * r * dzpost[i];
+        float sa = fabsf(dv[i]) + fabsf(dv[N + i]);
+#pragma unroll
+        for (int j = 0; j < N; ++j) {
+            dv[2 * N + i * N + j] = a2 * r * g[i][j];
+            sa += fabsf(dv[2 * N + i * N + j]);
+        }
+        sb[i] = sa;
+    }
+    const float gpre = (pr[0] + pr[1]) + (pr[2] + pr[3]);
+    const float gpost = (po[0] + po[1]) + (po[2] + po[3]);
+    const float gres = (gr[0] + gr[1]) + (gr[2] + gr[3]);
+    const float sabs = (sb[0] + sb[1]) + (sb[2] + sb[3]);
+    if (live) {
+        // du_hl row: bf16(du) in columns [0, O), the bf16 remainder in
+        // [O, 2O), H_post as bf16 hi | lo in [2O, 2O + 2n), zeros to 64
+        auto col = [&](int c) -> float {
+            if (c < O) return __bfloat162float(__float2bfloat16_rn(dv[c]));
+            if (c < 2 * O) {
+                const float v = dv[c - O];
+                return v - __bfloat162float(__float2bfloat16_rn(v));
+            }
+            if (c < 2 * O + N) return hq[c - 2 * O];
+            if (c < 2 * O + 2 * N) {
+                const float v = hq[c - 2 * O - N];
+                return v - __bfloat162float(__float2bfloat16_rn(v));
+            }
+            return 0.f;
+        };
+        uint4 *row = reinterpret_cast<uint4 *>(du_hl + t * kCh4DuCols);
+#pragma unroll
+        for (int c8 = 0; c8 < kCh4DuCols / 8; ++c8) {
+            float v8[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v8[k] = col(8 * c8 + k);
+            row[c8] = pack8(v8);
+        }
+        if (du_f32) {
+            float4 *d4 = reinterpret_cast<float4 *>(du_f32 + t * O);
+#pragma unroll
+            for (int q4 = 0; q4 < O / 4; ++q4)
+                d4[q4] = make_float4(dv[4 * q4], dv[4 * q4 + 1], dv[4 * q4 + 2], dv[4 * q4 + 3]);
+        }
+        const float dr = a0 * gpre + a1 * gpost + a2 * gres;
+        const float q = 1.0f / r - eps_rms;
+        coef[t] = (q > 0.f) ? -dr * r * r / (float(K) * q) : 0.f;
+        if (dub) dub[t] = sabs;
+    }
+    // this token's row of the block partial (zeros for a dead token)
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        red[tid][i] = live ? dzpre[i] : 0.f;
+        red[tid][N + i] = live ? dzpost[i] : 0.f;
+#pragma unroll
+        for (int j = 0; j < N; ++j) red[tid][2 * N + i * N + j] = live ? g[i][j] : 0.f;
+    }
+    red[tid][O] = live ? gpre * r : 0.f;
+    red[tid][O + 1] = live ? gpost * r : 0.f;
+    red[tid][O + 2] = live ? gres * r : 0.f;
+    red[tid][O + 3] = 0.f;
+    __syncwarp();
+    if (tid < PW) {
+        float acc = 0.f;
+        for (int k = 0; k < kCh4Bwd; ++k) acc += red[k][tid];
+        part[int64_t(blockIdx.x) * PW + tid] = acc;
+    }
+}
+
+// The compute_h forward launch (lane form for n = 8)
+template <int N>
+static void launch_ch_fwd(const float *upart, const float *spart, int S, const float *alpha,
+                          const float *b, int64_t T, int64_t K, int iters, float eps_sk,
+                          float eps_rms, float *Hpre, float *Hpost, float *Hres, float *u_save,
+                          float *r_save, cudaStream_t s)
+{
+    MHC_PROF("k_compute_h_fwd", s);
+    if constexpr (N == 4)
+        launch_k(k_compute_h_fwd4, dim3(unsigned((T + kCh4Fwd - 1) / kCh4Fwd)), dim3(kCh4Fwd), 0, s,
+                 upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, u_save,
+                 r_save);
+    else
+        launch_k(k_compute_h_fwd<N>, dim3(unsigned((T * N + 127) / 128)), dim3(128), 0, s, upart,
+                 spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, u_save,
+                 r_save);
+}
+
+// The compute_h backward launch: partial rows of 128 / n tokens per block
+template <int N>
+static cudaError_t launch_ch_bwd(const float *dHpre, const float *dHpost, const float *dHres,
+                                 const float *u_save, const float *r_save, const float *alpha,
+                                 const float *b, int64_t T, int64_t K, int iters, float eps_sk,
+                                 float eps_rms, bf16 *du_hl, int du_cols, float *coef,
+                                 float *part, const float *s_tot, float *du_f32, float *dub,
+                                 cudaStream_t s)
+{
+    const int64_t prows = (T * N + 127) / 128;
+    cudaError_t e;
+    if constexpr (N == 4) {
+        e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd4),
+                           int(size_t(8) * kMaxIters * kCh4Bwd * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        if (du_cols != kCh4DuCols) return cudaErrorInvalidValue;
+        MHC_PROF("k_compute_h_bwd", s);
+        launch_k(k_compute_h_bwd4, dim3(unsigned(prows)), dim3(kCh4Bwd),
+                 size_t(8) * iters * kCh4Bwd * sizeof(float), s, dHpre, dHpost, dHres, u_save,
+                 r_save, alpha, b, T, K, iters, eps_sk, eps_rms, du_hl, coef, part, s_tot, du_f32,
+                 dub);
+    } else {
+        e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd<N>),
+                           int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+        if (e != cudaSuccess) return e;
+        MHC_PROF("k_compute_h_bwd", s);
+        launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128),
+                 size_t(2) * iters * 128 * sizeof(float), s, dHpre, dHpost, dHres, u_save, r_save,
+                 alpha, b, T, K, iters, eps_sk, eps_rms, du_hl, du_cols, coef, part, s_tot, du_f32,
+                 dub);
+    }
+    return cudaGetLastError();
+}
+
 // Fixed-order sums of the backward's partials.  Blocks [0, wblocks):
 // dW[j] = sum_s dWpart[s][j]; the next bblocks: dbias[j] = sum_s
 // dbiaspart[s][j] (s ascending; both only when the residual-gradient pass
@@ -279,13 +532,8 @@ static cudaError_t proj_fwd_impl(const bf16 *x, const float *W, const float *alp
     int S_used = 1;
     cudaError_t e = launch_proj_partials(x, W, T, N, C, Whl, upart, spart, &S_used, fault, s);
     if (e != cudaSuccess) return e;
-    const int64_t threads = T * N;
-    {
-        MHC_PROF("k_compute_h_fwd", s);
-        launch_k(k_compute_h_fwd<N>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
-            upart, spart, S_used, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
-            u_save, r_save);
-    }
+    launch_ch_fwd<N>(upart, spart, S_used, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                     u_save, r_save, s);
     return cudaGetLastError();
 }
 
@@ -295,16 +543,13 @@ cudaError_t launch_compute_h_parts(const float *upart, const float *spart, int S
                                    float *Hpost, float *Hres, float *u_save, float *r_save,
                                    cudaStream_t s)
 {
-    const int64_t threads = T * n, K = int64_t(n) * C;
-    MHC_PROF("k_compute_h_fwd", s);
+    const int64_t K = int64_t(n) * C;
     if (n == 4)
-        launch_k(k_compute_h_fwd<4>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s,
-                 upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
-                 u_save, r_save);
+        launch_ch_fwd<4>(upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost,
+                         Hres, u_save, r_save, s);
     else
-        launch_k(k_compute_h_fwd<8>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s,
-                 upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
-                 u_save, r_save);
+        launch_ch_fwd<8>(upart, spart, S, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost,
+                         Hres, u_save, r_save, s);
     return cudaGetLastError();
 }
 
@@ -390,16 +635,9 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
         dHres = w.dHres;
     }
     const int64_t prows = (T * N + 127) / 128;
-    {
-        const size_t smem = size_t(2) * iters * 128 * sizeof(float);
-        e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd<N>),
-                           int(size_t(2) * kMaxIters * 128 * sizeof(float)));
-        if (e != cudaSuccess) return e;
-        MHC_PROF("k_compute_h_bwd", s);
-        launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
-            dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk, eps_rms, w.du_hl,
-            du_cols, w.coef, w.part, nullptr, w.du32, w.dub);
-    }
+    e = launch_ch_bwd<N>(dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk,
+                         eps_rms, w.du_hl, du_cols, w.coef, w.part, nullptr, w.du32, w.dub, s);
+    if (e != cudaSuccess) return e;
     // pass 2: residual gradient, dW and dbias on the tensor cores; an unsplit
     // pass writes dW and dbias directly
     const int tiles = int((T + 127) / 128);
@@ -504,16 +742,12 @@ cudaError_t launch_compute_h_fwd(const float *u, const float *s_tot, int64_t K,
                                  float eps_sk, float eps_rms, float *Hpre, float *Hpost,
                                  float *Hres, float *r_save, cudaStream_t s)
 {
-    const int64_t threads = T * n;
-    MHC_PROF("k_compute_h_fwd", s);
     if (n == 4)
-        launch_k(k_compute_h_fwd<4>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
-            u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
-            r_save);
+        launch_ch_fwd<4>(u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                         nullptr, r_save, s);
     else
-        launch_k(k_compute_h_fwd<8>, dim3(unsigned((threads + 127) / 128)), dim3(128), 0, s, 
-            u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres, nullptr,
-            r_save);
+        launch_ch_fwd<8>(u, s_tot, 1, alpha, b, T, K, iters, eps_sk, eps_rms, Hpre, Hpost, Hres,
+                         nullptr, r_save, s);
     return cudaGetLastError();
 }
 
@@ -538,16 +772,10 @@ static cudaError_t compute_h_bwd_impl(const float *dHpre, const float *dHpost,
     p += ws_align(size_t(T) * bwd_tc_du_cols(N) * 2);
     float *part = reinterpret_cast<float *>(p);
     const int64_t prows = (T * N + 127) / 128;
-    const size_t smem = size_t(2) * iters * 128 * sizeof(float);
-    cudaError_t e = set_smem_limit(reinterpret_cast<const void *>(k_compute_h_bwd<N>),
-                                   int(size_t(2) * kMaxIters * 128 * sizeof(float)));
+    cudaError_t e = launch_ch_bwd<N>(dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters,
+                                     eps_sk, eps_rms, du_hl, bwd_tc_du_cols(N), coef, part, s_tot,
+                                     du, nullptr, s);
     if (e != cudaSuccess) return e;
-    {
-        MHC_PROF("k_compute_h_bwd", s);
-        launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128), smem, s, 
-            dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters, eps_sk, eps_rms, du_hl,
-            bwd_tc_du_cols(N), coef, part, s_tot, du, nullptr);
-    }
     {
         MHC_PROF("k_bwd_finalize", s);
         launch_k(k_bwd_finalize, dim3(unsigned(O + 3)), dim3(256), 0, s, nullptr, nullptr, 0, 0, nullptr, nullptr, 0,

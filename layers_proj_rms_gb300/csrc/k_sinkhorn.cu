@@ -1,7 +1,8 @@
 // Batched Sinkhorn-Knopp forward and backward: one launch for all M
 // matrices (rwkv-ops mhu_ffi.cu SinkhornFwdHost/SinkhornBwdHost run one
-// launch per matrix from a host loop; here each lane owns one row and a
-// group of n lanes owns one matrix).
+// launch per matrix from a host loop).  n = 4: one thread per matrix, the
+// 16 entries in registers; n = 8: each lane owns one row and a group of n
+// lanes owns one matrix.
 #include "launch.h"
 #include "sinkhorn.cuh"
 
@@ -83,6 +84,70 @@ __global__ void __launch_bounds__(kSkThreads)
     if (live) store_row<N>(dlogits + row * N, g);
 }
 
+// n = 4, one thread per matrix (sk4_forward / sk4_backward); the backward
+// keeps the denominators in shared memory, thread-major.
+constexpr int kSk1Threads = 64;
+
+__device__ __forceinline__ void sk1_load(const float *p, float (&m)[4][4])
+{
+    const float4 *q = reinterpret_cast<const float4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float4 w = __ldg(q + i);
+        m[i][0] = w.x;
+        m[i][1] = w.y;
+        m[i][2] = w.z;
+        m[i][3] = w.w;
+    }
+}
+
+__device__ __forceinline__ void sk1_store(float *p, const float (&m)[4][4])
+{
+    float4 *q = reinterpret_cast<float4 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = make_float4(m[i][0], m[i][1], m[i][2], m[i][3]);
+}
+
+__global__ void __launch_bounds__(kSk1Threads)
+    k_sinkhorn1_fwd(const float *__restrict__ logits, float *__restrict__ P, int64_t M, int iters,
+                    float eps)
+{
+    pdl_wait();
+    const int64_t m = int64_t(blockIdx.x) * kSk1Threads + threadIdx.x;
+    if (m >= M) return;
+    float a[4][4];
+    sk1_load(logits + m * 16, a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[i][j] = expf(a[i][j]);
+    sk4_forward(a, iters, eps, nullptr, 0);
+    sk1_store(P + m * 16, a);
+}
+
+__global__ void __launch_bounds__(kSk1Threads)
+    k_sinkhorn1_bwd(const float *__restrict__ dP, const float *__restrict__ logits,
+                    float *__restrict__ dlogits, int64_t M, int iters, float eps)
+{
+    pdl_wait();
+    extern __shared__ float sk1_st[];   // [8 iters][kSk1Threads]
+    const int64_t m = int64_t(blockIdx.x) * kSk1Threads + threadIdx.x;
+    if (m >= M) return;
+    float e[4][4], a[4][4], g[4][4];
+    sk1_load(logits + m * 16, e);
+    sk1_load(dP + m * 16, g);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a[i][j] = e[i][j] = expf(e[i][j]);
+    float *store = sk1_st + threadIdx.x;
+    sk4_forward(a, iters, eps, store, kSk1Threads);
+    sk4_backward(g, a, e, iters, store, kSk1Threads);
+    sk1_store(dlogits + m * 16, g);
+}
+
+static size_t sk1_smem(int iters) { return size_t(8) * iters * kSk1Threads * sizeof(float); }
+
 static size_t sk_smem(int iters) { return size_t(2) * iters * kSkThreads * sizeof(float); }
 
 cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n, int iters,
@@ -92,7 +157,8 @@ cudaError_t launch_sinkhorn_fwd(const float *logits, float *P, int64_t M, int n,
     const unsigned grid = unsigned((rows + kSkThreads - 1) / kSkThreads);
     if (n == 4) {
         MHC_PROF("k_sinkhorn_fwd", s);
-        launch_k(k_sinkhorn_fwd<4>, dim3(grid), dim3(kSkThreads), 0, s, logits, P, rows, iters, eps);
+        launch_k(k_sinkhorn1_fwd, dim3(unsigned((M + kSk1Threads - 1) / kSk1Threads)),
+                 dim3(kSk1Threads), 0, s, logits, P, M, iters, eps);
     } else {
         MHC_PROF("k_sinkhorn_fwd", s);
         launch_k(k_sinkhorn_fwd<8>, dim3(grid), dim3(kSkThreads), 0, s, logits, P, rows, iters, eps);
@@ -108,11 +174,12 @@ cudaError_t launch_sinkhorn_bwd(const float *dP, const float *logits, float *dlo
     const size_t smem = sk_smem(iters);
     cudaError_t e;
     if (n == 4) {
-        e = set_smem_limit(reinterpret_cast<const void *>(k_sinkhorn_bwd<4>), int(sk_smem(64)));
+        e = set_smem_limit(reinterpret_cast<const void *>(k_sinkhorn1_bwd), int(sk1_smem(64)));
         if (e != cudaSuccess) return e;
         {
             MHC_PROF("k_sinkhorn_bwd", s);
-            launch_k(k_sinkhorn_bwd<4>, dim3(grid), dim3(kSkThreads), smem, s, dP, logits, dlogits, rows, iters, eps);
+            launch_k(k_sinkhorn1_bwd, dim3(unsigned((M + kSk1Threads - 1) / kSk1Threads)),
+                     dim3(kSk1Threads), sk1_smem(iters), s, dP, logits, dlogits, M, iters, eps);
         }
     } else {
         e = set_smem_limit(reinterpret_cast<const void *>(k_sinkhorn_bwd<8>), int(sk_smem(64)));

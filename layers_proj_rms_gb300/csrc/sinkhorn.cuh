@@ -104,4 +104,87 @@ __device__ __forceinline__ void sk_backward(float (&g)[N], float (&a)[N], const 
     for (int j = 0; j < N; ++j) g[j] = g[j] * e[j];
 }
 
+// ---------------------------------------------------------------------------
+// ---------------------------------------------------------------------------
+// n = 4 with one thread per matrix, the 16 entries in registers.  Row and
+// column sums are local (four independent chains per half-step instead of a
+// shuffle butterfly): row sums ((a0 + a1) + a2) + a3, column sums
+// (a0 + a1) + (a2 + a3), every product and sum explicitly rounded.  A
+// division by a denominator is a multiplication by the hardware's
+// approximate reciprocal (rcp.approx, within an ulp): with one thread per
+// matrix or token there are few warps per SM, so these kernels are bound by
+// their instruction count, of which the correctly rounded reciprocal took
+// half.  The backward reads the 8 denominators of every iteration that the
+// forward stored at store[(8k + d) * stride].
+// ---------------------------------------------------------------------------
+// store: denominators of iteration k at store[(8k + d) * stride], d < 4 the
+// row steps', d >= 4 the column steps' (or null)
+__device__ __forceinline__ void sk4_forward(float (&a)[4][4], int iters, float eps, float *store,
+                                            int stride)
+{
+    for (int k = 0; k < iters; ++k) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float rd =
+                __fadd_rn(__fadd_rn(__fadd_rn(__fadd_rn(a[i][0], a[i][1]), a[i][2]), a[i][3]), eps);
+            const float rinv = rcp_approx(rd);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) a[i][j] = __fmul_rn(a[i][j], rinv);
+            if (store) store[(8 * k + i) * stride] = rd;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float cd = __fadd_rn(
+                __fadd_rn(__fadd_rn(a[0][j], a[1][j]), __fadd_rn(a[2][j], a[3][j])), eps);
+            const float cinv = rcp_approx(cd);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i][j] = __fmul_rn(a[i][j], cinv);
+            if (store) store[(8 * k + 4 + j) * stride] = cd;
+        }
+    }
+}
+
+// Backward, walking the steps in reverse (the gradient sk_backward forms):
+//   column step Y = X / cd_j:  dX[i][j] = (dY[i][j] - sum_i' dY[i'][j] Y[i'][j]) / cd_j
+//   row step    Y = X / rd_i:  dX[i][j] = (dY[i][j] - sum_j' dY[i][j'] Y[i][j']) / rd_i
+// On entry g = dL/dP, a = P, e = exp(z); on exit g = dL/dz (a consumed).
+__device__ __forceinline__ void sk4_backward(float (&g)[4][4], float (&a)[4][4],
+                                             const float (&e)[4][4], int iters, const float *store,
+                                             int stride)
+{
+    for (int k = iters - 1; k >= 0; --k) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float cd = store[(8 * k + 4 + j) * stride];
+            float ga[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ga[i] = __fmul_rn(g[i][j], a[i][j]);
+            const float dot = __fadd_rn(__fadd_rn(ga[0], ga[1]), __fadd_rn(ga[2], ga[3]));
+            const float cinv = rcp_approx(cd);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                g[i][j] = __fmul_rn(__fsub_rn(g[i][j], dot), cinv);
+                a[i][j] = __fmul_rn(a[i][j], cd);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float rd = store[(8 * k + i) * stride];
+            float rdot = __fmul_rn(g[i][0], a[i][0]);
+#pragma unroll
+            for (int j = 1; j < 4; ++j) rdot = fmaf(g[i][j], a[i][j], rdot);
+            const float rinv = rcp_approx(rd);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                g[i][j] = __fmul_rn(__fsub_rn(g[i][j], rdot), rinv);
+                a[i][j] = __fmul_rn(a[i][j], rd);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) g[i][j] = __fmul_rn(g[i][j], e[i][j]);
+}
+
 }  // namespace mhc
