@@ -137,8 +137,11 @@ struct BwdTc {
     // Per-token inputs of a tile in shared memory, one tile ahead.  n = 4:
     // the epilogue copies them with cp.async (H_res row, H_pre row: 20 floats
     // per token; coef).  n = 8 (layer): the producer loads them by TMA, H_res
-    // as two 128-byte-swizzled boxes of 32 floats per token, H_pre and H_post
-    // as 32-byte-swizzled boxes of 8 floats (conflict-free row reads).
+    // transposed (the Hres argument is then HresT[t][i][j] = H_res[t][j][i],
+    // which the compute_h backward writes, so that a dout stream's eight
+    // weights are two 16-byte reads) as two 128-byte-swizzled boxes of 32
+    // floats per token, H_pre and H_post as 32-byte-swizzled boxes of 8
+    // floats (conflict-free row reads).
     static constexpr bool STAGE_P = N == 4;
     static constexpr bool TMA_P = N == 8;
     static constexpr int PAR_ROW = 20 * 4;
@@ -706,16 +709,29 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
 #pragma unroll
                         for (int p = 0; p < 4; ++p) df[p] = f2_fma(w2, dv[p], df[p]);
                     }
+                    // n = 8: the parameter buffer holds H_res transposed, so
+                    // H_res[t][0..8)[ii] are two 16-byte chunks of row ii of
+                    // HresT (128-byte-swizzled rows of 32 floats)
+                    float hcol[N];
+                    if (TP) {
+                        const uint32_t pb = tc::smem_u32(smem + P::PAR_OFF) +
+                                            ((ii * N) >> 5) * (P::TT * 128) + r * 128;
+#pragma unroll
+                        for (int c4 = 0; c4 < N / 4; ++c4) {
+                            const int chunk = (((ii * N) & 31) >> 2) + c4;
+                            const uint4 v = lds128(pb + ((chunk ^ (r & 7)) << 4));
+                            hcol[4 * c4] = __uint_as_float(v.x);
+                            hcol[4 * c4 + 1] = __uint_as_float(v.y);
+                            hcol[4 * c4 + 2] = __uint_as_float(v.z);
+                            hcol[4 * c4 + 3] = __uint_as_float(v.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < N; ++j) hcol[j] = hres[j * N + ii];
+                    }
 #pragma unroll
                     for (int j = 0; j < N; ++j) {
-                        // n = 8: H_res[t][j][ii] read where it is used from the
-                        // 128-byte-swizzled rows of the parameter buffer
-                        const int e = j * N + ii;
-                        const float hw =
-                            TP ? lds32f(tc::smem_u32(smem + P::PAR_OFF) + (e >> 5) * (P::TT * 128) +
-                                        r * 128 + ((((e & 31) >> 2) ^ (r & 7)) << 4) + (e & 3) * 4)
-                               : hres[e];
-                        const f32x2 w2 = f2_make(hw, hw);
+                        const f32x2 w2 = f2_make(hcol[j], hcol[j]);
 #pragma unroll
                         for (int p = 0; p < 4; ++p) mix[j][p] = f2_fma(w2, dv[p], mix[j][p]);
                     }

@@ -101,12 +101,25 @@ __global__ void __launch_bounds__(128)
                     float eps_rms, bf16 *__restrict__ du_hl, int du_cols,
                     float *__restrict__ coef, float *__restrict__ part,
                     const float *__restrict__ s_tot, float *__restrict__ du_f32,
-                    float *__restrict__ dub)
+                    float *__restrict__ dub, const float *__restrict__ Hres,
+                    float *__restrict__ HresT)
 {
     pdl_wait();
     constexpr int O = Dims<N>::O;
     constexpr int PW = O + 4, TB = 128 / N;
     extern __shared__ float sk_store[];  // [2*iters][blockDim.x]
+    if (HresT) {
+        // the layer's H_res transposed, HresT[t][i][j] = H_res[t][j][i], for
+        // the residual-gradient pass (lane i of a token copies row i of
+        // H_res into column i)
+        const int64_t gt0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+        const int64_t t0 = gt0 / N;
+        const int i0 = int(gt0 % N);
+        if (t0 < T) {
+#pragma unroll
+            for (int j = 0; j < N; ++j) HresT[(t0 * N + j) * N + i0] = __ldg(Hres + (t0 * N + i0) * N + j);
+        }
+    }
     __shared__ float red[TB][PW];
     const int64_t gt = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t t = gt / N;
@@ -430,7 +443,7 @@ static cudaError_t launch_ch_bwd(const float *dHpre, const float *dHpost, const 
                                  const float *b, int64_t T, int64_t K, int iters, float eps_sk,
                                  float eps_rms, bf16 *du_hl, int du_cols, float *coef,
                                  float *part, const float *s_tot, float *du_f32, float *dub,
-                                 cudaStream_t s)
+                                 const float *Hres, float *HresT, cudaStream_t s)
 {
     const int64_t prows = (T * N + 127) / 128;
     cudaError_t e;
@@ -452,7 +465,7 @@ static cudaError_t launch_ch_bwd(const float *dHpre, const float *dHpost, const 
         launch_k(k_compute_h_bwd<N>, dim3(unsigned(prows)), dim3(128),
                  size_t(2) * iters * 128 * sizeof(float), s, dHpre, dHpost, dHres, u_save, r_save,
                  alpha, b, T, K, iters, eps_sk, eps_rms, du_hl, du_cols, coef, part, s_tot, du_f32,
-                 dub);
+                 dub, Hres, HresT);
     }
     return cudaGetLastError();
 }
@@ -571,7 +584,7 @@ cudaError_t launch_proj_fwd(const bf16 *x, const float *W, const float *alpha, c
 //   (layer), dbias partials [S][C], dW partials [S][K][O] (only when S > 1)
 struct BwdWs {
     bf16 *du_hl;
-    float *du32, *dub, *coef, *part, *dHpre, *dHpost, *dHres, *dWpart, *dbiaspart;
+    float *du32, *dub, *coef, *part, *dHpre, *dHpost, *dHres, *HresT, *dWpart, *dbiaspart;
     int splits;
     size_t bytes;
 };
@@ -596,6 +609,7 @@ static BwdWs carve_bwd(void *base, int64_t T, int n, int64_t C)
     w.dHpre = reinterpret_cast<float *>(take(size_t(T * n) * 4));
     w.dHpost = reinterpret_cast<float *>(take(size_t(T * n) * 4));
     w.dHres = reinterpret_cast<float *>(take(size_t(T * n * n) * 4));
+    w.HresT = n == 8 ? reinterpret_cast<float *>(take(size_t(T * n * n) * 4)) : nullptr;
     w.dbiaspart = reinterpret_cast<float *>(take(size_t(w.splits) * size_t(C) * 4));
     w.dWpart = w.splits > 1 ? reinterpret_cast<float *>(take(size_t(w.splits) * size_t(K * O) * 4))
                             : nullptr;
@@ -635,8 +649,11 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
         dHres = w.dHres;
     }
     const int64_t prows = (T * N + 127) / 128;
+    // n = 8 (layer): H_res transposed for the residual-gradient pass's mix
+    const bool hT = L && N == 8;
     e = launch_ch_bwd<N>(dHpre, dHpost, dHres, u_save, r_save, alpha, b, T, K, iters, eps_sk,
-                         eps_rms, w.du_hl, du_cols, w.coef, w.part, nullptr, w.du32, w.dub, s);
+                         eps_rms, w.du_hl, du_cols, w.coef, w.part, nullptr, w.du32, w.dub,
+                         hT ? L->Hres : nullptr, hT ? w.HresT : nullptr, s);
     if (e != cudaSuccess) return e;
     // pass 2: residual gradient, dW and dbias on the tensor cores; an unsplit
     // pass writes dW and dbias directly
@@ -647,7 +664,8 @@ static cudaError_t bwd_impl(const float *dHpre, const float *dHpost, const float
     float *dbias = L ? L->dbias : nullptr;
     e = launch_bwd_tc(x, W, w.du_hl, w.du32, w.dub, w.coef, T, N, C, L ? L->dout : nullptr,
                       L ? L->dy : nullptr,
-                      L ? L->Hpre : nullptr, L ? L->Hres : nullptr, L ? L->Hpost : nullptr, dx,
+                      L ? L->Hpre : nullptr, L ? (hT ? w.HresT : L->Hres) : nullptr,
+                      L ? L->Hpost : nullptr, dx,
                       split ? w.dWpart : dW, (split || !dbias) ? w.dbiaspart : dbias,
                       splits_used, fault, s);
     if (e != cudaSuccess) return e;
@@ -774,7 +792,7 @@ static cudaError_t compute_h_bwd_impl(const float *dHpre, const float *dHpost,
     const int64_t prows = (T * N + 127) / 128;
     cudaError_t e = launch_ch_bwd<N>(dHpre, dHpost, dHres, u, nullptr, alpha, b, T, K, iters,
                                      eps_sk, eps_rms, du_hl, bwd_tc_du_cols(N), coef, part, s_tot,
-                                     du, nullptr, s);
+                                     du, nullptr, nullptr, nullptr, s);
     if (e != cudaSuccess) return e;
     {
         MHC_PROF("k_bwd_finalize", s);
