@@ -379,10 +379,14 @@ struct PostProj8 {
     static constexpr int WBOX = NB * RB;                                  // 7.5 KB
     static constexpr int WSTAGE = N * WBOX;                               // 60 KB
     static constexpr int XSTAGES = 3, WSTAGES = 2;
-    // x and f are also prefetched into L2 in boxes of PF_C channels (128-byte
+    // x and f are also prefetched into L2 in boxes of PF_C channels (64-byte
     // rows: a stage's own 32-byte rows, 14 KB apart, make poor DRAM bursts),
-    // PF_AHEAD stages ahead of the loads
-    static constexpr int PF_C = 64, PF_STAGES = PF_C / BC, PF_AHEAD = 8;
+    // PF_AHEAD stages ahead of the loads.  Measured at T = 8192, C = 7168:
+    // 32 channels 2 stages ahead 0.522 ms; 64 channels 4 ahead 0.530; none
+    // 0.545; 64 channels 8 ahead 0.579 and 128 channels 8 ahead 0.581 (what
+    // is prefetched that far ahead is evicted by the streaming out stores
+    // before use and read again: 623 MB of DRAM reads for 292 MB of inputs)
+    static constexpr int PF_C = 32, PF_STAGES = PF_C / BC, PF_AHEAD = 2;
     static constexpr int W_OFF = XSTAGES * XSTAGE;
     static constexpr int B_OFF = W_OFF + WSTAGES * WSTAGE;                // bias[16] per x stage,
     static constexpr int BSLOT = 128;                                     // TMA destinations 128-byte aligned
