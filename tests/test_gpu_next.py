@@ -330,7 +330,8 @@ def _post_proj_inputs(T, n, C, seed, alpha=(0.5, 0.8, 1.0), w_std=0.02):
 
 def _run_post_proj(M, p, T, n, C):
     O = n * n + 2 * n
-    d = {"res": dev_bf16(p["res"]), "f": dev_bf16(p["f"]), "bias": dev_bf16(p["bias"]),
+    d = {"res": dev_bf16(p["res"]), "f": dev_bf16(p["f"]),
+         "bias": None if p["bias"] is None else dev_bf16(p["bias"]),
          "Hres": dev_f32(p["Hres"]), "Hpost": dev_f32(p["Hpost"]), "W2": dev_f32(p["W2"]),
          "a2": dev_f32(p["a2"]), "b2": dev_f32(p["b2"])}
     bufs, o = {}, {}
@@ -391,7 +392,9 @@ def _check_post_proj(orc, p, o, n, idx):
     ti = torch.from_numpy(np.arange(o["out"].shape[0])[idx]).cuda()
     Tn = int(ti.numel())
     res = p["res"][idx]
-    comp = orc.h_post_bda_compute_h_fwd(_f64(res), _f64(p["f"][idx]), _f64(p["bias"]),
+    C = p["res"].shape[2]
+    bias64 = np.zeros(C) if p["bias"] is None else _f64(p["bias"])
+    comp = orc.h_post_bda_compute_h_fwd(_f64(res), _f64(p["f"][idx]), bias64,
                                         p["Hres"][idx], p["Hpost"][idx], p["W2"], p["a2"],
                                         p["b2"], n, ITERS, EPS_SK, EPS_RMS)
     out_k = host(o["out"][ti])
@@ -403,7 +406,7 @@ def _check_post_proj(orc, p, o, n, idx):
     ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(xr), 2.0 ** -126))) - 7)
     # where the post-mix cancels, the fp32 sum's own rounding (a few 2^-24 of
     # the sum of the terms' magnitudes) can exceed one ulp of the result
-    terms = (np.abs(p["Hpost"][idx])[:, :, None] * np.abs(_f64(p["f"][idx]) + _f64(p["bias"]))[:, None, :]
+    terms = (np.abs(p["Hpost"][idx])[:, :, None] * np.abs(_f64(p["f"][idx]) + bias64)[:, None, :]
              + np.einsum("tji,tjc->tic", np.abs(p["Hres"][idx]).astype(np.float64), np.abs(_f64(res))))
     slack = np.maximum(ulp, 2.0 ** -20 * terms.reshape(Tn, -1))
     assert np.all(np.abs(out_k.reshape(Tn, -1) - xr)[diff] <= slack[diff]), \
@@ -435,6 +438,22 @@ def test_post_bda_compute_h_fused_7b_sampled(M, orc):
     g = np.random.Generator(np.random.PCG64(9))
     idx = np.unique(np.concatenate([[0, 127, 128, T - 1], g.choice(T, 40, replace=False)]))
     _check_post_proj(orc, p, o, n, idx)
+
+
+@pytest.mark.parametrize("T,n,C", [(130, 4, 96), (1, 8, 16), (300, 8, 264)])
+def test_post_bda_compute_h_fused_no_bias(M, orc, T, n, C):
+    """bias = NULL (the n = 8 kernel then loads no bias box); one token at
+    n = 8; against the two ops run one after the other and the oracle."""
+    p = _post_proj_inputs(T, n, C, 900 + T + C)
+    p["bias"] = None
+    d, bufs, o = _run_post_proj(M, p, T, n, C)
+    out_sep = torch.empty_like(o["out"])
+    M.mhc_h_post_bda_fwd(d["res"], d["f"], None, d["Hres"], d["Hpost"], out_sep)
+    torch.cuda.synchronize()
+    for b in bufs.values():
+        check_canary(b)
+    assert torch.equal(o["out"], out_sep), "fused out differs from h_post_bda"
+    _check_post_proj(orc, p, o, n, slice(None))
 
 
 def test_post_bda_compute_h_fused_n8_sampled(M, orc):
