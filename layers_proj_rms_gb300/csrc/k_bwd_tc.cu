@@ -245,9 +245,9 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            // the MMAs' commit + every epilogue thread: each thread releases a
-            // buffer after its own reads of it (tc::mbar_release)
-            tc::mbar_init(&empty[s], 1 + 32 * P::EPI_WARPS);
+            // the MMAs' commit + one arrival per epilogue warp (the other
+            // buffers: every thread releases after its own reads, tc::mbar_release)
+            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
         }
         tc::mbar_init(&wfull, 32 * P::EPI_WARPS);
         for (int b = 0; b < 2; ++b) {
@@ -772,10 +772,16 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 }
             }
             // D2 buffer b and the stage have been read: release them
+            // (one arrival per warp: every value this thread read from the
+            // stage has been consumed by the dx stores above, so no read of
+            // the stage is in flight; a per-thread acq_rel fence here also
+            // waited for those global stores, 5 us per launch at n = 4)
             tc::tc_fence_before();
-            tc::mbar_release(&empty[s]);
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&d2empty[b]);
+            if (lane == 0) {
+                tc::mbar_arrive(&empty[s]);
+                tc::mbar_arrive(&d2empty[b]);
+            }
         }
         if (P::STAGE_P) tc::cp_async_wait_all();
         if (!ok) *abort_v = 1;
