@@ -8,10 +8,10 @@
 // Layout in registers: a group of N consecutive lanes (N in {4, 8}, aligned
 // to N) holds one matrix; lane i of the group holds row i as N floats.  Row
 // sums are local; column sums are a butterfly over the group's lanes.  A
-// division by a denominator is a multiplication by its correctly rounded
-// reciprocal (one reciprocal per row step, one per column; within an ulp of
-// the quotient).  All
-// 32 lanes of the warp must call these functions together (the shuffles use
+// division by a denominator is a multiplication by the hardware's
+// approximate reciprocal (rcp.approx, within an ulp of 1/d; one per row
+// step, one per column), as in the one-thread-per-matrix form below.  All 32
+// lanes of the warp must call these functions together (the shuffles use
 // the full mask); a group without work runs on dummy data.
 #pragma once
 
@@ -44,7 +44,7 @@ __device__ __forceinline__ void sk_forward(float (&a)[N], int iters, float eps, 
 #pragma unroll
         for (int j = 0; j < N; ++j) rs += a[j];
         const float rd = rs + eps;
-        const float rinv = 1.0f / rd;
+        const float rinv = rcp_approx(rd);
 #pragma unroll
         for (int j = 0; j < N; ++j) a[j] *= rinv;
         float cs[N];
@@ -53,7 +53,7 @@ __device__ __forceinline__ void sk_forward(float (&a)[N], int iters, float eps, 
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             const float cd = cs[j] + eps;
-            a[j] *= 1.0f / cd;
+            a[j] *= rcp_approx(cd);
             if (j == i) cd_mine = cd;
         }
         if (store) {
@@ -87,13 +87,13 @@ __device__ __forceinline__ void sk_backward(float (&g)[N], float (&a)[N], const 
         for (int j = 0; j < N; ++j) cd[j] = __shfl_sync(kFull, cd_mine, base + j);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
-            g[j] = (g[j] - dot[j]) * (1.0f / cd[j]);
+            g[j] = (g[j] - dot[j]) * rcp_approx(cd[j]);
             a[j] = a[j] * cd[j];
         }
         float rdot = 0.f;
 #pragma unroll
         for (int j = 0; j < N; ++j) rdot += g[j] * a[j];
-        const float rinv = 1.0f / rd;
+        const float rinv = rcp_approx(rd);
 #pragma unroll
         for (int j = 0; j < N; ++j) {
             g[j] = (g[j] - rdot) * rinv;
