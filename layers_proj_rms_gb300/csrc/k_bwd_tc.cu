@@ -774,8 +774,10 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             // D2 buffer b and the stage have been read: release them
             // (one arrival per warp: every value this thread read from the
             // stage has been consumed by the dx stores above, so no read of
-            // the stage is in flight; a per-thread acq_rel fence here also
+            // the stage is in flight, and the proxy fence orders the reads
+            // before the refill by TMA; a per-thread acq_rel fence here also
             // waited for those global stores, 5 us per launch at n = 4)
+            tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {

@@ -747,17 +747,23 @@ __global__ void __launch_bounds__(256) k_w_tile(const float *__restrict__ W, bf1
     }
     __syncthreads();
     uint8_t *dst = reinterpret_cast<uint8_t *>(Wt) + (int64_t(cb) * P::N + j) * P::WBOX;
-    for (int it = threadIdx.x; it < CHUNKS * P::NB; it += blockDim.x) {
-        const int cc = it / P::NB, r = it % P::NB;
-        const int part = r / O, o = r % O;
-        float v[8];
+    // item: output o and 16-byte chunk cc; its three terms go to rows o,
+    // O + o and 2O + o (zero rows past 3O by the items that follow)
+    for (int it = threadIdx.x; it < CHUNKS * O; it += blockDim.x) {
+        const int cc = it / O, o = it % O;
+        float hi[8], lo[8], lo2[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float hi = 0.f, lo = 0.f, lo2 = 0.f;
-            if (part < 3) w_terms(ws[(8 * cc + e) * OP + o], hi, lo, lo2);
-            v[e] = part == 0 ? hi : part == 1 ? lo : lo2;
+        for (int e = 0; e < 8; ++e) w_terms(ws[(8 * cc + e) * OP + o], hi[e], lo[e], lo2[e]);
+        *reinterpret_cast<uint4 *>(dst + P::chunk_off(o, cc)) = pack8(hi);
+        *reinterpret_cast<uint4 *>(dst + P::chunk_off(O + o, cc)) = pack8(lo);
+        *reinterpret_cast<uint4 *>(dst + P::chunk_off(2 * O + o, cc)) = pack8(lo2);
+    }
+    if constexpr (P::NB > 3 * O) {
+        constexpr int ZR = P::NB - 3 * O;
+        for (int it = threadIdx.x; it < CHUNKS * ZR; it += blockDim.x) {
+            const int cc = it / ZR, r = 3 * O + it % ZR;
+            *reinterpret_cast<uint4 *>(dst + P::chunk_off(r, cc)) = make_uint4(0, 0, 0, 0);
         }
-        *reinterpret_cast<uint4 *>(dst + P::chunk_off(r, cc)) = pack8(v);
     }
 }
 

@@ -124,21 +124,26 @@ __global__ void __launch_bounds__(256) k_w_split(const float *__restrict__ W, bf
     const int kn = int(K - k0 < kWsplitK ? K - k0 : kWsplitK);   // a multiple of 8
     for (int i = threadIdx.x; i < kn * O; i += blockDim.x) ws[(i / O) * OP + i % O] = __ldg(W + k0 * O + i);
     __syncthreads();
-    // item: output row ro (o of the hi, lo or lo2 rows; zero rows past 3O)
-    // and 8-wide group kg of the tile's k
+    // item: output o and 8-wide group kg of the tile's k; its three terms go
+    // to rows o, O + o and 2O + o (zero rows past 3O, if any, by the items
+    // that follow)
     constexpr int NB = w_split_rows(N);
-    for (int it = threadIdx.x; it < NB * (kWsplitK / 8); it += blockDim.x) {
-        const int ro = it / (kWsplitK / 8), kg = it % (kWsplitK / 8);
+    constexpr int KG = kWsplitK / 8;
+    for (int it = threadIdx.x; it < O * KG; it += blockDim.x) {
+        const int o = it / KG, kg = it % KG;
         if (kg * 8 >= kn) continue;
-        const int part = ro / O, o = ro % O;
-        float v[8];
+        float hi[8], lo[8], lo2[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            float hi = 0.f, lo = 0.f, lo2 = 0.f;
-            if (part < 3) w_terms(ws[(kg * 8 + e) * OP + o], hi, lo, lo2);
-            v[e] = part == 0 ? hi : part == 1 ? lo : lo2;
-        }
-        *reinterpret_cast<uint4 *>(Whl + int64_t(ro) * K + k0 + kg * 8) = pack8(v);
+        for (int e = 0; e < 8; ++e) w_terms(ws[(kg * 8 + e) * OP + o], hi[e], lo[e], lo2[e]);
+        bf16 *dst = Whl + int64_t(o) * K + k0 + kg * 8;
+        *reinterpret_cast<uint4 *>(dst) = pack8(hi);
+        *reinterpret_cast<uint4 *>(dst + int64_t(O) * K) = pack8(lo);
+        *reinterpret_cast<uint4 *>(dst + int64_t(2 * O) * K) = pack8(lo2);
+    }
+    for (int it = threadIdx.x; it < (NB - 3 * O) * KG; it += blockDim.x) {
+        const int ro = 3 * O + it / KG, kg = it % KG;
+        if (kg * 8 >= kn) continue;
+        *reinterpret_cast<uint4 *>(Whl + int64_t(ro) * K + k0 + kg * 8) = make_uint4(0, 0, 0, 0);
     }
 }
 

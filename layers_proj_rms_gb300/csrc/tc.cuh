@@ -48,14 +48,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 
 // A consumer thread's release of a buffer it has read (or written) with
 // ordinary shared-memory accesses, before the producer refills it by TMA (or
-// the tensor cores read it): fence.acq_rel.cta makes this thread's accesses
-// complete before its arrival.  Measured on GB300: without the fence, with
-// the arrival alone (also when spelled mbarrier.arrive.release.cta), a
-// thread's outstanding shared-memory loads could still be in flight when the
-// producer's refill landed, and results changed from run to run.
+// the tensor cores read it).  The refill is a write by the async proxy, so
+// this thread's generic-proxy accesses are ordered before it by a proxy
+// fence, and fence.acq_rel.cta makes them complete before the arrival.
+// Measured on GB300: with the arrival alone (also when spelled
+// mbarrier.arrive.release.cta) results changed from run to run at n = 8;
+// with the acq_rel fence but no proxy fence, about one backward in twenty
+// still read a few rows of the next tile's dout in the residual-gradient pass.
 __device__ __forceinline__ void mbar_release(uint64_t *bar)
 {
-    asm volatile("fence.acq_rel.cta;\n"
+    asm volatile("fence.proxy.async.shared::cta;\n"
+                 "fence.acq_rel.cta;\n"
                  "mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }

@@ -13,7 +13,7 @@ import pytest
 import torch
 
 import mhc_inputs as mi
-from tests._util import err_bf16, err_grad, err_h
+from tests._util import dev_bf16, dev_f32, err_bf16, err_grad, err_h
 from tests.test_gpu_ops import ITERS, EPS_SK, EPS_RMS, run_layer
 
 pytestmark = pytest.mark.gpu
@@ -86,3 +86,42 @@ def test_rmsnorm_16384x4096(M, orc):
     err_bf16(y[ti], ry)
     err_grad(rstd[ti], rr, rel=1e-6)
     err_bf16(dx[ti], orc.rmsnorm_bwd(inp["dy_norm"][idx], inp["x_norm"][idx], 1e-6))
+
+
+@pytest.mark.parametrize("T,n,C,reps", [(8192, 8, 7168, 30), (16384, 4, 4096, 15)])
+def test_layer_bwd_bitwise_repeats(M, T, n, C, reps):
+    """The layer backward repeated on the same inputs gives the same bits
+    every time.  Catches a buffer of the residual-gradient pass refilled by TMA
+    while some thread still reads the previous tile from it (seen on GB300
+    at n = 8 in about one backward in twenty, a few token rows of one
+    8-channel chunk reading the next tile's dout, before the consumers'
+    releases carried a proxy fence)."""
+    O = n * n + 2 * n
+    inp = mi.layer_inputs(T, n, C, 4 if n == 8 else 3, w_std=0.01 if n == 8 else 0.02)
+    t = {k: (dev_bf16(v) if v.dtype == np.uint16 else dev_f32(v)) for k, v in inp.items()
+         if v is not None}
+    e = lambda *s, dt=torch.float32: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    bf = torch.bfloat16
+    o = {"H_pre": e(T, n), "H_post": e(T, n), "H_res": e(T, n, n), "u": e(T, O), "r": e(T),
+         "y": e(T, C, dt=bf), "out": e(T, n, C, dt=bf), "dx": e(T, n, C, dt=bf),
+         "df": e(T, C, dt=bf), "dW": e(n * C, O), "dalpha": e(3), "db": e(O), "dbias": e(C)}
+    wsf = M.workspace(M.OP_LAYER_FWD, T, n, C)
+    wsb = M.workspace(M.OP_LAYER_BWD, T, n, C)
+    M.mhc_layer_fwd(t["x"], t["W"], t["alpha"], t["b"], t["f"], t["bias"], ITERS, EPS_SK,
+                    EPS_RMS, o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], o["y"],
+                    o["out"], wsf)
+
+    def bwd():
+        M.mhc_layer_bwd(t["dout"], t["dy"], t["x"], t["W"], t["alpha"], t["b"], t["f"],
+                        t["bias"], o["H_pre"], o["H_post"], o["H_res"], o["u"], o["r"], ITERS,
+                        EPS_SK, EPS_RMS, o["dx"], o["df"], o["dW"], o["dalpha"], o["db"],
+                        o["dbias"], wsb)
+
+    bwd()
+    torch.cuda.synchronize()
+    ref = {k: o[k].clone() for k in ("dx", "df", "dW", "dalpha", "db", "dbias")}
+    for rep in range(reps):
+        bwd()
+        torch.cuda.synchronize()
+        for k, v in ref.items():
+            assert torch.equal(o[k], v), f"repeat {rep}: {k} differs from the first backward"
