@@ -530,6 +530,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         const int64_t cc = c0 + h * 8;       // first channel of the chunk
         const bool cvalid = cc < C;          // the last slice may pass C
         float bias_acc = 0.f;                // lane l: running total of channel cc + (l % 8)
+        f32x2 dfacc[4] = {0ull, 0ull, 0ull, 0ull};
         bool ok = true;
         // The four warps of a quadrant share its 32 token rows: together they
         // copy the rows' inputs of a tile into shared memory one tile ahead
@@ -553,6 +554,13 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             tc::cp_async_commit();
         };
         if (P::STAGE_P && ntiles > 0) stage_params(tile0);
+        // n = 8: coef and sum |du| of a tile are loaded one tile ahead (a load
+        // issued at the tile's start comes back from L2 after its first use)
+        float coef_nx = 0.f, dub_nx = 0.f;
+        if (!P::STAGE_P && ntiles > 0 && int64_t(tile0) * P::TT + r < a.T) {
+            coef_nx = __ldg(a.coef + int64_t(tile0) * P::TT + r);
+            dub_nx = __ldg(a.dub + int64_t(tile0) * P::TT + r);
+        }
         for (int i = 0; i < ntiles; ++i) {
             const int s = i % P::STAGES, b = i & 1;
             const int64_t t = int64_t(tile0 + i) * P::TT + r;
@@ -592,9 +600,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 if (i + 1 < ntiles) stage_params(tile0 + i + 1);
                 if (!ok) continue;
             } else {
+                coef = coef_nx;
+                dub = dub_nx;
+                coef_nx = dub_nx = 0.f;
+                if (i + 1 < ntiles && t + P::TT < a.T) {
+                    coef_nx = __ldg(a.coef + t + P::TT);
+                    dub_nx = __ldg(a.dub + t + P::TT);
+                }
                 if (valid) {
-                    coef = __ldg(a.coef + t);
-                    dub = __ldg(a.dub + t);
                     if (LAYER && !TP) {
 #pragma unroll
                         for (int j = 0; j < N; ++j) {
@@ -690,7 +703,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             // (element pairs in f32x2 arithmetic)
             f32x2 mix[LAYER ? N : 1][4];
             if (LAYER) {
-                f32x2 gyv[4], df[4];
+                f32x2 gyv[4];
                 unpack8x2(gy, gyv);
 #pragma unroll
                 for (int j = 0; j < N; ++j) {
@@ -699,15 +712,13 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     for (int p = 0; p < 4; ++p) mix[j][p] = f2_mul(w2, gyv[p]);
                 }
 #pragma unroll
-                for (int p = 0; p < 4; ++p) df[p] = 0ull;
-#pragma unroll
                 for (int ii = 0; ii < N; ++ii) {
                     f32x2 dv[4];
                     unpack8x2(g[ii], dv);
                     if (!SG) {
                         const f32x2 w2 = f2_make(hpost[ii], hpost[ii]);
 #pragma unroll
-                        for (int p = 0; p < 4; ++p) df[p] = f2_fma(w2, dv[p], df[p]);
+                        for (int p = 0; p < 4; ++p) dfacc[p] = f2_fma(w2, dv[p], dfacc[p]);
                     }
                     // n = 8: the parameter buffer holds H_res transposed, so
                     // H_res[t][0..8)[ii] are two 16-byte chunks of row ii of
@@ -739,12 +750,6 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 if (TP) {
                     // this thread has read the parameter buffer
                     tc::mbar_release(&pempty);
-                }
-                if (!SG) {
-                    float dfs[8];
-#pragma unroll
-                    for (int p = 0; p < 4; ++p) f2_split(df[p], dfs[2 * p], dfs[2 * p + 1]);
-                    bias_acc += warp_column_sum<8>(dfs);
                 }
             }
             // dx_gemm of this chunk for every stream: all TMEM loads, one wait
@@ -823,6 +828,12 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                                 hi[4 * o4 + 2] + lo[4 * o4 + 2], hi[4 * o4 + 3] + lo[4 * o4 + 3]);
                 }
             }
+        }
+        if (LAYER && !SG) {
+            float dfs[8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) f2_split(dfacc[p], dfs[2 * p], dfs[2 * p + 1]);
+            bias_acc = warp_column_sum<8>(dfs);
         }
         if (LAYER && !SG && lane < 8) bias_red[q][h * 8 + lane] = bias_acc;
         if (SG && h == 0) {
