@@ -154,10 +154,16 @@ struct BwdTc {
     static constexpr int G1_BYTES = N == 4 ? 0 : (N + 1) * XBOX;       // 36 KB
     static constexpr int SMEM = G1_OFF + G1_BYTES + 1024;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
+    // dx leaves through shared memory: the epilogue writes each dx chunk over
+    // the x chunk it has just read (the stream boxes of the stage have dx's
+    // layout), and one thread per TMEM lane quadrant stores the quadrant's 32
+    // token rows of every stream by TMA (whole rows, where per-lane 16-byte
+    // global stores touched 32 rows per warp instruction)
+    static constexpr bool TMA_DX = true;
     static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0 && PAR_OFF % 1024 == 0 &&
                       W_OFF % 1024 == 0 && (N == 4 || G1_OFF % 1024 == 0),
                   "alignment");
-    static_assert(SMEM + 512 <= 232448, "shared memory");
+    static_assert(SMEM + 1024 <= 232448, "shared memory (dynamic + static)");
 };
 
 // Column sums over the 32 lanes of a warp: on entry every lane holds COLS
@@ -199,11 +205,17 @@ struct BwdTcArgs {
 // 16-byte chunk `chunk` of token row r of a stream box in the 64-byte (n=4)
 // or 32-byte (n=8) swizzle layout that TMA writes.
 template <int N>
-__device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
+__device__ __forceinline__ uint32_t box_chunk_addr(const uint8_t *box, int r, int chunk)
 {
     constexpr int XROW = BwdTc<N>::XROW;
     const int phys = N == 4 ? (chunk ^ ((r >> 1) & 3)) : (chunk ^ ((r >> 2) & 1));
-    return lds128(tc::smem_u32(box) + r * XROW + phys * 16);
+    return tc::smem_u32(box) + r * XROW + phys * 16;
+}
+
+template <int N>
+__device__ __forceinline__ uint4 box_chunk(const uint8_t *box, int r, int chunk)
+{
+    return lds128(box_chunk_addr<N>(box, r, chunk));
 }
 
 template <int N, bool LAYER>
@@ -212,7 +224,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
              const __grid_constant__ CUtensorMap tmg,
              const __grid_constant__ CUtensorMap tmy, const __grid_constant__ CUtensorMap tmdu2,
              const __grid_constant__ CUtensorMap tmhres, const __grid_constant__ CUtensorMap tmhpre,
-             const __grid_constant__ CUtensorMap tmhpost, const BwdTcArgs a)
+             const __grid_constant__ CUtensorMap tmhpost, const __grid_constant__ CUtensorMap tmdx,
+             const BwdTcArgs a)
 {
     pdl_wait();
     using P = BwdTc<N>;
@@ -222,6 +235,9 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     constexpr bool G1 = LAYER && N == 8;      // dout and dy in the G buffer
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t full[P::STAGES], empty[P::STAGES];
+    // xfree: the tile's MMAs have read the stage's x; dxfull[s][q]: quadrant
+    // q's dx rows are in the stage
+    __shared__ uint64_t xfree[P::STAGES], dxfull[P::STAGES][4];
     __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full, pfull, pempty, dufull, duempty,
         gfull, gempty;
     __shared__ uint32_t tmem_slot;
@@ -248,6 +264,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             // the MMAs' commit + one arrival per epilogue warp (the other
             // buffers: every thread releases after its own reads, tc::mbar_release)
             tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
+            tc::mbar_init(&xfree[s], 1);
+            for (int q = 0; q < 4; ++q) tc::mbar_init(&dxfull[s][q], 32 * P::CHUNKS);
         }
         tc::mbar_init(&wfull, 32 * P::EPI_WARPS);
         for (int b = 0; b < 2; ++b) {
@@ -276,6 +294,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmx);
             tc::tma_prefetch_desc(&tmdu);
+            if (P::TMA_DX) tc::tma_prefetch_desc(&tmdx);
             if (SG) {
                 tc::tma_prefetch_desc(&tmg);
                 tc::tma_prefetch_desc(&tmy);
@@ -442,6 +461,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         tc::mma_bf16(tmem + P::D1_COL + 128, ad, bd2, idesc_dw2, acc);
                     }
                 }
+                if (P::TMA_DX) tc::mma_commit(&xfree[s]);
                 if (SG) {
                     // dbias: dout^T [du_hl | H_post hi | H_post lo] over the tile
                     constexpr uint32_t idesc_db = tc::idesc_bf16_f32(128, P::D3_N, 1, 1);
@@ -755,6 +775,14 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             // dx_gemm of this chunk for every stream: all TMEM loads, one wait
             constexpr int JB = 2;  // streams per batch of TMEM loads
             const f32x2 coef2 = f2_make(coef, coef);
+            // dx overwrites x in the stage once the tile's dW MMAs have read it
+            if (P::TMA_DX &&
+                (*abort_v ||
+                 !tc::mbar_wait(&xfree[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutAcc))) {
+                ok = false;
+                if (P::STAGE_P) continue;
+                break;
+            }
 #pragma unroll
             for (int j0 = 0; j0 < N; j0 += JB) {
                 float acc[JB][8];
@@ -773,7 +801,40 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         o[p] = f2_fma(coef2, xv[p], f2_make(acc[jj][2 * p], acc[jj][2 * p + 1]));
                         if (LAYER) o[p] = f2_add(o[p], mix[j][p]);
                     }
-                    if (valid && cvalid) st_stream(a.dx + ((t * N + j) * C + cc), pack8x2(o));
+                    if (P::TMA_DX) {
+                        const uint4 v = pack8x2(o);
+                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                         box_chunk_addr<N>(st + j * P::XBOX, r, h)),
+                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                     : "memory");
+                    } else if (valid && cvalid) {
+                        st_stream(a.dx + ((t * N + j) * C + cc), pack8x2(o));
+                    }
+                }
+            }
+            if (P::TMA_DX) {
+                // this thread's dx chunks are in the stage (made visible to
+                // the TMA engine); the quadrant's chunk-0 lane 0 stores the
+                // quadrant's rows once all of them are (rows past T and
+                // channels past C are clipped by the store) and waits until
+                // the stores have read the stage before the stage goes back
+                tc::fence_proxy_async_smem();
+                tc::mbar_arrive(&dxfull[s][q]);
+                if (h == 0 && lane == 0) {
+                    if (tc::mbar_wait(&dxfull[s][q], (i / P::STAGES) & 1, a.fault,
+                                      tc::kFaultTimeoutFull)) {
+                        const int z = (tile0 + i) * P::TT + q * 32;
+                        if (z < a.T) {
+#pragma unroll 1
+                            for (int j = 0; j < N; ++j)
+                                tc::tma_store_3d(&tmdx, st + j * P::XBOX + q * 32 * P::XROW,
+                                                 int(c0), j, z);
+                            tc::bulk_commit_group();
+                            tc::bulk_wait_read_all();
+                        }
+                    } else {
+                        *abort_v = 1;
+                    }
                 }
             }
             // D2 buffer b and the stage have been read: release them
@@ -791,6 +852,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             }
         }
         if (P::STAGE_P) tc::cp_async_wait_all();
+        // the dx stores are complete before the CTA exits
+        if (P::TMA_DX && h == 0 && lane == 0) tc::bulk_wait_all();
         if (!ok) *abort_v = 1;
         // dW partial of this split: D1 rows are the 128 k of the slice; the
         // chunk-0 warps write it
@@ -882,13 +945,20 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
 {
     using P = BwdTc<N>;
     const int64_t T = args.T, C = args.C, K = int64_t(N) * C;
-    CUtensorMap tmx, tmdu, tmg, tmy, tmdu2, tmhres, tmhpre, tmhpost;
+    CUtensorMap tmx, tmdu, tmg, tmy, tmdu2, tmhres, tmhpre, tmhpost, tmdx;
     const CUtensorMapSwizzle xsw = N == 4 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
     if (!tmap_bf16_2d(&tmx, x, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
         !tmap_bf16_2d(&tmdu, du_hl, uint64_t(T), uint64_t(P::DU_COLS), P::TT, 64,
                CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    tmg = tmy = tmdu2 = tmhres = tmhpre = tmhpost = tmx;
+    tmg = tmy = tmdu2 = tmhres = tmhpre = tmhpost = tmdx = tmx;
+    if (P::TMA_DX) {
+        // dx as [T][n][C]: a stream's 32-token box of the slice's channels
+        const uint64_t dims[3] = {uint64_t(C), uint64_t(N), uint64_t(T)};
+        const uint64_t strides[2] = {uint64_t(C) * 2, uint64_t(C) * 2 * N};
+        const uint32_t box[3] = {uint32_t(P::CW), 1, 32};
+        if (!tmap_bf16(&tmdx, args.dx, 3, dims, strides, box, xsw)) return cudaErrorInvalidValue;
+    }
     if (LAYER) {
         if (!tmap_bf16_2d(&tmg, args.dout, uint64_t(T), uint64_t(K), P::TT, P::CW, xsw) ||
             !tmap_bf16_2d(&tmy, args.dy, uint64_t(T), uint64_t(C), P::TT, P::CW, xsw))
@@ -912,7 +982,7 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
     {
         MHC_PROF("k_bwd_tc", s);
         launch_k(k_bwd_tc<N, LAYER>, dim3(grid), dim3(P::THREADS), P::SMEM, s, tmx, tmdu, tmg, tmy,
-                 tmdu2, tmhres, tmhpre, tmhpost, args);
+                 tmdu2, tmhres, tmhpre, tmhpost, tmdx, args);
     }
     return cudaGetLastError();
 }
