@@ -153,13 +153,24 @@ struct BwdTc {
     static constexpr int G1_OFF = PAR_OFF + PAR_BYTES;
     static constexpr int G1_BYTES = N == 4 ? 0 : (N + 1) * XBOX;       // 36 KB
     static constexpr int SMEM = G1_OFF + G1_BYTES + 1024;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;  // 576 / 320
     // dx leaves through shared memory: the epilogue writes each dx chunk over
-    // the x chunk it has just read (the stream boxes of the stage have dx's
-    // layout), and one thread per TMEM lane quadrant stores the quadrant's 32
-    // token rows of every stream by TMA (whole rows, where per-lane 16-byte
-    // global stores touched 32 rows per warp instruction)
-    static constexpr bool TMA_DX = true;
+    // the x chunk it has just read (the stage's stream boxes have dx's
+    // layout) and the rows go out by TMA store (whole rows, where per-lane
+    // 16-byte global stores touched 32 token rows per warp instruction).
+    // n = 8: the stage producer stores a tile's dx before it refills the
+    // stage (the stores' reads of shared memory take a few thousand cycles,
+    // which then stay off the epilogue).  n = 4: lanes of each TMEM lane
+    // quadrant's first warp store the quadrant's rows (the 88 KB stage is
+    // back sooner when the stores go out per quadrant).
+    static constexpr bool STORER = N == 8;
+    // Warps before the epilogue: 0 the stage producer (x ring; n = 8 also the
+    // dx stores), 1 TMEM + MMA issue, 2 (n = 8) the single-buffer producer.
+    static constexpr int NPRE = N == 8 ? 3 : 2;
+    static constexpr int THREADS = 32 * NPRE + 32 * EPI_WARPS;  // 576 / 352
+    // n = 8: x is waited for where it is first read (the dW MMAs, the
+    // epilogue's output phase), not before the dx GEMM and the mix, which
+    // do not read it
+    static constexpr bool LATE_X = N == 8;
     static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0 && PAR_OFF % 1024 == 0 &&
                       W_OFF % 1024 == 0 && (N == 4 || G1_OFF % 1024 == 0),
                   "alignment");
@@ -234,10 +245,12 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     constexpr bool TP = LAYER && P::TMA_P;    // per-token inputs by TMA (n = 8)
     constexpr bool G1 = LAYER && N == 8;      // dout and dy in the G buffer
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t full[P::STAGES], empty[P::STAGES];
-    // xfree: the tile's MMAs have read the stage's x; dxfull[s][q]: quadrant
-    // q's dx rows are in the stage
-    __shared__ uint64_t xfree[P::STAGES], dxfull[P::STAGES][4];
+    // full: the stage has landed; empty: the tile's MMAs (n = 4: and the
+    // epilogue warps, after the quadrants' dx stores have read it) are done
+    // with it; xfree: the tile's dW MMAs have read its x; dxfull[s][0]
+    // (n = 8): every epilogue thread has written its dx chunks into the stage
+    // (and read what it needed); dxfull[s][q] (n = 4): quadrant q's threads
+    __shared__ uint64_t full[P::STAGES], empty[P::STAGES], xfree[P::STAGES], dxfull[P::STAGES][4];
     __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full, pfull, pempty, dufull, duempty,
         gfull, gempty;
     __shared__ uint32_t tmem_slot;
@@ -261,11 +274,12 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
-            // the MMAs' commit + one arrival per epilogue warp (the other
-            // buffers: every thread releases after its own reads, tc::mbar_release)
-            tc::mbar_init(&empty[s], 1 + P::EPI_WARPS);
+            tc::mbar_init(&empty[s], P::STORER ? 1 : 1 + P::EPI_WARPS);
             tc::mbar_init(&xfree[s], 1);
-            for (int q = 0; q < 4; ++q) tc::mbar_init(&dxfull[s][q], 32 * P::CHUNKS);
+            // (the single buffers: every epilogue thread releases after its
+            // own reads, tc::mbar_release)
+            for (int q = 0; q < 4; ++q)
+                tc::mbar_init(&dxfull[s][q], P::STORER ? 32 * P::EPI_WARPS : 32 * P::CHUNKS);
         }
         tc::mbar_init(&wfull, 32 * P::EPI_WARPS);
         for (int b = 0; b < 2; ++b) {
@@ -290,16 +304,93 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ------------------------------------------------- stage producer
+        // n = 8: before a stage is refilled, this warp stores the dx that the
+        // epilogue wrote into it (lane j: stream j's box of the tile's 128
+        // rows; rows past T and channels past C are clipped by the store)
+        // and waits until the stores have read it.  Lane 0 waits and issues
+        // the loads.
         if (lane == 0) {
             tc::tma_prefetch_desc(&tmx);
-            tc::tma_prefetch_desc(&tmdu);
-            if (P::TMA_DX) tc::tma_prefetch_desc(&tmdx);
+            tc::tma_prefetch_desc(&tmdx);
+            if (N == 4) tc::tma_prefetch_desc(&tmdu);
             if (SG) {
                 tc::tma_prefetch_desc(&tmg);
                 tc::tma_prefetch_desc(&tmy);
             }
-            if (N == 8) tc::tma_prefetch_desc(&tmdu2);
+        }
+        // lane 0 waits on `bar` (parity `par`); false (n = 8: for every lane)
+        // after a failure
+        auto lane0_wait = [&](uint64_t *bar, uint32_t par) -> bool {
+            int go = 1;
+            if (lane == 0) {
+                go = !*abort_v && tc::mbar_wait(bar, par, a.fault, tc::kFaultTimeoutEmpty);
+                if (!go) *abort_v = 1;
+            }
+            return P::STORER ? __shfl_sync(kFull, go, 0) != 0 : go != 0;
+        };
+        auto store_dx = [&](int k) -> bool {
+            const int sk = k % P::STAGES;
+            if (!lane0_wait(&dxfull[sk][0], (k / P::STAGES) & 1)) return false;
+            if (lane < N) {
+                tc::tma_store_3d(&tmdx, smem + sk * P::STAGE + lane * P::XBOX, int(c0), lane,
+                                 (tile0 + k) * P::TT);
+                tc::bulk_commit_group();
+            }
+            return true;
+        };
+        int issued = 0, stored = 0;   // stages loaded; tiles whose dx was stored
+        bool good = true;
+        // (n = 4: lane 0 alone)
+        for (int i = 0; (P::STORER || lane == 0) && i < ntiles; ++i) {
+            const int s = i % P::STAGES;
+            if (i >= P::STAGES) {
+                // n = 8: tile i - 2's dx out; then the stage is free once the
+                // MMAs (n = 4: and the epilogue) are done with it
+                if (P::STORER) {
+                    good = store_dx(i - P::STAGES);
+                    if (!good) break;
+                    stored = i - P::STAGES + 1;
+                    if (lane < N) tc::bulk_wait_read_all();
+                    __syncwarp();
+                }
+                good = lane0_wait(&empty[s], ((i / P::STAGES) - 1) & 1);
+                if (!good) break;
+            }
+            if (lane == 0) {
+                uint8_t *st = smem + s * P::STAGE;
+                const int t0 = (tile0 + i) * P::TT;
+                tc::mbar_arrive_expect_tx(&full[s], stage_tx);
+                for (int j = 0; j < N; ++j)
+                    tc::tma_load_2d(st + j * P::XBOX, &tmx, int(int64_t(j) * C + c0), t0, &full[s]);
+                if (N == 4) tc::tma_load_2d(st + P::DU_OFF, &tmdu, 0, t0, &full[s]);
+                if (SG) {
+                    for (int j = 0; j < N; ++j)
+                        tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
+                                        int(int64_t(j) * C + c0), t0, &full[s]);
+                    tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &full[s]);
+                }
+            }
+            issued = i + 1;
+        }
+        if (P::STORER) {
+            // the last tiles' dx
+            for (int k = stored; good && k < issued; ++k) good = store_dx(k);
+            if (lane < N) tc::bulk_wait_all();
+        }
+        // nothing may still be landing in shared memory when the CTA exits
+        if (lane == 0)
+            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
+                tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
+                              tc::kFaultTimeoutMisc);
+    } else if (P::NPRE == 3 && warp == 2) {
+        // ------------------------------------- single-buffer producer (n = 8)
+        // each buffer is refilled once the previous tile is done with it:
+        // du_hl after the tile's MMAs, the per-token inputs and dout/dy after
+        // the epilogue has read them
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&tmdu);
+            tc::tma_prefetch_desc(&tmdu2);
             if (TP) {
                 tc::tma_prefetch_desc(&tmhres);
                 tc::tma_prefetch_desc(&tmhpre);
@@ -312,74 +403,44 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             uint8_t *par = smem + P::PAR_OFF;
             uint8_t *du1 = smem + P::DU1_OFF;
             uint8_t *g1 = smem + P::G1_OFF;
-            // issued: ring stages; n1: tiles whose single-buffer loads were issued
-            int issued = 0, n1 = 0;
+            int n1 = 0;   // tiles whose loads were issued
             for (int i = 0; i < ntiles && !*abort_v; ++i) {
-                const int s = i % P::STAGES;
-                if (i >= P::STAGES &&
-                    !tc::mbar_wait(&empty[s], ((i / P::STAGES) & 1) ^ 1, a.fault,
-                                   tc::kFaultTimeoutEmpty)) {
+                const int t0 = (tile0 + i) * P::TT;
+                if (i >= 1 &&
+                    !tc::mbar_wait(&duempty, (i - 1) & 1, a.fault, tc::kFaultTimeoutEmpty)) {
                     *abort_v = 1;
                     break;
                 }
-                uint8_t *st = smem + s * P::STAGE;
-                const int t0 = (tile0 + i) * P::TT;
-                tc::mbar_arrive_expect_tx(&full[s], stage_tx);
-                for (int j = 0; j < N; ++j)
-                    tc::tma_load_2d(st + j * P::XBOX, &tmx, int(int64_t(j) * C + c0), t0, &full[s]);
-                if (N == 4)
-                    tc::tma_load_2d(st + P::DU_OFF, &tmdu, 0, t0, &full[s]);
-                if (SG) {
-                    for (int j = 0; j < N; ++j)
-                        tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
-                                        int(int64_t(j) * C + c0), t0, &full[s]);
-                    tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &full[s]);
-                }
-                issued = i + 1;
-                if (N == 8) {
-                    // single buffers, each refilled once the previous tile is
-                    // done with it: du_hl after the tile's MMAs, the per-token
-                    // inputs and dout/dy after the epilogue has read them
-                    if (i >= 1 && !tc::mbar_wait(&duempty, (i - 1) & 1, a.fault,
-                                                 tc::kFaultTimeoutEmpty)) {
+                tc::mbar_arrive_expect_tx(&dufull, P::DU_BYTES);
+                for (int u = 0; u < P::DU_ATOMS; ++u)
+                    tc::tma_load_2d(du1 + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0, &dufull);
+                tc::tma_load_2d(du1 + P::DU_TAIL, &tmdu2, 128, t0, &dufull);
+                if (G1) {
+                    if (i >= 1 &&
+                        !tc::mbar_wait(&gempty, (i - 1) & 1, a.fault, tc::kFaultTimeoutEmpty)) {
                         *abort_v = 1;
                         break;
                     }
-                    tc::mbar_arrive_expect_tx(&dufull, P::DU_BYTES);
-                    for (int u = 0; u < P::DU_ATOMS; ++u)
-                        tc::tma_load_2d(du1 + u * P::DU_ATOM_BYTES, &tmdu, u * 64, t0, &dufull);
-                    tc::tma_load_2d(du1 + P::DU_TAIL, &tmdu2, 128, t0, &dufull);
-                    if (G1) {
-                        if (i >= 1 && !tc::mbar_wait(&gempty, (i - 1) & 1, a.fault,
-                                                     tc::kFaultTimeoutEmpty)) {
-                            *abort_v = 1;
-                            break;
-                        }
-                        tc::mbar_arrive_expect_tx(&gfull, P::G1_BYTES);
-                        for (int j = 0; j < N; ++j)
-                            tc::tma_load_2d(g1 + j * P::XBOX, &tmg, int(int64_t(j) * C + c0), t0,
-                                            &gfull);
-                        tc::tma_load_2d(g1 + N * P::XBOX, &tmy, int(c0), t0, &gfull);
-                    }
-                    if (TP) {
-                        if (i >= 1 && !tc::mbar_wait(&pempty, (i - 1) & 1, a.fault,
-                                                     tc::kFaultTimeoutEmpty)) {
-                            *abort_v = 1;
-                            break;
-                        }
-                        tc::mbar_arrive_expect_tx(&pfull, P::PAR_BYTES);
-                        tc::tma_load_2d(par, &tmhres, 0, t0, &pfull);
-                        tc::tma_load_2d(par + P::TT * 128, &tmhres, 32, t0, &pfull);
-                        tc::tma_load_2d(par + P::PH_PRE, &tmhpre, 0, t0, &pfull);
-                        tc::tma_load_2d(par + P::PH_POST, &tmhpost, 0, t0, &pfull);
-                    }
-                    n1 = i + 1;
+                    tc::mbar_arrive_expect_tx(&gfull, P::G1_BYTES);
+                    for (int j = 0; j < N; ++j)
+                        tc::tma_load_2d(g1 + j * P::XBOX, &tmg, int(int64_t(j) * C + c0), t0,
+                                        &gfull);
+                    tc::tma_load_2d(g1 + N * P::XBOX, &tmy, int(c0), t0, &gfull);
                 }
+                if (TP) {
+                    if (i >= 1 &&
+                        !tc::mbar_wait(&pempty, (i - 1) & 1, a.fault, tc::kFaultTimeoutEmpty)) {
+                        *abort_v = 1;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(&pfull, P::PAR_BYTES);
+                    tc::tma_load_2d(par, &tmhres, 0, t0, &pfull);
+                    tc::tma_load_2d(par + P::TT * 128, &tmhres, 32, t0, &pfull);
+                    tc::tma_load_2d(par + P::PH_PRE, &tmhpre, 0, t0, &pfull);
+                    tc::tma_load_2d(par + P::PH_POST, &tmhpost, 0, t0, &pfull);
+                }
+                n1 = i + 1;
             }
-            // nothing may still be landing in shared memory when the CTA exits
-            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
-                tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
-                              tc::kFaultTimeoutMisc);
             if (n1 > 0) {
                 tc::mbar_wait(&dufull, (n1 - 1) & 1, a.fault, tc::kFaultTimeoutMisc);
                 if (TP) tc::mbar_wait(&pfull, (n1 - 1) & 1, a.fault, tc::kFaultTimeoutMisc);
@@ -396,7 +457,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % P::STAGES, b = i & 1;
                 if (*abort_v ||
-                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
+                    (!P::LATE_X &&
+                     !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) ||
                     (N == 8 && !tc::mbar_wait(&dufull, i & 1, a.fault, tc::kFaultTimeoutFull))) {
                     ok = false;
                     break;
@@ -439,6 +501,13 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&d2full[b]);
+                if (P::LATE_X) {
+                    if (!tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                }
                 // dW += x^T du_hl over the tile's 128 tokens, 16 per step
 #pragma unroll
                 for (int ks = 0; ks < P::TT / 16; ++ks) {
@@ -461,7 +530,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         tc::mma_bf16(tmem + P::D1_COL + 128, ad, bd2, idesc_dw2, acc);
                     }
                 }
-                if (P::TMA_DX) tc::mma_commit(&xfree[s]);
+                tc::mma_commit(&xfree[s]);
                 if (SG) {
                     // dbias: dout^T [du_hl | H_post hi | H_post lo] over the tile
                     constexpr uint32_t idesc_db = tc::idesc_bf16_f32(128, P::D3_N, 1, 1);
@@ -493,7 +562,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         // [W_hi [64,80) | W_lo [64,80)].
         constexpr int W_CHUNKS = P::W_PLANES * 128 * 8 + (N == 8 ? 128 * 4 : 0);
         float wmax = 0.f;   // max |W| of the values this thread loads
-        for (int idx = threadIdx.x - 64; idx < W_CHUNKS; idx += 32 * P::EPI_WARPS) {
+        for (int idx = threadIdx.x - 32 * P::NPRE; idx < W_CHUNKS; idx += 32 * P::EPI_WARPS) {
             int rr, col;
             bool lo;
             uint32_t dst;
@@ -544,7 +613,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         const float wbound = __uint_as_float(wmax_bits) * kSplitBound;
 
         const int q = warp & 3;              // TMEM lane quadrant
-        const int h = (warp - 2) >> 2;       // this thread's 8-channel chunk of every stream
+        const int h = (warp - P::NPRE) >> 2; // this thread's 8-channel chunk of every stream
         const int r = q * 32 + lane;         // token row in the tile / k row of dW
         const uint32_t trow = tmem + (uint32_t(q * 32) << 16);
         const int64_t cc = c0 + h * 8;       // first channel of the chunk
@@ -683,32 +752,39 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     tc::mbar_release(&gempty);
                 }
             }
-            if (*abort_v ||
-                !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
-                !tc::mbar_wait(&d2full[b], (i >> 1) & 1, a.fault, tc::kFaultTimeoutAcc)) {
+            // the stage (x) and the dx accumulator of this tile; then the exact
+            // path (rare: rows of near-zero RMS): a warp with such a token
+            // rewrites that token's dx_gemm values in TMEM with du.W^T from
+            // the fp32 values before the usual reads below
+            auto stage_and_acc = [&]() -> bool {
+                if (*abort_v ||
+                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
+                    !tc::mbar_wait(&d2full[b], (i >> 1) & 1, a.fault, tc::kFaultTimeoutAcc))
+                    return false;
+                tc::tc_fence_after();
+                const bool exact = valid && cvalid && dub * wbound > kExactAbove;
+                if (__any_sync(kFull, exact)) {
+                    const uint32_t tb = trow + P::D2_COL + b * 128 + h * 8;
+#pragma unroll 1
+                    for (int j = 0; j < N; ++j) {
+                        float v[8];
+                        tc::tmem_ld8_wait(tb + j * CW, v);
+                        if (exact) {
+                            const float *wrow = a.W + (int64_t(j) * C + cc) * O;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                v[e] = exact_du_w(a.du32 + t * O, wrow + e * O, O);
+                        }
+                        __syncwarp();
+                        tc::tmem_st8_wait(tb + j * CW, v);
+                    }
+                }
+                return true;
+            };
+            if (!P::LATE_X && !stage_and_acc()) {
                 ok = false;
                 if (P::STAGE_P) continue;
                 break;
-            }
-            tc::tc_fence_after();
-            // The exact path (rare: rows of near-zero RMS): a warp with such a
-            // token rewrites that token's dx_gemm values in TMEM with du.W^T
-            // from the fp32 values before the usual reads below.
-            const bool exact = valid && cvalid && dub * wbound > kExactAbove;
-            if (__any_sync(kFull, exact)) {
-                const uint32_t tb = trow + P::D2_COL + b * 128 + h * 8;
-#pragma unroll 1
-                for (int j = 0; j < N; ++j) {
-                    float v[8];
-                    tc::tmem_ld8_wait(tb + j * CW, v);
-                    if (exact) {
-                        const float *wrow = a.W + (int64_t(j) * C + cc) * O;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = exact_du_w(a.du32 + t * O, wrow + e * O, O);
-                    }
-                    __syncwarp();
-                    tc::tmem_st8_wait(tb + j * CW, v);
-                }
             }
             const uint8_t *st = smem + s * P::STAGE;
             // (releasing the stage right after these reads, before the
@@ -775,10 +851,15 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             // dx_gemm of this chunk for every stream: all TMEM loads, one wait
             constexpr int JB = 2;  // streams per batch of TMEM loads
             const f32x2 coef2 = f2_make(coef, coef);
-            // dx overwrites x in the stage once the tile's dW MMAs have read it
-            if (P::TMA_DX &&
-                (*abort_v ||
-                 !tc::mbar_wait(&xfree[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutAcc))) {
+            if (P::LATE_X && !stage_and_acc()) {
+                ok = false;
+                break;
+            }
+            // dx overwrites x in the stage (the stream boxes have dx's layout:
+            // each thread writes the chunk it has just read) once the tile's
+            // dW MMAs have read it
+            if (*abort_v ||
+                !tc::mbar_wait(&xfree[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutAcc)) {
                 ok = false;
                 if (P::STAGE_P) continue;
                 break;
@@ -801,34 +882,31 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                         o[p] = f2_fma(coef2, xv[p], f2_make(acc[jj][2 * p], acc[jj][2 * p + 1]));
                         if (LAYER) o[p] = f2_add(o[p], mix[j][p]);
                     }
-                    if (P::TMA_DX) {
-                        const uint4 v = pack8x2(o);
-                        asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
-                                         box_chunk_addr<N>(st + j * P::XBOX, r, h)),
-                                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                                     : "memory");
-                    } else if (valid && cvalid) {
-                        st_stream(a.dx + ((t * N + j) * C + cc), pack8x2(o));
-                    }
+                    const uint4 v = pack8x2(o);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                                     box_chunk_addr<N>(st + j * P::XBOX, r, h)),
+                                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                                 : "memory");
                 }
             }
-            if (P::TMA_DX) {
-                // this thread's dx chunks are in the stage (made visible to
-                // the TMA engine); the quadrant's chunk-0 lane 0 stores the
-                // quadrant's rows once all of them are (rows past T and
-                // channels past C are clipped by the store) and waits until
-                // the stores have read the stage before the stage goes back
-                tc::fence_proxy_async_smem();
+            // this thread is done with the stage and its dx chunks are there
+            // (visible to the TMA engine).  n = 8: the stage producer stores
+            // them once every thread's are.  n = 4: lane j of the quadrant's
+            // chunk-0 warp stores stream j's 32 rows once the quadrant's are,
+            // and the warp releases the stage after the stores have read it.
+            // D2 buffer b has been read.
+            tc::fence_proxy_async_smem();
+            if (P::STORER) {
+                tc::mbar_arrive(&dxfull[s][0]);
+            } else {
                 tc::mbar_arrive(&dxfull[s][q]);
-                if (h == 0 && lane == 0) {
+                if (h == 0 && lane < N) {
                     if (tc::mbar_wait(&dxfull[s][q], (i / P::STAGES) & 1, a.fault,
                                       tc::kFaultTimeoutFull)) {
                         const int z = (tile0 + i) * P::TT + q * 32;
                         if (z < a.T) {
-#pragma unroll 1
-                            for (int j = 0; j < N; ++j)
-                                tc::tma_store_3d(&tmdx, st + j * P::XBOX + q * 32 * P::XROW,
-                                                 int(c0), j, z);
+                            tc::tma_store_3d(&tmdx, st + lane * P::XBOX + q * 32 * P::XROW, int(c0),
+                                             lane, z);
                             tc::bulk_commit_group();
                             tc::bulk_wait_read_all();
                         }
@@ -837,23 +915,16 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
                 }
             }
-            // D2 buffer b and the stage have been read: release them
-            // (one arrival per warp: every value this thread read from the
-            // stage has been consumed by the dx stores above, so no read of
-            // the stage is in flight, and the proxy fence orders the reads
-            // before the refill by TMA; a per-thread acq_rel fence here also
-            // waited for those global stores, 5 us per launch at n = 4)
-            tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                tc::mbar_arrive(&empty[s]);
+                if (!P::STORER) tc::mbar_arrive(&empty[s]);
                 tc::mbar_arrive(&d2empty[b]);
             }
         }
         if (P::STAGE_P) tc::cp_async_wait_all();
-        // the dx stores are complete before the CTA exits
-        if (P::TMA_DX && h == 0 && lane == 0) tc::bulk_wait_all();
+        // (n = 4) the dx stores are complete before the CTA exits
+        if (!P::STORER && h == 0 && lane < N) tc::bulk_wait_all();
         if (!ok) *abort_v = 1;
         // dW partial of this split: D1 rows are the 128 k of the slice; the
         // chunk-0 warps write it
@@ -952,11 +1023,12 @@ static cudaError_t bwd_tc_impl(const bf16 *x, const bf16 *du_hl, const BwdTcArgs
                CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     tmg = tmy = tmdu2 = tmhres = tmhpre = tmhpost = tmdx = tmx;
-    if (P::TMA_DX) {
-        // dx as [T][n][C]: a stream's 32-token box of the slice's channels
+    {
+        // dx as [T][n][C]: a stream's box of the slice's channels over a tile
+        // (n = 8) or a quadrant's 32 tokens (n = 4)
         const uint64_t dims[3] = {uint64_t(C), uint64_t(N), uint64_t(T)};
         const uint64_t strides[2] = {uint64_t(C) * 2, uint64_t(C) * 2 * N};
-        const uint32_t box[3] = {uint32_t(P::CW), 1, 32};
+        const uint32_t box[3] = {uint32_t(P::CW), 1, P::STORER ? uint32_t(P::TT) : 32u};
         if (!tmap_bf16(&tmdx, args.dx, 3, dims, strides, box, xsw)) return cudaErrorInvalidValue;
     }
     if (LAYER) {
