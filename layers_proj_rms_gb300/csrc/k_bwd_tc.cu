@@ -32,7 +32,9 @@
 //          Both operands are read MN-major straight from the TMA tiles.
 //   MMA 3 (n = 4, dbias): D3[k][o'] += sum_t dout[t][k] du_hl[t][o'] with
 //          H_post hi | lo stored in du_hl columns [2O, 2O+2n)
-//   epilogue: D2 + the elementwise terms -> dx (bf16).
+//   epilogue: D2 + the elementwise terms -> dx (bf16), written over the x
+//          chunk each thread has just read in the stage (the stage's stream
+//          boxes have dx's layout), then stored by TMA.
 // D2 is double-buffered in TMEM so the next tile's MMAs overlap the
 // epilogue; D1 accumulates over the whole token range and is written as this
 // split's dW partial.  Every input of a tile arrives by TMA ahead of its use:
@@ -43,13 +45,16 @@
 // (released by the MMAs), the per-token inputs H_res, H_pre, H_post and dout
 // and dy (released once the epilogue has read them).  Per-lane global loads
 // of these inputs (each warp load touching 32 token rows) cost 2.8x the
-// time at n = 8.
-// Warps: 0 TMA producer, 1 TMEM + MMA issue, 2.. epilogue: CW/8 warps per
-// TMEM lane quadrant, each thread one token row x one 8-channel chunk of
-// every stream (16 epilogue warps for n = 4, 8 for n = 8).  Before their
-// first tile the epilogue warps build the slice's W tile in shared memory
-// from fp32 W (bf16 hi/lo split, swizzled for the MMA).  An unsplit pass
-// writes dW and dbias directly.
+// time at n = 8, and per-lane 16-byte dx stores half of the tile period.
+// Warps: 0 the stage producer (n = 8: also the dx stores of a tile, right
+// before it refills that stage), 1 TMEM + MMA issue, 2 (n = 8) the
+// single-buffer producer, then the epilogue: CW/8 warps per TMEM lane
+// quadrant, each thread one token row x one 8-channel chunk of every stream
+// (16 epilogue warps for n = 4, 8 for n = 8; at n = 4 lanes of each
+// quadrant's first warp store the quadrant's dx rows).  Before their first
+// tile the epilogue warps build the slice's W tile in shared memory from
+// fp32 W (bf16 hi/lo split, swizzled for the MMA).  An unsplit pass writes
+// dW and dbias directly.
 #include "launch.h"
 #include "tc.cuh"
 #include "tmap.h"
