@@ -172,10 +172,13 @@ struct BwdTc {
     // dx stores), 1 TMEM + MMA issue, 2 (n = 8) the single-buffer producer.
     static constexpr int NPRE = N == 8 ? 3 : 2;
     static constexpr int THREADS = 32 * NPRE + 32 * EPI_WARPS;  // 576 / 352
-    // n = 8: x is waited for where it is first read (the dW MMAs, the
-    // epilogue's output phase), not before the dx GEMM and the mix, which
-    // do not read it
-    static constexpr bool LATE_X = N == 8;
+    // x is waited for where it is first read (the dW MMAs, the epilogue's
+    // output phase), not before the dx GEMM and the mix, which do not read
+    // it.  n = 4: the stage's x and its other part (dout, dy, du_hl: the G
+    // part) have barriers of their own; the G part returns to the producer
+    // once the epilogue's mix and the tile's MMAs are done with it, x once
+    // the dx stores have read it.
+    static constexpr bool SPLIT = N == 4;
     static_assert(STAGE % 1024 == 0 && DU_OFF % 1024 == 0 && PAR_OFF % 1024 == 0 &&
                       W_OFF % 1024 == 0 && (N == 4 || G1_OFF % 1024 == 0),
                   "alignment");
@@ -256,6 +259,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     // (n = 8): every epilogue thread has written its dx chunks into the stage
     // (and read what it needed); dxfull[s][q] (n = 4): quadrant q's threads
     __shared__ uint64_t full[P::STAGES], empty[P::STAGES], xfree[P::STAGES], dxfull[P::STAGES][4];
+    // n = 4: the G part of a stage has landed / is free again
+    __shared__ uint64_t gsfull[P::STAGES], gsempty[P::STAGES];
     __shared__ uint64_t wfull, d2full[2], d2empty[2], d1full, pfull, pempty, dufull, duempty,
         gfull, gempty;
     __shared__ uint32_t tmem_slot;
@@ -274,13 +279,18 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
     const int split = blockIdx.y;
     const int tile0 = split * a.tiles_per_split;
     const int ntiles = min(a.tiles_total, tile0 + a.tiles_per_split) - tile0;
-    constexpr uint32_t stage_tx = SG || N == 8 ? P::STAGE : P::X_BYTES + P::DU_BYTES;
+    // bytes of a stage's x part (n = 8: the whole stage) and of its G part (n = 4)
+    constexpr uint32_t x_tx = P::X_BYTES;
+    constexpr uint32_t g_tx = P::SPLIT ? (SG ? P::G_BYTES + P::Y_BYTES : 0) + P::DU_BYTES : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < P::STAGES; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], P::STORER ? 1 : 1 + P::EPI_WARPS);
             tc::mbar_init(&xfree[s], 1);
+            // the MMAs' commit (+ one arrival per epilogue warp after the mix)
+            tc::mbar_init(&gsfull[s], 1);
+            tc::mbar_init(&gsempty[s], 1 + (LAYER ? P::EPI_WARPS : 0));
             // (the single buffers: every epilogue thread releases after its
             // own reads, tc::mbar_release)
             for (int q = 0; q < 4; ++q)
@@ -344,14 +354,34 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             }
             return true;
         };
-        int issued = 0, stored = 0;   // stages loaded; tiles whose dx was stored
+        int issued = 0, stored = 0;   // x parts loaded; tiles whose dx was stored
+        int gissued = 0;              // n = 4: G parts loaded
         bool good = true;
         // (n = 4: lane 0 alone)
         for (int i = 0; (P::STORER || lane == 0) && i < ntiles; ++i) {
             const int s = i % P::STAGES;
+            if (P::SPLIT && lane == 0) {
+                // n = 4: the G part first (the dx GEMM and the mix need it
+                // before x)
+                if (i >= P::STAGES) {
+                    good = lane0_wait(&gsempty[s], ((i / P::STAGES) - 1) & 1);
+                    if (!good) break;
+                }
+                uint8_t *st = smem + s * P::STAGE;
+                const int t0 = (tile0 + i) * P::TT;
+                tc::mbar_arrive_expect_tx(&gsfull[s], g_tx);
+                tc::tma_load_2d(st + P::DU_OFF, &tmdu, 0, t0, &gsfull[s]);
+                if (SG) {
+                    for (int j = 0; j < N; ++j)
+                        tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
+                                        int(int64_t(j) * C + c0), t0, &gsfull[s]);
+                    tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &gsfull[s]);
+                }
+                gissued = i + 1;
+            }
             if (i >= P::STAGES) {
-                // n = 8: tile i - 2's dx out; then the stage is free once the
-                // MMAs (n = 4: and the epilogue) are done with it
+                // n = 8: tile i - 2's dx out; then x is free once the MMAs
+                // (n = 4: and the epilogue) are done with it
                 if (P::STORER) {
                     good = store_dx(i - P::STAGES);
                     if (!good) break;
@@ -365,16 +395,9 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             if (lane == 0) {
                 uint8_t *st = smem + s * P::STAGE;
                 const int t0 = (tile0 + i) * P::TT;
-                tc::mbar_arrive_expect_tx(&full[s], stage_tx);
+                tc::mbar_arrive_expect_tx(&full[s], x_tx);
                 for (int j = 0; j < N; ++j)
                     tc::tma_load_2d(st + j * P::XBOX, &tmx, int(int64_t(j) * C + c0), t0, &full[s]);
-                if (N == 4) tc::tma_load_2d(st + P::DU_OFF, &tmdu, 0, t0, &full[s]);
-                if (SG) {
-                    for (int j = 0; j < N; ++j)
-                        tc::tma_load_2d(st + P::G_OFF + j * P::XBOX, &tmg,
-                                        int(int64_t(j) * C + c0), t0, &full[s]);
-                    tc::tma_load_2d(st + P::Y_OFF, &tmy, int(c0), t0, &full[s]);
-                }
             }
             issued = i + 1;
         }
@@ -385,8 +408,13 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
         }
         // nothing may still be landing in shared memory when the CTA exits
         if (lane == 0)
-            for (int i = max(0, issued - P::STAGES); i < issued; ++i)
+            for (int i = max(0, issued - P::STAGES); i < issued; ++i) {
                 tc::mbar_wait(&full[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
+                              tc::kFaultTimeoutMisc);
+            }
+        if (P::SPLIT && lane == 0)
+            for (int i = max(0, gissued - P::STAGES); i < gissued; ++i)
+                tc::mbar_wait(&gsfull[i % P::STAGES], (i / P::STAGES) & 1, a.fault,
                               tc::kFaultTimeoutMisc);
     } else if (P::NPRE == 3 && warp == 2) {
         // ------------------------------------- single-buffer producer (n = 8)
@@ -461,9 +489,10 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
             const uint32_t wb = tc::smem_u32(wtile);
             for (int i = 0; ok && i < ntiles; ++i) {
                 const int s = i % P::STAGES, b = i & 1;
+                // du_hl (n = 4: the stage's G part) before the dx GEMM; x later
                 if (*abort_v ||
-                    (!P::LATE_X &&
-                     !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) ||
+                    (N == 4 && !tc::mbar_wait(&gsfull[s], (i / P::STAGES) & 1, a.fault,
+                                              tc::kFaultTimeoutFull)) ||
                     (N == 8 && !tc::mbar_wait(&dufull, i & 1, a.fault, tc::kFaultTimeoutFull))) {
                     ok = false;
                     break;
@@ -506,13 +535,11 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     tc::mma_bf16(tmem + P::D2_COL + b * 128, ad, bd, idesc_dx, kk > 0 ? 1u : 0u);
                 }
                 tc::mma_commit(&d2full[b]);
-                if (P::LATE_X) {
-                    if (!tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::tc_fence_after();
+                if (!tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull)) {
+                    ok = false;
+                    break;
                 }
+                tc::tc_fence_after();
                 // dW += x^T du_hl over the tile's 128 tokens, 16 per step
 #pragma unroll
                 for (int ks = 0; ks < P::TT / 16; ++ks) {
@@ -536,6 +563,7 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(&xfree[s]);
+                if (P::SPLIT) tc::mma_commit(&empty[s]);
                 if (SG) {
                     // dbias: dout^T [du_hl | H_post hi | H_post lo] over the tile
                     constexpr uint32_t idesc_db = tc::idesc_bf16_f32(128, P::D3_N, 1, 1);
@@ -549,7 +577,10 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                                      (i > 0 || ks > 0) ? 1u : 0u);
                     }
                 }
-                tc::mma_commit(&empty[s]);
+                if (P::SPLIT)
+                    tc::mma_commit(&gsempty[s]);
+                else
+                    tc::mma_commit(&empty[s]);
                 if (N == 8) tc::mma_commit(&duempty);
             }
             if (!ok) *abort_v = 1;
@@ -757,13 +788,13 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     tc::mbar_release(&gempty);
                 }
             }
-            // the stage (x) and the dx accumulator of this tile; then the exact
-            // path (rare: rows of near-zero RMS): a warp with such a token
-            // rewrites that token's dx_gemm values in TMEM with du.W^T from
-            // the fp32 values before the usual reads below
-            auto stage_and_acc = [&]() -> bool {
+            // `bar` (n = 4: the stage's G part; n = 8: x) and the dx accumulator
+            // of this tile; then the exact path (rare: rows of near-zero RMS):
+            // a warp with such a token rewrites that token's dx_gemm values in
+            // TMEM with du.W^T from the fp32 values before the usual reads below
+            auto part_and_acc = [&](uint64_t *bar) -> bool {
                 if (*abort_v ||
-                    !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
+                    !tc::mbar_wait(bar, (i / P::STAGES) & 1, a.fault, tc::kFaultTimeoutFull) ||
                     !tc::mbar_wait(&d2full[b], (i >> 1) & 1, a.fault, tc::kFaultTimeoutAcc))
                     return false;
                 tc::tc_fence_after();
@@ -786,7 +817,8 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                 }
                 return true;
             };
-            if (!P::LATE_X && !stage_and_acc()) {
+            // n = 4: dout and dy (the G part) and the accumulator before the mix
+            if (P::SPLIT && !part_and_acc(&gsfull[s])) {
                 ok = false;
                 if (P::STAGE_P) continue;
                 break;
@@ -852,12 +884,23 @@ __global__ void __launch_bounds__(BwdTc<N>::THREADS, 1)
                     // this thread has read the parameter buffer
                     tc::mbar_release(&pempty);
                 }
+                if (P::SPLIT) {
+                    // n = 4: dout and dy have been read; the G part goes back
+                    // once the tile's MMAs are done with it too
+                    tc::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&gsempty[s]);
+                }
             }
             // dx_gemm of this chunk for every stream: all TMEM loads, one wait
             constexpr int JB = 2;  // streams per batch of TMEM loads
             const f32x2 coef2 = f2_make(coef, coef);
-            if (P::LATE_X && !stage_and_acc()) {
+            // x (n = 8: with the accumulator)
+            if (P::SPLIT ? (*abort_v || !tc::mbar_wait(&full[s], (i / P::STAGES) & 1, a.fault,
+                                                        tc::kFaultTimeoutFull))
+                         : !part_and_acc(&full[s])) {
                 ok = false;
+                if (P::STAGE_P) continue;
                 break;
             }
             // dx overwrites x in the stage (the stream boxes have dx's layout:
