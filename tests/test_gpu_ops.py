@@ -351,9 +351,13 @@ def test_layer(M, orc, T, n, C, seed, stress):
 # than one phase, with a ragged last tile and a ragged last channel slice
 # (C = 2056: 129 slices of 16 channels, one CTA per slice, six tiles each;
 # C = 64, T = 3000: 8 token splits of 3 tiles; n = 4, C = 1032: 33 slices of
-# 32 channels, 3 token splits of 2 tiles).
+# 32 channels, 3 token splits of 2 tiles; n = 4, C = 4096, T = 1000: one split
+# of 8 tiles, so each stage of the two-stage ring is reused three times and
+# the last tile holds 104 tokens; n = 8, C = 1032: 65 slices, the last of 8
+# channels, 2 token splits of 4 tiles).
 @pytest.mark.parametrize("T,n,C,seed", [(700, 8, 2056, 11), (3000, 8, 64, 12),
-                                        (700, 4, 1032, 13)])
+                                        (700, 4, 1032, 13), (1000, 4, 4096, 14),
+                                        (1000, 8, 1032, 15)])
 def test_layer_multi_tile(M, orc, T, n, C, seed):
     inp = _proj_inputs(T, n, C, seed, False)
     o = run_layer(M, inp, T, n, C)
